@@ -1,0 +1,284 @@
+// Plain, slow, FP64 CPU oracle for the Mamba-3 selective-state scan.
+//
+// TEST INFRASTRUCTURE ONLY. This file is the reference that the CUDA library is
+// checked against. Only the test suite, the smoke check and the benchmark's CPU
+// baseline leg load it; the product path never does. It shares no code, header
+// or constant with the CUDA sources.
+//
+// Source: oarust 0.8.6, `src/rs/ml/matrix/mamba3.rs` (docs.rs source view) and
+// the `oa::ml::matrix` API reference. Those pages give the operands, shapes,
+// limits, dataflow and docstrings of the Mamba-3 ops but print no formula. Each
+// function below names the passage it follows; every step the pages leave open
+// is marked READING and is listed, with the alternatives, in the design notes.
+//
+// Everything is computed in double from the float32 inputs the GPU also gets.
+// Parallelism: one std::thread per slice of (batch, head) pairs. No blocking,
+// fusion or reordering beyond the token-by-token recurrence itself.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+#include <algorithm>
+#include <functional>
+
+namespace {
+
+using i64 = int64_t;
+
+// Overflow-safe softplus: `softplus` in the `oa::ml::matrix` API reference is
+// "the overflow-safe Softplus formulation". log(1 + e^v) is returned as v once
+// e^-v is below double rounding.
+double softplus(double v) { return v > 36.0 ? v : std::log1p(std::exp(v)); }
+
+double sigmoid(double v) { return 1.0 / (1.0 + std::exp(-v)); }
+
+// SiLU gate, `has_z` in SsmConfig ("Apply the SiLU z gate").
+double silu(double v) { return v * sigmoid(v); }
+
+// Runs fn(i) for i in [0, n) on up to `threads` std::threads.
+void parallel_for(i64 n, int threads, const std::function<void(i64)>& fn) {
+  if (threads <= 1 || n <= 1) {
+    for (i64 i = 0; i < n; ++i) fn(i);
+    return;
+  }
+  int t = (int)std::min<i64>(threads, n);
+  std::vector<std::thread> pool;
+  for (int w = 0; w < t; ++w) {
+    pool.emplace_back([=, &fn]() {
+      for (i64 i = w; i < n; i += t) fn(i);
+    });
+  }
+  for (auto& th : pool) th.join();
+}
+
+// READING (rotation pairing): the rotary pairs of the state axis are split-half
+// over the first 2A state dims, pair a = (a, a + A), the same convention as the
+// `rope` op of the API reference ("split-half rotary"). Dims >= 2A are kept.
+// Rotation by theta: (u, v) -> (u cos - v sin, u sin + v cos).
+void rotate(std::vector<double>& vec, const std::vector<double>& theta, i64 A) {
+  for (i64 a = 0; a < A; ++a) {
+    double u = vec[a], v = vec[a + A];
+    double c = std::cos(theta[a]), s = std::sin(theta[a]);
+    vec[a] = u * c - v * s;
+    vec[a + A] = u * s + v * c;
+  }
+}
+
+struct Ssm {
+  i64 B, L, H, G, P, N, A, R;
+  int has_z, has_d, has_norm;
+};
+
+// Per-token scalars of one (b, t, h): the decay, gamma and scale values the
+// backward kernels of mamba3.rs recompute from (adt) and (dt, trap) alone.
+// READING (trapezoid gate): lambda = sigmoid(trap) ("raw trapezoidal gates");
+// gamma = lambda * dt weights the current token, scale = (1 - lambda) * dt the
+// previous one, decay = exp(adt).
+struct TokenCoef {
+  double decay, gamma, scale;
+};
+
+TokenCoef coef(double adt, double dt, double trap) {
+  double lam = sigmoid(trap);
+  return {std::exp(adt), lam * dt, (1.0 - lam) * dt};
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Fused projection preprocess. Follows `Mamba3PreprocessConfig`,
+// `Mamba3PreprocessResult` and `PreprocessGeometry::resolve` of mamba3.rs and the
+// `mamba3_preprocess` docstring (packed width 2I + 2GRN + 3H + A).
+//
+// READING (column order): z, x, B rows, C rows, dt, A, trap, angle - the order
+// of the kernel's output bindings (z before x, B before C).
+// READING (B/C rows): row j of the G*R rows sits at columns [j*N, (j+1)*N) of the
+// B (resp. C) slice; each row is divided by sqrt(mean square + epsilon); no
+// weight (the preprocess adjoint returns only d(projected) and d(dt_bias)).
+// READING (dt): dt = clamp(softplus(dt_raw + dt_bias[h]), dt_min, dt_max), the
+// bounds inclusive ("Inclusive lower/upper bound for transformed dt").
+// READING (adt): adt = -max(softplus(a_raw), a_floor) * dt ("positive floor for
+// the magnitude of the negative A token"; "negative A-times-dt log decays").
+// trap and angle pass through raw ("Raw trapezoidal gates", "Raw rotary angular
+// velocities").
+// Returns 0, or 1 for an invalid geometry.
+int m3o_preprocess(i64 rows, i64 inner, i64 N, i64 H, i64 A, i64 G, i64 R, double eps,
+                   double dt_min, double dt_max, double a_floor, const float* projected,
+                   const float* dt_bias, double* x, double* z, double* bh, double* ch,
+                   double* dt, double* adt, double* trap, double* angle, int threads) {
+  if (rows <= 0 || inner <= 0 || N <= 0 || H <= 0 || G <= 0 || R <= 0 || 2 * A > N) return 1;
+  const i64 bc = G * R * N;
+  const i64 W = 2 * inner + 2 * bc + 3 * H + A;
+  const i64 o_b = 2 * inner, o_c = o_b + bc, o_s = o_c + bc;
+  parallel_for(rows, threads, [&](i64 r) {
+    const float* p = projected + r * W;
+    for (i64 i = 0; i < inner; ++i) {
+      z[r * inner + i] = p[i];
+      x[r * inner + i] = p[inner + i];
+    }
+    for (int which = 0; which < 2; ++which) {
+      const float* src = p + (which == 0 ? o_b : o_c);
+      double* dst = (which == 0 ? bh : ch) + r * bc;
+      for (i64 j = 0; j < G * R; ++j) {
+        double ms = 0.0;
+        for (i64 n = 0; n < N; ++n) ms += (double)src[j * N + n] * (double)src[j * N + n];
+        ms /= (double)N;
+        double inv = 1.0 / std::sqrt(ms + eps);
+        for (i64 n = 0; n < N; ++n) dst[j * N + n] = (double)src[j * N + n] * inv;
+      }
+    }
+    for (i64 h = 0; h < H; ++h) {
+      double d = softplus((double)p[o_s + h] + (double)dt_bias[h]);
+      d = std::min(std::max(d, dt_min), dt_max);
+      double a_mag = std::max(softplus((double)p[o_s + H + h]), a_floor);
+      dt[r * H + h] = d;
+      adt[r * H + h] = -a_mag * d;
+      trap[r * H + h] = p[o_s + 2 * H + h];
+    }
+    for (i64 a = 0; a < A; ++a) angle[r * A + a] = p[o_s + 3 * H + a];
+  });
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// SISO / MIMO selective-state recurrence, token by token.
+//
+// Follows `mamba3_siso` / `mamba3_mimo` (operand layouts C/B [B,L,R*G,N],
+// x/z/out [B,L,H,P], adt/dt/trap [B,L,H], angle [B,L,A], biases [H,R,N],
+// D [H], mimo_x/z/o [H,R,P], norm_weight [H,P]; R = 1 for SISO), the
+// `SsmConfig` field docs, and the dataflow of the backward "prepare" and
+// "state" kernels, which recompute c_rot/b_rot (per head), theta [BH,L,A], qk,
+// decay, gamma and scale, and read the previous state, decay and gamma to form
+// the output.
+//
+// Per (b, h), with h_0 = 0, previous key/value 0, theta_{-1} = 0:
+//   theta_t[a] = theta_{t-1}[a] + dt_t * angle_t[a]      (READING: linear cumsum;
+//               "cumulative angle" is the step state)
+//   q_{t,r} = Rot(theta_t)(C_t[row(g,r)] + c_bias[h,r]),
+//   k_{t,r} = Rot(theta_t)(B_t[row(g,r)] + b_bias[h,r])    (bias before rotation)
+//   x_{t,r} = x_t * mimo_x[h,r]   (SISO: x_t)
+//   h_t = decay_t * h_{t-1} + scale_t * decay_t * sum_r x_{t-1,r} k_{t-1,r}^T
+//                            + gamma_t * sum_r x_{t,r} k_{t,r}^T
+//        READING: exponential-trapezoidal update; the previous-token term
+//        carries the current decay.
+//   y_{t,r} = h_t q_{t,r} + D[h] x_{t,r}                   (READING: D before gate)
+//   SISO: out_t = y_t * silu(z_t)
+//   MIMO: o_t = sum_r mimo_o[h,r] * y_{t,r} * silu(z_t * mimo_z[h,r])
+//         then, if has_output_norm, o_t / sqrt(mean_p o_t^2 + 1e-5) * norm_weight[h]
+//         (READING: per-rank gate, then the mimo_o contraction, then the norm;
+//         epsilon 1.0e-5 is the push constant of the MIMO dispatch).
+// Head h reads group g = h / (H / G) (READING: contiguous heads per group);
+// num_groups == 0 means G = H ("A zero num_groups means one Q/K group per head").
+// B/C row of (g, r) is g * R + r (READING: "Number of B/C rows per group").
+//
+// Optional recurrent state (all may be null, then zero in / not written):
+//   ssm [B,H,P,N], angle_state [B,H,A], k_state [B,H,R,N], v_state [B,H,R,P],
+// the `mamba3_siso_step` / `mamba3_mimo_step` state layouts. k_state holds the
+// rotated, biased key of the last token, v_state its (rank-scaled) value.
+// When state_in_out is nonzero the states are read first and written back.
+// Returns 0, or 1 for an invalid geometry.
+int m3o_scan(i64 B, i64 L, i64 H, i64 num_groups, i64 P, i64 N, i64 A, i64 R, int has_z,
+             int has_d, int has_norm, const float* c, const float* b, const float* x,
+             const float* z, const float* adt, const float* dt, const float* trap,
+             const float* angle, const float* c_bias, const float* b_bias, const float* d,
+             const float* mimo_x, const float* mimo_z, const float* mimo_o,
+             const float* norm_weight, double* out, double* ssm, double* angle_state,
+             double* k_state, double* v_state, int threads) {
+  const i64 G = num_groups == 0 ? H : num_groups;
+  if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || H % G != 0 || P <= 0 || N <= 0 || A < 0 ||
+      2 * A > N || R <= 0)
+    return 1;
+  const i64 heads_per_group = H / G;
+  const i64 RG = R * G;
+  parallel_for(B * H, threads, [&](i64 bh_idx) {
+    const i64 bb = bh_idx / H, h = bh_idx % H, g = h / heads_per_group;
+    std::vector<double> state(P * N, 0.0), theta(A, 0.0);
+    std::vector<double> k_prev(R * N, 0.0), v_prev(R * P, 0.0);
+    if (ssm) {
+      for (i64 i = 0; i < P * N; ++i) state[i] = ssm[bh_idx * P * N + i];
+      for (i64 a = 0; a < A; ++a) theta[a] = angle_state[bh_idx * A + a];
+      for (i64 i = 0; i < R * N; ++i) k_prev[i] = k_state[bh_idx * R * N + i];
+      for (i64 i = 0; i < R * P; ++i) v_prev[i] = v_state[bh_idx * R * P + i];
+    }
+    std::vector<double> q(R * N), k(R * N), v(R * P), tmp(N), y(R * P), o(P);
+    for (i64 t = 0; t < L; ++t) {
+      const i64 tok = bb * L + t;           // [B, L] index
+      const i64 sc = tok * H + h;           // [B, L, H] index
+      const TokenCoef cf = coef(adt[sc], dt[sc], trap[sc]);
+      for (i64 a = 0; a < A; ++a) theta[a] += (double)dt[sc] * (double)angle[tok * A + a];
+      for (i64 r = 0; r < R; ++r) {
+        const i64 row = tok * RG + g * R + r;
+        for (i64 n = 0; n < N; ++n) tmp[n] = (double)c[row * N + n] + (double)c_bias[(h * R + r) * N + n];
+        rotate(tmp, theta, A);
+        for (i64 n = 0; n < N; ++n) q[r * N + n] = tmp[n];
+        for (i64 n = 0; n < N; ++n) tmp[n] = (double)b[row * N + n] + (double)b_bias[(h * R + r) * N + n];
+        rotate(tmp, theta, A);
+        for (i64 n = 0; n < N; ++n) k[r * N + n] = tmp[n];
+        for (i64 p = 0; p < P; ++p) {
+          double xv = (double)x[sc * P + p];
+          v[r * P + p] = mimo_x ? xv * (double)mimo_x[(h * R + r) * P + p] : xv;
+        }
+      }
+      for (i64 p = 0; p < P; ++p) {
+        for (i64 n = 0; n < N; ++n) {
+          double prev_term = 0.0, cur_term = 0.0;
+          for (i64 r = 0; r < R; ++r) {
+            prev_term += v_prev[r * P + p] * k_prev[r * N + n];
+            cur_term += v[r * P + p] * k[r * N + n];
+          }
+          double& hs = state[p * N + n];
+          hs = cf.decay * hs + cf.scale * cf.decay * prev_term + cf.gamma * cur_term;
+        }
+      }
+      for (i64 r = 0; r < R; ++r) {
+        for (i64 p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (i64 n = 0; n < N; ++n) acc += state[p * N + n] * q[r * N + n];
+          if (has_d) acc += (double)d[h] * v[r * P + p];
+          y[r * P + p] = acc;
+        }
+      }
+      if (!mimo_o) {
+        // SISO readout and gate.
+        for (i64 p = 0; p < P; ++p) {
+          double val = y[p];
+          if (has_z) val *= silu((double)z[sc * P + p]);
+          out[sc * P + p] = val;
+        }
+      } else {
+        for (i64 p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (i64 r = 0; r < R; ++r) {
+            double val = y[r * P + p];
+            if (has_z) val *= silu((double)z[sc * P + p] * (double)mimo_z[(h * R + r) * P + p]);
+            acc += (double)mimo_o[(h * R + r) * P + p] * val;
+          }
+          o[p] = acc;
+        }
+        if (has_norm) {
+          double ms = 0.0;
+          for (i64 p = 0; p < P; ++p) ms += o[p] * o[p];
+          ms /= (double)P;
+          double inv = 1.0 / std::sqrt(ms + 1.0e-5);
+          for (i64 p = 0; p < P; ++p) o[p] = o[p] * inv * (double)norm_weight[h * P + p];
+        }
+        for (i64 p = 0; p < P; ++p) out[sc * P + p] = o[p];
+      }
+      k_prev = k;
+      v_prev = v;
+    }
+    if (ssm) {
+      for (i64 i = 0; i < P * N; ++i) ssm[bh_idx * P * N + i] = state[i];
+      for (i64 a = 0; a < A; ++a) angle_state[bh_idx * A + a] = theta[a];
+      for (i64 i = 0; i < R * N; ++i) k_state[bh_idx * R * N + i] = k_prev[i];
+      for (i64 i = 0; i < R * P; ++i) v_state[bh_idx * R * P + i] = v_prev[i];
+    }
+  });
+  return 0;
+}
+
+}  // extern "C"
