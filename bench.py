@@ -1,0 +1,465 @@
+"""Benchmark of the Mamba-3 hot path on GB300.
+
+One step = m3_preprocess of the packed projection of a SISO 1B-layer batch
+(B=8, L=2048, H=32, P=64, N=128, A=32, G=1; rows 16384 x width 4480) followed
+by m3_siso_forward over the 16384 tokens it produces, both through the C ABI
+with device-resident inputs. The metric is tokens/s (B*L per step, summed over
+ranks). The JSON line also carries the roofline of the dominant kernel, the
+CPU oracle baseline, an end-to-end figure with host buffers, sampled clocks,
+and supplementary timings of the MIMO and decode-step entry points.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
+                [--mode fp32|tf32] [--no-parts]
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas, weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_mamba3_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "Mamba-3 scan tokens/s at 1 GB300 (fwd) and % of roofline; step tokens/s"
+UNIT = "tokens/s"
+W_MAIN = gen.SISO_1B
+
+
+def bytes_per_token_scan(w):
+    """Algorithmic HBM bytes of one token of a scan: x, z, out [H,P]; B, C rows
+    [R*G, N]; adt, dt, trap [H]; angle [A] (float32, each read or written once)."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    return 4 * (3 * w.num_heads * w.head_dim + 2 * w.mimo_rank * G * w.state_size +
+                3 * w.num_heads + w.num_rope_angles)
+
+
+def bytes_per_row_preprocess(w):
+    """Algorithmic bytes of one preprocess row: the packed row read once and
+    the same number of floats written (x, z, bh, ch, dt, adt, trap, angle)."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    width = gen.packed_width(w.num_heads * w.head_dim, w.state_size, w.num_heads,
+                             w.num_rope_angles, G, w.mimo_rank)
+    return 4 * 2 * width
+
+
+def bytes_per_step_call(w):
+    """Algorithmic bytes of one decode-step call: ssm state read + written,
+    k/v/angle states read + written, per-token operands read, out written."""
+    B, H, P, N, A = w.batch_size, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    G = H if w.num_groups == 0 else w.num_groups
+    R = w.mimo_rank
+    state = 2 * B * H * (P * N + R * N + R * P + A)
+    tok = B * (3 * H * P + 2 * R * G * N + 3 * H + A)
+    return 4 * (state + tok)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def read_traffic(kernel):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary
+    (profiles/traffic.txt: `<kernel> <source sha1> <bytes per launch> <workload>`),
+    or None when absent or when the kernel's source has changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
+            src = os.path.join(ROOT, "selective_state_space_mamba3_gb300", "csrc", parts[0] + ".cu")
+            if not os.path.exists(src):
+                return None
+            sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+            return float(parts[2]) if sha == parts[1] else None
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------- m3 arm
+
+class Step:
+    """Device buffers and the two calls of one step (preprocess + SISO scan)."""
+
+    def __init__(self, w, mode):
+        import torch
+        import selective_state_space_mamba3_gb300 as m3
+        self.m3, self.torch, self.w = m3, torch, w
+        B, L, H, P, N, A = w.batch_size, w.sequence_length, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+        G = H if w.num_groups == 0 else w.num_groups
+        self.rows = B * L
+        proj = gen.layer_projection(w)
+        par = gen.scan_params(w)
+        self.h_proj = torch.from_numpy(proj["projected"]).pin_memory()
+        self.proj = self.h_proj.cuda()
+        self.dt_bias = torch.from_numpy(proj["dt_bias"]).cuda()
+        self.pcfg = m3.preprocess_config(inner_size=H * P, state_size=N, num_heads=H,
+                                         num_rope_angles=A, num_groups=G, mimo_rank=1,
+                                         **gen.PRE_DEFAULT)
+        e = lambda *s: torch.empty(*s, device="cuda")
+        self.x, self.z = e(B, L, H, P), e(B, L, H, P)
+        self.bh, self.ch = e(B, L, G, N), e(B, L, G, N)
+        self.dt, self.adt, self.trap = e(B, L, H), e(B, L, H), e(B, L, H)
+        self.angle = e(B, L, A)
+        self.out = e(B, L, H, P)
+        self.h_out = torch.empty(B, L, H, P).pin_memory()
+        self.cb, self.bb, self.d = (torch.from_numpy(par[k]).cuda() for k in ("c_bias", "b_bias", "d"))
+        self.scfg = m3.ssm_config(w.cfg(), mode)
+        wsb = m3.m3_siso_forward_workspace(self.scfg)
+        self.ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+
+    def preprocess(self):
+        self.m3.m3_preprocess(self.pcfg, self.rows, self.proj, self.dt_bias, self.x, self.z,
+                              self.bh, self.ch, self.dt, self.adt, self.trap, self.angle)
+
+    def scan(self):
+        self.m3.m3_siso_forward(self.scfg, self.ch, self.bh, self.x, self.z, self.adt, self.dt,
+                                self.trap, self.angle, self.cb, self.bb, self.d, self.out, self.ws)
+
+
+def time_events(torch, fn, reps):
+    """Average device time (ms) of fn() over reps launches, CUDA events on the
+    current stream."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(reps):
+        fn()
+    ev[1].record()
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[1]) / reps
+
+
+def parts_mimo(torch, m3, mode, peak):
+    """Supplementary: MIMO R4 forward at B4 L4096 H32 P64 N64 (device inputs)."""
+    w = gen.MIMO_R4
+    ins = gen.scan_inputs(w)
+    d = {k: torch.from_numpy(v).cuda() for k, v in ins.items()}
+    del ins
+    cfg = m3.ssm_config(w.cfg(), mode)
+    ws = torch.empty(max(m3.m3_mimo_forward_workspace(cfg), 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(d["x"])
+    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d",
+            "mimo_x", "mimo_z", "mimo_o", "norm_weight")
+    fn = lambda: m3.m3_mimo_forward(cfg, *[d[k] for k in keys], out, ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 10)
+    gbs = w.tokens * bytes_per_token_scan(w) / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "ms": round(ms, 4), "tokens_per_s": round(w.tokens / (ms * 1e-3)),
+            "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
+
+
+def parts_step(torch, m3, peak):
+    """Supplementary: decode step at B256 H32 P64 N128 A32, 512 single-token
+    calls cycling over 32 distinct token inputs, states resident on the device."""
+    w = gen.DECODE_STEP
+    ins = gen.decode_inputs(w, steps=32)
+    seq = {k: torch.from_numpy(ins[k]).cuda() for k in ("c", "b", "x", "z", "adt", "dt", "trap", "angle")}
+    toks = [[seq[k][:, t:t + 1].contiguous() for k in ("c", "b", "x", "z", "adt", "dt", "trap", "angle")]
+            for t in range(32)]
+    par = [torch.from_numpy(ins[k]).cuda() for k in ("c_bias", "b_bias", "d")]
+    B, H, P, N, A = w.batch_size, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    st = [torch.zeros(s, device="cuda") for s in ((B, H, P, N), (B, H, A), (B, H, N), (B, H, P))]
+    out = torch.empty(B, 1, H, P, device="cuda")
+    cfg = m3.ssm_config(w.cfg(sequence_length=1))
+    i = [0]
+
+    def fn():
+        m3.m3_siso_step(cfg, *toks[i[0] % 32], *par, *st, out)
+        i[0] += 1
+    for _ in range(5):
+        fn()
+    ms = time_events(torch, fn, w.steps)
+    gbs = bytes_per_step_call(w) / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "ms_per_call": round(ms, 4),
+            "tokens_per_s": round(B / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4)}
+
+
+def cpu_baseline_oracle(w, batch_rows):
+    """The CPU oracle (as it stands) on a bounded sample of the workload: the
+    first `batch_rows` batch rows, preprocess + SISO scan, all host threads."""
+    import oracle
+    oracle.build()
+    H, P, N, A = w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    G = H if w.num_groups == 0 else w.num_groups
+    L = w.sequence_length
+    proj = gen.layer_projection(w)
+    par = gen.scan_params(w)
+    rows = batch_rows * L
+    kw = dict(inner_size=H * P, state_size=N, num_heads=H, num_rope_angles=A, num_groups=G,
+              mimo_rank=1, **gen.PRE_DEFAULT)
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    pre = oracle.preprocess(proj["projected"][:rows], proj["dt_bias"], **kw)
+    f = lambda k, *s: pre[k].astype(np.float32).reshape(batch_rows, L, *s)
+    oracle.scan(w.cfg(batch_size=batch_rows), f("ch", G, N), f("bh", G, N), f("x", H, P),
+                f("z", H, P), f("adt", H), f("dt", H), f("trap", H), f("angle", A),
+                par["c_bias"], par["b_bias"], par["d"])
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"batch rows 0..{batch_rows - 1} of {w.batch_size} ({rows} of {w.tokens} "
+                      f"tokens), preprocess + SISO scan, FP64, {threads} threads, {dt:.2f} s",
+            "seconds": round(dt, 3)}
+
+
+def run_m3(args):
+    import torch
+    import selective_state_space_mamba3_gb300 as m3
+    from selective_state_space_mamba3_gb300 import build as m3build
+    world, rank, local = dist_setup(args)
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    m3build.build()
+    m3.load_library()
+    mode = m3.M3_MATH_TF32 if args.mode == "tf32" else m3.M3_MATH_FP32
+    peak, peak_kind = load_peaks()
+    w = W_MAIN
+    s = Step(w, mode)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        s.preprocess()
+        s.scan()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = m3.launch_count()
+    t_start.record()
+    for k in range(K):
+        ev[k][0].record()
+        s.preprocess()
+        ev[k][1].record()
+        s.scan()
+        ev[k][2].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    launches = m3.launch_count() - n0
+    barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    pre_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    scan_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    assert m3.m3_workspace_status(s.ws) == m3.M3_OK
+    tokens = w.tokens
+    value = world * tokens * K / (total_ms * 1e-3)
+
+    # roofline of the dominant kernel (algorithmic bytes / live event time)
+    scan_bytes = tokens * bytes_per_token_scan(w)
+    pre_bytes = s.rows * bytes_per_row_preprocess(w)
+    if scan_ms >= pre_ms:
+        kname, kms, kbytes = "k_scan", scan_ms, scan_bytes
+    else:
+        kname, kms, kbytes = "k_preprocess", pre_ms, pre_bytes
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "algorithmic_bytes": kbytes, "ms": round(kms, 4),
+            "traffic": read_traffic("k_scan_seq" if kname == "k_scan" else kname)}
+
+    # end to end through the public API with host buffers (pinned), rank-local
+    for _ in range(2):
+        s.proj.copy_(s.h_proj, non_blocking=True)
+        s.preprocess()
+        s.scan()
+        s.h_out.copy_(s.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    KE = max(3, min(K, 10))
+    e0.record()
+    for _ in range(KE):
+        s.proj.copy_(s.h_proj, non_blocking=True)
+        s.preprocess()
+        s.scan()
+        s.h_out.copy_(s.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / KE
+    e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
+           "h2d_bytes_per_step": s.h_proj.numel() * 4, "d2h_bytes_per_step": s.h_out.numel() * 4,
+           "ms_per_step": round(e2e_ms, 4)}
+
+    parts = {"preprocess": {"ms": round(pre_ms, 4), "hbm_gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+                            "frac_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / peak, 4),
+                            "algorithmic_bytes": pre_bytes},
+             "siso_scan": {"ms": round(scan_ms, 4), "tokens_per_s": round(tokens / (scan_ms * 1e-3)),
+                           "hbm_gbs": round(scan_bytes / (scan_ms * 1e-3) / 1e9, 1),
+                           "frac_hbm": round(scan_bytes / (scan_ms * 1e-3) / 1e9 / peak, 4),
+                           "algorithmic_bytes": scan_bytes}}
+    del s
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_parts:
+        parts["mimo_scan"] = parts_mimo(torch, m3, mode, peak)
+        torch.cuda.empty_cache()
+        parts["siso_step"] = parts_step(torch, m3, peak)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline_oracle(w, args.cpu_rows)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+                "steps": K, "warmup": args.warmup, "ms_per_step": round(total_ms / K, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "tf32" if mode == m3.M3_MATH_TF32 else "f32", "data": "synthetic",
+                "config": {"workload": w.name, "batch": w.batch_size, "seq_len": w.sequence_length,
+                           "heads": w.num_heads, "head_dim": w.head_dim, "state_size": w.state_size,
+                           "groups": w.num_groups, "rope_angles": w.num_rope_angles,
+                           "step": "m3_preprocess (16384 x 4480 packed rows) + m3_siso_forward",
+                           "math_mode": args.mode, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (293.6 MB packed projection read per step)"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+                "clocks": clk, "parts": parts}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# -------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as it stands, on the host cores, on the same workload's
+    configuration: each step is a bounded sample (one batch row: preprocess of
+    its 2048 packed rows + the SISO scan over them)."""
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    w = W_MAIN
+    for _ in range(args.warmup):
+        cpu_baseline_oracle(w, 1)
+    times = []
+    for _ in range(args.steps):
+        r = cpu_baseline_oracle(w, 1)
+        times.append(r["seconds"])
+    tot = float(np.sum(times))
+    tokens = w.sequence_length * args.steps
+    value = tokens / tot
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * tot / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch_size, "seq_len": w.sequence_length,
+                       "heads": w.num_heads, "head_dim": w.head_dim, "state_size": w.state_size,
+                       "groups": w.num_groups, "rope_angles": w.num_rope_angles,
+                       "step": "oracle preprocess + SISO scan of one batch row (2048 tokens)"},
+            "cpu_baseline": {"kind": "oracle", "cores": r["cores"], "sample": r["sample"],
+                             "value": round(value, 1), "unit": UNIT},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="m3", choices=["m3", "reference"])
+    ap.add_argument("--mode", default="fp32", choices=["fp32", "tf32"])
+    ap.add_argument("--no-parts", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=4)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "m3":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_m3(args)
+
+
+if __name__ == "__main__":
+    main()

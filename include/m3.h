@@ -1,0 +1,189 @@
+/*
+ * m3.h - C ABI of the GB300 (sm_103a) Mamba-3 selective-state scan library.
+ *
+ * Operations follow oarust 0.8.6 `src/rs/ml/matrix/mamba3.rs` (docs.rs source
+ * view) and the `oa::ml::matrix` API reference:
+ *   m3_preprocess     - `mamba3_preprocess`   (fused split + B/C RMS + dt/adt)
+ *   m3_siso_forward   - `mamba3_siso`         (SISO selective-state recurrence)
+ *   m3_mimo_forward   - `mamba3_mimo`         (shared-state MIMO recurrence)
+ *   m3_siso_step      - `mamba3_siso_step`    (one token, explicit state)
+ *   m3_mimo_step      - `mamba3_mimo_step`    (one MIMO token, explicit state)
+ *
+ * Conventions for every entry point:
+ *  - Every tensor is float32, dense row-major, in device memory owned by the
+ *    caller; the library allocates nothing and keeps no pointer after return.
+ *  - Every base pointer must be 16-byte aligned (M3_ERR_UNALIGNED otherwise).
+ *  - All checks run on the host before anything is enqueued. A rejected call
+ *    enqueues no work and leaves every output and state buffer untouched.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream). Calls return once the kernels are enqueued; they do not wait.
+ *  - Return value: an m3_status code; m3_status_string() describes it.
+ */
+#ifndef M3_H_
+#define M3_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. M3_ERR_INVALID_ARGUMENT mirrors the pages'
+ * `Error::invalid_argument` results of the geometry checks. */
+enum m3_status {
+  M3_OK = 0,
+  M3_ERR_INVALID_ARGUMENT = 1, /* geometry, limits, null pointer, overflow */
+  M3_ERR_UNALIGNED = 2,        /* a base pointer is not 16-byte aligned */
+  M3_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+  M3_ERR_CUDA = 4,             /* a CUDA launch or runtime call failed */
+  M3_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up */
+};
+
+/* Arithmetic of the scans' dense contractions (an extension of SsmConfig). */
+enum m3_math_mode {
+  M3_MATH_FP32 = 0, /* FP32-exact: FP32 FFMA or 3-pass split-TF32 tensor MMA */
+  M3_MATH_TF32 = 1  /* single-pass TF32 tensor MMA, FP32 accumulate */
+};
+
+typedef struct CUstream_st* m3_stream_t; /* same type as cudaStream_t */
+
+/* `Mamba3PreprocessConfig` (mamba3.rs): inner_size I, state_size N,
+ * num_heads H, num_rope_angles A, num_groups G (> 0 here: no zero rule),
+ * mimo_rank R (B/C rows per group), epsilon of the B/C RMS normalisation,
+ * inclusive dt bounds [dt_min, dt_max], a_floor = positive floor of |A|. */
+typedef struct {
+  int64_t inner_size;
+  int64_t state_size;
+  int64_t num_heads;
+  int64_t num_rope_angles;
+  int64_t num_groups;
+  int64_t mimo_rank;
+  float epsilon;
+  float dt_min;
+  float dt_max;
+  float a_floor;
+} m3_preprocess_config;
+
+/* `SsmConfig` (mamba3.rs): B, L, H, num_groups (0 means H), P = head_dim,
+ * N = state_size, A = num_rope_angles, R = mimo_rank, and the three optional
+ * paths. math_mode is an m3_math_mode (extension; 0 is FP32-exact). */
+typedef struct {
+  int64_t batch_size;
+  int64_t sequence_length;
+  int64_t num_heads;
+  int64_t num_groups;
+  int64_t head_dim;
+  int64_t state_size;
+  int64_t num_rope_angles;
+  int64_t mimo_rank;
+  int32_t has_z;
+  int32_t has_d;
+  int32_t has_output_norm;
+  int32_t math_mode;
+} m3_ssm_config;
+
+/*
+ * m3_preprocess - split and transform one packed Mamba-3 input projection
+ * (`mamba3_preprocess`, `PreprocessGeometry::resolve`).
+ *
+ * projected [rows, W], W = 2I + 2GRN + 3H + A, columns in the order
+ *   z | x | B rows (G*R rows of N) | C rows | dt_raw [H] | a_raw [H] | trap [H] | angle [A];
+ * dt_bias [H]. Outputs: x, z [rows, I]; bh, ch [rows, G*R*N] (each N-row divided
+ * by sqrt(mean square + epsilon)); dt, adt, trap [rows, H]; angle [rows, A]:
+ *   dt  = clamp(softplus(dt_raw + dt_bias[h]), dt_min, dt_max)
+ *   adt = -max(softplus(a_raw), a_floor) * dt;   trap, angle copied.
+ * Checks: rows, I, N, H, G, R > 0; 2A <= N; epsilon, dt_min, dt_max, a_floor
+ * finite; epsilon, dt_min, a_floor > 0; dt_min <= dt_max; W and every output
+ * element count below 2^32. `angle` may be NULL when A == 0.
+ */
+int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
+                  const float* dt_bias, float* x, float* z, float* bh, float* ch, float* dt,
+                  float* adt, float* trap, float* angle, m3_stream_t stream);
+
+/*
+ * m3_siso_forward - the Mamba-3 SISO selective-state recurrence over a whole
+ * sequence from a zero state (`mamba3_siso`, `Geometry::resolve`).
+ *
+ * Operands: c, b [B,L,G,N]; x, z [B,L,H,P]; adt, dt, trap [B,L,H]; angle
+ * [B,L,A] (may be NULL when A == 0); c_bias, b_bias [H,N]; d [H]. Output
+ * out [B,L,H,P]. Checks: B,L,H,G,P,N > 0, H % G == 0, P <= 128, N <= 128,
+ * A <= 64, 2A <= N, mimo_rank == 1, has_output_norm == 0, every element count
+ * below 2^32. z and d are read only when has_z / has_d are set but must be
+ * valid pointers regardless, as in the pages' shape checks.
+ * workspace: device scratch of at least m3_siso_forward_workspace() bytes,
+ * 16-byte aligned, used only during the call's kernels (may be NULL when that
+ * size is 0). Calls that share a workspace must not overlap on the GPU.
+ */
+int m3_siso_forward_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, float* out, void* workspace, size_t workspace_bytes,
+                    m3_stream_t stream);
+
+/*
+ * m3_mimo_forward - the shared-state Mamba-3 MIMO recurrence (`mamba3_mimo`,
+ * `MimoGeometry::resolve`).
+ *
+ * Operands as m3_siso_forward except c, b [B,L,R*G,N] (row g*R + r is rank r
+ * of group g) and c_bias, b_bias [H,R,N]; plus mimo_x, mimo_z, mimo_o [H,R,P]
+ * and norm_weight [H,P] (read only when has_output_norm; always required).
+ * Output RMS norm epsilon is 1.0e-5. Checks: as SISO but 1 <= R <= 8 and
+ * P*N <= 4096; has_output_norm allowed.
+ */
+int m3_mimo_forward_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, const float* mimo_x, const float* mimo_z,
+                    const float* mimo_o, const float* norm_weight, float* out,
+                    void* workspace, size_t workspace_bytes, m3_stream_t stream);
+
+/*
+ * m3_siso_step - advance one SISO token and update four recurrent states in
+ * place (`mamba3_siso_step`). cfg->sequence_length must be 1; operands are the
+ * length-one forms of m3_siso_forward. States (read, then overwritten):
+ *   ssm_state [B,H,P,N], angle_state [B,H,A] (cumulative angle; may be NULL
+ *   when A == 0), k_state [B,H,N] (rotated, biased key of the last token),
+ *   v_state [B,H,P] (value of the last token).
+ * A zero state equals the start of a sequence. A rejected call leaves the
+ * states untouched ("mutated only after the complete operation has been
+ * validated"). Output out [B,1,H,P].
+ */
+int m3_siso_step(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                 const float* z, const float* adt, const float* dt, const float* trap,
+                 const float* angle, const float* c_bias, const float* b_bias, const float* d,
+                 float* ssm_state, float* angle_state, float* k_state, float* v_state,
+                 float* out, m3_stream_t stream);
+
+/*
+ * m3_mimo_step - advance one MIMO token (`mamba3_mimo_step`). Operands as
+ * m3_mimo_forward with sequence_length == 1. States: ssm [B,H,P,N], angle
+ * [B,H,A], k_state [B,H,R,N], v_state [B,H,R,P] (rank-scaled values).
+ */
+int m3_mimo_step(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                 const float* z, const float* adt, const float* dt, const float* trap,
+                 const float* angle, const float* c_bias, const float* b_bias, const float* d,
+                 const float* mimo_x, const float* mimo_z, const float* mimo_o,
+                 const float* norm_weight, float* ssm_state, float* angle_state,
+                 float* k_state, float* v_state, float* out, m3_stream_t stream);
+
+/*
+ * m3_workspace_status - waits for `stream`, then reads the device status word
+ * that the scans' bounded waits write into `workspace`: M3_OK, or
+ * M3_ERR_TIMEOUT if a wait gave up during the last call that used it.
+ */
+int m3_workspace_status(const void* workspace, size_t workspace_bytes, m3_stream_t stream);
+
+/* Human-readable description of a status code (static string). */
+const char* m3_status_string(int status);
+
+/* Number of kernels this library has enqueued since it was loaded. */
+uint64_t m3_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3_H_ */

@@ -1,0 +1,15 @@
+"""GB300 (sm_103a) Mamba-3 selective-state scan.
+
+The product is the C-ABI library `libm3.so` (declared in include/m3.h):
+m3_preprocess, m3_siso_forward, m3_mimo_forward, m3_siso_step, m3_mimo_step.
+This package holds its CUDA sources (`csrc/`), the in-tree build (`build.py`),
+a ctypes binding with the same entry-point names (`_binding.py`) and the
+seeded synthetic input generators (`inputs.py`).
+"""
+from ._binding import (  # noqa: F401
+    M3_OK, M3_ERR_INVALID_ARGUMENT, M3_ERR_UNALIGNED, M3_ERR_WORKSPACE, M3_ERR_CUDA,
+    M3_ERR_TIMEOUT, M3_MATH_FP32, M3_MATH_TF32, EXPORTED, M3Error, PreprocessConfig, SsmConfig,
+    ssm_config, preprocess_config, load_library, status_string, launch_count, m3_preprocess,
+    m3_siso_forward_workspace, m3_siso_forward, m3_mimo_forward_workspace, m3_mimo_forward,
+    m3_siso_step, m3_mimo_step, m3_workspace_status, LIB_PATH)
+from . import inputs  # noqa: F401

@@ -1,0 +1,105 @@
+// Fused Mamba-3 projection preprocess (oarust mamba3.rs, `mamba3_preprocess`:
+// one packed projection row -> z, x, RMS-normalised B/C rows, clamped dt,
+// adt = -max(softplus(a_raw), a_floor) * dt, raw trap and angle).
+//
+// HBM-bound streaming: every byte of `projected` is read once and every output
+// byte written once. One 256-thread block handles one row at a time
+// (grid-stride over rows): the z|x slices move as 128-bit streaming loads and
+// stores, each B/C row is owned by one warp whose lanes hold one float4 each
+// (N <= 128) and reduce the mean square with shuffles, and the 3H + A scalar
+// columns are mapped by the first threads. Rows whose width or slice offsets
+// are not multiples of 4 floats take the scalar path of the same kernel.
+#include "m3_internal.cuh"
+
+namespace m3 {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <bool VEC>
+__global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float* __restrict__ proj,
+                                                         const float* __restrict__ dt_bias,
+                                                         PreOut o) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nwarps = kThreads / 32;
+  const int I = g.I, N = g.N, H = g.H, A = g.A, W = g.W;
+  const int RG = g.G * g.R;
+  const int BC = RG * N;
+  for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
+    const float* p = proj + r * (int64_t)W;
+    // z | x slices (columns [0, 2I)).
+    if (VEC) {
+      const float4* p4 = reinterpret_cast<const float4*>(p);
+      const int I4 = I >> 2;
+      float4* z4 = reinterpret_cast<float4*>(o.z + r * (int64_t)I);
+      float4* x4 = reinterpret_cast<float4*>(o.x + r * (int64_t)I);
+      for (int i = tid; i < 2 * I4; i += kThreads) {
+        float4 v = __ldcs(p4 + i);
+        if (i < I4)
+          __stcs(z4 + i, v);
+        else
+          __stcs(x4 + (i - I4), v);
+      }
+    } else {
+      for (int i = tid; i < 2 * I; i += kThreads) {
+        float v = __ldcs(p + i);
+        if (i < I)
+          __stcs(o.z + r * (int64_t)I + i, v);
+        else
+          __stcs(o.x + r * (int64_t)I + (i - I), v);
+      }
+    }
+    // B rows then C rows (columns [2I, 2I + 2BC)), one warp per N-row.
+    for (int j = warp; j < 2 * RG; j += nwarps) {
+      const float* src = p + 2 * I + (int64_t)j * N;
+      float* dst = (j < RG ? o.bh + r * (int64_t)BC + (int64_t)j * N
+                           : o.ch + r * (int64_t)BC + (int64_t)(j - RG) * N);
+      if (VEC && N <= 128) {
+        const int N4 = N >> 2;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < N4) v = __ldcs(reinterpret_cast<const float4*>(src) + lane);
+        float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+        const float inv = 1.0f / sqrtf(ss / (float)N + g.eps);
+        if (lane < N4)
+          __stcs(reinterpret_cast<float4*>(dst) + lane,
+                 make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv));
+      } else {
+        float ss = 0.f;
+        for (int n = lane; n < N; n += 32) {
+          float v = src[n];
+          ss += v * v;
+        }
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)N + g.eps);
+        for (int n = lane; n < N; n += 32) __stcs(dst + n, src[n] * inv);
+      }
+    }
+    // dt_raw | a_raw | trap (H each) | angle (A).
+    const float* s = p + 2 * I + 2 * BC;
+    for (int h = tid; h < H; h += kThreads) {
+      float d = softplus_f(__ldcs(s + h) + __ldg(dt_bias + h));
+      d = fminf(fmaxf(d, g.dt_min), g.dt_max);
+      const float a_mag = fmaxf(softplus_f(__ldcs(s + H + h)), g.a_floor);
+      __stcs(o.dt + r * (int64_t)H + h, d);
+      __stcs(o.adt + r * (int64_t)H + h, -a_mag * d);
+      __stcs(o.trap + r * (int64_t)H + h, __ldcs(s + 2 * H + h));
+    }
+    for (int a = tid; a < A; a += kThreads) __stcs(o.angle + r * (int64_t)A + a, __ldcs(s + 3 * H + a));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const float* dt_bias,
+                              const PreOut& o, cudaStream_t s) {
+  const bool vec = (g.W % 4 == 0) && (g.I % 4 == 0) && (g.N % 4 == 0);
+  const int64_t blocks = g.rows < (int64_t)(1 << 20) ? g.rows : (int64_t)(1 << 20);
+  if (vec)
+    k_preprocess<true><<<(unsigned)blocks, kThreads, 0, s>>>(g, projected, dt_bias, o);
+  else
+    k_preprocess<false><<<(unsigned)blocks, kThreads, 0, s>>>(g, projected, dt_bias, o);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace m3

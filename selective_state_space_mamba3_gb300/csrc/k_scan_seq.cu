@@ -1,0 +1,290 @@
+// Token-sequential Mamba-3 scan on the CUDA cores, FP32 throughout (oarust
+// mamba3.rs, `mamba3_siso` / `mamba3_mimo`: the recurrence run token by token).
+//
+// The rows p of the [P, N] state evolve independently given the per-token
+// q, k, decay and trapezoid weights, so a block owns one (b, h) and a tile of
+// PT state rows; four lanes share a row, each holding 4 * NPT4 state values in
+// registers (float4-interleaved so that shared-memory reads are conflict-free).
+// Per tile of kT tokens the block stages the coefficients, the cumulative
+// rotary angle, the rotated q/k rows and x/z in shared memory, runs the
+// recurrence over the tile, then writes the gated outputs coalesced. MIMO
+// blocks own all P rows so that the output RMS norm is block-local.
+//
+// This is the FP32 reference path of the library and the fallback for shapes
+// outside the tensor-core chunked kernels.
+#include "m3_internal.cuh"
+
+namespace m3 {
+namespace {
+
+constexpr int kT = 16;  // tokens per staging tile
+
+struct SeqLayout {
+  int Npad, PT, R, A;
+  size_t q, k, coef, theta, xs, zs, ys, os, bytes;
+};
+
+__host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
+  SeqLayout l;
+  l.Npad = (N + 15) / 16 * 16;
+  l.PT = PT;
+  l.R = R;
+  l.A = A;
+  size_t off = 0;
+  auto take = [&](size_t floats) {
+    size_t o = off;
+    off += (floats + 3) / 4 * 4;  // keep 16-byte alignment
+    return o;
+  };
+  l.q = take((size_t)kT * R * l.Npad);
+  l.k = take((size_t)(kT + 1) * R * l.Npad);
+  l.coef = take((size_t)kT * 4);
+  l.theta = take((size_t)kT * (A > 0 ? A : 1));
+  l.xs = take((size_t)kT * PT);
+  l.zs = take((size_t)kT * PT);
+  l.ys = take((size_t)kT * R * PT);
+  l.os = take((size_t)kT * PT);
+  l.bytes = off * sizeof(float);
+  return l;
+}
+
+template <int NPT4, int RMAX>
+__global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay) {
+  extern __shared__ __align__(16) float sm[];
+  float* sq = sm + lay.q;
+  float* sk = sm + lay.k;
+  float* scoef = sm + lay.coef;
+  float* sth = sm + lay.theta;
+  float* sx = sm + lay.xs;
+  float* sz = sm + lay.zs;
+  float* sy = sm + lay.ys;
+  float* so = sm + lay.os;
+
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int P = g.P, N = g.N, A = g.A, R = g.R, L = g.L, H = g.H;
+  const int Npad = lay.Npad, PT = lay.PT;
+  const int ptiles = (P + PT - 1) / PT;
+  const int bh = blockIdx.x / ptiles;
+  const int p0 = (blockIdx.x % ptiles) * PT;
+  const int b = bh / H, h = bh % H;
+  const int grp = h / (H / g.G);
+  const int pi = tid >> 2, j = tid & 3;
+  const int p = p0 + pi;
+  const bool row_ok = (pi < PT) && (p < P);
+
+  float hst[NPT4 * 4];
+#pragma unroll
+  for (int i = 0; i < NPT4 * 4; ++i) hst[i] = 0.f;
+  float mx[RMAX], xprev[RMAX];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    mx[r] = (r < R && row_ok) ? (a.mimo_x ? a.mimo_x[((int64_t)h * R + r) * P + p] : 1.f) : 0.f;
+    xprev[r] = 0.f;
+  }
+  const float dskip = g.has_d ? a.d[h] : 0.f;
+  // previous-token key slot starts at zero; the running angle lives in sth[(kT-1)*A + a]
+  for (int i = tid; i < R * Npad; i += nthr) sk[i] = 0.f;
+  for (int i = tid; i < A; i += nthr) sth[(kT - 1) * A + i] = 0.f;
+  __syncthreads();
+
+  for (int t0 = 0; t0 < L; t0 += kT) {
+    const int tv = min(kT, L - t0);
+    // 1. per-token coefficients, cumulative angle, x/z tiles
+    for (int t = tid; t < tv; t += nthr) {
+      const int64_t sc = ((int64_t)b * L + t0 + t) * H + h;
+      const float dtv = a.dt[sc];
+      const float lam = sigmoid_f(a.trap[sc]);
+      const float dec = expf(a.adt[sc]);
+      scoef[t * 4 + 0] = dec;
+      scoef[t * 4 + 1] = lam * dtv;
+      scoef[t * 4 + 2] = (1.0f - lam) * dtv * dec;
+    }
+    for (int i = tid; i < A; i += nthr) {
+      float th = sth[(kT - 1) * A + i];  // running angle from the previous tile
+      for (int t = 0; t < tv; ++t) {
+        const int64_t tok = (int64_t)b * L + t0 + t;
+        th += a.dt[tok * H + h] * a.angle[tok * A + i];
+        sth[t * A + i] = th;
+      }
+      for (int t = tv; t < kT; ++t) sth[t * A + i] = th;
+    }
+    for (int i = tid; i < kT * PT; i += nthr) {
+      const int t = i / PT, pp = i % PT;
+      float xv = 0.f, zv = 0.f;
+      if (t < tv && p0 + pp < P) {
+        const int64_t off = (((int64_t)b * L + t0 + t) * H + h) * P + p0 + pp;
+        xv = a.x[off];
+        zv = a.z[off];
+      }
+      sx[i] = xv;
+      sz[i] = zv;
+    }
+    __syncthreads();
+    // 2. rotated q/k rows (zero-padded to Npad), k into slots 1..kT
+    for (int i = tid; i < kT * R * Npad; i += nthr) {
+      const int t = i / (R * Npad);
+      const int rem = i - t * R * Npad;
+      const int r = rem / Npad, n = rem - r * Npad;
+      float qv = 0.f, kv = 0.f;
+      if (t < tv && n < N) {
+        const int64_t tok = (int64_t)b * L + t0 + t;
+        const int64_t row = (tok * g.G * R + (int64_t)grp * R + r) * N;
+        const float* cb = a.c_bias + ((int64_t)h * R + r) * N;
+        const float* bb = a.b_bias + ((int64_t)h * R + r) * N;
+        if (n < 2 * A) {
+          const int pa = n < A ? n : n - A;
+          float sn, cs;
+          sincosf(sth[t * A + pa], &sn, &cs);
+          const float qu = a.c[row + pa] + cb[pa], qw = a.c[row + pa + A] + cb[pa + A];
+          const float ku = a.b[row + pa] + bb[pa], kw = a.b[row + pa + A] + bb[pa + A];
+          if (n < A) {
+            qv = qu * cs - qw * sn;
+            kv = ku * cs - kw * sn;
+          } else {
+            qv = qu * sn + qw * cs;
+            kv = ku * sn + kw * cs;
+          }
+        } else {
+          qv = a.c[row + n] + cb[n];
+          kv = a.b[row + n] + bb[n];
+        }
+      }
+      sq[i] = qv;
+      sk[R * Npad + i] = kv;
+    }
+    __syncthreads();
+    // 3. recurrence over the tile
+    for (int t = 0; t < tv; ++t) {
+      const float dec = scoef[t * 4 + 0], gam = scoef[t * 4 + 1], sdec = scoef[t * 4 + 2];
+      const float xv = row_ok ? sx[t * PT + pi] : 0.f;
+      float cp[RMAX], cc[RMAX], xr[RMAX], acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        xr[r] = xv * mx[r];
+        cp[r] = sdec * xprev[r];
+        cc[r] = gam * xr[r];
+        acc[r] = 0.f;
+      }
+      const float4* kp4 = reinterpret_cast<const float4*>(sk + (size_t)t * R * Npad);
+      const float4* kc4 = reinterpret_cast<const float4*>(sk + (size_t)(t + 1) * R * Npad);
+      const float4* q4 = reinterpret_cast<const float4*>(sq + (size_t)t * R * Npad);
+#pragma unroll
+      for (int i = 0; i < NPT4; ++i) {
+        const int n4 = j + 4 * i;
+        if (n4 * 4 < Npad) {
+          float ux = 0.f, uy = 0.f, uz = 0.f, uw = 0.f;
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) {
+            if (r < R) {
+              const float4 kp = kp4[r * (Npad / 4) + n4];
+              const float4 kc = kc4[r * (Npad / 4) + n4];
+              ux += cp[r] * kp.x + cc[r] * kc.x;
+              uy += cp[r] * kp.y + cc[r] * kc.y;
+              uz += cp[r] * kp.z + cc[r] * kc.z;
+              uw += cp[r] * kp.w + cc[r] * kc.w;
+            }
+          }
+          float* hh = hst + 4 * i;
+          hh[0] = dec * hh[0] + ux;
+          hh[1] = dec * hh[1] + uy;
+          hh[2] = dec * hh[2] + uz;
+          hh[3] = dec * hh[3] + uw;
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) {
+            if (r < R) {
+              const float4 qq = q4[r * (Npad / 4) + n4];
+              acc[r] += hh[0] * qq.x + hh[1] * qq.y + hh[2] * qq.z + hh[3] * qq.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 1);
+        acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
+        if (r < R && j == 0 && row_ok) sy[(t * R + r) * PT + pi] = acc[r] + dskip * xr[r];
+        xprev[r] = xr[r];
+      }
+    }
+    __syncthreads();
+    // 4. outputs
+    if (!a.mimo_o) {
+      for (int i = tid; i < tv * PT; i += nthr) {
+        const int t = i / PT, pp = i % PT;
+        if (p0 + pp < P) {
+          float yv = sy[t * PT + pp];
+          if (g.has_z) yv *= silu_f(sz[i]);
+          a.out[(((int64_t)b * L + t0 + t) * H + h) * P + p0 + pp] = yv;
+        }
+      }
+    } else {
+      // MIMO: PT == P
+      for (int i = tid; i < tv * P; i += nthr) {
+        const int t = i / P, pp = i % P;
+        float ov = 0.f;
+        for (int r = 0; r < R; ++r) {
+          float yv = sy[(t * R + r) * P + pp];
+          if (g.has_z) yv *= silu_f(sz[i] * a.mimo_z[((int64_t)h * R + r) * P + pp]);
+          ov += a.mimo_o[((int64_t)h * R + r) * P + pp] * yv;
+        }
+        so[i] = ov;
+      }
+      __syncthreads();
+      const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+      for (int t = warp; t < tv; t += nw) {
+        float inv = 1.f;
+        if (g.has_norm) {
+          float ss = 0.f;
+          for (int pp = lane; pp < P; pp += 32) ss += so[t * P + pp] * so[t * P + pp];
+          ss = warp_sum(ss);
+          inv = 1.0f / sqrtf(ss / (float)P + 1.0e-5f);
+        }
+        for (int pp = lane; pp < P; pp += 32) {
+          float ov = so[t * P + pp];
+          if (g.has_norm) ov = ov * inv * a.norm_weight[(int64_t)h * P + pp];
+          a.out[(((int64_t)b * L + t0 + t) * H + h) * P + pp] = ov;
+        }
+      }
+    }
+    // carry the last token's key into slot 0
+    for (int i = tid; i < R * Npad; i += nthr) sk[i] = sk[(size_t)tv * R * Npad + i];
+    if (tv < kT) {
+      // final tile: nothing follows
+    }
+    __syncthreads();
+  }
+}
+
+template <int NPT4, int RMAX>
+cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
+  const int PT = (RMAX > 1 || a.mimo_o) ? g.P : (g.P < 32 ? g.P : 32);
+  const SeqLayout lay = seq_layout(g.N, PT, g.R, g.A);
+  const int threads = ((PT * 4 + 31) / 32) * 32;
+  const int ptiles = (g.P + PT - 1) / PT;
+  cudaError_t e = cudaFuncSetAttribute(k_scan_seq<NPT4, RMAX>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)lay.bytes);
+  if (e != cudaSuccess) return e;
+  k_scan_seq<NPT4, RMAX><<<(unsigned)(g.B * g.H * ptiles), threads, lay.bytes, s>>>(g, a, lay);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+template <int RMAX>
+cudaError_t launch_seq_r(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
+  const int npt4 = ((g.N + 15) / 16);
+  if (npt4 <= 1) return launch_seq_t<1, RMAX>(g, a, s);
+  if (npt4 <= 2) return launch_seq_t<2, RMAX>(g, a, s);
+  if (npt4 <= 4) return launch_seq_t<4, RMAX>(g, a, s);
+  return launch_seq_t<8, RMAX>(g, a, s);
+}
+
+}  // namespace
+
+cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
+  if (g.R == 1 && !a.mimo_o) return launch_seq_r<1>(g, a, s);
+  if (g.R <= 4) return launch_seq_r<4>(g, a, s);
+  return launch_seq_r<8>(g, a, s);
+}
+
+}  // namespace m3

@@ -1,0 +1,247 @@
+// C ABI of libm3: host-side validation and kernel dispatch.
+//
+// The geometry rules mirror oarust 0.8.6 `src/rs/ml/matrix/mamba3.rs`:
+// `Geometry::resolve` (SISO), `MimoGeometry::resolve` (MIMO),
+// `PreprocessGeometry::resolve` (preprocess), the step functions' L == 1 and
+// state-shape checks, and `shader_u32` (every element count below 2^32).
+// Every check runs before anything is enqueued, so a rejected call changes no
+// buffer (the step docstring: states are mutated only after validation).
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <initializer_list>
+
+#include "m3_internal.cuh"
+
+namespace m3 {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr uint64_t kU32 = 1ull << 32;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Product of non-negative extents, false on overflow or when >= 2^32.
+bool count_below_u32(std::initializer_list<int64_t> dims) {
+  uint64_t c = 1;
+  for (int64_t d : dims) {
+    if (d < 0) return false;
+    if (d != 0 && c > (kU32 - 1) / (uint64_t)d) return false;
+    c *= (uint64_t)d;
+  }
+  return c < kU32;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? M3_OK : M3_ERR_CUDA; }
+
+// Shared SISO/MIMO geometry check. Fills g; returns M3_OK or an error code.
+int resolve_ssm(const m3_ssm_config* cfg, bool mimo, ScanGeom* g) {
+  if (!cfg) return M3_ERR_INVALID_ARGUMENT;
+  const int64_t B = cfg->batch_size, L = cfg->sequence_length, H = cfg->num_heads;
+  const int64_t G = cfg->num_groups == 0 ? H : cfg->num_groups;
+  const int64_t P = cfg->head_dim, N = cfg->state_size, A = cfg->num_rope_angles;
+  const int64_t R = cfg->mimo_rank;
+  if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || cfg->num_groups < 0 || H % G != 0) return M3_ERR_INVALID_ARGUMENT;
+  if (P <= 0 || P > 128 || N <= 0 || N > 128 || A < 0 || A > 64 || 2 * A > N) return M3_ERR_INVALID_ARGUMENT;
+  if (mimo) {
+    if (R < 1 || R > 8 || P * N > 4096) return M3_ERR_INVALID_ARGUMENT;
+  } else {
+    if (R != 1 || cfg->has_output_norm) return M3_ERR_INVALID_ARGUMENT;
+  }
+  if (cfg->math_mode != M3_MATH_FP32 && cfg->math_mode != M3_MATH_TF32) return M3_ERR_INVALID_ARGUMENT;
+  // every operand element count below 2^32 (`shader_u32`)
+  if (!count_below_u32({B, L, R * G, N}) || !count_below_u32({B, L, H, P}) ||
+      !count_below_u32({B, L, H}) || !count_below_u32({B, L, A}) ||
+      !count_below_u32({H, R, N}) || !count_below_u32({H, R, P}) || !count_below_u32({B, H}))
+    return M3_ERR_INVALID_ARGUMENT;
+  g->B = (int)B; g->L = (int)L; g->H = (int)H; g->G = (int)G; g->P = (int)P; g->N = (int)N;
+  g->A = (int)A; g->R = (int)R;
+  g->has_z = cfg->has_z != 0; g->has_d = cfg->has_d != 0;
+  g->has_norm = mimo && cfg->has_output_norm != 0;
+  g->math_mode = cfg->math_mode;
+  return M3_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> required) {
+  for (const void* p : required)
+    if (!p) return M3_ERR_INVALID_ARGUMENT;
+  for (const void* p : required)
+    if (!aligned16(p)) return M3_ERR_UNALIGNED;
+  return M3_OK;
+}
+
+int check_angle_ptr(const void* p, int A) {
+  if (A == 0) return (p && !aligned16(p)) ? M3_ERR_UNALIGNED : M3_OK;
+  if (!p) return M3_ERR_INVALID_ARGUMENT;
+  return aligned16(p) ? M3_OK : M3_ERR_UNALIGNED;
+}
+
+}  // namespace
+
+// Scan dispatch: the token-sequential CUDA-core kernel handles every geometry.
+size_t scan_workspace_bytes(const ScanGeom&) { return 0; }
+
+cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, void*, size_t, cudaStream_t s) {
+  return launch_scan_seq(g, a, s);
+}
+
+}  // namespace m3
+
+using namespace m3;
+
+extern "C" {
+
+const char* m3_status_string(int status) {
+  switch (status) {
+    case M3_OK: return "ok";
+    case M3_ERR_INVALID_ARGUMENT: return "invalid argument: geometry, limit, null pointer or overflow";
+    case M3_ERR_UNALIGNED: return "a base pointer is not 16-byte aligned";
+    case M3_ERR_WORKSPACE: return "workspace missing or smaller than required";
+    case M3_ERR_CUDA: return "a CUDA launch or runtime call failed";
+    case M3_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    default: return "unknown status";
+  }
+}
+
+uint64_t m3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
+                  const float* dt_bias, float* x, float* z, float* bh, float* ch, float* dt,
+                  float* adt, float* trap, float* angle, m3_stream_t stream) {
+  if (!cfg) return M3_ERR_INVALID_ARGUMENT;
+  const int64_t I = cfg->inner_size, N = cfg->state_size, H = cfg->num_heads;
+  const int64_t A = cfg->num_rope_angles, G = cfg->num_groups, R = cfg->mimo_rank;
+  if (rows <= 0 || I <= 0 || N <= 0 || H <= 0 || G <= 0 || R <= 0 || A < 0 || A > N / 2)
+    return M3_ERR_INVALID_ARGUMENT;
+  const float eps = cfg->epsilon, lo = cfg->dt_min, hi = cfg->dt_max, fl = cfg->a_floor;
+  if (!std::isfinite(eps) || eps <= 0.f || !std::isfinite(lo) || !std::isfinite(hi) ||
+      lo <= 0.f || lo > hi || !std::isfinite(fl) || fl <= 0.f)
+    return M3_ERR_INVALID_ARGUMENT;
+  if (!count_below_u32({G, R, N}) || !count_below_u32({I, 2}) || !count_below_u32({H, 3}))
+    return M3_ERR_INVALID_ARGUMENT;
+  const int64_t bc = G * R * N;
+  const int64_t W = 2 * I + 2 * bc + 3 * H + A;
+  if (!count_below_u32({W}) || !count_below_u32({rows, W}) || !count_below_u32({rows, I}) ||
+      !count_below_u32({rows, bc}) || !count_below_u32({rows, H}) || !count_below_u32({rows, A}))
+    return M3_ERR_INVALID_ARGUMENT;
+  int st = check_ptrs({projected, dt_bias, x, z, bh, ch, dt, adt, trap});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(angle, (int)A)) != M3_OK) return st;
+  PreGeom g;
+  g.rows = rows; g.I = (int)I; g.N = (int)N; g.H = (int)H; g.A = (int)A; g.G = (int)G;
+  g.R = (int)R; g.W = (int)W;
+  g.eps = eps; g.dt_min = lo; g.dt_max = hi; g.a_floor = fl;
+  PreOut o{x, z, bh, ch, dt, adt, trap, angle};
+  return cuda_status(launch_preprocess(g, projected, dt_bias, o, (cudaStream_t)stream));
+}
+
+int m3_siso_forward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  int st = resolve_ssm(cfg, false, &g);
+  if (st != M3_OK) return st;
+  *bytes = scan_workspace_bytes(g);
+  return M3_OK;
+}
+
+int m3_mimo_forward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  int st = resolve_ssm(cfg, true, &g);
+  if (st != M3_OK) return st;
+  *bytes = scan_workspace_bytes(g);
+  return M3_OK;
+}
+
+static int scan_common(const m3_ssm_config* cfg, bool mimo, const ScanArgs& a, void* ws,
+                       size_t ws_bytes, m3_stream_t stream) {
+  ScanGeom g;
+  int st = resolve_ssm(cfg, mimo, &g);
+  if (st != M3_OK) return st;
+  st = check_ptrs({a.c, a.b, a.x, a.z, a.adt, a.dt, a.trap, a.c_bias, a.b_bias, a.d, a.out});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(a.angle, g.A)) != M3_OK) return st;
+  if (mimo && (st = check_ptrs({a.mimo_x, a.mimo_z, a.mimo_o, a.norm_weight})) != M3_OK) return st;
+  const size_t need = scan_workspace_bytes(g);
+  if (need > 0 && (!ws || ws_bytes < need)) return M3_ERR_WORKSPACE;
+  if (ws && !aligned16(ws)) return M3_ERR_UNALIGNED;
+  return cuda_status(launch_scan(g, a, ws, ws_bytes, (cudaStream_t)stream));
+}
+
+int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, float* out, void* workspace, size_t workspace_bytes,
+                    m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             nullptr, nullptr, nullptr, nullptr, out};
+  return scan_common(cfg, false, a, workspace, workspace_bytes, stream);
+}
+
+int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, const float* mimo_x, const float* mimo_z,
+                    const float* mimo_o, const float* norm_weight, float* out,
+                    void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             mimo_x, mimo_z, mimo_o, norm_weight, out};
+  return scan_common(cfg, true, a, workspace, workspace_bytes, stream);
+}
+
+static int step_common(const m3_ssm_config* cfg, bool mimo, const ScanArgs& a,
+                       const StepState& s, m3_stream_t stream) {
+  ScanGeom g;
+  int st = resolve_ssm(cfg, mimo, &g);
+  if (st != M3_OK) return st;
+  if (g.L != 1) return M3_ERR_INVALID_ARGUMENT;
+  // state element counts (`shader_u32` on the four state shapes)
+  if (!count_below_u32({g.B, g.H, g.P, g.N}) || !count_below_u32({g.B, g.H, g.A}) ||
+      !count_below_u32({g.B, g.H, g.R, g.N}) || !count_below_u32({g.B, g.H, g.R, g.P}))
+    return M3_ERR_INVALID_ARGUMENT;
+  st = check_ptrs({a.c, a.b, a.x, a.z, a.adt, a.dt, a.trap, a.c_bias, a.b_bias, a.d, a.out,
+                   s.ssm, s.k, s.v});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(a.angle, g.A)) != M3_OK) return st;
+  if ((st = check_angle_ptr(s.angle, g.A)) != M3_OK) return st;
+  if (mimo && (st = check_ptrs({a.mimo_x, a.mimo_z, a.mimo_o, a.norm_weight})) != M3_OK) return st;
+  return cuda_status(launch_step(g, a, s, (cudaStream_t)stream));
+}
+
+int m3_siso_step(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                 const float* z, const float* adt, const float* dt, const float* trap,
+                 const float* angle, const float* c_bias, const float* b_bias, const float* d,
+                 float* ssm_state, float* angle_state, float* k_state, float* v_state,
+                 float* out, m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             nullptr, nullptr, nullptr, nullptr, out};
+  StepState s{ssm_state, angle_state, k_state, v_state};
+  return step_common(cfg, false, a, s, stream);
+}
+
+int m3_mimo_step(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                 const float* z, const float* adt, const float* dt, const float* trap,
+                 const float* angle, const float* c_bias, const float* b_bias, const float* d,
+                 const float* mimo_x, const float* mimo_z, const float* mimo_o,
+                 const float* norm_weight, float* ssm_state, float* angle_state,
+                 float* k_state, float* v_state, float* out, m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             mimo_x, mimo_z, mimo_o, norm_weight, out};
+  StepState s{ssm_state, angle_state, k_state, v_state};
+  return step_common(cfg, true, a, s, stream);
+}
+
+int m3_workspace_status(const void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  if (!workspace || workspace_bytes < 16) return M3_ERR_INVALID_ARGUMENT;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return M3_ERR_CUDA;
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return M3_ERR_CUDA;
+  return word == kStatusTimeout ? M3_ERR_TIMEOUT : M3_OK;
+}
+
+}  // extern "C"

@@ -179,3 +179,21 @@ def decode_inputs(w: Workload, steps=None, salt: int = 0):
     length-`steps` sequence (workload distributions), sliced one token per call."""
     steps = steps or w.steps
     return scan_inputs(w, salt, length=steps)
+
+
+def scan_params(w: Workload, salt: int = 0):
+    """Per-head parameters only (no per-token operands): c_bias, b_bias
+    ~ N(0, 0.1^2), D = 1, and for MIMO mimo_x/z/o ~ N(0, 1/R), norm_weight
+    = 1 + N(0, 0.02^2)."""
+    rng = rng_for(w, 300 + salt)
+    H, P, N, R = w.num_heads, w.head_dim, w.state_size, w.mimo_rank
+    bias_shape = (H, N) if R == 1 else (H, R, N)
+    out = dict(c_bias=_normal(rng, bias_shape, 0.1), b_bias=_normal(rng, bias_shape, 0.1),
+               d=np.ones((H,), dtype=np.float32))
+    if R > 1 or w.has_output_norm:
+        s = 1.0 / math.sqrt(R)
+        out["mimo_x"] = _normal(rng, (H, R, P), s)
+        out["mimo_z"] = _normal(rng, (H, R, P), s)
+        out["mimo_o"] = _normal(rng, (H, R, P), s)
+        out["norm_weight"] = (1.0 + _normal(rng, (H, P), 0.02)).astype(np.float32)
+    return out
