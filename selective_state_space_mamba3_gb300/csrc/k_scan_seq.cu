@@ -21,7 +21,7 @@ constexpr int kT = 16;  // tokens per staging tile
 
 struct SeqLayout {
   int Npad, PT, R, A;
-  size_t q, k, coef, theta, xs, zs, ys, os, bytes;
+  size_t q, k, coef, theta, cs, xs, zs, ys, os, bytes;
 };
 
 __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
@@ -40,6 +40,7 @@ __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
   l.k = take((size_t)(kT + 1) * R * l.Npad);
   l.coef = take((size_t)kT * 4);
   l.theta = take((size_t)kT * (A > 0 ? A : 1));
+  l.cs = take((size_t)2 * kT * (A > 0 ? A : 1));
   l.xs = take((size_t)kT * PT);
   l.zs = take((size_t)kT * PT);
   l.ys = take((size_t)kT * R * PT);
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   float* sk = sm + lay.k;
   float* scoef = sm + lay.coef;
   float* sth = sm + lay.theta;
+  float* scs = sm + lay.cs;
   float* sx = sm + lay.xs;
   float* sz = sm + lay.zs;
   float* sy = sm + lay.ys;
@@ -99,15 +101,24 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
       scoef[t * 4 + 1] = lam * dtv;
       scoef[t * 4 + 2] = (1.0f - lam) * dtv * dec;
     }
+    // dt * angle increments of the tile, loaded coalesced into the sin/cos
+    // table's slot (it is overwritten below once the running sums exist)
+    for (int i = tid; i < tv * A; i += nthr) {
+      const int t = i / A, aa = i - t * A;
+      const int64_t tok = (int64_t)b * L + t0 + t;
+      scs[i] = a.dt[tok * H + h] * a.angle[tok * A + aa];
+    }
+    __syncthreads();
     for (int i = tid; i < A; i += nthr) {
       float th = sth[(kT - 1) * A + i];  // running angle from the previous tile
       for (int t = 0; t < tv; ++t) {
-        const int64_t tok = (int64_t)b * L + t0 + t;
-        th += a.dt[tok * H + h] * a.angle[tok * A + i];
+        th += scs[t * A + i];
         sth[t * A + i] = th;
       }
       for (int t = tv; t < kT; ++t) sth[t * A + i] = th;
     }
+    __syncthreads();
+    for (int i = tid; i < tv * A; i += nthr) sincosf(sth[i], &scs[2 * i + 1], &scs[2 * i]);
     for (int i = tid; i < kT * PT; i += nthr) {
       const int t = i / PT, pp = i % PT;
       float xv = 0.f, zv = 0.f;
@@ -133,8 +144,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
         const float* bb = a.b_bias + ((int64_t)h * R + r) * N;
         if (n < 2 * A) {
           const int pa = n < A ? n : n - A;
-          float sn, cs;
-          sincosf(sth[t * A + pa], &sn, &cs);
+          const float cs = scs[2 * (t * A + pa)], sn = scs[2 * (t * A + pa) + 1];
           const float qu = a.c[row + pa] + cb[pa], qw = a.c[row + pa + A] + cb[pa + A];
           const float ku = a.b[row + pa] + bb[pa], kw = a.b[row + pa + A] + bb[pa + A];
           if (n < A) {

@@ -41,6 +41,18 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
   const int P = g.P, N = g.N, A = g.A, R = g.R;
   const int64_t sc = (int64_t)b * g.H + h;  // [B,1,H] index
 
+  // 0. issue the loads of this warp's state rows first (one float4 per lane per
+  // row, rows p = warp + 8i) so that their latency overlaps the staging below.
+  float* hs = st.ssm + sc * (int64_t)P * N;
+  constexpr int kRowsPerWarp = 128 / kWarps;
+  float4 hreg[VEC ? kRowsPerWarp : 1];
+  if (VEC) {
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int p = warp + kWarps * i;
+      if (p < P && lane < (N >> 2)) hreg[i] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
+    }
+  }
   const float dtv = a.dt[sc];
   // 1. cumulative angle theta = angle_state + dt * angle (per head).
   for (int i = tid; i < A; i += kThreads) {
@@ -88,16 +100,27 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
   const float gam = lam * dtv;
   const float sdec = (1.0f - lam) * dtv * decay;
   const float dskip = g.has_d ? a.d[h] : 0.0f;
-  float* hs = st.ssm + sc * (int64_t)P * N;
-  for (int p = warp; p < P; p += kWarps) {
-    float acc[RMAX];
+  // Readout of row p: y_r[p] = sum_n h[p][n] q_r[n] (+ D v_r[p]).
+  auto finish_row = [&](int p, const float* acc) {
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-    if (VEC) {
-      const int N4 = N >> 2;
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const float yv = warp_sum(acc[r]);
+        if (lane == 0) sm.y[r * P + p] = yv + dskip * sm.v[r * P + p];
+      }
+    }
+  };
+  if (VEC) {
+    const int N4 = N >> 2;
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+      const int p = warp + kWarps * i;
+      if (p >= P) break;
+      float acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
       if (lane < N4) {
-        float4* hp = reinterpret_cast<float4*>(hs + (int64_t)p * N) + lane;
-        float4 hv = *hp;
+        float4 hv = hreg[i];
         float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
@@ -115,7 +138,7 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
         hv.y = decay * hv.y + upd.y;
         hv.z = decay * hv.z + upd.z;
         hv.w = decay * hv.w + upd.w;
-        *hp = hv;
+        __stcs(reinterpret_cast<float4*>(hs + (int64_t)p * N) + lane, hv);
 #pragma unroll
         for (int r = 0; r < RMAX; ++r) {
           if (r < R) {
@@ -124,24 +147,24 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
           }
         }
       }
-    } else {
+      finish_row(p, acc);
+    }
+  } else {
+    for (int p = warp; p < P; p += kWarps) {
+      float acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
       for (int n = lane; n < N; n += 32) {
         float upd = 0.f;
         for (int r = 0; r < R; ++r)
           upd += sdec * sm.vp[r * P + p] * sm.kp[r * N + n] + gam * sm.v[r * P + p] * sm.k[r * N + n];
-        float hv = decay * hs[(int64_t)p * N + n] + upd;
+        const float hv = decay * hs[(int64_t)p * N + n] + upd;
         hs[(int64_t)p * N + n] = hv;
 #pragma unroll
         for (int r = 0; r < RMAX; ++r)
           if (r < R) acc[r] += hv * sm.q[r * N + n];
       }
-    }
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < R) {
-        const float yv = warp_sum(acc[r]);
-        if (lane == 0) sm.y[r * P + p] = yv + dskip * sm.v[r * P + p];
-      }
+      finish_row(p, acc);
     }
   }
   __syncthreads();

@@ -206,7 +206,7 @@ def run_gpu_steps(w, ins, steps, mimo=False):
         par.update({k: dev(ins[k]) for k in MIMO_KEYS})
     outs = torch.empty(steps, B, 1, H, P, device="cuda")
     for t in range(steps):
-        tok = [seq[k][:, t:t + 1].contiguous() for k in SCAN_KEYS[:8]]
+        tok = [seq[k][:, t:t + 1].clone() for k in SCAN_KEYS[:8]]   # fresh, 16-byte aligned
         if A == 0:
             tok[7] = None
         if mimo:
