@@ -1,0 +1,450 @@
+// Chunked Mamba-3 scan on the tcgen05 tensor cores (TF32 operands, FP32
+// accumulation in tensor memory). Covers `mamba3_siso` and `mamba3_mimo`
+// (oarust mamba3.rs) for mimo_rank R in {1, 2, 4, 8}, P <= 128, N <= 128.
+//
+// Algebra. Unrolling the exponential-trapezoidal recurrence gives, for a chunk
+// starting at token t0 with cum_t = sum_{t0 <= i <= t} adt_i,
+//   h_t = e^{cum_t} g_{t0-1} + sum_{t0 <= s <= t} e^{cum_t - cum_s} c_{t,s} x_s k_s^T,
+//   c_{t,s} = gamma_s + scale_{s+1} [s < t],
+// where g is the "pre-loaded" state (h plus the next token's trapezoid term),
+// carried from chunk to chunk as
+//   g_end = e^{cum_end} g_{t0-1} + sum_s e^{cum_end - cum_s} (gamma_s + scale_{s+1}) x_s k_s^T.
+// MIMO expands every token into R rows (t, r) that share the token's decay
+// and rotation; SISO is R = 1. A chunk holds 64 such rows.
+//
+// Per chunk and (b, h), all contractions run as tcgen05.mma (kind::tf32):
+//   S    = Q K^T               [64 x 64],  K = N     (A, B in shared memory)
+//   Yo^T = G Q^T               [P  x 64],  K = N     (A = state G in TMEM)
+//   Yi^T = X^T (M o S)^T       [P  x 64],  K = 64    (decay/trapezoid mask M)
+//   G   += X^T (w K)           [P  x N],   K = 64    (after G *= e^{cum_end})
+// with the state G [P x N] resident in TMEM for the whole sequence and the
+// outputs produced transposed (TMEM lane = p), so the epilogue of one thread
+// owns one output column p: D skip, SiLU gate, the MIMO mimo_o contraction
+// over its R rows, and (through shared memory) the MIMO output RMS norm.
+// Rotary cos/sin, the local log-decay cumsum and the trapezoid weights are
+// formed by the CUDA cores while staging the operands; every operand is
+// rounded to TF32 with round-to-nearest.
+//
+// One CTA of 128 threads runs one (b, h) sequence chunk after chunk; thread 0
+// issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit
+// (bounded waits: on timeout the kernel records a status word and exits).
+#include "m3_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace m3 {
+namespace {
+
+constexpr int kRows = 64;       // (token, rank) rows per chunk
+constexpr int kThreads = 128;
+constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
+
+struct ChunkLayout {
+  int Npad, MP;
+  int q, k, kt, xt, p, cs, th, bias, tok, thbase;  // float offsets
+  size_t bytes;
+};
+
+ChunkLayout chunk_layout(int N, int P, int A, int R) {
+  ChunkLayout l;
+  l.Npad = (N + 15) / 16 * 16;
+  l.MP = P <= 64 ? 64 : 128;
+  int off = 0;
+  auto take = [&](int floats) {
+    int o = off;
+    off += (floats + 31) / 32 * 32;  // 128-byte aligned
+    return o;
+  };
+  l.q = take(kRows * l.Npad);
+  l.k = take(kRows * (l.Npad > l.MP ? l.Npad : l.MP));  // also MIMO epilogue staging [Qt][MP]
+  l.kt = take(l.Npad * kRows);
+  l.xt = take(l.MP * kRows);
+  l.p = take(kRows * kRows);
+  l.cs = take(kRows * 2 * (A > 0 ? A : 1));
+  l.th = take(kRows * (A + 1));
+  l.bias = take(2 * R * l.Npad);
+  l.tok = take(8 * kTok);
+  l.thbase = take(64);
+  l.bytes = (size_t)off * sizeof(float);
+  return l;
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, uint32_t* status) {
+  extern __shared__ __align__(1024) float sm[];
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = g.H, L = g.L, P = g.P, N = g.N, A = g.A, R = g.R;
+  const int Npad = lay.Npad;
+  const int Qt = kRows / R;  // tokens per chunk
+  const int b = blockIdx.x / H, h = blockIdx.x % H;
+  const int grp = h / (H / g.G);
+
+  float* sQ = sm + lay.q;    // [64 rows][Npad]   K-major, K = n
+  float* sK = sm + lay.k;    // [64 rows][Npad]   K-major, K = n
+  float* sKt = sm + lay.kt;  // [Npad][64 rows]   K-major, K = row  (w-scaled keys)
+  float* sXt = sm + lay.xt;  // [MP][64 rows]     K-major, K = row  (values)
+  float* sP = sm + lay.p;    // [64][64]          K-major           (masked scores)
+  float* sCS = sm + lay.cs;  // [Qt][A] (cos, sin)
+  float* sTh = sm + lay.th;  // [Qt][A + 1] angle increments
+  float* sBiasC = sm + lay.bias;
+  float* sBiasB = sBiasC + R * Npad;
+  float* tAdt = sm + lay.tok;
+  float* tCum = tAdt + kTok;
+  float* tEc = tCum + kTok;   // e^{cum_t}
+  float* tGam = tEc + kTok;   // gamma_t
+  float* tScl = tGam + kTok;  // scale_t, t in [0, Qt]
+  float* tW = tScl + kTok;    // gamma_t + scale_{t+1}
+  float* tOm = tW + kTok;     // e^{cum_end - cum_t} * tW[t]
+  float* tDt = tOm + kTok;
+  float* sThBase = sm + lay.thbase;
+  float* sO = sK;             // MIMO epilogue staging, reuses sK after its MMA
+
+  if (tid == 0) {
+    tc::bar_init(&bars[0], 1);
+    tc::bar_init(&bars[1], 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;");
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  for (int i = tid; i < R * Npad; i += kThreads) {
+    const int r = i / Npad, n = i - r * Npad;
+    sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
+    sBiasB[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
+  }
+  for (int i = tid; i < A; i += kThreads) sThBase[i] = 0.f;
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = tmem_slot;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const uint32_t tG = tbase, tS = tbase + 128, tYo = tbase + 192;
+  {
+    float zero[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) zero[i] = 0.f;
+    for (int c = 0; c < Npad; c += 16) tc::tmem_st16(tG + lane_base + c, zero);
+  }
+  // row p of the transposed tiles held by this thread (TMEM data-path layout:
+  // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant)
+  const int prow = (MP == 64) ? (lane < 16 ? 16 * warp + lane : -1) : 32 * warp + lane;
+  const bool pvalid = prow >= 0 && prow < P;
+  const bool mimo = a.mimo_o != nullptr;
+  float mxr[8], mzr[8], mor[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const bool ok = mimo && pvalid && r < R;
+    mxr[r] = ok ? a.mimo_x[((int64_t)h * R + r) * P + prow] : 1.f;
+    mzr[r] = ok ? a.mimo_z[((int64_t)h * R + r) * P + prow] : 1.f;
+    mor[r] = ok ? a.mimo_o[((int64_t)h * R + r) * P + prow] : 0.f;
+  }
+  const float dsk = g.has_d ? a.d[h] : 0.f;
+  const uint32_t id_S = tc::idesc_tf32(64, 64);
+  const uint32_t id_Y = tc::idesc_tf32(MP, 64);
+  const uint32_t id_D = tc::idesc_tf32(MP, Npad);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+
+  int it = 0;
+  for (int c0 = 0; c0 < L; c0 += Qt, ++it) {
+    const int tv = min(Qt, L - c0);
+    // (1) per-token scalars of tokens c0 .. c0 + Qt (the last one is the next
+    // chunk's first token: only its trapezoid scale is used)
+    if (tid <= Qt) {
+      const int t = tid;
+      float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
+      if (c0 + t < L) {
+        const int64_t sc = ((int64_t)b * L + c0 + t) * H + h;
+        dtv = a.dt[sc];
+        adtv = a.adt[sc];
+        const float lam = sigmoid_f(a.trap[sc]);
+        gam = lam * dtv;
+        scl = (1.0f - lam) * dtv;
+      }
+      tScl[t] = scl;
+      if (t < Qt) {
+        const bool in = t < tv;
+        tAdt[t] = in ? adtv : 0.f;
+        tGam[t] = in ? gam : 0.f;
+        tDt[t] = in ? dtv : 0.f;
+      }
+    }
+    for (int i = tid; i < Qt * A; i += kThreads) {
+      const int t = i / A, aa = i - t * A;
+      sTh[t * (A + 1) + aa] = t < tv ? a.angle[((int64_t)b * L + c0 + t) * A + aa] : 0.f;
+    }
+    __syncthreads();
+    // (2) local cumulative log decay (warp 0, two tokens per lane)
+    if (warp == 0) {
+      const int t0 = 2 * lane, t1 = 2 * lane + 1;
+      const float a0 = t0 < Qt ? tAdt[t0] : 0.f, a1 = t1 < Qt ? tAdt[t1] : 0.f;
+      float s = a0 + a1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+      }
+      const float ex = s - (a0 + a1);
+      if (t0 < Qt) tCum[t0] = ex + a0;
+      if (t1 < Qt) tCum[t1] = ex + a0 + a1;
+    }
+    // rotary angle: per-angle scan of dt * angle over the chunk, plus sin/cos
+    for (int aa = warp; aa < A; aa += kThreads / 32) {
+      float v0 = lane < Qt ? tDt[lane] * sTh[lane * (A + 1) + aa] : 0.f;
+      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sTh[(lane + 32) * (A + 1) + aa] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, v0, o);
+        const float u1 = __shfl_up_sync(0xffffffffu, v1, o);
+        if (lane >= o) {
+          v0 += u0;
+          v1 += u1;
+        }
+      }
+      v1 += __shfl_sync(0xffffffffu, v0, 31);
+      const float base = sThBase[aa];
+      const float th0 = base + v0, th1 = base + v1;
+      if (lane < Qt) sincosf(th0, &sCS[(lane * A + aa) * 2 + 1], &sCS[(lane * A + aa) * 2]);
+      if (lane + 32 < Qt) sincosf(th1, &sCS[((lane + 32) * A + aa) * 2 + 1], &sCS[((lane + 32) * A + aa) * 2]);
+      const float last = __shfl_sync(0xffffffffu, Qt > 32 ? th1 : th0, Qt > 32 ? Qt - 33 : Qt - 1);
+      __syncwarp();
+      if (lane == 0) sThBase[aa] = last;
+    }
+    __syncthreads();
+    // (3) decay / trapezoid coefficients
+    if (tid < Qt) {
+      const int t = tid;
+      const float cum = tCum[t], cend = tCum[Qt - 1];
+      const float w = tGam[t] + tScl[t + 1];
+      tEc[t] = expf(cum);
+      tW[t] = w;
+      tOm[t] = expf(cend - cum) * w;
+    }
+    __syncthreads();
+    // (4) operand tiles: rotated q/k rows, w-scaled transposed keys, values
+    {
+      const int NQ = Npad >> 2;
+      for (int i = tid; i < kRows * NQ; i += kThreads) {
+        const int quad = i / kRows, rho = i - quad * kRows;
+        const int t = rho / R, r = rho - t * R;
+        const int n0 = quad * 4;
+        float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < tv) {
+          const int64_t rowoff =
+              (((int64_t)b * L + c0 + t) * g.G * R + (int64_t)grp * R + r) * (int64_t)N;
+          const float* cr = a.c + rowoff;
+          const float* br = a.b + rowoff;
+          const float* cb = sBiasC + r * Npad;
+          const float* bb = sBiasB + r * Npad;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = n0 + e;
+            if (n < N) {
+              if (n < A) {
+                const float cs = sCS[(t * A + n) * 2], sn = sCS[(t * A + n) * 2 + 1];
+                const float qu = cr[n] + cb[n], qw = cr[n + A] + cb[n + A];
+                const float ku = br[n] + bb[n], kw = br[n + A] + bb[n + A];
+                qv[e] = qu * cs - qw * sn;
+                kv[e] = ku * cs - kw * sn;
+              } else if (n < 2 * A) {
+                const int m = n - A;
+                const float cs = sCS[(t * A + m) * 2], sn = sCS[(t * A + m) * 2 + 1];
+                const float qu = cr[m] + cb[m], qw = cr[n] + cb[n];
+                const float ku = br[m] + bb[m], kw = br[n] + bb[n];
+                qv[e] = qu * sn + qw * cs;
+                kv[e] = ku * sn + kw * cs;
+              } else {
+                qv[e] = cr[n] + cb[n];
+                kv[e] = br[n] + bb[n];
+              }
+            }
+          }
+        }
+        const float om = t < tv ? tOm[t] : 0.f;
+        *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) =
+            make_float4(tc::to_tf32(qv[0]), tc::to_tf32(qv[1]), tc::to_tf32(qv[2]), tc::to_tf32(qv[3]));
+        *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) =
+            make_float4(tc::to_tf32(kv[0]), tc::to_tf32(kv[1]), tc::to_tf32(kv[2]), tc::to_tf32(kv[3]));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sKt[tc::kmaj(n0 + e, rho, kRows)] = tc::to_tf32(om * kv[e]);
+      }
+      const int PQ = MP >> 2;
+      for (int i = tid; i < kRows * PQ; i += kThreads) {
+        const int pq = i / kRows, rho = i - pq * kRows;
+        const int t = rho / R, r = rho - t * R;
+        const int p0 = pq * 4;
+        float xv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < tv) {
+          const float* xr = a.x + (((int64_t)b * L + c0 + t) * H + h) * P;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int p = p0 + e;
+            if (p < P) xv[e] = xr[p] * (mimo ? a.mimo_x[((int64_t)h * R + r) * P + p] : 1.f);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sXt[tc::kmaj(p0 + e, rho, kRows)] = tc::to_tf32(xv[e]);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    // (5) S = Q K^T and Yo^T = G Q^T
+    if (tid == 0) {
+      for (int ks = 0; ks < Npad / 8; ++ks)
+        tc::mma_ss(tS, tc::kdesc(sQ, Npad, ks), tc::kdesc(sK, Npad, ks), id_S, ks > 0);
+      for (int ks = 0; ks < Npad / 8; ++ks)
+        tc::mma_ts(tYo, tG + ks * 8, tc::kdesc(sQ, Npad, ks), id_Y, ks > 0);
+      tc::commit(&bars[0]);
+    }
+    if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
+    tc::fence_after();
+    __syncthreads();
+    if (abort_flag) break;
+    // (6) masked scores P = M o S (rows of S: TMEM M = 64 layout), and G *= e^{cum_end}
+    {
+      const int rho = 16 * warp + lane;
+      const int t = rho / R;
+      const float cum_t = lane < 16 ? tCum[t] : 0.f;
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[16];
+        tc::tmem_ld16(tS + lane_base + cb * 16, v);
+        if (lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int s = (cb * 16 + j) / R;
+            float m = 0.f;
+            if (s < t)
+              m = __expf(cum_t - tCum[s]) * tW[s];
+            else if (s == t)
+              m = tGam[t];
+            v[j] = tc::to_tf32(v[j] * m);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4*>(sP + tc::kmaj(rho, cb * 16 + 4 * u, kRows)) =
+                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        }
+      }
+      const float ec = expf(tCum[Qt - 1]);
+      for (int c = 0; c < Npad; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tG + lane_base + c, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(v[j] * ec);
+        tc::tmem_st16(tG + lane_base + c, v);
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    // (7) Yi^T = X^T P^T and G += X^T (w K)
+    if (tid == 0) {
+      for (int ks = 0; ks < kRows / 8; ++ks)
+        tc::mma_ss(tS, tc::kdesc(sXt, kRows, ks), tc::kdesc(sP, kRows, ks), id_Y, ks > 0);
+      for (int ks = 0; ks < kRows / 8; ++ks)
+        tc::mma_ss(tG, tc::kdesc(sXt, kRows, ks), tc::kdesc(sKt, kRows, ks), id_D, 1);
+      tc::commit(&bars[1]);
+    }
+    if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
+    tc::fence_after();
+    __syncthreads();
+    if (abort_flag) break;
+    // (8) epilogue: column p of the outputs of this chunk
+    for (int cb = 0; cb < 4; ++cb) {
+      float yo[16], yi[16];
+      tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
+      tc::tmem_ld16(tS + lane_base + cb * 16, yi);
+      if (!pvalid) continue;
+      if (!mimo) {
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+          const int t = cb * 16 + j;
+          if (t < tv) {
+            const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
+            float y = tEc[t] * yo[j] + yi[j] + dsk * a.x[off];
+            if (g.has_z) y *= silu_f(a.z[off]);
+            a.out[off] = y;
+          }
+        }
+      } else {
+        const int tpb = 16 / R;  // tokens per 16-column block
+        for (int tt = 0; tt < tpb; ++tt) {
+          const int t = cb * tpb + tt;
+          if (t >= tv) break;
+          const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
+          const float xv = a.x[off];
+          const float zv = a.z[off];
+          float o = 0.f;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r < R) {
+              const int j = tt * R + r;
+              float y = tEc[t] * yo[j] + yi[j] + dsk * xv * mxr[r];
+              if (g.has_z) y *= silu_f(zv * mzr[r]);
+              o += mor[r] * y;
+            }
+          }
+          if (g.has_norm)
+            sO[t * MP + prow] = o;
+          else
+            a.out[off] = o;
+        }
+      }
+    }
+    if (mimo && g.has_norm) {
+      __syncthreads();
+      for (int t = warp; t < tv; t += kThreads / 32) {
+        float ss = 0.f;
+        for (int p = lane; p < P; p += 32) ss += sO[t * MP + p] * sO[t * MP + p];
+        ss = warp_sum(ss);
+        const float inv = 1.0f / sqrtf(ss / (float)P + 1.0e-5f);
+        const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P;
+        for (int p = lane; p < P; p += 32)
+          a.out[off + p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
+      }
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+  }
+  if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_free(tbase, 256);
+}
+
+}  // namespace
+
+bool chunk_supported(const ScanGeom& g) {
+  return (g.R == 1 || g.R == 2 || g.R == 4 || g.R == 8) && g.N <= 128 && g.P <= 128;
+}
+
+cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
+                              cudaStream_t s) {
+  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
+  const unsigned grid = (unsigned)(g.B * g.H);
+  cudaError_t e;
+  if (lay.MP == 64) {
+    e = cudaFuncSetAttribute(k_scan_chunk<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)lay.bytes);
+    if (e != cudaSuccess) return e;
+    k_scan_chunk<64><<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
+  } else {
+    e = cudaFuncSetAttribute(k_scan_chunk<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)lay.bytes);
+    if (e != cudaSuccess) return e;
+    k_scan_chunk<128><<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace m3

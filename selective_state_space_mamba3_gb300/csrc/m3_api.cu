@@ -81,10 +81,23 @@ int check_angle_ptr(const void* p, int A) {
 
 }  // namespace
 
-// Scan dispatch: the token-sequential CUDA-core kernel handles every geometry.
-size_t scan_workspace_bytes(const ScanGeom&) { return 0; }
+// Scan dispatch. TF32 mode runs the tcgen05 chunked kernel where its tiles
+// apply (R in {1,2,4,8}, P, N <= 128); FP32-exact mode and every other shape
+// run the token-sequential FP32 kernel on the CUDA cores. The chunked kernel
+// needs a workspace for its device status word.
+static bool use_chunk(const ScanGeom& g) {
+  return g.math_mode == M3_MATH_TF32 && chunk_supported(g);
+}
 
-cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, void*, size_t, cudaStream_t s) {
+size_t scan_workspace_bytes(const ScanGeom& g) { return use_chunk(g) ? 256 : 0; }
+
+cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, void* ws, size_t, cudaStream_t s) {
+  if (use_chunk(g)) {
+    uint32_t* status = static_cast<uint32_t*>(ws);
+    cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+    if (e != cudaSuccess) return e;
+    return launch_scan_chunk(g, a, status, s);
+  }
   return launch_scan_seq(g, a, s);
 }
 

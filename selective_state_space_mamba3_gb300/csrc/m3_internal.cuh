@@ -47,6 +47,9 @@ cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const fl
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                         cudaStream_t s);
 cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, cudaStream_t s);
+bool chunk_supported(const ScanGeom& g);
+cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
+                              cudaStream_t s);
 
 // Scan entry chosen by the host: workspace bytes for geometry g, then launch.
 size_t scan_workspace_bytes(const ScanGeom& g);
