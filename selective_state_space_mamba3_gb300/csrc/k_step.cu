@@ -41,16 +41,16 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
   const int P = g.P, N = g.N, A = g.A, R = g.R;
   const int64_t sc = (int64_t)b * g.H + h;  // [B,1,H] index
 
-  // 0. issue the loads of this warp's state rows first (one float4 per lane per
-  // row, rows p = warp + 8i) so that their latency overlaps the staging below.
+  // 0. issue the loads of this warp's first group of state rows (one float4 per
+  // lane per row, rows p = warp + 8i) so that their latency overlaps staging.
   float* hs = st.ssm + sc * (int64_t)P * N;
-  constexpr int kRowsPerWarp = 128 / kWarps;
-  float4 hreg[VEC ? kRowsPerWarp : 1];
+  constexpr int kGroup = 4;
+  float4 hreg[kGroup];
   if (VEC) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int p = warp + kWarps * i;
-      if (p < P && lane < (N >> 2)) hreg[i] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
+    for (int u = 0; u < kGroup; ++u) {
+      const int p = warp + kWarps * u;
+      if (p < P && lane < (N >> 2)) hreg[u] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
     }
   }
   const float dtv = a.dt[sc];
@@ -112,42 +112,51 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
   };
   if (VEC) {
     const int N4 = N >> 2;
+    for (int i0 = 0; warp + kWarps * i0 < P; i0 += kGroup) {
+      if (i0 > 0) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerWarp; ++i) {
-      const int p = warp + kWarps * i;
-      if (p >= P) break;
-      float acc[RMAX];
-#pragma unroll
-      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-      if (lane < N4) {
-        float4 hv = hreg[i];
-        float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r) {
-          if (r < R) {
-            const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
-            const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[lane];
-            const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[lane];
-            upd.x += cp * kp4.x + cc * k4.x;
-            upd.y += cp * kp4.y + cc * k4.y;
-            upd.z += cp * kp4.z + cc * k4.z;
-            upd.w += cp * kp4.w + cc * k4.w;
-          }
-        }
-        hv.x = decay * hv.x + upd.x;
-        hv.y = decay * hv.y + upd.y;
-        hv.z = decay * hv.z + upd.z;
-        hv.w = decay * hv.w + upd.w;
-        __stcs(reinterpret_cast<float4*>(hs + (int64_t)p * N) + lane, hv);
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r) {
-          if (r < R) {
-            const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[lane];
-            acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
-          }
+        for (int u = 0; u < kGroup; ++u) {
+          const int p = warp + kWarps * (i0 + u);
+          if (p < P && lane < N4) hreg[u] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
         }
       }
-      finish_row(p, acc);
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+        const int p = warp + kWarps * (i0 + u);
+        if (p >= P) break;
+        float acc[RMAX];
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+        if (lane < N4) {
+          float4 hv = hreg[u];
+          float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) {
+            if (r < R) {
+              const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
+              const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[lane];
+              const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[lane];
+              upd.x += cp * kp4.x + cc * k4.x;
+              upd.y += cp * kp4.y + cc * k4.y;
+              upd.z += cp * kp4.z + cc * k4.z;
+              upd.w += cp * kp4.w + cc * k4.w;
+            }
+          }
+          hv.x = decay * hv.x + upd.x;
+          hv.y = decay * hv.y + upd.y;
+          hv.z = decay * hv.z + upd.z;
+          hv.w = decay * hv.w + upd.w;
+          __stcs(reinterpret_cast<float4*>(hs + (int64_t)p * N) + lane, hv);
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) {
+            if (r < R) {
+              const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[lane];
+              acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
+            }
+          }
+        }
+        finish_row(p, acc);
+      }
     }
   } else {
     for (int p = warp; p < P; p += kWarps) {

@@ -35,11 +35,17 @@ __device__ __forceinline__ uint64_t kdesc(const float* tile, int kext, int kstep
   return sdesc(smem_u32(tile) + (uint32_t)kstep * 256u, 128u, (uint32_t)kext * 32u);
 }
 
-// Instruction descriptor: kind::tf32, dense, D = F32, A = B = TF32, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor: kind::tf32, dense, D = F32, A = B = TF32, A
+// K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1, bit 16), N >> 3 at
+// bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, int b_mn = 0) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// L2 prefetch of a byte range (start and size multiples of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,

@@ -5,6 +5,9 @@ Tolerance metric (normwise max-relative error): max|gpu - oracle| / max|oracle|
 per output tensor. FP32-exact paths must stay below 1e-5, TF32 tensor-core
 paths below 2e-3.
 """
+import json
+import os
+
 import numpy as np
 
 import oracle
@@ -70,3 +73,16 @@ def oracle_scan(cfg, ins, mimo=None, batch=None):
         ins = {k: (v[batch] if k in SCAN_KEYS[:8] else v) for k, v in ins.items()}
     extra = {k: ins[k] for k in MIMO_KEYS} if mimo else {}
     return oracle.scan(cfg, *[ins[k] for k in SCAN_KEYS], **extra)
+
+
+def check_close(got, ref, tol, label=""):
+    """Asserts normwise(got, ref) <= tol; when M3_PARITY_REPORT names a file,
+    appends the test id, label, error and tolerance to it as a JSON line."""
+    err = normwise(got, ref)
+    path = os.environ.get("M3_PARITY_REPORT")
+    if path:
+        name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+        with open(path, "a") as f:
+            f.write(json.dumps({"test": name, "label": label, "err": err, "tol": tol}) + "\n")
+    assert err <= tol, (label, err, tol)
+    return err

@@ -15,7 +15,8 @@ import oracle
 import selective_state_space_mamba3_gb300 as m3
 from selective_state_space_mamba3_gb300 import inputs as gen
 
-from m3_testutil import (SCAN_KEYS, MIMO_KEYS, TOL, dev, normwise, gpu_scan, oracle_scan)
+from m3_testutil import (SCAN_KEYS, MIMO_KEYS, TOL, dev, normwise, gpu_scan, oracle_scan,
+                         check_close)
 
 pytestmark = pytest.mark.gpu
 FP32, TF32 = m3.M3_MATH_FP32, m3.M3_MATH_TF32
@@ -109,7 +110,7 @@ def test_tiny_chain(mode):
     w, gins, oins = tiny_chain()
     got = gpu_scan(w.cfg(), gins, mode)
     ref = oracle_scan(w.cfg(), oins)
-    assert normwise(got, ref) <= TOL[mode]
+    check_close(got, ref, TOL[mode])
 
 
 EDGE = [
@@ -140,7 +141,7 @@ def test_siso_edge_shapes(shape, mode):
     w, ins = edge_case(**shape)
     got = gpu_scan(w.cfg(), ins, mode)
     ref = oracle_scan(w.cfg(), ins)
-    assert normwise(got, ref) <= TOL[mode]
+    check_close(got, ref, TOL[mode])
 
 
 @pytest.mark.parametrize("mode", [FP32, TF32])
@@ -153,7 +154,7 @@ def test_siso_full_size(w, mode):
     assert np.all(np.isfinite(got))
     for bsl in (slice(0, 1), slice(w.batch_size - 1, w.batch_size)):
         ref = oracle_scan(w.cfg(), ins, batch=bsl)
-        assert normwise(got[bsl], ref) <= TOL[mode]
+        check_close(got[bsl], ref, TOL[mode])
 
 
 # --------------------------------------------------------------- MIMO scans
@@ -174,7 +175,7 @@ def test_mimo_edge_shapes(shape, mode):
     cfg = w.cfg()
     got = gpu_scan(cfg, ins, mode, mimo=True)
     ref = oracle_scan(cfg, ins, mimo=True)
-    assert normwise(got, ref) <= TOL[mode]
+    check_close(got, ref, TOL[mode])
 
 
 @pytest.mark.parametrize("mode", [FP32, TF32])
@@ -184,7 +185,7 @@ def test_mimo_full_size(mode):
     got = gpu_scan(w.cfg(), ins, mode, mimo=True)
     assert np.all(np.isfinite(got))
     ref = oracle_scan(w.cfg(), ins, mimo=True, batch=slice(0, 1))
-    assert normwise(got[0:1], ref) <= TOL[mode]
+    check_close(got[0:1], ref, TOL[mode])
 
 
 # --------------------------------------------------------------------- step
@@ -233,11 +234,11 @@ def test_decode_step_512_tokens():
     ostate = oracle.zero_state(cfg)
     sub = {k: (v[bsl] if k in SCAN_KEYS[:8] else v) for k, v in ins.items()}
     ref = oracle.scan(cfg, *[sub[k] for k in SCAN_KEYS], state=ostate)
-    assert normwise(got[bsl], ref) <= 1e-5
-    assert normwise(st["ssm"][bsl], ostate["ssm"]) <= 1e-5
-    assert normwise(st["k"][bsl], ostate["k"]) <= 1e-5
-    assert normwise(st["v"][bsl], ostate["v"]) <= 1e-6
-    assert normwise(st["angle"][bsl], ostate["angle"]) <= 1e-5
+    check_close(got[bsl], ref, 1e-5)
+    check_close(st["ssm"][bsl], ostate["ssm"], 1e-5)
+    check_close(st["k"][bsl], ostate["k"], 1e-5)
+    check_close(st["v"][bsl], ostate["v"], 1e-6)
+    check_close(st["angle"][bsl], ostate["angle"], 1e-5)
 
 
 @pytest.mark.parametrize("shape", [dict(B=2, L=24, H=4, G=2, P=17, N=17, A=8),
@@ -246,7 +247,7 @@ def test_siso_step_odd_shapes(shape):
     w, ins = edge_case(**shape)
     got, _ = run_gpu_steps(w, ins, w.sequence_length)
     ref = oracle_scan(w.cfg(), ins)
-    assert normwise(got, ref) <= 1e-5
+    check_close(got, ref, 1e-5)
 
 
 @pytest.mark.parametrize("shape", [dict(B=2, L=16, H=2, G=1, P=64, N=64, A=32, R=4, norm=1),
@@ -255,7 +256,7 @@ def test_mimo_step(shape):
     w, ins = edge_case(**shape)
     got, _ = run_gpu_steps(w, ins, w.sequence_length, mimo=True)
     ref = oracle_scan(w.cfg(), ins, mimo=True)
-    assert normwise(got, ref) <= 1e-5
+    check_close(got, ref, 1e-5)
 
 
 def test_rejected_step_leaves_state_untouched():
