@@ -8,26 +8,30 @@
 //   c_{t,s} = gamma_s + scale_{s+1} [s < t],
 // where g is the "pre-loaded" state (h plus the next token's trapezoid term),
 // carried from chunk to chunk as
-//   g_end = e^{cum_end} g_{t0-1} + sum_s e^{cum_end - cum_s} (gamma_s + scale_{s+1}) x_s k_s^T.
+//   g_end = e^{cum_end} g_{t0-1} + sum_s w_s x_s k_s^T,
+//   w_s = e^{cum_end - cum_s} (gamma_s + scale_{s+1}).
 // MIMO expands every token into R rows (t, r) that share the token's decay
 // and rotation; SISO is R = 1. A chunk holds 64 such rows.
 //
-// Per chunk and (b, h), all contractions run as tcgen05.mma (kind::tf32):
+// Per chunk and (b, h), every contraction is a tcgen05.mma (kind::tf32):
 //   S    = Q K^T               [64 x 64],  K = N     (A, B in shared memory)
 //   Yo^T = G Q^T               [P  x 64],  K = N     (A = state G in TMEM)
 //   Yi^T = X^T (M o S)^T       [P  x 64],  K = 64    (decay/trapezoid mask M)
 //   G   += X^T (w K)           [P  x N],   K = 64    (after G *= e^{cum_end})
-// with the state G [P x N] resident in TMEM for the whole sequence and the
-// outputs produced transposed (TMEM lane = p), so the epilogue of one thread
-// owns one output column p: D skip, SiLU gate, the MIMO mimo_o contraction
-// over its R rows, and (through shared memory) the MIMO output RMS norm.
-// Rotary cos/sin, the local log-decay cumsum and the trapezoid weights are
-// formed by the CUDA cores while staging the operands; every operand is
-// rounded to TF32 with round-to-nearest.
+// The state G [P x N] stays in TMEM for the whole sequence; outputs come out
+// transposed (TMEM lane = p) so one thread owns one output column p for the
+// D skip, the SiLU gate, the MIMO mimo_o contraction over its R rows and
+// (through shared memory) the MIMO output RMS norm. Rotary cos/sin, the local
+// log-decay cumsum and the trapezoid weights are formed by the CUDA cores
+// while staging operands; every operand is rounded to TF32 (round to nearest).
 //
 // One CTA of 128 threads runs one (b, h) sequence chunk after chunk; thread 0
-// issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit
-// (bounded waits: on timeout the kernel records a status word and exits).
+// issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit.
+// Waits are bounded: on timeout the kernel records a status word and exits.
+// Shared memory (about 100 KB for P <= 64, N = 128: the tiles share three
+// regions whose contents change phase by phase) and TMEM (256 columns) admit
+// two CTAs per SM, and the next chunk's inputs are prefetched into L2 while
+// the current chunk runs.
 #include "m3_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -38,38 +42,39 @@ constexpr int kRows = 64;       // (token, rank) rows per chunk
 constexpr int kThreads = 128;
 constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
-
 struct ChunkLayout {
   int Npad, MP;
-  int q, k, kt, xt, p, cs, th, bias, tok, thbase;  // float offsets
+  int q, k, kt, tok, thbase;  // float offsets of the regions
   size_t bytes;
 };
 
-ChunkLayout chunk_layout(int N, int P, int A, int R) {
+int imax(int a, int b) { return a > b ? a : b; }
+
+ChunkLayout chunk_layout(int N, int P, int A) {
   ChunkLayout l;
   l.Npad = (N + 15) / 16 * 16;
   l.MP = P <= 64 ? 64 : 128;
   int off = 0;
   auto take = [&](int floats) {
     int o = off;
-    off += (floats + 31) / 32 * 32;  // 128-byte aligned
+    off += (floats + 31) / 32 * 32;  // 128-byte aligned regions
     return o;
   };
-  l.q = take(kRows * l.Npad);
-  l.k = take(kRows * (l.Npad > l.MP ? l.Npad : l.MP));  // also MIMO epilogue staging [Qt][MP]
-  l.kt = take(l.Npad * kRows);
-  l.xt = take(l.MP * kRows);
-  l.p = take(kRows * kRows);
-  l.cs = take(kRows * 2 * (A > 0 ? A : 1));
-  l.th = take(kRows * (A + 1));
-  l.bias = take(2 * R * l.Npad);
+  // Q region: q tile [64][Npad] until the first MMA batch completes, then the
+  // masked scores [64][64] followed by the values X^T [MP][64].
+  l.q = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
+  // K region: k tile [64][Npad]; MIMO norm staging [64][MP] in the epilogue.
+  l.k = take(kRows * imax(l.Npad, l.MP));
+  // Kt region: rotary angles [64][A + 1] while the q/k tiles are formed, then
+  // the w-scaled transposed keys [Npad][64].
+  l.kt = take(imax(l.Npad * kRows, kRows * (A + 1)));
   l.tok = take(8 * kTok);
   l.thbase = take(64);
   l.bytes = (size_t)off * sizeof(float);
   return l;
 }
 
-template <int MP>
+template <int MP, bool MIMO>
 __global__ void __launch_bounds__(kThreads, 1)
     k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, uint32_t* status) {
   extern __shared__ __align__(1024) float sm[];
@@ -84,15 +89,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int grp = h / (H / g.G);
 
-  float* sQ = sm + lay.q;    // [64 rows][Npad]   K-major, K = n
-  float* sK = sm + lay.k;    // [64 rows][Npad]   K-major, K = n
-  float* sKt = sm + lay.kt;  // [Npad][64 rows]   K-major, K = row  (w-scaled keys)
-  float* sXt = sm + lay.xt;  // [MP][64 rows]     K-major, K = row  (values)
-  float* sP = sm + lay.p;    // [64][64]          K-major           (masked scores)
-  float* sCS = sm + lay.cs;  // [Qt][A] (cos, sin)
-  float* sTh = sm + lay.th;  // [Qt][A + 1] angle increments
-  float* sBiasC = sm + lay.bias;
-  float* sBiasB = sBiasC + R * Npad;
+  float* sQ = sm + lay.q;              // [64 rows][Npad] K-major, K = n
+  float* sP = sQ;                      // [64][64]        masked scores (after batch 1)
+  float* sXt = sQ + kRows * kRows;     // [MP][64 rows]   values (after batch 1)
+  float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
+  float* sO = sK;                      // [Qt][MP]        MIMO epilogue staging
+  float* sTh = sm + lay.kt;            // [Qt][A + 1]     angles (phases 1-4a)
+  float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
   float* tAdt = sm + lay.tok;
   float* tCum = tAdt + kTok;
   float* tEc = tCum + kTok;   // e^{cum_t}
@@ -102,7 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* tOm = tW + kTok;     // e^{cum_end - cum_t} * tW[t]
   float* tDt = tOm + kTok;
   float* sThBase = sm + lay.thbase;
-  float* sO = sK;             // MIMO epilogue staging, reuses sK after its MMA
 
   if (tid == 0) {
     tc::bar_init(&bars[0], 1);
@@ -111,11 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
-  for (int i = tid; i < R * Npad; i += kThreads) {
-    const int r = i / Npad, n = i - r * Npad;
-    sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
-    sBiasB[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
-  }
   for (int i = tid; i < A; i += kThreads) sThBase[i] = 0.f;
   tc::fence_before();
   __syncthreads();
@@ -129,14 +126,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 16; ++i) zero[i] = 0.f;
     for (int c = 0; c < Npad; c += 16) tc::tmem_st16(tG + lane_base + c, zero);
   }
-  // row p of the transposed tiles held by this thread (TMEM data-path layout:
-  // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant)
+  // Row p of the transposed tiles held by this thread (TMEM data-path layout:
+  // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant).
   const int prow = (MP == 64) ? (lane < 16 ? 16 * warp + lane : -1) : 32 * warp + lane;
   const bool pvalid = prow >= 0 && prow < P;
-  const bool mimo = a.mimo_o != nullptr;
-  float mxr[8], mzr[8], mor[8];
+  constexpr bool mimo = MIMO;
+  constexpr int kRmax = MIMO ? 8 : 1;
+  float mxr[kRmax], mzr[kRmax], mor[kRmax];
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
+  for (int r = 0; r < kRmax; ++r) {
     const bool ok = mimo && pvalid && r < R;
     mxr[r] = ok ? a.mimo_x[((int64_t)h * R + r) * P + prow] : 1.f;
     mzr[r] = ok ? a.mimo_z[((int64_t)h * R + r) * P + prow] : 1.f;
@@ -146,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_S = tc::idesc_tf32(64, 64);
   const uint32_t id_Y = tc::idesc_tf32(MP, 64);
   const uint32_t id_D = tc::idesc_tf32(MP, Npad);
+  const bool pf_rows = (N % 4 == 0) && (P % 4 == 0);
+  const bool pf_tok = (H % 4 == 0) && (A % 4 == 0);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -153,8 +153,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it = 0;
   for (int c0 = 0; c0 < L; c0 += Qt, ++it) {
     const int tv = min(Qt, L - c0);
+    // (0) L2 prefetch of the next chunk's operands
+    {
+      const int n0 = c0 + Qt;
+      if (n0 < L) {
+        const int nv = min(Qt, L - n0);
+        if (pf_rows && tid < nv) {
+          const int64_t tok = (int64_t)b * L + n0 + tid;
+          const int64_t row = (tok * g.G * R + (int64_t)grp * R) * N;
+          tc::prefetch_l2(a.c + row, (uint32_t)(R * N * 4));
+          tc::prefetch_l2(a.b + row, (uint32_t)(R * N * 4));
+          tc::prefetch_l2(a.x + (tok * H + h) * P, (uint32_t)(P * 4));
+          tc::prefetch_l2(a.z + (tok * H + h) * P, (uint32_t)(P * 4));
+        }
+        if (pf_tok && tid == 64) {
+          const int64_t tok = (int64_t)b * L + n0;
+          tc::prefetch_l2(a.dt + tok * H, (uint32_t)(nv * H * 4));
+          tc::prefetch_l2(a.adt + tok * H, (uint32_t)(nv * H * 4));
+          tc::prefetch_l2(a.trap + tok * H, (uint32_t)(nv * H * 4));
+          if (A > 0) tc::prefetch_l2(a.angle + tok * A, (uint32_t)(nv * A * 4));
+        }
+      }
+    }
     // (1) per-token scalars of tokens c0 .. c0 + Qt (the last one is the next
-    // chunk's first token: only its trapezoid scale is used)
+    // chunk's first token: only its trapezoid scale is used); angle increments
     if (tid <= Qt) {
       const int t = tid;
       float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
@@ -179,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       sTh[t * (A + 1) + aa] = t < tv ? a.angle[((int64_t)b * L + c0 + t) * A + aa] : 0.f;
     }
     __syncthreads();
-    // (2) local cumulative log decay (warp 0, two tokens per lane)
+    // (2) local cumulative log decay (warp 0, two tokens per lane); rotary
+    // angle: per-angle scan of dt * angle over the chunk (in place)
     if (warp == 0) {
       const int t0 = 2 * lane, t1 = 2 * lane + 1;
       const float a0 = t0 < Qt ? tAdt[t0] : 0.f, a1 = t1 < Qt ? tAdt[t1] : 0.f;
@@ -193,7 +216,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t0 < Qt) tCum[t0] = ex + a0;
       if (t1 < Qt) tCum[t1] = ex + a0 + a1;
     }
-    // rotary angle: per-angle scan of dt * angle over the chunk, plus sin/cos
     for (int aa = warp; aa < A; aa += kThreads / 32) {
       float v0 = lane < Qt ? tDt[lane] * sTh[lane * (A + 1) + aa] : 0.f;
       float v1 = lane + 32 < Qt ? tDt[lane + 32] * sTh[(lane + 32) * (A + 1) + aa] : 0.f;
@@ -209,8 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       v1 += __shfl_sync(0xffffffffu, v0, 31);
       const float base = sThBase[aa];
       const float th0 = base + v0, th1 = base + v1;
-      if (lane < Qt) sincosf(th0, &sCS[(lane * A + aa) * 2 + 1], &sCS[(lane * A + aa) * 2]);
-      if (lane + 32 < Qt) sincosf(th1, &sCS[((lane + 32) * A + aa) * 2 + 1], &sCS[((lane + 32) * A + aa) * 2]);
+      __syncwarp();
+      if (lane < Qt) sTh[lane * (A + 1) + aa] = th0;
+      if (lane + 32 < Qt) sTh[(lane + 32) * (A + 1) + aa] = th1;
       const float last = __shfl_sync(0xffffffffu, Qt > 32 ? th1 : th0, Qt > 32 ? Qt - 33 : Qt - 1);
       __syncwarp();
       if (lane == 0) sThBase[aa] = last;
@@ -225,71 +248,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       tW[t] = w;
       tOm[t] = expf(cend - cum) * w;
     }
-    __syncthreads();
-    // (4) operand tiles: rotated q/k rows, w-scaled transposed keys, values
+    // (4a) rotated, biased q / k rows. Unit u of a row is the rotary pair
+    // (u, u + A) for u < A, else the single dim u + A. Lane l takes row
+    // 8 * block + l % 8 and unit 4 * ublock + l / 8, so that the 32 lanes of
+    // a store hit 32 distinct banks of the K-major tiles.
     {
-      const int NQ = Npad >> 2;
-      for (int i = tid; i < kRows * NQ; i += kThreads) {
-        const int quad = i / kRows, rho = i - quad * kRows;
+      const int U = N - A;
+      const int U4 = (U + 3) >> 2;
+      const int items = (kRows / 8) * U4 * 32;
+      for (int i = tid; i < items; i += kThreads) {
+        const int l = i & 31, blk = i >> 5;
+        const int rho = (blk / U4) * 8 + (l & 7);
+        const int u = (blk % U4) * 4 + (l >> 3);
+        if (u >= U) continue;
         const int t = rho / R, r = rho - t * R;
-        const int n0 = quad * 4;
-        float qv[4] = {0.f, 0.f, 0.f, 0.f}, kv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < tv) {
-          const int64_t rowoff =
-              (((int64_t)b * L + c0 + t) * g.G * R + (int64_t)grp * R + r) * (int64_t)N;
-          const float* cr = a.c + rowoff;
-          const float* br = a.b + rowoff;
-          const float* cb = sBiasC + r * Npad;
-          const float* bb = sBiasB + r * Npad;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int n = n0 + e;
-            if (n < N) {
-              if (n < A) {
-                const float cs = sCS[(t * A + n) * 2], sn = sCS[(t * A + n) * 2 + 1];
-                const float qu = cr[n] + cb[n], qw = cr[n + A] + cb[n + A];
-                const float ku = br[n] + bb[n], kw = br[n + A] + bb[n + A];
-                qv[e] = qu * cs - qw * sn;
-                kv[e] = ku * cs - kw * sn;
-              } else if (n < 2 * A) {
-                const int m = n - A;
-                const float cs = sCS[(t * A + m) * 2], sn = sCS[(t * A + m) * 2 + 1];
-                const float qu = cr[m] + cb[m], qw = cr[n] + cb[n];
-                const float ku = br[m] + bb[m], kw = br[n] + bb[n];
-                qv[e] = qu * sn + qw * cs;
-                kv[e] = ku * sn + kw * cs;
-              } else {
-                qv[e] = cr[n] + cb[n];
-                kv[e] = br[n] + bb[n];
-              }
-            }
+        const bool in = t < tv;
+        const int64_t rowoff =
+            (((int64_t)b * L + c0 + t) * g.G * R + (int64_t)grp * R + r) * (int64_t)N;
+        const float* cbias = a.c_bias + ((int64_t)h * R + r) * N;
+        const float* bbias = a.b_bias + ((int64_t)h * R + r) * N;
+        if (u < A) {
+          float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
+          if (in) {
+            float sn, cs;
+            sincosf(sTh[t * (A + 1) + u], &sn, &cs);
+            const float qu = a.c[rowoff + u] + cbias[u], qw = a.c[rowoff + u + A] + cbias[u + A];
+            const float ku = a.b[rowoff + u] + bbias[u], kw = a.b[rowoff + u + A] + bbias[u + A];
+            q0 = qu * cs - qw * sn;
+            q1 = qu * sn + qw * cs;
+            k0 = ku * cs - kw * sn;
+            k1 = ku * sn + kw * cs;
           }
-        }
-        const float om = t < tv ? tOm[t] : 0.f;
-        *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) =
-            make_float4(tc::to_tf32(qv[0]), tc::to_tf32(qv[1]), tc::to_tf32(qv[2]), tc::to_tf32(qv[3]));
-        *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) =
-            make_float4(tc::to_tf32(kv[0]), tc::to_tf32(kv[1]), tc::to_tf32(kv[2]), tc::to_tf32(kv[3]));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sKt[tc::kmaj(n0 + e, rho, kRows)] = tc::to_tf32(om * kv[e]);
-      }
-      const int PQ = MP >> 2;
-      for (int i = tid; i < kRows * PQ; i += kThreads) {
-        const int pq = i / kRows, rho = i - pq * kRows;
-        const int t = rho / R, r = rho - t * R;
-        const int p0 = pq * 4;
-        float xv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (t < tv) {
-          const float* xr = a.x + (((int64_t)b * L + c0 + t) * H + h) * P;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int p = p0 + e;
-            if (p < P) xv[e] = xr[p] * (mimo ? a.mimo_x[((int64_t)h * R + r) * P + p] : 1.f);
+          sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
+          sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
+          sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
+          sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
+        } else {
+          const int n = u + A;
+          float qv = 0.f, kv = 0.f;
+          if (in) {
+            qv = a.c[rowoff + n] + cbias[n];
+            kv = a.b[rowoff + n] + bbias[n];
           }
+          sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
+          sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sXt[tc::kmaj(p0 + e, rho, kRows)] = tc::to_tf32(xv[e]);
       }
+      // zero padding columns N .. Npad
+      for (int i = tid; i < kRows * (Npad - N); i += kThreads) {
+        const int rho = i / (Npad - N), n = N + i % (Npad - N);
+        sQ[tc::kmaj(rho, n, Npad)] = 0.f;
+        sK[tc::kmaj(rho, n, Npad)] = 0.f;
+      }
+    }
+    __syncthreads();
+    // (4b) w-scaled transposed keys Kt[n][row] = w_t * k[row][n] (from the
+    // TF32 k tile); lane l takes n = 8 * nblock + l % 8 and row
+    // rho = 4 * rblock + l / 8 (conflict-free scalar stores)
+    for (int i = tid; i < (Npad / 8) * (kRows / 4) * 32; i += kThreads) {
+      const int l = i & 31, blk = i >> 5;
+      const int n = (blk % (Npad / 8)) * 8 + (l & 7);
+      const int rho = (blk / (Npad / 8)) * 4 + (l >> 3);
+      const int t = rho / R;
+      const float kv = sK[tc::kmaj(rho, n, Npad)];
+      sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(t < tv ? tOm[t] * kv : 0.f);
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     __syncthreads();
     if (abort_flag) break;
-    // (6) masked scores P = M o S (rows of S: TMEM M = 64 layout), and G *= e^{cum_end}
+    // (6) masked scores P = M o S (rows of S: TMEM M = 64 layout), G *= e^{cum_end}
     {
       const int rho = 16 * warp + lane;
       const int t = rho / R;
@@ -331,6 +353,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(sP + tc::kmaj(rho, cb * 16 + 4 * u, kRows)) =
                 make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         }
+      }
+      // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pblock +
+      // l % 8 and row rho = 4 * rblock + l / 8 (conflict-free scalar stores)
+      for (int i = tid; i < (MP / 8) * (kRows / 4) * 32; i += kThreads) {
+        const int l = i & 31, blk = i >> 5;
+        const int p = (blk % (MP / 8)) * 8 + (l & 7);
+        const int rho2 = (blk / (MP / 8)) * 4 + (l >> 3);
+        const int t2 = rho2 / R, r2 = rho2 - t2 * R;
+        float xv = 0.f;
+        if (t2 < tv && p < P) {
+          xv = a.x[(((int64_t)b * L + c0 + t2) * H + h) * P + p];
+          if (mimo) xv *= a.mimo_x[((int64_t)h * R + r2) * P + p];
+        }
+        sXt[tc::kmaj(p, rho2, kRows)] = tc::to_tf32(xv);
       }
       const float ec = expf(tCum[Qt - 1]);
       for (int c = 0; c < Npad; c += 16) {
@@ -364,13 +400,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld16(tS + lane_base + cb * 16, yi);
       if (!pvalid) continue;
       if (!mimo) {
-#pragma unroll 4
+        float xv[16], zv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t = cb * 16 + j;
+          const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
+          xv[j] = t < tv ? a.x[off] : 0.f;
+          zv[j] = (t < tv && g.has_z) ? a.z[off] : 0.f;
+        }
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int t = cb * 16 + j;
           if (t < tv) {
             const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
-            float y = tEc[t] * yo[j] + yi[j] + dsk * a.x[off];
-            if (g.has_z) y *= silu_f(a.z[off]);
+            float y = tEc[t] * yo[j] + yi[j] + dsk * xv[j];
+            if (g.has_z) y *= silu_f(zv[j]);
             a.out[off] = y;
           }
         }
@@ -384,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float zv = a.z[off];
           float o = 0.f;
 #pragma unroll
-          for (int r = 0; r < 8; ++r) {
+          for (int r = 0; r < kRmax; ++r) {
             if (r < R) {
               const int j = tt * R + r;
               float y = tEc[t] * yo[j] + yi[j] + dsk * xv * mxr[r];
@@ -429,20 +473,22 @@ bool chunk_supported(const ScanGeom& g) {
 
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
                               cudaStream_t s) {
-  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
+  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A);
   const unsigned grid = (unsigned)(g.B * g.H);
+  const bool mimo = a.mimo_o != nullptr;
+  auto run = [&](auto kernel) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)lay.bytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
+    return cudaSuccess;
+  };
   cudaError_t e;
-  if (lay.MP == 64) {
-    e = cudaFuncSetAttribute(k_scan_chunk<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)lay.bytes);
-    if (e != cudaSuccess) return e;
-    k_scan_chunk<64><<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
-  } else {
-    e = cudaFuncSetAttribute(k_scan_chunk<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)lay.bytes);
-    if (e != cudaSuccess) return e;
-    k_scan_chunk<128><<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
-  }
+  if (lay.MP == 64)
+    e = mimo ? run(k_scan_chunk<64, true>) : run(k_scan_chunk<64, false>);
+  else
+    e = mimo ? run(k_scan_chunk<128, true>) : run(k_scan_chunk<128, false>);
+  if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
 }
