@@ -19,11 +19,12 @@
 //   Yi^T = X^T (M o S)^T       [P  x 64],  K = 64    (decay/trapezoid mask M)
 //   G   += X^T (w K)           [P  x N],   K = 64    (after G *= e^{cum_end})
 // The state G [P x N] stays in TMEM for the whole sequence; outputs come out
-// transposed (TMEM lane = p) so one thread owns one output column p for the
-// D skip, the SiLU gate, the MIMO mimo_o contraction over its R rows and
-// (through shared memory) the MIMO output RMS norm. Rotary cos/sin, the local
-// log-decay cumsum and the trapezoid weights are formed by the CUDA cores
-// while staging operands; every operand is rounded to TF32 (round to nearest).
+// transposed (TMEM lane = p): each output column p is finished by the two
+// lanes that share its TMEM row (D skip, SiLU gate, the MIMO mimo_o
+// contraction over its R rows) and, through shared memory, the MIMO output
+// RMS norm. Rotary cos/sin, the local log-decay cumsum and the trapezoid
+// weights are formed by the CUDA cores while staging operands; every operand
+// is rounded to TF32 (round to nearest).
 //
 // One CTA of 128 threads runs one (b, h) sequence chunk after chunk; thread 0
 // issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit.
@@ -40,8 +41,10 @@ namespace {
 
 constexpr int kRows = 64;       // (token, rank) rows per chunk
 constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
 constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
+
 struct ChunkLayout {
   int Npad, MP;
   int q, k, kt, tok, thbase;  // float offsets of the regions
@@ -65,14 +68,18 @@ ChunkLayout chunk_layout(int N, int P, int A) {
   l.q = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
   // K region: k tile [64][Npad]; MIMO norm staging [64][MP] in the epilogue.
   l.k = take(kRows * imax(l.Npad, l.MP));
-  // Kt region: rotary angles [64][A + 1] while the q/k tiles are formed, then
-  // the w-scaled transposed keys [Npad][64].
-  l.kt = take(imax(l.Npad * kRows, kRows * (A + 1)));
+  // Kt region: rotary cos / sin tables [64][A + 1] each while the q/k tiles
+  // are formed, then the w-scaled transposed keys [Npad][64].
+  l.kt = take(imax(l.Npad * kRows, 2 * kRows * (A + 1)));
   l.tok = take(8 * kTok);
   l.thbase = take(64);
   l.bytes = (size_t)off * sizeof(float);
   return l;
 }
+
+// SiLU with the hardware exp / divide approximations (relative error a few
+// float32 ulps, far inside the scan tolerances).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 template <int MP, bool MIMO>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -84,17 +91,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = g.H, L = g.L, P = g.P, N = g.N, A = g.A, R = g.R;
+  const int lgR = __ffs(R) - 1;  // R is a power of two here
   const int Npad = lay.Npad;
-  const int Qt = kRows / R;  // tokens per chunk
+  const int Qt = kRows >> lgR;  // tokens per chunk
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int grp = h / (H / g.G);
+  const int RG = g.G * R;
 
   float* sQ = sm + lay.q;              // [64 rows][Npad] K-major, K = n
   float* sP = sQ;                      // [64][64]        masked scores (after batch 1)
   float* sXt = sQ + kRows * kRows;     // [MP][64 rows]   values (after batch 1)
   float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
   float* sO = sK;                      // [Qt][MP]        MIMO epilogue staging
-  float* sTh = sm + lay.kt;            // [Qt][A + 1]     angles (phases 1-4a)
+  float* sCos = sm + lay.kt;           // [Qt][A + 1]     angle increments, then cos
+  float* sSin = sCos + kRows * (A + 1);  // [Qt][A + 1]   sin
   float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
   float* tAdt = sm + lay.tok;
   float* tCum = tAdt + kTok;
@@ -126,10 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 16; ++i) zero[i] = 0.f;
     for (int c = 0; c < Npad; c += 16) tc::tmem_st16(tG + lane_base + c, zero);
   }
-  // Row p of the transposed tiles held by this thread (TMEM data-path layout:
-  // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant).
-  const int prow = (MP == 64) ? (lane < 16 ? 16 * warp + lane : -1) : 32 * warp + lane;
-  const bool pvalid = prow >= 0 && prow < P;
+  // Row p of the transposed tiles handled by this thread (TMEM data path:
+  // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant, and
+  // lane l + 16 shares the row of lane l, taking the upper half of the columns).
+  const int half = (MP == 64) ? (lane >> 4) : 0;
+  const int prow = (MP == 64) ? 16 * warp + (lane & 15) : 32 * warp + lane;
+  const bool pvalid = prow < P;
   constexpr bool mimo = MIMO;
   constexpr int kRmax = MIMO ? 8 : 1;
   float mxr[kRmax], mzr[kRmax], mor[kRmax];
@@ -146,6 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t id_D = tc::idesc_tf32(MP, Npad);
   const bool pf_rows = (N % 4 == 0) && (P % 4 == 0);
   const bool pf_tok = (H % 4 == 0) && (A % 4 == 0);
+  const int64_t HP = (int64_t)H * P;
+  const float* cbias_h = a.c_bias + (int64_t)h * R * N;
+  const float* bbias_h = a.b_bias + (int64_t)h * R * N;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -153,26 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   int it = 0;
   for (int c0 = 0; c0 < L; c0 += Qt, ++it) {
     const int tv = min(Qt, L - c0);
+    const int64_t tok0 = (int64_t)b * L + c0;   // first token of the chunk in [B, L]
     // (0) L2 prefetch of the next chunk's operands
-    {
-      const int n0 = c0 + Qt;
-      if (n0 < L) {
-        const int nv = min(Qt, L - n0);
-        if (pf_rows && tid < nv) {
-          const int64_t tok = (int64_t)b * L + n0 + tid;
-          const int64_t row = (tok * g.G * R + (int64_t)grp * R) * N;
-          tc::prefetch_l2(a.c + row, (uint32_t)(R * N * 4));
-          tc::prefetch_l2(a.b + row, (uint32_t)(R * N * 4));
-          tc::prefetch_l2(a.x + (tok * H + h) * P, (uint32_t)(P * 4));
-          tc::prefetch_l2(a.z + (tok * H + h) * P, (uint32_t)(P * 4));
-        }
-        if (pf_tok && tid == 64) {
-          const int64_t tok = (int64_t)b * L + n0;
-          tc::prefetch_l2(a.dt + tok * H, (uint32_t)(nv * H * 4));
-          tc::prefetch_l2(a.adt + tok * H, (uint32_t)(nv * H * 4));
-          tc::prefetch_l2(a.trap + tok * H, (uint32_t)(nv * H * 4));
-          if (A > 0) tc::prefetch_l2(a.angle + tok * A, (uint32_t)(nv * A * 4));
-        }
+    if (c0 + Qt < L) {
+      const int nv = min(Qt, L - c0 - Qt);
+      const int64_t ntok = tok0 + Qt;
+      if (pf_rows && tid < nv) {
+        const int64_t tok = ntok + tid;
+        const int64_t row = (tok * RG + (int64_t)grp * R) * N;
+        tc::prefetch_l2(a.c + row, (uint32_t)(R * N * 4));
+        tc::prefetch_l2(a.b + row, (uint32_t)(R * N * 4));
+        tc::prefetch_l2(a.x + tok * HP + (int64_t)h * P, (uint32_t)(P * 4));
+        tc::prefetch_l2(a.z + tok * HP + (int64_t)h * P, (uint32_t)(P * 4));
+      }
+      if (pf_tok && tid == 64) {
+        tc::prefetch_l2(a.dt + ntok * H, (uint32_t)(nv * H * 4));
+        tc::prefetch_l2(a.adt + ntok * H, (uint32_t)(nv * H * 4));
+        tc::prefetch_l2(a.trap + ntok * H, (uint32_t)(nv * H * 4));
+        if (A > 0) tc::prefetch_l2(a.angle + ntok * A, (uint32_t)(nv * A * 4));
       }
     }
     // (1) per-token scalars of tokens c0 .. c0 + Qt (the last one is the next
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = tid;
       float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
       if (c0 + t < L) {
-        const int64_t sc = ((int64_t)b * L + c0 + t) * H + h;
+        const int64_t sc = (tok0 + t) * H + h;
         dtv = a.dt[sc];
         adtv = a.adt[sc];
         const float lam = sigmoid_f(a.trap[sc]);
@@ -196,13 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tDt[t] = in ? dtv : 0.f;
       }
     }
-    for (int i = tid; i < Qt * A; i += kThreads) {
-      const int t = i / A, aa = i - t * A;
-      sTh[t * (A + 1) + aa] = t < tv ? a.angle[((int64_t)b * L + c0 + t) * A + aa] : 0.f;
-    }
+    for (int t = warp; t < Qt; t += kWarps)
+      for (int aa = lane; aa < A; aa += 32)
+        sCos[t * (A + 1) + aa] = t < tv ? a.angle[(tok0 + t) * A + aa] : 0.f;
     __syncthreads();
     // (2) local cumulative log decay (warp 0, two tokens per lane); rotary
-    // angle: per-angle scan of dt * angle over the chunk (in place)
+    // angle: per-angle scan of dt * angle over the chunk, then cos / sin of
+    // each (token, angle) once
     if (warp == 0) {
       const int t0 = 2 * lane, t1 = 2 * lane + 1;
       const float a0 = t0 < Qt ? tAdt[t0] : 0.f, a1 = t1 < Qt ? tAdt[t1] : 0.f;
@@ -216,9 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t0 < Qt) tCum[t0] = ex + a0;
       if (t1 < Qt) tCum[t1] = ex + a0 + a1;
     }
-    for (int aa = warp; aa < A; aa += kThreads / 32) {
-      float v0 = lane < Qt ? tDt[lane] * sTh[lane * (A + 1) + aa] : 0.f;
-      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sTh[(lane + 32) * (A + 1) + aa] : 0.f;
+    for (int aa = warp; aa < A; aa += kWarps) {
+      float v0 = lane < Qt ? tDt[lane] * sCos[lane * (A + 1) + aa] : 0.f;
+      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sCos[(lane + 32) * (A + 1) + aa] : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float u0 = __shfl_up_sync(0xffffffffu, v0, o);
@@ -231,10 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       v1 += __shfl_sync(0xffffffffu, v0, 31);
       const float base = sThBase[aa];
       const float th0 = base + v0, th1 = base + v1;
-      __syncwarp();
-      if (lane < Qt) sTh[lane * (A + 1) + aa] = th0;
-      if (lane + 32 < Qt) sTh[(lane + 32) * (A + 1) + aa] = th1;
       const float last = __shfl_sync(0xffffffffu, Qt > 32 ? th1 : th0, Qt > 32 ? Qt - 33 : Qt - 1);
+      if (lane < Qt) sincosf(th0, &sSin[lane * (A + 1) + aa], &sCos[lane * (A + 1) + aa]);
+      if (lane + 32 < Qt)
+        sincosf(th1, &sSin[(lane + 32) * (A + 1) + aa], &sCos[(lane + 32) * (A + 1) + aa]);
       __syncwarp();
       if (lane == 0) sThBase[aa] = last;
     }
@@ -250,48 +263,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // (4a) rotated, biased q / k rows. Unit u of a row is the rotary pair
     // (u, u + A) for u < A, else the single dim u + A. Lane l takes row
-    // 8 * block + l % 8 and unit 4 * ublock + l / 8, so that the 32 lanes of
-    // a store hit 32 distinct banks of the K-major tiles.
+    // 8 * rb + l % 8 and unit 4 * ub + l / 8, so that the 32 lanes of a store
+    // hit 32 distinct banks of the K-major tiles.
     {
       const int U = N - A;
       const int U4 = (U + 3) >> 2;
-      const int items = (kRows / 8) * U4 * 32;
-      for (int i = tid; i < items; i += kThreads) {
-        const int l = i & 31, blk = i >> 5;
-        const int rho = (blk / U4) * 8 + (l & 7);
-        const int u = (blk % U4) * 4 + (l >> 3);
-        if (u >= U) continue;
-        const int t = rho / R, r = rho - t * R;
+      const int rl = lane & 7, ul = lane >> 3;
+      for (int rb = 0; rb < kRows / 8; ++rb) {
+        const int rho = 8 * rb + rl;
+        const int t = rho >> lgR, r = rho & (R - 1);
         const bool in = t < tv;
-        const int64_t rowoff =
-            (((int64_t)b * L + c0 + t) * g.G * R + (int64_t)grp * R + r) * (int64_t)N;
-        const float* cbias = a.c_bias + ((int64_t)h * R + r) * N;
-        const float* bbias = a.b_bias + ((int64_t)h * R + r) * N;
-        if (u < A) {
-          float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
-          if (in) {
-            float sn, cs;
-            sincosf(sTh[t * (A + 1) + u], &sn, &cs);
-            const float qu = a.c[rowoff + u] + cbias[u], qw = a.c[rowoff + u + A] + cbias[u + A];
-            const float ku = a.b[rowoff + u] + bbias[u], kw = a.b[rowoff + u + A] + bbias[u + A];
-            q0 = qu * cs - qw * sn;
-            q1 = qu * sn + qw * cs;
-            k0 = ku * cs - kw * sn;
-            k1 = ku * sn + kw * cs;
+        const float* crow = a.c + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+        const float* brow = a.b + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+        const float* cb = cbias_h + r * N;
+        const float* bb = bbias_h + r * N;
+        const float* cst = sCos + t * (A + 1);
+        const float* snt = sSin + t * (A + 1);
+        for (int ub = warp; ub < U4; ub += kWarps) {
+          const int u = 4 * ub + ul;
+          if (u >= U) continue;
+          if (u < A) {
+            float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
+            if (in) {
+              const float cs = cst[u], sn = snt[u];
+              const float qu = crow[u] + cb[u], qw = crow[u + A] + cb[u + A];
+              const float ku = brow[u] + bb[u], kw = brow[u + A] + bb[u + A];
+              q0 = qu * cs - qw * sn;
+              q1 = qu * sn + qw * cs;
+              k0 = ku * cs - kw * sn;
+              k1 = ku * sn + kw * cs;
+            }
+            sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
+            sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
+            sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
+            sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
+          } else {
+            const int n = u + A;
+            float qv = 0.f, kv = 0.f;
+            if (in) {
+              qv = crow[n] + cb[n];
+              kv = brow[n] + bb[n];
+            }
+            sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
+            sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
           }
-          sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
-          sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
-          sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
-          sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
-        } else {
-          const int n = u + A;
-          float qv = 0.f, kv = 0.f;
-          if (in) {
-            qv = a.c[rowoff + n] + cbias[n];
-            kv = a.b[rowoff + n] + bbias[n];
-          }
-          sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
-          sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
         }
       }
       // zero padding columns N .. Npad
@@ -303,15 +318,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     // (4b) w-scaled transposed keys Kt[n][row] = w_t * k[row][n] (from the
-    // TF32 k tile); lane l takes n = 8 * nblock + l % 8 and row
-    // rho = 4 * rblock + l / 8 (conflict-free scalar stores)
-    for (int i = tid; i < (Npad / 8) * (kRows / 4) * 32; i += kThreads) {
-      const int l = i & 31, blk = i >> 5;
-      const int n = (blk % (Npad / 8)) * 8 + (l & 7);
-      const int rho = (blk / (Npad / 8)) * 4 + (l >> 3);
-      const int t = rho / R;
-      const float kv = sK[tc::kmaj(rho, n, Npad)];
-      sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(t < tv ? tOm[t] * kv : 0.f);
+    // TF32 k tile); lane l takes n = 8 * nb + l % 8 and row 4 * rb + l / 8
+    // (conflict-free scalar stores)
+    {
+      const int nl = lane & 7, rl = lane >> 3;
+      for (int rb = warp; rb < kRows / 4; rb += kWarps) {
+        const int rho = 4 * rb + rl;
+        const int t = rho >> lgR;
+        const float om = t < tv ? tOm[t] : 0.f;
+        for (int nb = 0; nb < Npad / 8; ++nb) {
+          const int n = 8 * nb + nl;
+          sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(om * sK[tc::kmaj(rho, n, Npad)]);
+        }
+      }
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -329,44 +348,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     __syncthreads();
     if (abort_flag) break;
-    // (6) masked scores P = M o S (rows of S: TMEM M = 64 layout), G *= e^{cum_end}
+    // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
+    // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
+    // block of row l), values X^T, and G *= e^{cum_end}
     {
-      const int rho = 16 * warp + lane;
-      const int t = rho / R;
-      const float cum_t = lane < 16 ? tCum[t] : 0.f;
+      const int rho = 16 * warp + (lane & 15);
+      const int t = rho >> lgR;
+      const float cum_t = tCum[t];
+      const float gam_t = tGam[t];
+      const int sh = lane >> 4;
       for (int cb = 0; cb < 4; ++cb) {
         float v[16];
         tc::tmem_ld16(tS + lane_base + cb * 16, v);
-        if (lane < 16) {
+        float w8[8];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int s = (cb * 16 + j) / R;
-            float m = 0.f;
-            if (s < t)
-              m = __expf(cum_t - tCum[s]) * tW[s];
-            else if (s == t)
-              m = tGam[t];
-            v[j] = tc::to_tf32(v[j] * m);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<float4*>(sP + tc::kmaj(rho, cb * 16 + 4 * u, kRows)) =
-                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        for (int j = 0; j < 8; ++j) {
+          const float hi = __shfl_sync(0xffffffffu, v[j + 8], lane & 15);
+          w8[j] = sh ? hi : v[j];
         }
+        const int col0 = cb * 16 + 8 * sh;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int s = (col0 + j) >> lgR;
+          float m = 0.f;
+          if (s < t)
+            m = __expf(cum_t - tCum[s]) * tW[s];
+          else if (s == t)
+            m = gam_t;
+          w8[j] = tc::to_tf32(w8[j] * m);
+        }
+        *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0, kRows)) =
+            make_float4(w8[0], w8[1], w8[2], w8[3]);
+        *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0 + 4, kRows)) =
+            make_float4(w8[4], w8[5], w8[6], w8[7]);
       }
-      // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pblock +
-      // l % 8 and row rho = 4 * rblock + l / 8 (conflict-free scalar stores)
-      for (int i = tid; i < (MP / 8) * (kRows / 4) * 32; i += kThreads) {
-        const int l = i & 31, blk = i >> 5;
-        const int p = (blk % (MP / 8)) * 8 + (l & 7);
-        const int rho2 = (blk / (MP / 8)) * 4 + (l >> 3);
-        const int t2 = rho2 / R, r2 = rho2 - t2 * R;
-        float xv = 0.f;
-        if (t2 < tv && p < P) {
-          xv = a.x[(((int64_t)b * L + c0 + t2) * H + h) * P + p];
-          if (mimo) xv *= a.mimo_x[((int64_t)h * R + r2) * P + p];
+      // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pb +
+      // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores)
+      {
+        const int pl = lane & 7, rl = lane >> 3;
+        for (int rb = warp; rb < kRows / 4; rb += kWarps) {
+          const int rho2 = 4 * rb + rl;
+          const int t2 = rho2 >> lgR, r2 = rho2 & (R - 1);
+          const bool in = t2 < tv;
+          const float* xrow = a.x + (tok0 + t2) * HP + (int64_t)h * P;
+          const float* mx = mimo ? a.mimo_x + ((int64_t)h * R + r2) * P : nullptr;
+          for (int pb = 0; pb < MP / 8; ++pb) {
+            const int p = 8 * pb + pl;
+            float xv = 0.f;
+            if (in && p < P) {
+              xv = xrow[p];
+              if (mimo) xv *= mx[p];
+            }
+            sXt[tc::kmaj(p, rho2, kRows)] = tc::to_tf32(xv);
+          }
         }
-        sXt[tc::kmaj(p, rho2, kRows)] = tc::to_tf32(xv);
       }
       const float ec = expf(tCum[Qt - 1]);
       for (int c = 0; c < Npad; c += 16) {
@@ -393,66 +428,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     __syncthreads();
     if (abort_flag) break;
-    // (8) epilogue: column p of the outputs of this chunk
-    for (int cb = 0; cb < 4; ++cb) {
-      float yo[16], yi[16];
-      tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
-      tc::tmem_ld16(tS + lane_base + cb * 16, yi);
-      if (!pvalid) continue;
-      if (!mimo) {
-        float xv[16], zv[16];
+    // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
+    // two lanes of a row split each 16-column block into 8 + 8 columns.
+    {
+      constexpr int kCols = (MP == 64) ? 8 : 16;
+      const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
+      const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+      float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
+      for (int cb = 0; cb < 4; ++cb) {
+        float yo[16], yi[16];
+        tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
+        tc::tmem_ld16(tS + lane_base + cb * 16, yi);
+        if (MP == 64) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = cb * 16 + j;
-          const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
-          xv[j] = t < tv ? a.x[off] : 0.f;
-          zv[j] = (t < tv && g.has_z) ? a.z[off] : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = cb * 16 + j;
-          if (t < tv) {
-            const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
-            float y = tEc[t] * yo[j] + yi[j] + dsk * xv[j];
-            if (g.has_z) y *= silu_f(zv[j]);
-            a.out[off] = y;
-          }
-        }
-      } else {
-        const int tpb = 16 / R;  // tokens per 16-column block
-        for (int tt = 0; tt < tpb; ++tt) {
-          const int t = cb * tpb + tt;
-          if (t >= tv) break;
-          const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P + prow;
-          const float xv = a.x[off];
-          const float zv = a.z[off];
-          float o = 0.f;
-#pragma unroll
-          for (int r = 0; r < kRmax; ++r) {
-            if (r < R) {
-              const int j = tt * R + r;
-              float y = tEc[t] * yo[j] + yi[j] + dsk * xv * mxr[r];
-              if (g.has_z) y *= silu_f(zv * mzr[r]);
-              o += mor[r] * y;
+          for (int j = 0; j < 8; ++j) {
+            const float ho = __shfl_sync(0xffffffffu, yo[j + 8], lane & 15);
+            const float hi = __shfl_sync(0xffffffffu, yi[j + 8], lane & 15);
+            if (half) {
+              yo[j] = ho;
+              yi[j] = hi;
             }
           }
-          if (g.has_norm)
-            sO[t * MP + prow] = o;
-          else
-            a.out[off] = o;
+        }
+        if (!pvalid) continue;
+        const int col0 = cb * 16 + 8 * half;
+        if (!mimo) {
+          float xv[kCols], zv[kCols];
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            const int t = col0 + j;
+            xv[j] = t < tv ? xcol[t * HP] : 0.f;
+            zv[j] = (t < tv && g.has_z) ? zcol[t * HP] : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            const int t = col0 + j;
+            if (t < tv) {
+              float y = tEc[t] * yo[j] + yi[j] + dsk * xv[j];
+              if (g.has_z) y *= silu_fast(zv[j]);
+              ocol[t * HP] = y;
+            }
+          }
+        } else {
+          const int tpb = kCols >> lgR;  // whole tokens in this lane's columns
+          for (int tt = 0; tt < tpb; ++tt) {
+            const int t = (col0 >> lgR) + tt;
+            if (t >= tv) break;
+            const float xv = xcol[t * HP];
+            const float zv = g.has_z ? zcol[t * HP] : 0.f;
+            const float ec = tEc[t];
+            float o = 0.f;
+#pragma unroll
+            for (int r = 0; r < kRmax; ++r) {
+              if (r < R) {
+                const int j = (tt << lgR) + r;
+                float y = ec * yo[j] + yi[j] + dsk * xv * mxr[r];
+                if (g.has_z) y *= silu_fast(zv * mzr[r]);
+                o += mor[r] * y;
+              }
+            }
+            if (g.has_norm)
+              sO[t * MP + prow] = o;
+            else
+              ocol[t * HP] = o;
+          }
         }
       }
     }
     if (mimo && g.has_norm) {
       __syncthreads();
-      for (int t = warp; t < tv; t += kThreads / 32) {
+      for (int t = warp; t < tv; t += kWarps) {
         float ss = 0.f;
         for (int p = lane; p < P; p += 32) ss += sO[t * MP + p] * sO[t * MP + p];
         ss = warp_sum(ss);
         const float inv = 1.0f / sqrtf(ss / (float)P + 1.0e-5f);
-        const int64_t off = (((int64_t)b * L + c0 + t) * H + h) * P;
+        float* orow = a.out + (tok0 + t) * HP + (int64_t)h * P;
         for (int p = lane; p < P; p += 32)
-          a.out[off + p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
+          orow[p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
       }
     }
     tc::fence_before();
