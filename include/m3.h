@@ -141,6 +141,29 @@ int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     void* workspace, size_t workspace_bytes, m3_stream_t stream);
 
 /*
+ * m3_siso_forward_static - m3_siso_forward without a workspace argument, for
+ * callers that cannot allocate device memory (code running inside a host that
+ * owns every device allocation, such as a framework plugin or an inference
+ * runtime with its own pool, or a latency-critical loop where a cudaMalloc
+ * would synchronize the device). The source pages have no counterpart: this
+ * entry point belongs to this library's C ABI only.
+ *
+ * Operands, checks and results are those of m3_siso_forward. The scratch the
+ * scan needs comes from a fixed 1 MiB array in the library's device image
+ * (held by every GPU that loads the library until the process exits); this
+ * call allocates nothing. Geometries whose m3_siso_forward_workspace() size
+ * exceeds 1 MiB are rejected with M3_ERR_WORKSPACE. The first call on a device
+ * looks up the array's device address with cudaGetSymbolAddress (with that
+ * device current); make that first call before any stream capture. All calls
+ * on a device share the array: calls that overlap on the GPU race and must not
+ * be issued; each call clears what must start at zero.
+ */
+int m3_siso_forward_static(const m3_ssm_config* cfg, const float* c, const float* b,
+                           const float* x, const float* z, const float* adt, const float* dt,
+                           const float* trap, const float* angle, const float* c_bias,
+                           const float* b_bias, const float* d, float* out, m3_stream_t stream);
+
+/*
  * m3_siso_step - advance one SISO token and update four recurrent states in
  * place (`mamba3_siso_step`). cfg->sequence_length must be 1; operands are the
  * length-one forms of m3_siso_forward. States (read, then overwritten):

@@ -25,6 +25,7 @@ M3_MATH_FP32 = 0
 M3_MATH_TF32 = 1
 
 EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
+            "m3_siso_forward_static",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_status_string", "m3_launch_count")
 
@@ -88,6 +89,7 @@ def load_library():
         lib.m3_mimo_forward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_forward.argtypes = [cfgp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_forward.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+        lib.m3_siso_forward_static.argtypes = [cfgp] + [_vp] * 12 + [_vp]
         lib.m3_siso_step.argtypes = [cfgp] + [_vp] * 16 + [_vp]
         lib.m3_mimo_step.argtypes = [cfgp] + [_vp] * 20 + [_vp]
         lib.m3_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
@@ -166,6 +168,15 @@ def m3_siso_forward(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_
     _check(load_library().m3_siso_forward(ctypes.byref(cfg), *[_ptr(t) for t in (
         c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, out)], wp, wn, _stream(stream)),
         "m3_siso_forward")
+
+
+def m3_siso_forward_static(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+                           out, stream=None):
+    """m3_siso_forward without a workspace: the library's fixed device scratch
+    array is used instead (for callers that cannot allocate device memory)."""
+    _check(load_library().m3_siso_forward_static(ctypes.byref(cfg), *[_ptr(t) for t in (
+        c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, out)], _stream(stream)),
+        "m3_siso_forward_static")
 
 
 def m3_mimo_forward(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,
