@@ -46,17 +46,18 @@ constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
 
 struct ChunkLayout {
-  int Npad, MP;
-  int q, k, kt, tok, thbase;  // float offsets of the regions
+  int Npad, MP, CS;
+  int q, k, kt, bias, tok, thbase;  // float offsets of the regions
   size_t bytes;
 };
 
 int imax(int a, int b) { return a > b ? a : b; }
 
-ChunkLayout chunk_layout(int N, int P, int A) {
+ChunkLayout chunk_layout(int N, int P, int A, int R) {
   ChunkLayout l;
   l.Npad = (N + 15) / 16 * 16;
   l.MP = P <= 64 ? 64 : 128;
+  l.CS = (A + 4) & ~3;  // cos / sin table row stride (16-byte rows, A + 1 <= CS)
   int off = 0;
   auto take = [&](int floats) {
     int o = off;
@@ -68,13 +69,29 @@ ChunkLayout chunk_layout(int N, int P, int A) {
   l.q = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
   // K region: k tile [64][Npad]; MIMO norm staging [64][MP] in the epilogue.
   l.k = take(kRows * imax(l.Npad, l.MP));
-  // Kt region: rotary cos / sin tables [64][A + 1] each while the q/k tiles
-  // are formed, then the w-scaled transposed keys [Npad][64].
-  l.kt = take(imax(l.Npad * kRows, 2 * kRows * (A + 1)));
+  // Kt region: rotary angle increments, then cos / sin tables [64][CS] each
+  // while the q/k tiles are formed, then the w-scaled transposed keys [Npad][64].
+  l.kt = take(imax(l.Npad * kRows, 2 * kRows * l.CS));
+  l.bias = take(2 * R * l.Npad);  // c_bias, b_bias of this head, zero-padded
   l.tok = take(8 * kTok);
   l.thbase = take(64);
   l.bytes = (size_t)off * sizeof(float);
   return l;
+}
+
+// sin and cos of v: Cody-Waite reduction by 2 pi (2 pi split into its float
+// value and the float remainder), then the SFU sine / cosine on [-pi, pi]
+// (absolute error about 2^-21). Arguments beyond 2^15 take sincosf.
+__device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
+  if (fabsf(v) > 32768.0f) {
+    sincosf(v, s, c);
+    return;
+  }
+  const float k = rintf(v * 0.159154943f);
+  float r = fmaf(-k, 6.28318548f, v);
+  r = fmaf(-k, -1.74845553e-7f, r);
+  *s = __sinf(r);
+  *c = __cosf(r);
 }
 
 // SiLU with the hardware exp / divide approximations (relative error a few
@@ -103,8 +120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sXt = sQ + kRows * kRows;     // [MP][64 rows]   values (after batch 1)
   float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
   float* sO = sK;                      // [Qt][MP]        MIMO epilogue staging
-  float* sCos = sm + lay.kt;           // [Qt][A + 1]     angle increments, then cos
-  float* sSin = sCos + kRows * (A + 1);  // [Qt][A + 1]   sin
+  const int CS = lay.CS;
+  float* sCos = sm + lay.kt;           // [Qt][CS]        angle increments, then cos
+  float* sSin = sCos + kRows * CS;     // [Qt][CS]        sin
+  float* sBiasC = sm + lay.bias;       // [R][Npad]
+  float* sBiasB = sBiasC + R * Npad;   // [R][Npad]
   float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
   float* tAdt = sm + lay.tok;
   float* tCum = tAdt + kTok;
@@ -124,6 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
   for (int i = tid; i < A; i += kThreads) sThBase[i] = 0.f;
+  for (int i = tid; i < R * Npad; i += kThreads) {
+    const int r = i / Npad, n = i - r * Npad;
+    sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
+    sBiasB[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
+  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -159,8 +184,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool pf_rows = (N % 4 == 0) && (P % 4 == 0);
   const bool pf_tok = (H % 4 == 0) && (A % 4 == 0);
   const int64_t HP = (int64_t)H * P;
-  const float* cbias_h = a.c_bias + (int64_t)h * R * N;
-  const float* bbias_h = a.b_bias + (int64_t)h * R * N;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -211,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = warp; t < Qt; t += kWarps)
       for (int aa = lane; aa < A; aa += 32)
-        sCos[t * (A + 1) + aa] = t < tv ? a.angle[(tok0 + t) * A + aa] : 0.f;
+        sCos[t * CS + aa] = t < tv ? a.angle[(tok0 + t) * A + aa] : 0.f;
     __syncthreads();
     // (2) local cumulative log decay (warp 0, two tokens per lane); rotary
     // angle: per-angle scan of dt * angle over the chunk, then cos / sin of
@@ -230,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t1 < Qt) tCum[t1] = ex + a0 + a1;
     }
     for (int aa = warp; aa < A; aa += kWarps) {
-      float v0 = lane < Qt ? tDt[lane] * sCos[lane * (A + 1) + aa] : 0.f;
-      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sCos[(lane + 32) * (A + 1) + aa] : 0.f;
+      float v0 = lane < Qt ? tDt[lane] * sCos[lane * CS + aa] : 0.f;
+      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sCos[(lane + 32) * CS + aa] : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float u0 = __shfl_up_sync(0xffffffffu, v0, o);
@@ -245,9 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float base = sThBase[aa];
       const float th0 = base + v0, th1 = base + v1;
       const float last = __shfl_sync(0xffffffffu, Qt > 32 ? th1 : th0, Qt > 32 ? Qt - 33 : Qt - 1);
-      if (lane < Qt) sincosf(th0, &sSin[lane * (A + 1) + aa], &sCos[lane * (A + 1) + aa]);
-      if (lane + 32 < Qt)
-        sincosf(th1, &sSin[(lane + 32) * (A + 1) + aa], &sCos[(lane + 32) * (A + 1) + aa]);
+      if (lane < Qt) sincos_fast(th0, &sSin[lane * CS + aa], &sCos[lane * CS + aa]);
+      if (lane + 32 < Qt) sincos_fast(th1, &sSin[(lane + 32) * CS + aa], &sCos[(lane + 32) * CS + aa]);
       __syncwarp();
       if (lane == 0) sThBase[aa] = last;
     }
@@ -261,11 +283,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       tW[t] = w;
       tOm[t] = expf(cend - cum) * w;
     }
-    // (4a) rotated, biased q / k rows. Unit u of a row is the rotary pair
-    // (u, u + A) for u < A, else the single dim u + A. Lane l takes row
-    // 8 * rb + l % 8 and unit 4 * ub + l / 8, so that the 32 lanes of a store
-    // hit 32 distinct banks of the K-major tiles.
-    {
+    // (4a) rotated, biased q / k rows into the K-major q / k tiles.
+    if ((A & 3) == 0 && (N & 3) == 0) {
+      // Vector path: an item is 4 consecutive dims n0..n0+3 of one row; for
+      // n0 < A it also produces their rotary partners n0+A..n0+A+3. Lane l
+      // takes row 8 * rb + l % 8 and item 4 * jb + l / 8, so that each 16-byte
+      // store of the warp lands in a distinct 16-byte slot (512 contiguous
+      // bytes per warp).
+      const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
+      const int rl = lane & 7, jl = lane >> 3;
+      for (int rb = 0; rb < kRows / 8; ++rb) {
+        const int rho = 8 * rb + rl;
+        const int t = rho >> lgR, r = rho & (R - 1);
+        const bool in = t < tv;
+        const int64_t roff = ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+        const float* crow = a.c + roff;
+        const float* brow = a.b + roff;
+        const float* cb = sBiasC + r * Npad;
+        const float* bb = sBiasB + r * Npad;
+#pragma unroll 2
+        for (int jb = warp; jb < QW4; jb += kWarps) {
+          const int j = 4 * jb + jl;
+          if (j >= QW) continue;
+          if (j < PQ) {
+            const int n0 = 4 * j;
+            float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, k0 = q0, k1 = q0;
+            if (in) {
+              const float4 cu = *reinterpret_cast<const float4*>(crow + n0);
+              const float4 cw = *reinterpret_cast<const float4*>(crow + n0 + A);
+              const float4 bu = *reinterpret_cast<const float4*>(brow + n0);
+              const float4 bw = *reinterpret_cast<const float4*>(brow + n0 + A);
+              const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
+              const float4 cbw = *reinterpret_cast<const float4*>(cb + n0 + A);
+              const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
+              const float4 bbw = *reinterpret_cast<const float4*>(bb + n0 + A);
+              const float4 cs = *reinterpret_cast<const float4*>(sCos + t * CS + n0);
+              const float4 sn = *reinterpret_cast<const float4*>(sSin + t * CS + n0);
+#define M3_ROT(E)                                                            \
+  {                                                                          \
+    const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
+    const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
+    q0.E = qu * cs.E - qw * sn.E;                                            \
+    q1.E = qu * sn.E + qw * cs.E;                                            \
+    k0.E = ku * cs.E - kw * sn.E;                                            \
+    k1.E = ku * sn.E + kw * cs.E;                                            \
+  }
+              M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
+#undef M3_ROT
+            }
+            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
+            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
+            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
+            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
+          } else {
+            const int n0 = 2 * A + 4 * (j - PQ);
+            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv;
+            if (in) {
+              const float4 cu = *reinterpret_cast<const float4*>(crow + n0);
+              const float4 bu = *reinterpret_cast<const float4*>(brow + n0);
+              const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
+              const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
+              qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
+              kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
+            }
+            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
+            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
+          }
+        }
+      }
+    } else {
+      // Scalar path for A or N not a multiple of 4: unit u of a row is the
+      // rotary pair (u, u + A) for u < A, else the single dim u + A.
       const int U = N - A;
       const int U4 = (U + 3) >> 2;
       const int rl = lane & 7, ul = lane >> 3;
@@ -275,17 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool in = t < tv;
         const float* crow = a.c + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
         const float* brow = a.b + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-        const float* cb = cbias_h + r * N;
-        const float* bb = bbias_h + r * N;
-        const float* cst = sCos + t * (A + 1);
-        const float* snt = sSin + t * (A + 1);
+        const float* cb = sBiasC + r * Npad;
+        const float* bb = sBiasB + r * Npad;
         for (int ub = warp; ub < U4; ub += kWarps) {
           const int u = 4 * ub + ul;
           if (u >= U) continue;
           if (u < A) {
             float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
             if (in) {
-              const float cs = cst[u], sn = snt[u];
+              const float cs = sCos[t * CS + u], sn = sSin[t * CS + u];
               const float qu = crow[u] + cb[u], qw = crow[u + A] + cb[u + A];
               const float ku = brow[u] + bb[u], kw = brow[u + A] + bb[u + A];
               q0 = qu * cs - qw * sn;
@@ -309,26 +395,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // zero padding columns N .. Npad
-      for (int i = tid; i < kRows * (Npad - N); i += kThreads) {
-        const int rho = i / (Npad - N), n = N + i % (Npad - N);
-        sQ[tc::kmaj(rho, n, Npad)] = 0.f;
-        sK[tc::kmaj(rho, n, Npad)] = 0.f;
-      }
+    }
+    // zero padding columns N .. Npad
+    for (int i = tid; i < kRows * (Npad - N); i += kThreads) {
+      const int rho = i / (Npad - N), n = N + i % (Npad - N);
+      sQ[tc::kmaj(rho, n, Npad)] = 0.f;
+      sK[tc::kmaj(rho, n, Npad)] = 0.f;
     }
     __syncthreads();
-    // (4b) w-scaled transposed keys Kt[n][row] = w_t * k[row][n] (from the
-    // TF32 k tile); lane l takes n = 8 * nb + l % 8 and row 4 * rb + l / 8
-    // (conflict-free scalar stores)
+    // (4b) w-scaled transposed keys Kt[n][row] = w_t * k[row][n] from the
+    // TF32 k tile: lane l reads the 16 bytes of row 8 * rb + l % 8, dims
+    // 4 * (4 * nb + l / 8) .. +3 (conflict-free), and writes them as four
+    // scalars of column `row` of Kt.
     {
-      const int nl = lane & 7, rl = lane >> 3;
-      for (int rb = warp; rb < kRows / 4; rb += kWarps) {
-        const int rho = 4 * rb + rl;
+      const int rl = lane & 7, nl = lane >> 3;
+      const int NQ = Npad >> 2;
+      for (int rb = 0; rb < kRows / 8; ++rb) {
+        const int rho = 8 * rb + rl;
         const int t = rho >> lgR;
         const float om = t < tv ? tOm[t] : 0.f;
-        for (int nb = 0; nb < Npad / 8; ++nb) {
-          const int n = 8 * nb + nl;
-          sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(om * sK[tc::kmaj(rho, n, Npad)]);
+        for (int nb = warp; nb < (NQ >> 2); nb += kWarps) {
+          const int n0 = 4 * (4 * nb + nl);
+          const float4 kv = *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad));
+          sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(om * kv.x);
+          sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(om * kv.y);
+          sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(om * kv.z);
+          sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(om * kv.w);
         }
       }
     }
@@ -392,15 +484,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool in = t2 < tv;
           const float* xrow = a.x + (tok0 + t2) * HP + (int64_t)h * P;
           const float* mx = mimo ? a.mimo_x + ((int64_t)h * R + r2) * P : nullptr;
+          float xv[MP / 8];
+#pragma unroll
           for (int pb = 0; pb < MP / 8; ++pb) {
             const int p = 8 * pb + pl;
-            float xv = 0.f;
-            if (in && p < P) {
-              xv = xrow[p];
-              if (mimo) xv *= mx[p];
-            }
-            sXt[tc::kmaj(p, rho2, kRows)] = tc::to_tf32(xv);
+            xv[pb] = (in && p < P) ? xrow[p] : 0.f;
+            if (mimo && in && p < P) xv[pb] *= mx[p];
           }
+#pragma unroll
+          for (int pb = 0; pb < MP / 8; ++pb)
+            sXt[tc::kmaj(8 * pb + pl, rho2, kRows)] = tc::to_tf32(xv[pb]);
         }
       }
       const float ec = expf(tCum[Qt - 1]);
@@ -525,7 +618,7 @@ bool chunk_supported(const ScanGeom& g) {
 
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
                               cudaStream_t s) {
-  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A);
+  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
   const unsigned grid = (unsigned)(g.B * g.H);
   const bool mimo = a.mimo_o != nullptr;
   auto run = [&](auto kernel) -> cudaError_t {
