@@ -26,7 +26,7 @@
 // weights are formed by the CUDA cores while staging operands; every operand
 // is rounded to TF32 (round to nearest).
 //
-// One CTA of 128 threads runs one (b, h) sequence chunk after chunk; thread 0
+// One CTA of 256 threads runs one (b, h) sequence chunk after chunk; thread 0
 // issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit.
 // Waits are bounded: on timeout the kernel records a status word and exits.
 // Shared memory (about 100 KB for P <= 64, N = 128: the tiles share three
@@ -40,7 +40,7 @@ namespace m3 {
 namespace {
 
 constexpr int kRows = 64;       // (token, rank) rows per chunk
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
@@ -99,7 +99,7 @@ __device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 template <int MP, bool MIMO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, uint32_t* status) {
   extern __shared__ __align__(1024) float sm[];
   __shared__ __align__(8) uint64_t bars[2];
@@ -153,19 +153,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = tmem_slot;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  // TMEM lane quadrant of this warp (warps w and w + 4 share quadrant w % 4 and
+  // split the columns of the row-wise TMEM work between them)
+  const int quad = warp & 3, wg = warp >> 2;
+  const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const uint32_t tG = tbase, tS = tbase + 128, tYo = tbase + 192;
   {
     float zero[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) zero[i] = 0.f;
-    for (int c = 0; c < Npad; c += 16) tc::tmem_st16(tG + lane_base + c, zero);
+    for (int c = 16 * wg; c < Npad; c += 32) tc::tmem_st16(tG + lane_base + c, zero);
   }
   // Row p of the transposed tiles handled by this thread (TMEM data path:
   // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant, and
   // lane l + 16 shares the row of lane l, taking the upper half of the columns).
   const int half = (MP == 64) ? (lane >> 4) : 0;
-  const int prow = (MP == 64) ? 16 * warp + (lane & 15) : 32 * warp + lane;
+  const int prow = (MP == 64) ? 16 * quad + (lane & 15) : 32 * quad + lane;
   const bool pvalid = prow < P;
   constexpr bool mimo = MIMO;
   constexpr int kRmax = MIMO ? 8 : 1;
@@ -444,12 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
     // block of row l), values X^T, and G *= e^{cum_end}
     {
-      const int rho = 16 * warp + (lane & 15);
+      const int rho = 16 * quad + (lane & 15);
       const int t = rho >> lgR;
       const float cum_t = tCum[t];
       const float gam_t = tGam[t];
       const int sh = lane >> 4;
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
         float v[16];
         tc::tmem_ld16(tS + lane_base + cb * 16, v);
         float w8[8];
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float ec = expf(tCum[Qt - 1]);
-      for (int c = 0; c < Npad; c += 16) {
+      for (int c = 16 * wg; c < Npad; c += 32) {
         float v[16];
         tc::tmem_ld16(tG + lane_base + c, v);
 #pragma unroll
@@ -528,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
       const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
       float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
         float yo[16], yi[16];
         tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
         tc::tmem_ld16(tS + lane_base + cb * 16, yi);
