@@ -94,6 +94,35 @@ __device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
   *c = __cosf(r);
 }
 
+// Per-token scalars and angle increments of one chunk, loaded into registers
+// one chunk ahead (thread t <= Qt holds token t's dt / adt / trap; the angle
+// increments follow the (token = warp + 8 i, angle = lane + 32 j) tiling of
+// the staging loop).
+struct TokenPreload {
+  float dt, adt, trap;
+  float ang[16];
+};
+
+__device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs& a, int64_t tok,
+                                               int cn, int L, int Qt, int A, int H, int h,
+                                               int tid, int warp, int lane) {
+  pl.dt = pl.adt = pl.trap = 0.f;
+  if (tid <= Qt && cn + tid < L) {
+    const int64_t sc = (tok + tid) * H + h;
+    pl.dt = a.dt[sc];
+    pl.adt = a.adt[sc];
+    pl.trap = a.trap[sc];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int t = warp + 8 * i, aa = lane + 32 * j;
+      pl.ang[2 * i + j] = (t < Qt && aa < A && cn + t < L) ? a.angle[(tok + t) * A + aa] : 0.f;
+    }
+  }
+}
+
 // SiLU with the hardware exp / divide approximations (relative error a few
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
@@ -184,34 +213,44 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t id_S = tc::idesc_tf32(64, 64);
   const uint32_t id_Y = tc::idesc_tf32(MP, 64);
   const uint32_t id_D = tc::idesc_tf32(MP, Npad);
-  const bool pf_rows = (N % 4 == 0) && (P % 4 == 0);
-  const bool pf_tok = (H % 4 == 0) && (A % 4 == 0);
   const int64_t HP = (int64_t)H * P;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
 
+  TokenPreload pl;
+  preload_tokens(pl, a, (int64_t)b * L, 0, L, Qt, A, H, h, tid, warp, lane);
+
   int it = 0;
   for (int c0 = 0; c0 < L; c0 += Qt, ++it) {
     const int tv = min(Qt, L - c0);
     const int64_t tok0 = (int64_t)b * L + c0;   // first token of the chunk in [B, L]
-    // (0) L2 prefetch of the next chunk's operands
-    if (c0 + Qt < L) {
+    // (0) L2 prefetch of the next chunk's operands. The next chunk's blocks of
+    // x, z, C, B, dt, adt, trap and angle are contiguous across the heads of a
+    // batch row, so the H CTAs of that row (resident together) each prefetch
+    // one 16-byte-aligned slice of every block.
+    if (c0 + Qt < L && tid < 8) {
       const int nv = min(Qt, L - c0 - Qt);
       const int64_t ntok = tok0 + Qt;
-      if (pf_rows && tid < nv) {
-        const int64_t tok = ntok + tid;
-        const int64_t row = (tok * RG + (int64_t)grp * R) * N;
-        tc::prefetch_l2(a.c + row, (uint32_t)(R * N * 4));
-        tc::prefetch_l2(a.b + row, (uint32_t)(R * N * 4));
-        tc::prefetch_l2(a.x + tok * HP + (int64_t)h * P, (uint32_t)(P * 4));
-        tc::prefetch_l2(a.z + tok * HP + (int64_t)h * P, (uint32_t)(P * 4));
+      const float* base = nullptr;
+      int64_t floats = 0;
+      switch (tid) {
+        case 0: base = a.x + ntok * HP; floats = (int64_t)nv * HP; break;
+        case 1: base = a.z + ntok * HP; floats = (int64_t)nv * HP; break;
+        case 2: base = a.c + ntok * RG * N; floats = (int64_t)nv * RG * N; break;
+        case 3: base = a.b + ntok * RG * N; floats = (int64_t)nv * RG * N; break;
+        case 4: base = a.dt + ntok * H; floats = (int64_t)nv * H; break;
+        case 5: base = a.adt + ntok * H; floats = (int64_t)nv * H; break;
+        case 6: base = a.trap + ntok * H; floats = (int64_t)nv * H; break;
+        default: base = a.angle + ntok * A; floats = (int64_t)nv * A; break;
       }
-      if (pf_tok && tid == 64) {
-        tc::prefetch_l2(a.dt + ntok * H, (uint32_t)(nv * H * 4));
-        tc::prefetch_l2(a.adt + ntok * H, (uint32_t)(nv * H * 4));
-        tc::prefetch_l2(a.trap + ntok * H, (uint32_t)(nv * H * 4));
-        if (A > 0) tc::prefetch_l2(a.angle + ntok * A, (uint32_t)(nv * A * 4));
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+      const uintptr_t hi = reinterpret_cast<uintptr_t>(base + floats);
+      if (floats > 0 && (lo & 15) == 0 && (hi & 15) == 0) {
+        const uintptr_t span = hi - lo;
+        const uintptr_t s0 = lo + (span * h / H & ~uintptr_t(15));
+        const uintptr_t s1 = (h + 1 == H) ? hi : lo + (span * (h + 1) / H & ~uintptr_t(15));
+        if (s1 > s0) tc::prefetch_l2(reinterpret_cast<const void*>(s0), (uint32_t)(s1 - s0));
       }
     }
     // (1) per-token scalars of tokens c0 .. c0 + Qt (the last one is the next
@@ -220,10 +259,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int t = tid;
       float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
       if (c0 + t < L) {
-        const int64_t sc = (tok0 + t) * H + h;
-        dtv = a.dt[sc];
-        adtv = a.adt[sc];
-        const float lam = sigmoid_f(a.trap[sc]);
+        dtv = pl.dt;
+        adtv = pl.adt;
+        const float lam = sigmoid_f(pl.trap);
         gam = lam * dtv;
         scl = (1.0f - lam) * dtv;
       }
@@ -235,9 +273,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         tDt[t] = in ? dtv : 0.f;
       }
     }
-    for (int t = warp; t < Qt; t += kWarps)
-      for (int aa = lane; aa < A; aa += 32)
-        sCos[t * CS + aa] = t < tv ? a.angle[(tok0 + t) * A + aa] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int t = warp + 8 * i, aa = lane + 32 * j;
+        if (t < Qt && aa < A) sCos[t * CS + aa] = pl.ang[2 * i + j];
+      }
+    }
     __syncthreads();
     // (2) local cumulative log decay (warp 0, two tokens per lane); rotary
     // angle: per-angle scan of dt * angle over the chunk, then cos / sin of
@@ -295,7 +338,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       // bytes per warp).
       const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
       const int rl = lane & 7, jl = lane >> 3;
-      for (int rb = 0; rb < kRows / 8; ++rb) {
+#pragma unroll 2
+      for (int item = warp; item < (kRows / 8) * QW4; item += kWarps) {
+        const int rb = item / QW4, jb = item - rb * QW4;
         const int rho = 8 * rb + rl;
         const int t = rho >> lgR, r = rho & (R - 1);
         const bool in = t < tv;
@@ -304,8 +349,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float* brow = a.b + roff;
         const float* cb = sBiasC + r * Npad;
         const float* bb = sBiasB + r * Npad;
-#pragma unroll 2
-        for (int jb = warp; jb < QW4; jb += kWarps) {
+        {
           const int j = 4 * jb + jl;
           if (j >= QW) continue;
           if (j < PQ) {
@@ -445,8 +489,30 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (abort_flag) break;
     // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
     // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
-    // block of row l), values X^T, and G *= e^{cum_end}
+    // block of row l), values X^T, and G *= e^{cum_end}. The value loads are
+    // issued first so that their latency overlaps the mask.
     {
+      constexpr int kXr = (kRows / 4 + kWarps - 1) / kWarps;  // row blocks per warp
+      float xreg[kXr][MP / 8];
+      {
+        const int pl8 = lane & 7, rl = lane >> 3;
+#pragma unroll
+        for (int q = 0; q < kXr; ++q) {
+          const int rb = warp + kWarps * q;
+          const int rho2 = 4 * rb + rl;
+          const int t2 = rho2 >> lgR, r2 = rho2 & (R - 1);
+          const bool in = rb < kRows / 4 && t2 < tv;
+          const float* xrow = a.x + (tok0 + t2) * HP + (int64_t)h * P;
+          const float* mx = mimo ? a.mimo_x + ((int64_t)h * R + r2) * P : nullptr;
+#pragma unroll
+          for (int pb = 0; pb < MP / 8; ++pb) {
+            const int p = 8 * pb + pl8;
+            float xv = (in && p < P) ? xrow[p] : 0.f;
+            if (mimo && in && p < P) xv *= mx[p];
+            xreg[q][pb] = xv;
+          }
+        }
+      }
       const int rho = 16 * quad + (lane & 15);
       const int t = rho >> lgR;
       const float cum_t = tCum[t];
@@ -480,23 +546,15 @@ __global__ void __launch_bounds__(kThreads, 2)
       // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pb +
       // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores)
       {
-        const int pl = lane & 7, rl = lane >> 3;
-        for (int rb = warp; rb < kRows / 4; rb += kWarps) {
-          const int rho2 = 4 * rb + rl;
-          const int t2 = rho2 >> lgR, r2 = rho2 & (R - 1);
-          const bool in = t2 < tv;
-          const float* xrow = a.x + (tok0 + t2) * HP + (int64_t)h * P;
-          const float* mx = mimo ? a.mimo_x + ((int64_t)h * R + r2) * P : nullptr;
-          float xv[MP / 8];
+        const int pl8 = lane & 7, rl = lane >> 3;
 #pragma unroll
-          for (int pb = 0; pb < MP / 8; ++pb) {
-            const int p = 8 * pb + pl;
-            xv[pb] = (in && p < P) ? xrow[p] : 0.f;
-            if (mimo && in && p < P) xv[pb] *= mx[p];
-          }
+        for (int q = 0; q < kXr; ++q) {
+          const int rb = warp + kWarps * q;
+          if (rb >= kRows / 4) break;
+          const int rho2 = 4 * rb + rl;
 #pragma unroll
           for (int pb = 0; pb < MP / 8; ++pb)
-            sXt[tc::kmaj(8 * pb + pl, rho2, kRows)] = tc::to_tf32(xv[pb]);
+            sXt[tc::kmaj(8 * pb + pl8, rho2, kRows)] = tc::to_tf32(xreg[q][pb]);
         }
       }
       const float ec = expf(tCum[Qt - 1]);
@@ -520,6 +578,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::mma_ss(tG, tc::kdesc(sXt, kRows, ks), tc::kdesc(sKt, kRows, ks), id_D, 1);
       tc::commit(&bars[1]);
     }
+    // next chunk's per-token scalars and angles: loads in flight during the
+    // state-update MMA and the epilogue
+    if (c0 + Qt < L) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, Qt, A, H, h, tid, warp, lane);
     if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
     tc::fence_after();
     __syncthreads();
