@@ -131,7 +131,8 @@ template <int MP, bool MIMO>
 __global__ void __launch_bounds__(kThreads, 2)
     k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, uint32_t* status) {
   extern __shared__ __align__(1024) float sm[];
-  __shared__ __align__(8) uint64_t bars[2];
+  // MMA completion barriers: S, Yo, Yi, state update (each completes once per chunk)
+  __shared__ __align__(8) uint64_t bars[4];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -166,8 +167,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sThBase = sm + lay.thbase;
 
   if (tid == 0) {
-    tc::bar_init(&bars[0], 1);
-    tc::bar_init(&bars[1], 1);
+    for (int i = 0; i < 4; ++i) tc::bar_init(&bars[i], 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -479,9 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
       for (int ks = 0; ks < Npad / 8; ++ks)
         tc::mma_ss(tS, tc::kdesc(sQ, Npad, ks), tc::kdesc(sK, Npad, ks), id_S, ks > 0);
+      tc::commit(&bars[0]);
       for (int ks = 0; ks < Npad / 8; ++ks)
         tc::mma_ts(tYo, tG + ks * 8, tc::kdesc(sQ, Npad, ks), id_Y, ks > 0);
-      tc::commit(&bars[0]);
+      tc::commit(&bars[1]);
     }
     if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
     tc::fence_after();
@@ -557,6 +558,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             sXt[tc::kmaj(8 * pb + pl8, rho2, kRows)] = tc::to_tf32(xreg[q][pb]);
         }
       }
+      // G may be rescaled only once Yo^T = G Q^T has read it
+      if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
       const float ec = expf(tCum[Qt - 1]);
       for (int c = 16 * wg; c < Npad; c += 32) {
         float v[16];
@@ -571,24 +575,45 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc::fence_after();
     // (7) Yi^T = X^T P^T and G += X^T (w K)
+    if (abort_flag) break;
     if (tid == 0) {
       for (int ks = 0; ks < kRows / 8; ++ks)
         tc::mma_ss(tS, tc::kdesc(sXt, kRows, ks), tc::kdesc(sP, kRows, ks), id_Y, ks > 0);
+      tc::commit(&bars[2]);
       for (int ks = 0; ks < kRows / 8; ++ks)
         tc::mma_ss(tG, tc::kdesc(sXt, kRows, ks), tc::kdesc(sKt, kRows, ks), id_D, 1);
-      tc::commit(&bars[1]);
+      tc::commit(&bars[3]);
     }
     // next chunk's per-token scalars and angles: loads in flight during the
-    // state-update MMA and the epilogue
+    // MMAs and the epilogue
     if (c0 + Qt < L) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, Qt, A, H, h, tid, warp, lane);
-    if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
+    // SISO epilogue operands x, z of this thread's output column, loaded while
+    // the MMAs run
+    constexpr int kCols = (MP == 64) ? 8 : 16;
+    float xe[2][kCols], ze[2][kCols];
+    if (!mimo) {
+      const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
+      const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int col0 = (2 * wg + u) * 16 + 8 * half;
+#pragma unroll
+        for (int j = 0; j < kCols; ++j) {
+          const int t = col0 + j;
+          const bool ok = pvalid && t < tv;
+          xe[u][j] = ok ? xcol[t * HP] : 0.f;
+          ze[u][j] = (ok && g.has_z) ? zcol[t * HP] : 0.f;
+        }
+      }
+    }
+    // the epilogue needs Yi only; the state update runs on under it
+    if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
     tc::fence_after();
     __syncthreads();
     if (abort_flag) break;
     // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
     // two lanes of a row split each 16-column block into 8 + 8 columns.
     {
-      constexpr int kCols = (MP == 64) ? 8 : 16;
       const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
       const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
       float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
@@ -610,19 +635,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!pvalid) continue;
         const int col0 = cb * 16 + 8 * half;
         if (!mimo) {
-          float xv[kCols], zv[kCols];
-#pragma unroll
-          for (int j = 0; j < kCols; ++j) {
-            const int t = col0 + j;
-            xv[j] = t < tv ? xcol[t * HP] : 0.f;
-            zv[j] = (t < tv && g.has_z) ? zcol[t * HP] : 0.f;
-          }
+          const int u = cb - 2 * wg;
 #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const int t = col0 + j;
             if (t < tv) {
-              float y = tEc[t] * yo[j] + yi[j] + dsk * xv[j];
-              if (g.has_z) y *= silu_fast(zv[j]);
+              const float xv = u ? xe[1][j] : xe[0][j];
+              const float zv = u ? ze[1][j] : ze[0][j];
+              float y = tEc[t] * yo[j] + yi[j] + dsk * xv;
+              if (g.has_z) y *= silu_fast(zv);
               ocol[t * HP] = y;
             }
           }
@@ -664,9 +685,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           orow[p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
       }
     }
+    // the state update must finish before the next chunk rewrites the tiles it
+    // reads and issues Yo^T = G Q^T
+    if (!tc::bar_wait(&bars[3], it & 1, kWaitBudget)) abort_flag = 1;
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (abort_flag) break;
   }
   if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
   tc::fence_before();
