@@ -8,6 +8,8 @@
  *   m3_mimo_forward   - `mamba3_mimo`         (shared-state MIMO recurrence)
  *   m3_siso_step      - `mamba3_siso_step`    (one token, explicit state)
  *   m3_mimo_step      - `mamba3_mimo_step`    (one MIMO token, explicit state)
+ *   m3_siso_prefill / m3_mimo_prefill - the forward scans from / to an
+ *                       explicit step state (prefill -> decode hand-off)
  *
  * Conventions for every entry point:
  *  - Every tensor is float32, dense row-major, in device memory owned by the
@@ -138,6 +140,37 @@ int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* angle, const float* c_bias, const float* b_bias,
                     const float* d, const float* mimo_x, const float* mimo_z,
                     const float* mimo_o, const float* norm_weight, float* out,
+                    void* workspace, size_t workspace_bytes, m3_stream_t stream);
+
+/*
+ * m3_siso_prefill / m3_mimo_prefill - the scan of m3_siso_forward /
+ * m3_mimo_forward continued from, and handing over, an explicit recurrent
+ * state: the prefill -> decode hand-off between the full-sequence ops and the
+ * step ops (`mamba3_siso` / `mamba3_siso_step`, `mamba3_mimo` /
+ * `mamba3_mimo_step`).
+ *
+ * The four states use the step layouts: ssm_state [B,H,P,N], angle_state
+ * [B,H,A] (may be NULL when A == 0), k_state [B,H,R,N] (rotated, biased key
+ * of the last token), v_state [B,H,R,P] (its rank-scaled value). They are read
+ * as the state before token 0 (all zero = the start of a sequence) and
+ * overwritten with the state after token L-1, so that m3_siso_step can take
+ * over at token L. Operands and checks are those of the forward calls;
+ * workspace: at least m3_*_prefill_workspace() bytes.
+ */
+int m3_siso_prefill_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_siso_prefill(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, float* ssm_state, float* angle_state, float* k_state,
+                    float* v_state, float* out, void* workspace, size_t workspace_bytes,
+                    m3_stream_t stream);
+int m3_mimo_prefill_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_mimo_prefill(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, const float* mimo_x, const float* mimo_z,
+                    const float* mimo_o, const float* norm_weight, float* ssm_state,
+                    float* angle_state, float* k_state, float* v_state, float* out,
                     void* workspace, size_t workspace_bytes, m3_stream_t stream);
 
 /*

@@ -25,7 +25,8 @@ M3_MATH_FP32 = 0
 M3_MATH_TF32 = 1
 
 EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
-            "m3_siso_forward_static",
+            "m3_siso_forward_static", "m3_siso_prefill_workspace", "m3_siso_prefill",
+            "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_status_string", "m3_launch_count")
 
@@ -90,6 +91,10 @@ def load_library():
         lib.m3_siso_forward.argtypes = [cfgp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_forward.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
         lib.m3_siso_forward_static.argtypes = [cfgp] + [_vp] * 12 + [_vp]
+        lib.m3_siso_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_mimo_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_siso_prefill.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
+        lib.m3_mimo_prefill.argtypes = [cfgp] + [_vp] * 21 + [ctypes.c_size_t, _vp]
         lib.m3_siso_step.argtypes = [cfgp] + [_vp] * 16 + [_vp]
         lib.m3_mimo_step.argtypes = [cfgp] + [_vp] * 20 + [_vp]
         lib.m3_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
@@ -177,6 +182,38 @@ def m3_siso_forward_static(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_b
     _check(load_library().m3_siso_forward_static(ctypes.byref(cfg), *[_ptr(t) for t in (
         c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, out)], _stream(stream)),
         "m3_siso_forward_static")
+
+
+def m3_siso_prefill_workspace(cfg: SsmConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_siso_prefill_workspace(ctypes.byref(cfg), ctypes.byref(n)),
+           "m3_siso_prefill_workspace")
+    return n.value
+
+
+def m3_mimo_prefill_workspace(cfg: SsmConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_mimo_prefill_workspace(ctypes.byref(cfg), ctypes.byref(n)),
+           "m3_mimo_prefill_workspace")
+    return n.value
+
+
+def m3_siso_prefill(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+                    ssm_state, angle_state, k_state, v_state, out, workspace=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_siso_prefill(ctypes.byref(cfg), *[_ptr(t) for t in (
+        c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, ssm_state, angle_state, k_state,
+        v_state, out)], wp, wn, _stream(stream)), "m3_siso_prefill")
+
+
+def m3_mimo_prefill(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,
+                    mimo_z, mimo_o, norm_weight, ssm_state, angle_state, k_state, v_state, out,
+                    workspace=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_mimo_prefill(ctypes.byref(cfg), *[_ptr(t) for t in (
+        c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x, mimo_z, mimo_o,
+        norm_weight, ssm_state, angle_state, k_state, v_state, out)], wp, wn, _stream(stream)),
+        "m3_mimo_prefill")
 
 
 def m3_mimo_forward(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,

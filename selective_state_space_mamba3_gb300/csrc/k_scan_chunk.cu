@@ -127,9 +127,9 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-template <int MP, bool MIMO>
+template <int MP, bool MIMO, bool SUMMARY>
 __global__ void __launch_bounds__(kThreads, 2)
-    k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, uint32_t* status) {
+    k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, ChunkIO io, uint32_t* status) {
   extern __shared__ __align__(1024) float sm[];
   // MMA completion barriers: S, Yo, Yi, state update (each completes once per chunk)
   __shared__ __align__(8) uint64_t bars[4];
@@ -141,7 +141,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int lgR = __ffs(R) - 1;  // R is a power of two here
   const int Npad = lay.Npad;
   const int Qt = kRows >> lgR;  // tokens per chunk
-  const int b = blockIdx.x / H, h = blockIdx.x % H;
+  const int cta = blockIdx.x;
+  const int bh = cta / io.nseg, seg = cta - bh * io.nseg;
+  const int b = bh / H, h = bh % H;
+  const int l0 = seg * io.seg_len, l1 = min(L, l0 + io.seg_len);
+  // the summary of the last segment is never used
+  if (SUMMARY && seg == io.nseg - 1) return;
   const int grp = h / (H / g.G);
   const int RG = g.G * R;
 
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
-  for (int i = tid; i < A; i += kThreads) sThBase[i] = 0.f;
+  for (int i = tid; i < A; i += kThreads) sThBase[i] = io.th0 ? io.th0[(int64_t)cta * A + i] : 0.f;
   for (int i = tid; i < R * Npad; i += kThreads) {
     const int r = i / Npad, n = i - r * Npad;
     sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
@@ -187,18 +192,23 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int quad = warp & 3, wg = warp >> 2;
   const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
   const uint32_t tG = tbase, tS = tbase + 128, tYo = tbase + 192;
-  {
-    float zero[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) zero[i] = 0.f;
-    for (int c = 16 * wg; c < Npad; c += 32) tc::tmem_st16(tG + lane_base + c, zero);
-  }
   // Row p of the transposed tiles handled by this thread (TMEM data path:
   // M = 128 -> lane p; M = 64 -> lanes 0..15 of each 32-lane quadrant, and
   // lane l + 16 shares the row of lane l, taking the upper half of the columns).
   const int half = (MP == 64) ? (lane >> 4) : 0;
   const int prow = (MP == 64) ? 16 * quad + (lane & 15) : 32 * quad + lane;
   const bool pvalid = prow < P;
+  const bool g_lane = pvalid && (MP == 128 || half == 0);  // TMEM lane holding row prow
+  {
+    // initial state G (zero, or this segment's entry state)
+    const float* g0 = io.g0 ? io.g0 + ((int64_t)cta * P + prow) * N : nullptr;
+    for (int c = 16 * wg; c < Npad; c += 32) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = (g0 && g_lane && c + j < N) ? g0[c + j] : 0.f;
+      tc::tmem_st16(tG + lane_base + c, v);
+    }
+  }
   constexpr bool mimo = MIMO;
   constexpr int kRmax = MIMO ? 8 : 1;
   float mxr[kRmax], mzr[kRmax], mor[kRmax];
@@ -219,18 +229,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc::fence_after();
 
   TokenPreload pl;
-  preload_tokens(pl, a, (int64_t)b * L, 0, L, Qt, A, H, h, tid, warp, lane);
+  preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, Qt, A, H, h, tid, warp, lane);
+  float esum = 0.f;  // sum of adt over the segment
 
   int it = 0;
-  for (int c0 = 0; c0 < L; c0 += Qt, ++it) {
-    const int tv = min(Qt, L - c0);
+  for (int c0 = l0; c0 < l1; c0 += Qt, ++it) {
+    const int tv = min(Qt, l1 - c0);
     const int64_t tok0 = (int64_t)b * L + c0;   // first token of the chunk in [B, L]
     // (0) L2 prefetch of the next chunk's operands. The next chunk's blocks of
     // x, z, C, B, dt, adt, trap and angle are contiguous across the heads of a
     // batch row, so the H CTAs of that row (resident together) each prefetch
     // one 16-byte-aligned slice of every block.
-    if (c0 + Qt < L && tid < 8) {
-      const int nv = min(Qt, L - c0 - Qt);
+    if (c0 + Qt < l1 && tid < 8) {
+      const int nv = min(Qt, l1 - c0 - Qt);
       const int64_t ntok = tok0 + Qt;
       const float* base = nullptr;
       int64_t floats = 0;
@@ -321,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
     // (3) decay / trapezoid coefficients
+    esum += tCum[Qt - 1];
     if (tid < Qt) {
       const int t = tid;
       const float cum = tCum[t], cend = tCum[Qt - 1];
@@ -378,8 +390,10 @@ __global__ void __launch_bounds__(kThreads, 2)
               M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
 #undef M3_ROT
             }
-            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
-            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
+            if (!SUMMARY) {
+              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
+              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
+            }
             *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
             *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
           } else {
@@ -393,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
               kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
             }
-            *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
+            if (!SUMMARY) *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
             *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
           }
         }
@@ -426,8 +440,10 @@ __global__ void __launch_bounds__(kThreads, 2)
               k0 = ku * cs - kw * sn;
               k1 = ku * sn + kw * cs;
             }
-            sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
-            sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
+            if (!SUMMARY) {
+              sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
+              sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
+            }
             sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
             sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
           } else {
@@ -437,9 +453,27 @@ __global__ void __launch_bounds__(kThreads, 2)
               qv = crow[n] + cb[n];
               kv = brow[n] + bb[n];
             }
-            sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
+            if (!SUMMARY) sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
             sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
           }
+        }
+      }
+    }
+    // key of the sequence's last token in fp32 for the step state (last chunk only)
+    if (io.k_last && c0 + tv == L) {
+      const int t = tv - 1;
+      for (int i = tid; i < R * (N - A); i += kThreads) {
+        const int r = i / (N - A), u = i - r * (N - A);
+        const float* brow = a.b + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+        const float* bb = sBiasB + r * Npad;
+        float* kl = io.k_last + ((int64_t)bh * R + r) * N;
+        if (u < A) {
+          const float cs = sCos[t * CS + u], sn = sSin[t * CS + u];
+          const float ku = brow[u] + bb[u], kw = brow[u + A] + bb[u + A];
+          kl[u] = ku * cs - kw * sn;
+          kl[u + A] = ku * sn + kw * cs;
+        } else {
+          kl[u + A] = brow[u + A] + bb[u + A];
         }
       }
     }
@@ -476,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     tc::fence_after();
     // (5) S = Q K^T and Yo^T = G Q^T
-    if (tid == 0) {
+    if (!SUMMARY && tid == 0) {
       for (int ks = 0; ks < Npad / 8; ++ks)
         tc::mma_ss(tS, tc::kdesc(sQ, Npad, ks), tc::kdesc(sK, Npad, ks), id_S, ks > 0);
       tc::commit(&bars[0]);
@@ -484,10 +518,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::mma_ts(tYo, tG + ks * 8, tc::kdesc(sQ, Npad, ks), id_Y, ks > 0);
       tc::commit(&bars[1]);
     }
-    if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
-    tc::fence_after();
-    __syncthreads();
-    if (abort_flag) break;
+    if (!SUMMARY) {
+      if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
+      __syncthreads();
+      if (abort_flag) break;
+    }
     // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
     // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
     // block of row l), values X^T, and G *= e^{cum_end}. The value loads are
@@ -514,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
+      if (!SUMMARY) {
       const int rho = 16 * quad + (lane & 15);
       const int t = rho >> lgR;
       const float cum_t = tCum[t];
@@ -544,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0 + 4, kRows)) =
             make_float4(w8[4], w8[5], w8[6], w8[7]);
       }
+      }
       // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pb +
       // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores)
       {
@@ -558,9 +596,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             sXt[tc::kmaj(8 * pb + pl8, rho2, kRows)] = tc::to_tf32(xreg[q][pb]);
         }
       }
+      // value of the sequence's last token for the step state (last chunk only)
+      if (io.v_last && c0 + tv == L) {
+        const float* xrow = a.x + (tok0 + tv - 1) * HP + (int64_t)h * P;
+        for (int i = tid; i < R * P; i += kThreads) {
+          const int r = i / P, p = i - r * P;
+          io.v_last[((int64_t)bh * R + r) * P + p] =
+              mimo ? xrow[p] * a.mimo_x[((int64_t)h * R + r) * P + p] : xrow[p];
+        }
+      }
       // G may be rescaled only once Yo^T = G Q^T has read it
-      if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
-      tc::fence_after();
+      if (!SUMMARY) {
+        if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
+        tc::fence_after();
+      }
       const float ec = expf(tCum[Qt - 1]);
       for (int c = 16 * wg; c < Npad; c += 32) {
         float v[16];
@@ -577,112 +626,116 @@ __global__ void __launch_bounds__(kThreads, 2)
     // (7) Yi^T = X^T P^T and G += X^T (w K)
     if (abort_flag) break;
     if (tid == 0) {
-      for (int ks = 0; ks < kRows / 8; ++ks)
-        tc::mma_ss(tS, tc::kdesc(sXt, kRows, ks), tc::kdesc(sP, kRows, ks), id_Y, ks > 0);
-      tc::commit(&bars[2]);
+      if (!SUMMARY) {
+        for (int ks = 0; ks < kRows / 8; ++ks)
+          tc::mma_ss(tS, tc::kdesc(sXt, kRows, ks), tc::kdesc(sP, kRows, ks), id_Y, ks > 0);
+        tc::commit(&bars[2]);
+      }
       for (int ks = 0; ks < kRows / 8; ++ks)
         tc::mma_ss(tG, tc::kdesc(sXt, kRows, ks), tc::kdesc(sKt, kRows, ks), id_D, 1);
       tc::commit(&bars[3]);
     }
     // next chunk's per-token scalars and angles: loads in flight during the
     // MMAs and the epilogue
-    if (c0 + Qt < L) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, Qt, A, H, h, tid, warp, lane);
-    // SISO epilogue operands x, z of this thread's output column, loaded while
-    // the MMAs run
-    constexpr int kCols = (MP == 64) ? 8 : 16;
-    float xe[2][kCols], ze[2][kCols];
-    if (!mimo) {
-      const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
-      const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int col0 = (2 * wg + u) * 16 + 8 * half;
-#pragma unroll
-        for (int j = 0; j < kCols; ++j) {
-          const int t = col0 + j;
-          const bool ok = pvalid && t < tv;
-          xe[u][j] = ok ? xcol[t * HP] : 0.f;
-          ze[u][j] = (ok && g.has_z) ? zcol[t * HP] : 0.f;
-        }
-      }
-    }
-    // the epilogue needs Yi only; the state update runs on under it
-    if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
-    tc::fence_after();
-    __syncthreads();
-    if (abort_flag) break;
-    // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
-    // two lanes of a row split each 16-column block into 8 + 8 columns.
-    {
-      const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
-      const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
-      float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
-      for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
-        float yo[16], yi[16];
-        tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
-        tc::tmem_ld16(tS + lane_base + cb * 16, yi);
-        if (MP == 64) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float ho = __shfl_sync(0xffffffffu, yo[j + 8], lane & 15);
-            const float hi = __shfl_sync(0xffffffffu, yi[j + 8], lane & 15);
-            if (half) {
-              yo[j] = ho;
-              yi[j] = hi;
-            }
-          }
-        }
-        if (!pvalid) continue;
-        const int col0 = cb * 16 + 8 * half;
-        if (!mimo) {
-          const int u = cb - 2 * wg;
-#pragma unroll
+    if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, Qt, A, H, h, tid, warp, lane);
+    if (!SUMMARY) {
+      // SISO epilogue operands x, z of this thread's output column, loaded while
+      // the MMAs run
+      constexpr int kCols = (MP == 64) ? 8 : 16;
+      float xe[2][kCols], ze[2][kCols];
+      if (!mimo) {
+        const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
+        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+  #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col0 = (2 * wg + u) * 16 + 8 * half;
+  #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const int t = col0 + j;
-            if (t < tv) {
-              const float xv = u ? xe[1][j] : xe[0][j];
-              const float zv = u ? ze[1][j] : ze[0][j];
-              float y = tEc[t] * yo[j] + yi[j] + dsk * xv;
-              if (g.has_z) y *= silu_fast(zv);
-              ocol[t * HP] = y;
-            }
-          }
-        } else {
-          const int tpb = kCols >> lgR;  // whole tokens in this lane's columns
-          for (int tt = 0; tt < tpb; ++tt) {
-            const int t = (col0 >> lgR) + tt;
-            if (t >= tv) break;
-            const float xv = xcol[t * HP];
-            const float zv = g.has_z ? zcol[t * HP] : 0.f;
-            const float ec = tEc[t];
-            float o = 0.f;
-#pragma unroll
-            for (int r = 0; r < kRmax; ++r) {
-              if (r < R) {
-                const int j = (tt << lgR) + r;
-                float y = ec * yo[j] + yi[j] + dsk * xv * mxr[r];
-                if (g.has_z) y *= silu_fast(zv * mzr[r]);
-                o += mor[r] * y;
-              }
-            }
-            if (g.has_norm)
-              sO[t * MP + prow] = o;
-            else
-              ocol[t * HP] = o;
+            const bool ok = pvalid && t < tv;
+            xe[u][j] = ok ? xcol[t * HP] : 0.f;
+            ze[u][j] = (ok && g.has_z) ? zcol[t * HP] : 0.f;
           }
         }
       }
-    }
-    if (mimo && g.has_norm) {
+      // the epilogue needs Yi only; the state update runs on under it
+      if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
       __syncthreads();
-      for (int t = warp; t < tv; t += kWarps) {
-        float ss = 0.f;
-        for (int p = lane; p < P; p += 32) ss += sO[t * MP + p] * sO[t * MP + p];
-        ss = warp_sum(ss);
-        const float inv = 1.0f / sqrtf(ss / (float)P + 1.0e-5f);
-        float* orow = a.out + (tok0 + t) * HP + (int64_t)h * P;
-        for (int p = lane; p < P; p += 32)
-          orow[p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
+      if (abort_flag) break;
+      // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
+      // two lanes of a row split each 16-column block into 8 + 8 columns.
+      {
+        const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
+        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+        float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
+        for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
+          float yo[16], yi[16];
+          tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
+          tc::tmem_ld16(tS + lane_base + cb * 16, yi);
+          if (MP == 64) {
+  #pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float ho = __shfl_sync(0xffffffffu, yo[j + 8], lane & 15);
+              const float hi = __shfl_sync(0xffffffffu, yi[j + 8], lane & 15);
+              if (half) {
+                yo[j] = ho;
+                yi[j] = hi;
+              }
+            }
+          }
+          if (!pvalid) continue;
+          const int col0 = cb * 16 + 8 * half;
+          if (!mimo) {
+            const int u = cb - 2 * wg;
+  #pragma unroll
+            for (int j = 0; j < kCols; ++j) {
+              const int t = col0 + j;
+              if (t < tv) {
+                const float xv = u ? xe[1][j] : xe[0][j];
+                const float zv = u ? ze[1][j] : ze[0][j];
+                float y = tEc[t] * yo[j] + yi[j] + dsk * xv;
+                if (g.has_z) y *= silu_fast(zv);
+                ocol[t * HP] = y;
+              }
+            }
+          } else {
+            const int tpb = kCols >> lgR;  // whole tokens in this lane's columns
+            for (int tt = 0; tt < tpb; ++tt) {
+              const int t = (col0 >> lgR) + tt;
+              if (t >= tv) break;
+              const float xv = xcol[t * HP];
+              const float zv = g.has_z ? zcol[t * HP] : 0.f;
+              const float ec = tEc[t];
+              float o = 0.f;
+  #pragma unroll
+              for (int r = 0; r < kRmax; ++r) {
+                if (r < R) {
+                  const int j = (tt << lgR) + r;
+                  float y = ec * yo[j] + yi[j] + dsk * xv * mxr[r];
+                  if (g.has_z) y *= silu_fast(zv * mzr[r]);
+                  o += mor[r] * y;
+                }
+              }
+              if (g.has_norm)
+                sO[t * MP + prow] = o;
+              else
+                ocol[t * HP] = o;
+            }
+          }
+        }
+      }
+      if (mimo && g.has_norm) {
+        __syncthreads();
+        for (int t = warp; t < tv; t += kWarps) {
+          float ss = 0.f;
+          for (int p = lane; p < P; p += 32) ss += sO[t * MP + p] * sO[t * MP + p];
+          ss = warp_sum(ss);
+          const float inv = 1.0f / sqrtf(ss / (float)P + 1.0e-5f);
+          float* orow = a.out + (tok0 + t) * HP + (int64_t)h * P;
+          for (int p = lane; p < P; p += 32)
+            orow[p] = sO[t * MP + p] * inv * a.norm_weight[(int64_t)h * P + p];
+        }
       }
     }
     // the state update must finish before the next chunk rewrites the tiles it
@@ -694,6 +747,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (abort_flag) break;
   }
   if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
+  if (!abort_flag) {
+    // final state, cumulative angle and decay of this segment
+    if (io.g1) {
+      float* g1 = io.g1 + ((int64_t)cta * P + prow) * N;
+      for (int c = 16 * wg; c < Npad; c += 32) {
+        float v[16];
+        tc::tmem_ld16(tG + lane_base + c, v);
+        if (g_lane) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < N) g1[c + j] = v[j];
+        }
+      }
+    }
+    if (io.g_last && l1 == L) {
+      float* gl = io.g_last + ((int64_t)bh * P + prow) * N;
+      for (int c = 16 * wg; c < Npad; c += 32) {
+        float v[16];
+        tc::tmem_ld16(tG + lane_base + c, v);
+        if (g_lane) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c + j < N) gl[c + j] = v[j];
+        }
+      }
+    }
+    if (io.th1)
+      for (int i = tid; i < A; i += kThreads) io.th1[(int64_t)cta * A + i] = sThBase[i];
+    if (io.th_last && l1 == L)
+      for (int i = tid; i < A; i += kThreads) io.th_last[(int64_t)bh * A + i] = sThBase[i];
+    if (io.e1 && tid == 0) io.e1[cta] = expf(esum);
+  }
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);
@@ -705,23 +790,32 @@ bool chunk_supported(const ScanGeom& g) {
   return (g.R == 1 || g.R == 2 || g.R == 4 || g.R == 8) && g.N <= 128 && g.P <= 128;
 }
 
+int chunk_rows_per_token(const ScanGeom& g) { return kRows / g.R; }
+
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
-                              cudaStream_t s) {
+                              const ChunkIO& io, bool summary, cudaStream_t s) {
   const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
-  const unsigned grid = (unsigned)(g.B * g.H);
+  const unsigned grid = (unsigned)(g.B * g.H * io.nseg);
   const bool mimo = a.mimo_o != nullptr;
   auto run = [&](auto kernel) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)lay.bytes);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, status);
+    kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, io, status);
     return cudaSuccess;
   };
   cudaError_t e;
-  if (lay.MP == 64)
-    e = mimo ? run(k_scan_chunk<64, true>) : run(k_scan_chunk<64, false>);
-  else
-    e = mimo ? run(k_scan_chunk<128, true>) : run(k_scan_chunk<128, false>);
+  if (summary) {
+    if (lay.MP == 64)
+      e = mimo ? run(k_scan_chunk<64, true, true>) : run(k_scan_chunk<64, false, true>);
+    else
+      e = mimo ? run(k_scan_chunk<128, true, true>) : run(k_scan_chunk<128, false, true>);
+  } else {
+    if (lay.MP == 64)
+      e = mimo ? run(k_scan_chunk<64, true, false>) : run(k_scan_chunk<64, false, false>);
+    else
+      e = mimo ? run(k_scan_chunk<128, true, false>) : run(k_scan_chunk<128, false, false>);
+  }
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();

@@ -50,7 +50,8 @@ __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
 }
 
 template <int NPT4, int RMAX>
-__global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay) {
+__global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay,
+                                                  StepState st) {
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
   float* sk = sm + lay.k;
@@ -74,19 +75,35 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   const int p = p0 + pi;
   const bool row_ok = (pi < PT) && (p < P);
 
+  // Recurrent state: zero, or (with st.ssm set; one block per (b, h) then) the
+  // step state h [P,N], previous key [R,N], previous value [R,P] and cumulative
+  // angle, which are read here and overwritten with the final state at the end.
+  const bool has_state = st.ssm != nullptr;
+  float* hrow = has_state && row_ok ? st.ssm + ((int64_t)bh * P + p) * N : nullptr;
   float hst[NPT4 * 4];
 #pragma unroll
-  for (int i = 0; i < NPT4 * 4; ++i) hst[i] = 0.f;
+  for (int i = 0; i < NPT4; ++i) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int n = 4 * (j + 4 * i) + e;
+      hst[4 * i + e] = (hrow && n < N) ? hrow[n] : 0.f;
+    }
+  }
   float mx[RMAX], xprev[RMAX];
 #pragma unroll
   for (int r = 0; r < RMAX; ++r) {
     mx[r] = (r < R && row_ok) ? (a.mimo_x ? a.mimo_x[((int64_t)h * R + r) * P + p] : 1.f) : 0.f;
-    xprev[r] = 0.f;
+    xprev[r] = (has_state && r < R && row_ok) ? st.v[((int64_t)bh * R + r) * P + p] : 0.f;
   }
   const float dskip = g.has_d ? a.d[h] : 0.f;
-  // previous-token key slot starts at zero; the running angle lives in sth[(kT-1)*A + a]
-  for (int i = tid; i < R * Npad; i += nthr) sk[i] = 0.f;
-  for (int i = tid; i < A; i += nthr) sth[(kT - 1) * A + i] = 0.f;
+  // previous-token key slot (zero or the state's key); the running angle lives
+  // in sth[(kT-1)*A + a]
+  for (int i = tid; i < R * Npad; i += nthr) {
+    const int r = i / Npad, n = i - r * Npad;
+    sk[i] = (has_state && n < N) ? st.k[((int64_t)bh * R + r) * N + n] : 0.f;
+  }
+  for (int i = tid; i < A; i += nthr)
+    sth[(kT - 1) * A + i] = (has_state && st.angle) ? st.angle[(int64_t)bh * A + i] : 0.f;
   __syncthreads();
 
   for (int t0 = 0; t0 < L; t0 += kT) {
@@ -258,16 +275,37 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
     }
     // carry the last token's key into slot 0
     for (int i = tid; i < R * Npad; i += nthr) sk[i] = sk[(size_t)tv * R * Npad + i];
-    if (tv < kT) {
-      // final tile: nothing follows
-    }
     __syncthreads();
+  }
+  if (has_state) {
+#pragma unroll
+    for (int i = 0; i < NPT4; ++i) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int n = 4 * (j + 4 * i) + e;
+        if (hrow && n < N) hrow[n] = hst[4 * i + e];
+      }
+    }
+    for (int i = tid; i < R * Npad; i += nthr) {
+      const int r = i / Npad, n = i - r * Npad;
+      if (n < N) st.k[((int64_t)bh * R + r) * N + n] = sk[i];
+    }
+    if (row_ok && j == 0) {
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+        if (r < R) st.v[((int64_t)bh * R + r) * P + p] = xprev[r];
+    }
+    if (st.angle)
+      for (int i = tid; i < A; i += nthr) st.angle[(int64_t)bh * A + i] = sth[(kT - 1) * A + i];
   }
 }
 
 template <int NPT4, int RMAX>
-cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
-  const int PT = (RMAX > 1 || a.mimo_o) ? g.P : (g.P < 32 ? g.P : 32);
+cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                         cudaStream_t s) {
+  // one block per (b, h) for MIMO (block-local output norm) and with state
+  // (the per-(b, h) key / angle state is read first and written last)
+  const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
   const SeqLayout lay = seq_layout(g.N, PT, g.R, g.A);
   const int threads = ((PT * 4 + 31) / 32) * 32;
   const int ptiles = (g.P + PT - 1) / PT;
@@ -275,26 +313,29 @@ cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)lay.bytes);
   if (e != cudaSuccess) return e;
-  k_scan_seq<NPT4, RMAX><<<(unsigned)(g.B * g.H * ptiles), threads, lay.bytes, s>>>(g, a, lay);
+  k_scan_seq<NPT4, RMAX><<<(unsigned)(g.B * g.H * ptiles), threads, lay.bytes, s>>>(g, a, lay,
+                                                                                    st);
   count_launches(1);
   return cudaGetLastError();
 }
 
 template <int RMAX>
-cudaError_t launch_seq_r(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
+cudaError_t launch_seq_r(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                         cudaStream_t s) {
   const int npt4 = ((g.N + 15) / 16);
-  if (npt4 <= 1) return launch_seq_t<1, RMAX>(g, a, s);
-  if (npt4 <= 2) return launch_seq_t<2, RMAX>(g, a, s);
-  if (npt4 <= 4) return launch_seq_t<4, RMAX>(g, a, s);
-  return launch_seq_t<8, RMAX>(g, a, s);
+  if (npt4 <= 1) return launch_seq_t<1, RMAX>(g, a, st, s);
+  if (npt4 <= 2) return launch_seq_t<2, RMAX>(g, a, st, s);
+  if (npt4 <= 4) return launch_seq_t<4, RMAX>(g, a, st, s);
+  return launch_seq_t<8, RMAX>(g, a, st, s);
 }
 
 }  // namespace
 
-cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, cudaStream_t s) {
-  if (g.R == 1 && !a.mimo_o) return launch_seq_r<1>(g, a, s);
-  if (g.R <= 4) return launch_seq_r<4>(g, a, s);
-  return launch_seq_r<8>(g, a, s);
+cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                            cudaStream_t s) {
+  if (g.R == 1 && !a.mimo_o) return launch_seq_r<1>(g, a, st, s);
+  if (g.R <= 4) return launch_seq_r<4>(g, a, st, s);
+  return launch_seq_r<8>(g, a, st, s);
 }
 
 }  // namespace m3

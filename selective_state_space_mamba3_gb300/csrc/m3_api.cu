@@ -83,22 +83,107 @@ int check_angle_ptr(const void* p, int A) {
 
 // Scan dispatch. TF32 mode runs the tcgen05 chunked kernel where its tiles
 // apply (R in {1,2,4,8}, P, N <= 128); FP32-exact mode and every other shape
-// run the token-sequential FP32 kernel on the CUDA cores. The chunked kernel
-// needs a workspace for its device status word.
+// run the token-sequential FP32 kernel on the CUDA cores.
 static bool use_chunk(const ScanGeom& g) {
   return g.math_mode == M3_MATH_TF32 && chunk_supported(g);
 }
 
-size_t scan_workspace_bytes(const ScanGeom& g) { return use_chunk(g) ? 256 : 0; }
+// Sequences per launch below two per SM (GB300: 152 SMs) are split into
+// segments of whole chunks, at least four chunks long: a summary pass, a
+// prefix over segments and the main pass then replace one long serial chain.
+static int choose_nseg(const ScanGeom& g) {
+  const int64_t bh = (int64_t)g.B * g.H;
+  const int64_t target = 2 * 152;
+  if (bh >= target) return 1;
+  const int64_t qt = chunk_rows_per_token(g);
+  const int64_t max_seg = g.L / (4 * qt);
+  int64_t n = target / bh;
+  if (n > max_seg) n = max_seg;
+  if (n > 4096) n = 4096;
+  return n < 1 ? 1 : (int)n;
+}
 
-cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, void* ws, size_t, cudaStream_t s) {
-  if (use_chunk(g)) {
-    uint32_t* status = static_cast<uint32_t*>(ws);
-    cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+namespace {
+// Workspace layout of the chunked path (byte offsets, 256-byte aligned).
+struct ChunkWs {
+  size_t status, gsum, thsum, esum, gentry, thentry, g0, th0, bytes;
+  int nseg, seg_len;
+};
+
+ChunkWs chunk_ws(const ScanGeom& g, bool with_state) {
+  ChunkWs w;
+  const size_t bh = (size_t)g.B * g.H, pn = (size_t)g.P * g.N, A = (size_t)g.A;
+  w.nseg = choose_nseg(g);
+  const int qt = chunk_rows_per_token(g);
+  const int per = (g.L + w.nseg - 1) / w.nseg;
+  w.seg_len = (per + qt - 1) / qt * qt;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  w.status = take(256);
+  const size_t ns = w.nseg > 1 ? bh * (size_t)w.nseg : 0;
+  w.gsum = take(ns * pn * 4);
+  w.thsum = take(ns * A * 4);
+  w.esum = take(ns * 4);
+  w.gentry = take(ns * pn * 4);
+  w.thentry = take(ns * A * 4);
+  w.g0 = take(with_state ? bh * pn * 4 : 0);
+  w.th0 = take(with_state ? bh * A * 4 : 0);
+  w.bytes = off;
+  return w;
+}
+}  // namespace
+
+size_t scan_workspace_bytes(const ScanGeom& g, bool with_state) {
+  return use_chunk(g) ? chunk_ws(g, with_state).bytes : 0;
+}
+
+cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
+                        size_t, cudaStream_t s) {
+  if (!use_chunk(g)) return launch_scan_seq(g, a, st ? *st : StepState{}, s);
+  const ChunkWs w = chunk_ws(g, st != nullptr);
+  char* base = static_cast<char*>(ws);
+  auto f = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
+  uint32_t* status = reinterpret_cast<uint32_t*>(base + w.status);
+  cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+  if (e != cudaSuccess) return e;
+  if (st) {
+    e = launch_state_init(g, a, *st, f(w.g0), f(w.th0), s);
     if (e != cudaSuccess) return e;
-    return launch_scan_chunk(g, a, status, s);
   }
-  return launch_scan_seq(g, a, s);
+  ChunkIO io{};
+  io.seg_len = w.seg_len;
+  io.nseg = w.nseg;
+  if (st) {
+    io.g_last = st->ssm;
+    io.th_last = st->angle;
+    io.k_last = st->k;
+    io.v_last = st->v;
+  }
+  if (w.nseg == 1) {
+    if (st) {
+      io.g0 = f(w.g0);
+      io.th0 = f(w.th0);
+    }
+    return launch_scan_chunk(g, a, status, io, false, s);
+  }
+  ChunkIO sum{};
+  sum.seg_len = w.seg_len;
+  sum.nseg = w.nseg;
+  sum.g1 = f(w.gsum);
+  sum.th1 = f(w.thsum);
+  sum.e1 = f(w.esum);
+  e = launch_scan_chunk(g, a, status, sum, true, s);
+  if (e != cudaSuccess) return e;
+  e = launch_state_prefix(g, w.nseg, st ? f(w.g0) : nullptr, st ? f(w.th0) : nullptr, f(w.gsum),
+                          f(w.thsum), f(w.esum), f(w.gentry), f(w.thentry), s);
+  if (e != cudaSuccess) return e;
+  io.g0 = f(w.gentry);
+  io.th0 = f(w.thentry);
+  return launch_scan_chunk(g, a, status, io, false, s);
 }
 
 }  // namespace m3
@@ -156,7 +241,7 @@ int m3_siso_forward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
   if (!bytes) return M3_ERR_INVALID_ARGUMENT;
   int st = resolve_ssm(cfg, false, &g);
   if (st != M3_OK) return st;
-  *bytes = scan_workspace_bytes(g);
+  *bytes = scan_workspace_bytes(g, false);
   return M3_OK;
 }
 
@@ -165,23 +250,31 @@ int m3_mimo_forward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
   if (!bytes) return M3_ERR_INVALID_ARGUMENT;
   int st = resolve_ssm(cfg, true, &g);
   if (st != M3_OK) return st;
-  *bytes = scan_workspace_bytes(g);
+  *bytes = scan_workspace_bytes(g, false);
   return M3_OK;
 }
 
-static int scan_common(const m3_ssm_config* cfg, bool mimo, const ScanArgs& a, void* ws,
-                       size_t ws_bytes, m3_stream_t stream) {
+static int scan_common(const m3_ssm_config* cfg, bool mimo, const ScanArgs& a,
+                       const StepState* st, void* ws, size_t ws_bytes, m3_stream_t stream) {
   ScanGeom g;
-  int st = resolve_ssm(cfg, mimo, &g);
-  if (st != M3_OK) return st;
-  st = check_ptrs({a.c, a.b, a.x, a.z, a.adt, a.dt, a.trap, a.c_bias, a.b_bias, a.d, a.out});
-  if (st != M3_OK) return st;
-  if ((st = check_angle_ptr(a.angle, g.A)) != M3_OK) return st;
-  if (mimo && (st = check_ptrs({a.mimo_x, a.mimo_z, a.mimo_o, a.norm_weight})) != M3_OK) return st;
-  const size_t need = scan_workspace_bytes(g);
+  int status = resolve_ssm(cfg, mimo, &g);
+  if (status != M3_OK) return status;
+  status = check_ptrs({a.c, a.b, a.x, a.z, a.adt, a.dt, a.trap, a.c_bias, a.b_bias, a.d, a.out});
+  if (status != M3_OK) return status;
+  if ((status = check_angle_ptr(a.angle, g.A)) != M3_OK) return status;
+  if (mimo && (status = check_ptrs({a.mimo_x, a.mimo_z, a.mimo_o, a.norm_weight})) != M3_OK)
+    return status;
+  if (st) {
+    if (!count_below_u32({g.B, g.H, g.P, g.N}) || !count_below_u32({g.B, g.H, g.R, g.N}) ||
+        !count_below_u32({g.B, g.H, g.R, g.P}) || !count_below_u32({g.B, g.H, g.A}))
+      return M3_ERR_INVALID_ARGUMENT;
+    if ((status = check_ptrs({st->ssm, st->k, st->v})) != M3_OK) return status;
+    if ((status = check_angle_ptr(st->angle, g.A)) != M3_OK) return status;
+  }
+  const size_t need = scan_workspace_bytes(g, st != nullptr);
   if (need > 0 && (!ws || ws_bytes < need)) return M3_ERR_WORKSPACE;
   if (ws && !aligned16(ws)) return M3_ERR_UNALIGNED;
-  return cuda_status(launch_scan(g, a, ws, ws_bytes, (cudaStream_t)stream));
+  return cuda_status(launch_scan(g, a, st, ws, ws_bytes, (cudaStream_t)stream));
 }
 
 int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
@@ -191,7 +284,7 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     m3_stream_t stream) {
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              nullptr, nullptr, nullptr, nullptr, out};
-  return scan_common(cfg, false, a, workspace, workspace_bytes, stream);
+  return scan_common(cfg, false, a, nullptr, workspace, workspace_bytes, stream);
 }
 
 int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
@@ -202,7 +295,50 @@ int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     void* workspace, size_t workspace_bytes, m3_stream_t stream) {
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              mimo_x, mimo_z, mimo_o, norm_weight, out};
-  return scan_common(cfg, true, a, workspace, workspace_bytes, stream);
+  return scan_common(cfg, true, a, nullptr, workspace, workspace_bytes, stream);
+}
+
+int m3_siso_prefill_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  int st = resolve_ssm(cfg, false, &g);
+  if (st != M3_OK) return st;
+  *bytes = scan_workspace_bytes(g, true);
+  return M3_OK;
+}
+
+int m3_mimo_prefill_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  int st = resolve_ssm(cfg, true, &g);
+  if (st != M3_OK) return st;
+  *bytes = scan_workspace_bytes(g, true);
+  return M3_OK;
+}
+
+int m3_siso_prefill(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, float* ssm_state, float* angle_state, float* k_state,
+                    float* v_state, float* out, void* workspace, size_t workspace_bytes,
+                    m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             nullptr, nullptr, nullptr, nullptr, out};
+  StepState s{ssm_state, angle_state, k_state, v_state};
+  return scan_common(cfg, false, a, &s, workspace, workspace_bytes, stream);
+}
+
+int m3_mimo_prefill(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
+                    const float* z, const float* adt, const float* dt, const float* trap,
+                    const float* angle, const float* c_bias, const float* b_bias,
+                    const float* d, const float* mimo_x, const float* mimo_z,
+                    const float* mimo_o, const float* norm_weight, float* ssm_state,
+                    float* angle_state, float* k_state, float* v_state, float* out,
+                    void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             mimo_x, mimo_z, mimo_o, norm_weight, out};
+  StepState s{ssm_state, angle_state, k_state, v_state};
+  return scan_common(cfg, true, a, &s, workspace, workspace_bytes, stream);
 }
 
 static int step_common(const m3_ssm_config* cfg, bool mimo, const ScanArgs& a,

@@ -37,6 +37,24 @@ struct PreOut {
   float *x, *z, *bh, *ch, *dt, *adt, *trap, *angle;
 };
 
+// Recurrent-state inputs / outputs of the chunked scan. A CTA handles segment
+// `seg` of sequence `bh`: tokens [seg * seg_len, min(L, (seg + 1) * seg_len)).
+// States are "pre-loaded" (h plus the next token's trapezoid term), fp32,
+// [cta][P][N] with cta = bh * nseg + seg; angles [cta][A].
+struct ChunkIO {
+  int seg_len, nseg;
+  const float* g0;   // initial state per CTA (null: zero)
+  const float* th0;  // initial cumulative angle per CTA (null: zero)
+  float* g1;         // final state per CTA (null: not written)
+  float* th1;        // final cumulative angle per CTA
+  float* e1;         // exp(sum of adt over the segment) per CTA
+  // written by the CTA whose segment ends the sequence, indexed by bh:
+  float* g_last;     // [BH][P][N] final state (= h after token L-1)
+  float* th_last;    // [BH][A] final cumulative angle
+  float* k_last;     // [BH][R][N] rotated, biased key of token L-1 (fp32)
+  float* v_last;     // [BH][R][P] rank-scaled value of token L-1
+};
+
 // Device status word written by bounded waits (lives in the caller's workspace).
 constexpr uint32_t kStatusTimeout = 0x54494d45u;  // "TIME"
 
@@ -46,15 +64,26 @@ cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const fl
                               const PreOut& o, cudaStream_t s);
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                         cudaStream_t s);
-cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, cudaStream_t s);
+// st: optional step state (null ssm: zero state, nothing written back).
+cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                            cudaStream_t s);
+cudaError_t launch_state_init(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                              float* g0, float* th0, cudaStream_t s);
+cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, const float* g_init,
+                                const float* th_init, const float* gsum, const float* thsum,
+                                const float* esum, float* g_entry, float* th_entry,
+                                cudaStream_t s);
 bool chunk_supported(const ScanGeom& g);
+// summary: state-only pass (no outputs), used to split long sequences.
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
-                              cudaStream_t s);
+                              const ChunkIO& io, bool summary, cudaStream_t s);
+int chunk_rows_per_token(const ScanGeom& g);  // 64 / R: tokens per chunk
 
-// Scan entry chosen by the host: workspace bytes for geometry g, then launch.
-size_t scan_workspace_bytes(const ScanGeom& g);
-cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, void* ws, size_t ws_bytes,
-                        cudaStream_t s);
+// Scan entry chosen by the host: workspace bytes for geometry g (with or
+// without a recurrent state), then launch (st null: zero state).
+size_t scan_workspace_bytes(const ScanGeom& g, bool with_state);
+cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
+                        size_t ws_bytes, cudaStream_t s);
 
 void count_launches(uint64_t n);
 
