@@ -3,181 +3,117 @@
 // [B,H,A], previous key [B,H,R,N], previous value [B,H,R,P]).
 //
 // One 256-thread block per (b, h). The [P, N] state is the only large operand
-// (96% of the bytes at decode shapes), so the kernel is an HBM stream over it:
-// warp w owns rows p = w, w + 8, ...; lane l owns the float4 at n = 4l (N <= 128
-// gives one float4 per lane per row), reads it once with a 128-bit load,
-// applies the exponential-trapezoidal update
+// (96% of the bytes at decode shapes), so the kernel is an HBM stream over it.
+// When N is a multiple of 4 the block moves the whole state with two bulk
+// copies (cp.async.bulk): the load is issued first and lands in shared memory
+// while the block stages the rotated q / k rows and the previous key / value;
+// the state is then updated in place by the exponential-trapezoidal rule
 //   h = decay * h + scale * decay * sum_r v_prev[r][p] k_prev[r][n]
 //                 + gamma * sum_r v[r][p] k[r][n]
-// and writes it back once, while the readout h . q_r is reduced across the
-// warp with shuffles. The rotated q/k rows, the previous key/value and the
-// new angle are staged in shared memory first; k/v/angle states are written
-// after the block has read their previous values.
+// (warp w owns rows w, w + 8, ..., lane l the float4 at n = 4l; the readout
+// h . q_r is reduced with shuffles) and goes back with one bulk store that
+// overlaps the output stage. Other N take a register path with the same
+// arithmetic. The k / v / angle states are written after the block has read
+// their previous values.
 #include "m3_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace m3 {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr long long kWaitBudget = 2000000000LL;  // clock cycles (about a second)
 
+template <int RMAX>
 struct StepSmem {
-  float q[8 * 128], k[8 * 128], kp[8 * 128];  // [R][N]
-  float v[8 * 128], vp[8 * 128];              // [R][P]
-  float y[8 * 128];                           // [R][P] readouts
+  float q[RMAX * 128], k[RMAX * 128], kp[RMAX * 128];  // [R][N]
+  float v[RMAX * 128], vp[RMAX * 128];                 // [R][P]
+  float y[RMAX * 128];                                 // [R][P] readouts
   float zz[128];
   float theta[64];
   float red[kWarps];
 };
 
-template <int RMAX, bool VEC>
-__global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepState st) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  StepSmem& sm = *reinterpret_cast<StepSmem*>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / g.H, h = bh % g.H;
+template <int RMAX>
+__host__ __device__ constexpr size_t step_smem_head() {
+  return (sizeof(StepSmem<RMAX>) + 127) / 128 * 128;
+}
+
+// Stages the per-(b, h) operands: the new cumulative angle, the rotated biased
+// q / k per rank, the previous key / value, the rank-scaled value and z. The
+// units (one rotary pair or lone column of q / k per rank, one value element
+// per rank, one z element) are spread over the block so that each thread's
+// loads are independent and issue together; all state writes (angle, key,
+// value) follow a single block barrier, after every previous value is read.
+template <int RMAX>
+__device__ __forceinline__ void stage_step(StepSmem<RMAX>& sm, const ScanGeom& g,
+                                           const ScanArgs& a, const StepState& st, int b, int h,
+                                           int64_t sc, float dtv) {
+  const int tid = threadIdx.x;
   const int grp = h / (g.H / g.G);
   const int P = g.P, N = g.N, A = g.A, R = g.R;
-  const int64_t sc = (int64_t)b * g.H + h;  // [B,1,H] index
+  const int UQ = R * N, UV = R * P, U = UQ + UV + P;
+  for (int u = tid; u < U; u += kThreads) {
+    if (u < UQ) {
+      const int r = u / N, n = u - r * N;
+      const int64_t row = ((int64_t)b * g.G * R + (int64_t)grp * R + r) * N;
+      const float* cb = a.c_bias + ((int64_t)h * R + r) * N;
+      const float* bb = a.b_bias + ((int64_t)h * R + r) * N;
+      sm.kp[u] = st.k[sc * R * N + u];
+      if (n < A) {
+        const float th = st.angle[sc * A + n] + dtv * a.angle[(int64_t)b * A + n];
+        const float qu = a.c[row + n] + cb[n], qv = a.c[row + n + A] + cb[n + A];
+        const float ku = a.b[row + n] + bb[n], kv = a.b[row + n + A] + bb[n + A];
+        if (r == 0) sm.theta[n] = th;
+        float sn, cs;
+        sincosf(th, &sn, &cs);
+        sm.q[r * N + n] = qu * cs - qv * sn;
+        sm.q[r * N + n + A] = qu * sn + qv * cs;
+        sm.k[r * N + n] = ku * cs - kv * sn;
+        sm.k[r * N + n + A] = ku * sn + kv * cs;
+      } else if (n >= 2 * A) {
+        sm.q[u] = a.c[row + n] + cb[n];
+        sm.k[u] = a.b[row + n] + bb[n];
+      }
+    } else if (u < UQ + UV) {
+      const int i = u - UQ;
+      const int r = i / P, p = i - r * P;
+      const float xv = a.x[sc * P + p];
+      sm.vp[i] = st.v[sc * R * P + i];
+      sm.v[i] = a.mimo_x ? xv * a.mimo_x[((int64_t)h * R + r) * P + p] : xv;
+    } else {
+      const int p = u - UQ - UV;
+      sm.zz[p] = a.z[sc * P + p];
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < A; i += kThreads) st.angle[sc * A + i] = sm.theta[i];
+  for (int i = tid; i < R * N; i += kThreads) st.k[sc * R * N + i] = sm.k[i];
+  for (int i = tid; i < R * P; i += kThreads) st.v[sc * R * P + i] = sm.v[i];
+}
 
-  // 0. issue the loads of this warp's first group of state rows (one float4 per
-  // lane per row, rows p = warp + 8i) so that their latency overlaps staging.
-  float* hs = st.ssm + sc * (int64_t)P * N;
-  constexpr int kGroup = 4;
-  float4 hreg[kGroup];
-  if (VEC) {
+// Readout of row p: y_r[p] = sum_n h[p][n] q_r[n] (+ D v_r[p]); acc holds the
+// lane's partial sums.
+template <int RMAX>
+__device__ __forceinline__ void finish_row(StepSmem<RMAX>& sm, int R, int P, int p, float dskip,
+                                           const float* acc) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int u = 0; u < kGroup; ++u) {
-      const int p = warp + kWarps * u;
-      if (p < P && lane < (N >> 2)) hreg[u] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
+  for (int r = 0; r < RMAX; ++r) {
+    if (r < R) {
+      const float yv = warp_sum(acc[r]);
+      if (lane == 0) sm.y[r * P + p] = yv + dskip * sm.v[r * P + p];
     }
   }
-  const float dtv = a.dt[sc];
-  // 1. cumulative angle theta = angle_state + dt * angle (per head).
-  for (int i = tid; i < A; i += kThreads) {
-    const float th = st.angle[sc * A + i] + dtv * a.angle[(int64_t)b * A + i];
-    sm.theta[i] = th;
-    st.angle[sc * A + i] = th;
-  }
-  __syncthreads();
-  // 2. rotated, biased q/k per rank; previous key/value; x, z.
-  for (int idx = tid; idx < R * N; idx += kThreads) {
-    const int r = idx / N, n = idx - r * N;
-    const int64_t row = ((int64_t)b * g.G * R + (int64_t)grp * R + r) * N;
-    const float* cb = a.c_bias + ((int64_t)h * R + r) * N;
-    const float* bb = a.b_bias + ((int64_t)h * R + r) * N;
-    sm.kp[idx] = st.k[(sc * R + r) * N + n];
-    if (n < A) {
-      float sn, cs;
-      sincosf(sm.theta[n], &sn, &cs);
-      const float qu = a.c[row + n] + cb[n], qv = a.c[row + n + A] + cb[n + A];
-      const float ku = a.b[row + n] + bb[n], kv = a.b[row + n + A] + bb[n + A];
-      sm.q[r * N + n] = qu * cs - qv * sn;
-      sm.q[r * N + n + A] = qu * sn + qv * cs;
-      sm.k[r * N + n] = ku * cs - kv * sn;
-      sm.k[r * N + n + A] = ku * sn + kv * cs;
-    } else if (n >= 2 * A) {
-      sm.q[idx] = a.c[row + n] + cb[n];
-      sm.k[idx] = a.b[row + n] + bb[n];
-    }
-  }
-  for (int idx = tid; idx < R * P; idx += kThreads) {
-    const int r = idx / P, p = idx - r * P;
-    const float xv = a.x[sc * P + p];
-    sm.v[idx] = a.mimo_x ? xv * a.mimo_x[((int64_t)h * R + r) * P + p] : xv;
-    sm.vp[idx] = st.v[(sc * R + r) * P + p];
-  }
-  for (int p = tid; p < P; p += kThreads) sm.zz[p] = a.z[sc * P + p];
-  __syncthreads();
-  // 3. new previous-key / previous-value states (old values already staged).
-  for (int idx = tid; idx < R * N; idx += kThreads) st.k[sc * R * N + idx] = sm.k[idx];
-  for (int idx = tid; idx < R * P; idx += kThreads) st.v[sc * R * P + idx] = sm.v[idx];
+}
 
-  // 4. state update + readout. Coefficients of the exponential-trapezoidal rule.
-  const float lam = sigmoid_f(a.trap[sc]);
-  const float decay = expf(a.adt[sc]);
-  const float gam = lam * dtv;
-  const float sdec = (1.0f - lam) * dtv * decay;
-  const float dskip = g.has_d ? a.d[h] : 0.0f;
-  // Readout of row p: y_r[p] = sum_n h[p][n] q_r[n] (+ D v_r[p]).
-  auto finish_row = [&](int p, const float* acc) {
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < R) {
-        const float yv = warp_sum(acc[r]);
-        if (lane == 0) sm.y[r * P + p] = yv + dskip * sm.v[r * P + p];
-      }
-    }
-  };
-  if (VEC) {
-    const int N4 = N >> 2;
-    for (int i0 = 0; warp + kWarps * i0 < P; i0 += kGroup) {
-      if (i0 > 0) {
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-          const int p = warp + kWarps * (i0 + u);
-          if (p < P && lane < N4) hreg[u] = __ldcs(reinterpret_cast<const float4*>(hs + (int64_t)p * N) + lane);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        const int p = warp + kWarps * (i0 + u);
-        if (p >= P) break;
-        float acc[RMAX];
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-        if (lane < N4) {
-          float4 hv = hreg[u];
-          float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
-              const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[lane];
-              const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[lane];
-              upd.x += cp * kp4.x + cc * k4.x;
-              upd.y += cp * kp4.y + cc * k4.y;
-              upd.z += cp * kp4.z + cc * k4.z;
-              upd.w += cp * kp4.w + cc * k4.w;
-            }
-          }
-          hv.x = decay * hv.x + upd.x;
-          hv.y = decay * hv.y + upd.y;
-          hv.z = decay * hv.z + upd.z;
-          hv.w = decay * hv.w + upd.w;
-          __stcs(reinterpret_cast<float4*>(hs + (int64_t)p * N) + lane, hv);
-#pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[lane];
-              acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
-            }
-          }
-        }
-        finish_row(p, acc);
-      }
-    }
-  } else {
-    for (int p = warp; p < P; p += kWarps) {
-      float acc[RMAX];
-#pragma unroll
-      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-      for (int n = lane; n < N; n += 32) {
-        float upd = 0.f;
-        for (int r = 0; r < R; ++r)
-          upd += sdec * sm.vp[r * P + p] * sm.kp[r * N + n] + gam * sm.v[r * P + p] * sm.k[r * N + n];
-        const float hv = decay * hs[(int64_t)p * N + n] + upd;
-        hs[(int64_t)p * N + n] = hv;
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-          if (r < R) acc[r] += hv * sm.q[r * N + n];
-      }
-      finish_row(p, acc);
-    }
-  }
-  __syncthreads();
-  // 5. gate (SISO) or per-rank gate + mimo_o contraction + output norm (MIMO).
+// Gate (SISO), or per-rank gate + mimo_o contraction + output RMS norm (MIMO).
+template <int RMAX>
+__device__ __forceinline__ void step_output(StepSmem<RMAX>& sm, const ScanGeom& g,
+                                            const ScanArgs& a, int h, int64_t sc) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = g.P, R = g.R;
   float* outp = a.out + sc * P;
   if (!a.mimo_o) {
     for (int p = tid; p < P; p += kThreads) {
@@ -207,29 +143,168 @@ __global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepS
   if (p < P) outp[p] = ov;
 }
 
+// Bulk-copy path (N % 4 == 0): the state travels HBM -> shared -> HBM as two
+// cp.async.bulk transfers of P * N * 4 bytes (a multiple of 16; the state base
+// is 16-byte aligned by the host checks).
+template <int RMAX>
+__global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : 4) k_step_bulk(ScanGeom g, ScanArgs a, StepState st) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  StepSmem<RMAX>& sm = *reinterpret_cast<StepSmem<RMAX>*>(smem_raw);
+  float* hsm = reinterpret_cast<float*>(smem_raw + step_smem_head<RMAX>());
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int arrived;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / g.H, h = bh % g.H;
+  const int P = g.P, N = g.N, R = g.R;
+  const int64_t sc = (int64_t)b * g.H + h;  // [B,1,H] index
+  float* hs = st.ssm + sc * (int64_t)P * N;
+  const uint32_t bytes = (uint32_t)(P * N) * 4u;
+  if (tid == 0) {
+    tc::bar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(&bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_u32(hsm)),
+        "l"(hs), "r"(bytes), "r"(tc::smem_u32(&bar))
+        : "memory");
+    arrived = 1;
+  }
+  const float dtv = a.dt[sc];
+  stage_step<RMAX>(sm, g, a, st, b, h, sc, dtv);
+  const float lam = sigmoid_f(a.trap[sc]);
+  const float decay = expf(a.adt[sc]);
+  const float gam = lam * dtv;
+  const float sdec = (1.0f - lam) * dtv * decay;
+  const float dskip = g.has_d ? a.d[h] : 0.0f;
+  if (!tc::bar_wait(&bar, 0, kWaitBudget)) arrived = 0;
+  __syncthreads();
+  if (!arrived) {
+    // The copy did not complete in time: the ssm state row stays as it was and
+    // the output row is NaN. Wait (bounded) once more so that no copy into
+    // shared memory outlives the block.
+    tc::bar_wait(&bar, 0, kWaitBudget);
+    for (int p = tid; p < P; p += kThreads) a.out[sc * P + p] = __int_as_float(0x7fc00000);
+    return;
+  }
+  const int N4 = N >> 2;
+  for (int p = warp; p < P; p += kWarps) {
+    float acc[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+    if (lane < N4) {
+      float4* hp = reinterpret_cast<float4*>(hsm + p * N) + lane;
+      float4 hv = *hp;
+      float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        if (r < R) {
+          const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
+          const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[lane];
+          const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[lane];
+          upd.x += cp * kp4.x + cc * k4.x;
+          upd.y += cp * kp4.y + cc * k4.y;
+          upd.z += cp * kp4.z + cc * k4.z;
+          upd.w += cp * kp4.w + cc * k4.w;
+        }
+      }
+      hv.x = decay * hv.x + upd.x;
+      hv.y = decay * hv.y + upd.y;
+      hv.z = decay * hv.z + upd.z;
+      hv.w = decay * hv.w + upd.w;
+      *hp = hv;
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) {
+        if (r < R) {
+          const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[lane];
+          acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
+        }
+      }
+    }
+    finish_row<RMAX>(sm, R, P, p, dskip, acc);
+  }
+  // generic-proxy writes of the updated rows -> visible to the bulk store
+  tc::fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(hs),
+                 "r"(tc::smem_u32(hsm)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  step_output<RMAX>(sm, g, a, h, sc);
+  // shared memory must stay valid until the store has read it
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Register path for N not a multiple of 4.
+template <int RMAX>
+__global__ void __launch_bounds__(kThreads) k_step(ScanGeom g, ScanArgs a, StepState st) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  StepSmem<RMAX>& sm = *reinterpret_cast<StepSmem<RMAX>*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / g.H, h = bh % g.H;
+  const int P = g.P, N = g.N, R = g.R;
+  const int64_t sc = (int64_t)b * g.H + h;
+  float* hs = st.ssm + sc * (int64_t)P * N;
+  const float dtv = a.dt[sc];
+  stage_step<RMAX>(sm, g, a, st, b, h, sc, dtv);
+  const float lam = sigmoid_f(a.trap[sc]);
+  const float decay = expf(a.adt[sc]);
+  const float gam = lam * dtv;
+  const float sdec = (1.0f - lam) * dtv * decay;
+  const float dskip = g.has_d ? a.d[h] : 0.0f;
+  for (int p = warp; p < P; p += kWarps) {
+    float acc[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+    for (int n = lane; n < N; n += 32) {
+      float upd = 0.f;
+      for (int r = 0; r < R; ++r)
+        upd += sdec * sm.vp[r * P + p] * sm.kp[r * N + n] + gam * sm.v[r * P + p] * sm.k[r * N + n];
+      const float hv = decay * hs[(int64_t)p * N + n] + upd;
+      hs[(int64_t)p * N + n] = hv;
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r)
+        if (r < R) acc[r] += hv * sm.q[r * N + n];
+    }
+    finish_row<RMAX>(sm, R, P, p, dskip, acc);
+  }
+  __syncthreads();
+  step_output<RMAX>(sm, g, a, h, sc);
+}
+
+template <int RMAX>
+cudaError_t launch_step_r(const ScanGeom& g, const ScanArgs& a, const StepState& st,
+                          cudaStream_t s) {
+  const unsigned grid = (unsigned)(g.B * g.H);
+  cudaError_t e;
+  if (g.N % 4 == 0) {
+    const size_t smem = step_smem_head<RMAX>() + (size_t)g.P * g.N * 4;
+    e = cudaFuncSetAttribute(k_step_bulk<RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    k_step_bulk<RMAX><<<grid, kThreads, smem, s>>>(g, a, st);
+  } else {
+    const size_t smem = sizeof(StepSmem<RMAX>);
+    e = cudaFuncSetAttribute(k_step<RMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    k_step<RMAX><<<grid, kThreads, smem, s>>>(g, a, st);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                         cudaStream_t s) {
-  const bool vec = (g.N % 4 == 0);
-  const size_t smem = sizeof(StepSmem);
-  const unsigned grid = (unsigned)(g.B * g.H);
-  cudaError_t e;
-#define M3_STEP_LAUNCH(RM, V)                                                              \
-  do {                                                                                     \
-    e = cudaFuncSetAttribute(k_step<RM, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                             (int)smem);                                                   \
-    if (e != cudaSuccess) return e;                                                        \
-    k_step<RM, V><<<grid, kThreads, smem, s>>>(g, a, st);                                  \
-  } while (0)
-  if (g.R == 1) {
-    if (vec) M3_STEP_LAUNCH(1, true); else M3_STEP_LAUNCH(1, false);
-  } else {
-    if (vec) M3_STEP_LAUNCH(8, true); else M3_STEP_LAUNCH(8, false);
-  }
-#undef M3_STEP_LAUNCH
-  count_launches(1);
-  return cudaGetLastError();
+  return g.R == 1 ? launch_step_r<1>(g, a, st, s) : launch_step_r<8>(g, a, st, s);
 }
 
 }  // namespace m3
