@@ -22,17 +22,22 @@
 // transposed (TMEM lane = p): each output column p is finished by the two
 // lanes that share its TMEM row (D skip, SiLU gate, the MIMO mimo_o
 // contraction over its R rows) and, through shared memory, the MIMO output
-// RMS norm. Rotary cos/sin, the local log-decay cumsum and the trapezoid
-// weights are formed by the CUDA cores while staging operands; every operand
-// is rounded to TF32 (round to nearest).
+// RMS norm. Every operand is rounded to TF32 (round to nearest).
 //
 // One CTA of 256 threads runs one (b, h) sequence chunk after chunk; thread 0
-// issues the MMAs and the CTA waits on mbarriers signalled by tcgen05.commit.
+// issues the MMAs, and threads wait on mbarriers signalled by tcgen05.commit.
+// Staging is warp-local: warp w owns rows 8w .. 8w + 7 of the chunk (its
+// tokens' scalars, rotary angles and the q / k / w-scaled transposed key
+// tiles), so only three block barriers remain per chunk (after the per-warp
+// totals, before the first and before the second MMA batch). The state update
+// of a chunk runs on under its epilogue and the next chunk's scalar work.
 // Waits are bounded: on timeout the kernel records a status word and exits.
-// Shared memory (about 100 KB for P <= 64, N = 128: the tiles share three
-// regions whose contents change phase by phase) and TMEM (256 columns) admit
-// two CTAs per SM, and the next chunk's inputs are prefetched into L2 while
-// the current chunk runs.
+// Shared memory (about 101 KB for P <= 64, N = 128) and TMEM (256 columns)
+// admit two CTAs per SM, and the next chunk's inputs are prefetched into L2
+// while the current chunk runs.
+//
+// The kernel is a template over the shape: the generic instance reads N, A, R
+// and P at run time; instances for common shapes have them as constants.
 #include "m3_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -42,42 +47,47 @@ namespace {
 constexpr int kRows = 64;       // (token, rank) rows per chunk
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTok = 72;        // per-token scalar array stride (>= 65)
+constexpr int kTok = 72;        // per-token array stride (>= 65)
+constexpr int kAngMax = 64;     // A <= 64
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
 
 struct ChunkLayout {
-  int Npad, MP, CS;
-  int q, k, kt, bias, tok, thbase;  // float offsets of the regions
+  int Npad, MP;
+  int q, k, kt, tot, bias, tok, thbase;  // float offsets of the regions
   size_t bytes;
 };
 
 int imax(int a, int b) { return a > b ? a : b; }
 
 ChunkLayout chunk_layout(int N, int P, int A, int R) {
+  (void)A;
   ChunkLayout l;
   l.Npad = (N + 15) / 16 * 16;
   l.MP = P <= 64 ? 64 : 128;
-  l.CS = (A + 4) & ~3;  // cos / sin table row stride (16-byte rows, A + 1 <= CS)
+  const int Qt = kRows / R;
   int off = 0;
   auto take = [&](int floats) {
     int o = off;
     off += (floats + 31) / 32 * 32;  // 128-byte aligned regions
     return o;
   };
-  // Q region: q tile [64][Npad] until the first MMA batch completes, then the
-  // masked scores [64][64] followed by the values X^T [MP][64].
-  l.q = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
-  // K region: k tile [64][Npad]; MIMO norm staging [64][MP] in the epilogue.
-  l.k = take(kRows * imax(l.Npad, l.MP));
-  // Kt region: rotary angle increments, then cos / sin tables [64][CS] each
-  // while the q/k tiles are formed, then the w-scaled transposed keys [Npad][64].
-  l.kt = take(imax(l.Npad * kRows, 2 * kRows * l.CS));
-  l.bias = take(2 * R * l.Npad);  // c_bias, b_bias of this head, zero-padded
-  l.tok = take(8 * kTok);
-  l.thbase = take(64);
+  // Q region: q tile [64][Npad]; each warp's 8-row block first holds that
+  // warp's rotary angles; MIMO norm staging [Qt][MP] in the epilogue.
+  l.q = take(imax(kRows * l.Npad, Qt * l.MP));
+  // K region: k tile [64][Npad] until S = Q K^T completes, then the masked
+  // scores [64][64] followed by the values X^T [MP][64].
+  l.k = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
+  // Kt region: w-scaled transposed keys [Npad][64] (K-major, K = row).
+  l.kt = take(l.Npad * kRows);
+  l.tot = take(kWarps * kAngMax + kWarps);  // per-warp angle / log-decay totals
+  l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
+  l.tok = take(4 * kTok);                   // cum, e^cum, gamma, w per token
+  l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
   l.bytes = (size_t)off * sizeof(float);
   return l;
 }
+
+__host__ __device__ constexpr int ilog2c(int v) { return v <= 1 ? 0 : 1 + ilog2c(v >> 1); }
 
 // sin and cos of v: Cody-Waite reduction by 2 pi (2 pi split into its float
 // value and the float remainder), then the SFU sine / cosine on [-pi, pi]
@@ -95,20 +105,23 @@ __device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
 }
 
 // Per-token scalars and angle increments of one chunk, loaded into registers
-// one chunk ahead (thread t <= Qt holds token t's dt / adt / trap; the angle
-// increments follow the (token = warp + 8 i, angle = lane + 32 j) tiling of
-// the staging loop).
+// one chunk ahead. Warp w owns tokens TPW * w .. TPW * w + TPW - 1 (TPW = 8 /
+// R); lane i <= TPW holds the dt / adt / trap of token TPW * w + i (lane TPW:
+// the first token after the warp's, whose trapezoid scale the warp's last
+// token needs), and ang[2 i + j] is the increment of angle lane + 32 j of the
+// warp's token i.
 struct TokenPreload {
   float dt, adt, trap;
   float ang[16];
 };
 
 __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs& a, int64_t tok,
-                                               int cn, int L, int Qt, int A, int H, int h,
-                                               int tid, int warp, int lane) {
+                                               int cn, int L, int TPW, int A, int H, int h,
+                                               int warp, int lane) {
   pl.dt = pl.adt = pl.trap = 0.f;
-  if (tid <= Qt && cn + tid < L) {
-    const int64_t sc = (tok + tid) * H + h;
+  const int tw = TPW * warp + lane;
+  if (lane <= TPW && cn + tw < L) {
+    const int64_t sc = (tok + tw) * H + h;
     pl.dt = a.dt[sc];
     pl.adt = a.adt[sc];
     pl.trap = a.trap[sc];
@@ -117,8 +130,9 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
   for (int i = 0; i < 8; ++i) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const int t = warp + 8 * i, aa = lane + 32 * j;
-      pl.ang[2 * i + j] = (t < Qt && aa < A && cn + t < L) ? a.angle[(tok + t) * A + aa] : 0.f;
+      const int t = TPW * warp + i, aa = lane + 32 * j;
+      pl.ang[2 * i + j] =
+          (i < TPW && aa < A && cn + t < L) ? a.angle[(tok + t) * A + aa] : 0.f;
     }
   }
 }
@@ -127,7 +141,7 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-template <int MP, bool MIMO, bool SUMMARY>
+template <int MP, bool MIMO, bool SUMMARY, int KN, int KA, int KR, int KP>
 __global__ void __launch_bounds__(kThreads, 2)
     k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, ChunkIO io, uint32_t* status) {
   extern __shared__ __align__(1024) float sm[];
@@ -137,10 +151,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = g.H, L = g.L, P = g.P, N = g.N, A = g.A, R = g.R;
-  const int lgR = __ffs(R) - 1;  // R is a power of two here
-  const int Npad = lay.Npad;
+  const int H = g.H, L = g.L;
+  const int P = KP ? KP : g.P;
+  const int N = KN ? KN : g.N;
+  const int A = KA ? KA : g.A;
+  const int R = KR ? KR : g.R;
+  const int lgR = KR ? ilog2c(KR) : __ffs(R) - 1;  // R is a power of two here
+  const int Npad = KN ? (KN + 15) / 16 * 16 : lay.Npad;
   const int Qt = kRows >> lgR;  // tokens per chunk
+  const int TPW = Qt >> 3;      // tokens per warp
   const int cta = blockIdx.x;
   const int bh = cta / io.nseg, seg = cta - bh * io.nseg;
   const int b = bh / H, h = bh % H;
@@ -151,25 +170,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int RG = g.G * R;
 
   float* sQ = sm + lay.q;              // [64 rows][Npad] K-major, K = n
-  float* sP = sQ;                      // [64][64]        masked scores (after batch 1)
-  float* sXt = sQ + kRows * kRows;     // [MP][64 rows]   values (after batch 1)
+  float* sO = sQ;                      // [Qt][MP]        MIMO epilogue staging
   float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
-  float* sO = sK;                      // [Qt][MP]        MIMO epilogue staging
-  const int CS = lay.CS;
-  float* sCos = sm + lay.kt;           // [Qt][CS]        angle increments, then cos
-  float* sSin = sCos + kRows * CS;     // [Qt][CS]        sin
+  float* sP = sK;                      // [64][64]        masked scores (after S)
+  float* sXt = sK + kRows * kRows;     // [MP][64 rows]   values (after S)
+  float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
+  float* sTot = sm + lay.tot;          // [8 warps][64]   per-warp angle totals
+  float* sTotAdt = sTot + kWarps * kAngMax;  // [8 warps] per-warp log-decay totals
   float* sBiasC = sm + lay.bias;       // [R][Npad]
   float* sBiasB = sBiasC + R * Npad;   // [R][Npad]
-  float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
-  float* tAdt = sm + lay.tok;
-  float* tCum = tAdt + kTok;
-  float* tEc = tCum + kTok;   // e^{cum_t}
-  float* tGam = tEc + kTok;   // gamma_t
-  float* tScl = tGam + kTok;  // scale_t, t in [0, Qt]
-  float* tW = tScl + kTok;    // gamma_t + scale_{t+1}
-  float* tOm = tW + kTok;     // e^{cum_end - cum_t} * tW[t]
-  float* tDt = tOm + kTok;
-  float* sThBase = sm + lay.thbase;
+  float* tCum = sm + lay.tok;          // local cumulative log decay
+  float* tEc = tCum + kTok;            // e^{cum_t}
+  float* tGam = tEc + kTok;            // gamma_t
+  float* tW = tGam + kTok;             // gamma_t + scale_{t+1}
+  float* sThBase = sm + lay.thbase;    // [2][64] cumulative angle before the chunk
+  const int AS = A + 4;                // angle row stride of a warp's angle block
+  float* sTh = sQ + warp * 8 * Npad;   // this warp's angles [TPW][AS] (in its q rows)
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) tc::bar_init(&bars[i], 1);
@@ -182,6 +198,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int r = i / Npad, n = i - r * Npad;
     sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
     sBiasB[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
+  }
+  // padding rows N .. Npad of the transposed key tile stay zero
+  for (int i = tid; i < (Npad - N) * kRows; i += kThreads) {
+    const int n = N + i / kRows, rho = i % kRows;
+    sKt[tc::kmaj(n, rho, kRows)] = 0.f;
   }
   tc::fence_before();
   __syncthreads();
@@ -229,13 +250,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc::fence_after();
 
   TokenPreload pl;
-  preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, Qt, A, H, h, tid, warp, lane);
+  preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
   float esum = 0.f;  // sum of adt over the segment
 
   int it = 0;
   for (int c0 = l0; c0 < l1; c0 += Qt, ++it) {
     const int tv = min(Qt, l1 - c0);
     const int64_t tok0 = (int64_t)b * L + c0;   // first token of the chunk in [B, L]
+    const float* thb_cur = sThBase + (it & 1) * kAngMax;
+    float* thb_next = sThBase + ((it & 1) ^ 1) * kAngMax;
     // (0) L2 prefetch of the next chunk's operands. The next chunk's blocks of
     // x, z, C, B, dt, adt, trap and angle are contiguous across the heads of a
     // batch row, so the H CTAs of that row (resident together) each prefetch
@@ -264,104 +287,114 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (s1 > s0) tc::prefetch_l2(reinterpret_cast<const void*>(s0), (uint32_t)(s1 - s0));
       }
     }
-    // (1) per-token scalars of tokens c0 .. c0 + Qt (the last one is the next
-    // chunk's first token: only its trapezoid scale is used); angle increments
-    if (tid <= Qt) {
-      const int t = tid;
-      float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
-      if (c0 + t < L) {
+    // (1) per-warp token scalars; local (within the warp's tokens) inclusive
+    // sums of the log decay and of dt * angle, whose warp totals go to shared
+    // memory. Lane i <= TPW: token TPW * warp + i.
+    const int tw = TPW * warp + lane;
+    float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
+    if (lane <= TPW) {
+      const float lam = sigmoid_f(pl.trap);
+      if (c0 + tw < L) scl = (1.0f - lam) * pl.dt;
+      if (tw < tv && lane < TPW) {
         dtv = pl.dt;
         adtv = pl.adt;
-        const float lam = sigmoid_f(pl.trap);
-        gam = lam * dtv;
-        scl = (1.0f - lam) * dtv;
+        gam = lam * pl.dt;
       }
-      tScl[t] = scl;
-      if (t < Qt) {
-        const bool in = t < tv;
-        tAdt[t] = in ? adtv : 0.f;
-        tGam[t] = in ? gam : 0.f;
-        tDt[t] = in ? dtv : 0.f;
+    }
+    float cl = adtv;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, cl, o);
+      if (o < TPW && lane >= o) cl += u;
+    }
+    const float adt_tot = __shfl_sync(0xffffffffu, cl, TPW - 1);
+    if (lane == 0) sTotAdt[warp] = adt_tot;
+    float thl[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float d = __shfl_sync(0xffffffffu, dtv, i);
+        if (i < TPW) s = fmaf(d, pl.ang[2 * i + j], s);
+        thl[j][i] = s;
       }
+      const int aa = lane + 32 * j;
+      if (aa < A) sTot[warp * kAngMax + aa] = s;
+    }
+    __syncthreads();  // B1: totals visible; previous chunk's epilogue finished
+    if (abort_flag) break;
+    // (2) per-token coefficients (lane i < TPW) and this warp's angles
+    float cend = 0.f, cbase = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float v = sTotAdt[w];
+      if (w < warp) cbase += v;
+      cend += v;
+    }
+    esum += cend;
+    const float cum = cbase + cl;
+    const float wt = gam + __shfl_down_sync(0xffffffffu, scl, 1);
+    const float om = (lane < TPW && tw < tv) ? expf(cend - cum) * wt : 0.f;
+    if (lane < TPW) {
+      tCum[tw] = cum;
+      tEc[tw] = expf(cum);
+      tGam[tw] = gam;
+      tW[tw] = wt;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int j = 0; j < 2; ++j) {
+      const int aa = lane + 32 * j;
+      if (aa < A) {
+        float base = thb_cur[aa];
+        for (int w = 0; w < warp; ++w) base += sTot[w * kAngMax + aa];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int t = warp + 8 * i, aa = lane + 32 * j;
-        if (t < Qt && aa < A) sCos[t * CS + aa] = pl.ang[2 * i + j];
+        for (int i = 0; i < 8; ++i)
+          if (i < TPW) sTh[i * AS + aa] = base + thl[j][i];
+        if (warp == kWarps - 1) thb_next[aa] = base + thl[j][TPW - 1];
       }
     }
-    __syncthreads();
-    // (2) local cumulative log decay (warp 0, two tokens per lane); rotary
-    // angle: per-angle scan of dt * angle over the chunk, then cos / sin of
-    // each (token, angle) once
-    if (warp == 0) {
-      const int t0 = 2 * lane, t1 = 2 * lane + 1;
-      const float a0 = t0 < Qt ? tAdt[t0] : 0.f, a1 = t1 < Qt ? tAdt[t1] : 0.f;
-      float s = a0 + a1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float v = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += v;
-      }
-      const float ex = s - (a0 + a1);
-      if (t0 < Qt) tCum[t0] = ex + a0;
-      if (t1 < Qt) tCum[t1] = ex + a0 + a1;
+    __syncwarp();
+    // the previous chunk's state update must finish before its tiles are
+    // rewritten (and before the next Yo reads G)
+    if (it > 0) {
+      if (!tc::bar_wait(&bars[3], (it - 1) & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
     }
-    for (int aa = warp; aa < A; aa += kWarps) {
-      float v0 = lane < Qt ? tDt[lane] * sCos[lane * CS + aa] : 0.f;
-      float v1 = lane + 32 < Qt ? tDt[lane + 32] * sCos[(lane + 32) * CS + aa] : 0.f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float u0 = __shfl_up_sync(0xffffffffu, v0, o);
-        const float u1 = __shfl_up_sync(0xffffffffu, v1, o);
-        if (lane >= o) {
-          v0 += u0;
-          v1 += u1;
-        }
-      }
-      v1 += __shfl_sync(0xffffffffu, v0, 31);
-      const float base = sThBase[aa];
-      const float th0 = base + v0, th1 = base + v1;
-      const float last = __shfl_sync(0xffffffffu, Qt > 32 ? th1 : th0, Qt > 32 ? Qt - 33 : Qt - 1);
-      if (lane < Qt) sincos_fast(th0, &sSin[lane * CS + aa], &sCos[lane * CS + aa]);
-      if (lane + 32 < Qt) sincos_fast(th1, &sSin[(lane + 32) * CS + aa], &sCos[(lane + 32) * CS + aa]);
-      __syncwarp();
-      if (lane == 0) sThBase[aa] = last;
-    }
-    __syncthreads();
-    // (3) decay / trapezoid coefficients
-    esum += tCum[Qt - 1];
-    if (tid < Qt) {
-      const int t = tid;
-      const float cum = tCum[t], cend = tCum[Qt - 1];
-      const float w = tGam[t] + tScl[t + 1];
-      tEc[t] = expf(cum);
-      tW[t] = w;
-      tOm[t] = expf(cend - cum) * w;
-    }
-    // (4a) rotated, biased q / k rows into the K-major q / k tiles.
-    if ((A & 3) == 0 && (N & 3) == 0) {
-      // Vector path: an item is 4 consecutive dims n0..n0+3 of one row; for
-      // n0 < A it also produces their rotary partners n0+A..n0+A+3. Lane l
-      // takes row 8 * rb + l % 8 and item 4 * jb + l / 8, so that each 16-byte
-      // store of the warp lands in a distinct 16-byte slot (512 contiguous
-      // bytes per warp).
-      const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
+    // (4) rows 8 * warp .. 8 * warp + 7: rotated, biased q / k into the K-major
+    // q / k tiles, w-scaled keys into the transposed key tile. Lane l takes
+    // row 8 * warp + l % 8 and items 4 * jb + l / 8, so that each 16-byte
+    // store of the warp lands in a distinct 16-byte slot.
+    const bool last_chunk = io.k_last && c0 + tv == L;
+    {
       const int rl = lane & 7, jl = lane >> 3;
+      const int rho = 8 * warp + rl;
+      const int t = rho >> lgR, r = rho & (R - 1);
+      const int ti = t - TPW * warp;  // token index within the warp
+      const bool in = t < tv;
+      const float omr = __shfl_sync(0xffffffffu, om, ti);
+      const int64_t roff = ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+      const float* crow = a.c + roff;
+      const float* brow = a.b + roff;
+      const float* cb = sBiasC + r * Npad;
+      const float* bb = sBiasB + r * Npad;
+      float* kl = last_chunk && t == tv - 1 ? io.k_last + ((int64_t)bh * R + r) * N : nullptr;
+      if ((A & 3) == 0 && (N & 3) == 0) {
+        // Vector path: an item is 4 consecutive dims n0..n0+3 of one row; for
+        // n0 < A it also produces their rotary partners n0+A..n0+A+3.
+        const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
+        // angles of this lane's rotary items, read before the q rows (which
+        // share this warp's angle block) are written
+        float4 th4[4];
+#pragma unroll
+        for (int jb = 0; jb < 4; ++jb) {
+          const int j = 4 * jb + jl;
+          th4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(sTh + ti * AS + 4 * j)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
 #pragma unroll 2
-      for (int item = warp; item < (kRows / 8) * QW4; item += kWarps) {
-        const int rb = item / QW4, jb = item - rb * QW4;
-        const int rho = 8 * rb + rl;
-        const int t = rho >> lgR, r = rho & (R - 1);
-        const bool in = t < tv;
-        const int64_t roff = ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-        const float* crow = a.c + roff;
-        const float* brow = a.b + roff;
-        const float* cb = sBiasC + r * Npad;
-        const float* bb = sBiasB + r * Npad;
-        {
+        for (int jb = 0; jb < QW4; ++jb) {
           const int j = 4 * jb + jl;
           if (j >= QW) continue;
           if (j < PQ) {
@@ -376,16 +409,23 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float4 cbw = *reinterpret_cast<const float4*>(cb + n0 + A);
               const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
               const float4 bbw = *reinterpret_cast<const float4*>(bb + n0 + A);
-              const float4 cs = *reinterpret_cast<const float4*>(sCos + t * CS + n0);
-              const float4 sn = *reinterpret_cast<const float4*>(sSin + t * CS + n0);
+              float4 th;
+              switch (jb) {  // registers, not a local array
+                case 0: th = th4[0]; break;
+                case 1: th = th4[1]; break;
+                case 2: th = th4[2]; break;
+                default: th = th4[3]; break;
+              }
 #define M3_ROT(E)                                                            \
   {                                                                          \
+    float sn, cs;                                                            \
+    sincos_fast(th.E, &sn, &cs);                                             \
     const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
     const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
-    q0.E = qu * cs.E - qw * sn.E;                                            \
-    q1.E = qu * sn.E + qw * cs.E;                                            \
-    k0.E = ku * cs.E - kw * sn.E;                                            \
-    k1.E = ku * sn.E + kw * cs.E;                                            \
+    q0.E = qu * cs - qw * sn;                                                \
+    q1.E = qu * sn + qw * cs;                                                \
+    k0.E = ku * cs - kw * sn;                                                \
+    k1.E = ku * sn + kw * cs;                                                \
   }
               M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
 #undef M3_ROT
@@ -393,9 +433,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!SUMMARY) {
               *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
               *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
+              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
+              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
             }
-            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
-            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
+            sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * k0.x);
+            sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * k0.y);
+            sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * k0.z);
+            sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * k0.w);
+            sKt[tc::kmaj(n0 + A, rho, kRows)] = tc::to_tf32(omr * k1.x);
+            sKt[tc::kmaj(n0 + A + 1, rho, kRows)] = tc::to_tf32(omr * k1.y);
+            sKt[tc::kmaj(n0 + A + 2, rho, kRows)] = tc::to_tf32(omr * k1.z);
+            sKt[tc::kmaj(n0 + A + 3, rho, kRows)] = tc::to_tf32(omr * k1.w);
+            if (kl) {
+              *reinterpret_cast<float4*>(kl + n0) = k0;
+              *reinterpret_cast<float4*>(kl + n0 + A) = k1;
+            }
           } else {
             const int n0 = 2 * A + 4 * (j - PQ);
             float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv;
@@ -407,32 +459,41 @@ __global__ void __launch_bounds__(kThreads, 2)
               qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
               kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
             }
-            if (!SUMMARY) *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
-            *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
+            if (!SUMMARY) {
+              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
+              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
+            }
+            sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * kv.x);
+            sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * kv.y);
+            sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * kv.z);
+            sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * kv.w);
+            if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
           }
         }
-      }
-    } else {
-      // Scalar path for A or N not a multiple of 4: unit u of a row is the
-      // rotary pair (u, u + A) for u < A, else the single dim u + A.
-      const int U = N - A;
-      const int U4 = (U + 3) >> 2;
-      const int rl = lane & 7, ul = lane >> 3;
-      for (int rb = 0; rb < kRows / 8; ++rb) {
-        const int rho = 8 * rb + rl;
-        const int t = rho >> lgR, r = rho & (R - 1);
-        const bool in = t < tv;
-        const float* crow = a.c + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-        const float* brow = a.b + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-        const float* cb = sBiasC + r * Npad;
-        const float* bb = sBiasB + r * Npad;
-        for (int ub = warp; ub < U4; ub += kWarps) {
-          const int u = 4 * ub + ul;
+      } else {
+        // Scalar path for A or N not a multiple of 4: unit u of a row is the
+        // rotary pair (u, u + A) for u < A, else the single dim u + A.
+        const int U = N - A;
+        const int U4 = (U + 3) >> 2;
+        float thr[16];
+#pragma unroll
+        for (int ub = 0; ub < 16; ++ub) {
+          const int u = 4 * ub + jl;
+          thr[ub] = u < A ? sTh[ti * AS + u] : 0.f;
+        }
+        __syncwarp();
+        for (int ub = 0; ub < U4; ++ub) {
+          const int u = 4 * ub + jl;
           if (u >= U) continue;
           if (u < A) {
             float q0 = 0.f, q1 = 0.f, k0 = 0.f, k1 = 0.f;
             if (in) {
-              const float cs = sCos[t * CS + u], sn = sSin[t * CS + u];
+              float th = 0.f;
+#pragma unroll
+              for (int x = 0; x < 16; ++x)
+                if (x == ub) th = thr[x];
+              float sn, cs;
+              sincos_fast(th, &sn, &cs);
               const float qu = crow[u] + cb[u], qw = crow[u + A] + cb[u + A];
               const float ku = brow[u] + bb[u], kw = brow[u + A] + bb[u + A];
               q0 = qu * cs - qw * sn;
@@ -443,9 +504,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!SUMMARY) {
               sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
               sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
+              sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
+              sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
             }
-            sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
-            sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
+            sKt[tc::kmaj(u, rho, kRows)] = tc::to_tf32(omr * k0);
+            sKt[tc::kmaj(u + A, rho, kRows)] = tc::to_tf32(omr * k1);
+            if (kl) {
+              kl[u] = k0;
+              kl[u + A] = k1;
+            }
           } else {
             const int n = u + A;
             float qv = 0.f, kv = 0.f;
@@ -453,62 +520,30 @@ __global__ void __launch_bounds__(kThreads, 2)
               qv = crow[n] + cb[n];
               kv = brow[n] + bb[n];
             }
-            if (!SUMMARY) sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
-            sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
+            if (!SUMMARY) {
+              sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
+              sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
+            }
+            sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(omr * kv);
+            if (kl) kl[n] = kv;
           }
         }
       }
-    }
-    // key of the sequence's last token in fp32 for the step state (last chunk only)
-    if (io.k_last && c0 + tv == L) {
-      const int t = tv - 1;
-      for (int i = tid; i < R * (N - A); i += kThreads) {
-        const int r = i / (N - A), u = i - r * (N - A);
-        const float* brow = a.b + ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-        const float* bb = sBiasB + r * Npad;
-        float* kl = io.k_last + ((int64_t)bh * R + r) * N;
-        if (u < A) {
-          const float cs = sCos[t * CS + u], sn = sSin[t * CS + u];
-          const float ku = brow[u] + bb[u], kw = brow[u + A] + bb[u + A];
-          kl[u] = ku * cs - kw * sn;
-          kl[u + A] = ku * sn + kw * cs;
-        } else {
-          kl[u + A] = brow[u + A] + bb[u + A];
-        }
-      }
-    }
-    // zero padding columns N .. Npad
-    for (int i = tid; i < kRows * (Npad - N); i += kThreads) {
-      const int rho = i / (Npad - N), n = N + i % (Npad - N);
-      sQ[tc::kmaj(rho, n, Npad)] = 0.f;
-      sK[tc::kmaj(rho, n, Npad)] = 0.f;
-    }
-    __syncthreads();
-    // (4b) w-scaled transposed keys Kt[n][row] = w_t * k[row][n] from the
-    // TF32 k tile: lane l reads the 16 bytes of row 8 * rb + l % 8, dims
-    // 4 * (4 * nb + l / 8) .. +3 (conflict-free), and writes them as four
-    // scalars of column `row` of Kt.
-    {
-      const int rl = lane & 7, nl = lane >> 3;
-      const int NQ = Npad >> 2;
-      for (int rb = 0; rb < kRows / 8; ++rb) {
-        const int rho = 8 * rb + rl;
-        const int t = rho >> lgR;
-        const float om = t < tv ? tOm[t] : 0.f;
-        for (int nb = warp; nb < (NQ >> 2); nb += kWarps) {
-          const int n0 = 4 * (4 * nb + nl);
-          const float4 kv = *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad));
-          sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(om * kv.x);
-          sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(om * kv.y);
-          sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(om * kv.z);
-          sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(om * kv.w);
+      // zero padding columns N .. Npad of this warp's q / k rows
+      if (!SUMMARY && Npad > N) {
+        const int pad = Npad > N ? Npad - N : 1;
+        for (int i = lane; i < 8 * (Npad - N); i += 32) {
+          const int rr = 8 * warp + i / pad, n = N + i % pad;
+          sQ[tc::kmaj(rr, n, Npad)] = 0.f;
+          sK[tc::kmaj(rr, n, Npad)] = 0.f;
         }
       }
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    __syncthreads();  // B2: tiles complete
     tc::fence_after();
+    if (abort_flag) break;
     // (5) S = Q K^T and Yo^T = G Q^T
     if (!SUMMARY && tid == 0) {
       for (int ks = 0; ks < Npad / 8; ++ks)
@@ -518,16 +553,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::mma_ts(tYo, tG + ks * 8, tc::kdesc(sQ, Npad, ks), id_Y, ks > 0);
       tc::commit(&bars[1]);
     }
-    if (!SUMMARY) {
-      if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
-      tc::fence_after();
-      __syncthreads();
-      if (abort_flag) break;
-    }
     // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
     // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
-    // block of row l), values X^T, and G *= e^{cum_end}. The value loads are
-    // issued first so that their latency overlaps the mask.
+    // block of row l) and values X^T, both into the K region once S is done;
+    // then G *= e^{cum_end} once Yo has read G. The value loads are issued
+    // first so that their latency overlaps the wait.
     {
       constexpr int kXr = (kRows / 4 + kWarps - 1) / kWarps;  // row blocks per warp
       float xreg[kXr][MP / 8];
@@ -551,36 +581,38 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (!SUMMARY) {
-      const int rho = 16 * quad + (lane & 15);
-      const int t = rho >> lgR;
-      const float cum_t = tCum[t];
-      const float gam_t = tGam[t];
-      const int sh = lane >> 4;
-      for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
-        float v[16];
-        tc::tmem_ld16(tS + lane_base + cb * 16, v);
-        float w8[8];
+        if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
+        tc::fence_after();
+        const int rho = 16 * quad + (lane & 15);
+        const int t = rho >> lgR;
+        const float cum_t = tCum[t];
+        const float gam_t = tGam[t];
+        const int sh = lane >> 4;
+        for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
+          float v[16];
+          tc::tmem_ld16(tS + lane_base + cb * 16, v);
+          float w8[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float hi = __shfl_sync(0xffffffffu, v[j + 8], lane & 15);
-          w8[j] = sh ? hi : v[j];
-        }
-        const int col0 = cb * 16 + 8 * sh;
+          for (int j = 0; j < 8; ++j) {
+            const float hi = __shfl_sync(0xffffffffu, v[j + 8], lane & 15);
+            w8[j] = sh ? hi : v[j];
+          }
+          const int col0 = cb * 16 + 8 * sh;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int s = (col0 + j) >> lgR;
-          float m = 0.f;
-          if (s < t)
-            m = __expf(cum_t - tCum[s]) * tW[s];
-          else if (s == t)
-            m = gam_t;
-          w8[j] = tc::to_tf32(w8[j] * m);
+          for (int j = 0; j < 8; ++j) {
+            const int s = (col0 + j) >> lgR;
+            float m = 0.f;
+            if (s < t)
+              m = __expf(cum_t - tCum[s]) * tW[s];
+            else if (s == t)
+              m = gam_t;
+            w8[j] = tc::to_tf32(w8[j] * m);
+          }
+          *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0, kRows)) =
+              make_float4(w8[0], w8[1], w8[2], w8[3]);
+          *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0 + 4, kRows)) =
+              make_float4(w8[4], w8[5], w8[6], w8[7]);
         }
-        *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0, kRows)) =
-            make_float4(w8[0], w8[1], w8[2], w8[3]);
-        *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0 + 4, kRows)) =
-            make_float4(w8[4], w8[5], w8[6], w8[7]);
-      }
       }
       // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pb +
       // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores)
@@ -610,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
         tc::fence_after();
       }
-      const float ec = expf(tCum[Qt - 1]);
+      const float ec = expf(cend);
       for (int c = 16 * wg; c < Npad; c += 32) {
         float v[16];
         tc::tmem_ld16(tG + lane_base + c, v);
@@ -621,10 +653,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    __syncthreads();  // B3: scores, values and the rescaled state complete
     tc::fence_after();
-    // (7) Yi^T = X^T P^T and G += X^T (w K)
     if (abort_flag) break;
+    // (7) Yi^T = X^T P^T and G += X^T (w K)
     if (tid == 0) {
       if (!SUMMARY) {
         for (int ks = 0; ks < kRows / 8; ++ks)
@@ -637,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     // next chunk's per-token scalars and angles: loads in flight during the
     // MMAs and the epilogue
-    if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, Qt, A, H, h, tid, warp, lane);
+    if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, TPW, A, H, h, warp, lane);
     if (!SUMMARY) {
       // SISO epilogue operands x, z of this thread's output column, loaded while
       // the MMAs run
@@ -646,10 +678,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!mimo) {
         const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
         const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
-  #pragma unroll
+#pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int col0 = (2 * wg + u) * 16 + 8 * half;
-  #pragma unroll
+#pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const int t = col0 + j;
             const bool ok = pvalid && t < tv;
@@ -661,8 +693,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       // the epilogue needs Yi only; the state update runs on under it
       if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
       tc::fence_after();
-      __syncthreads();
-      if (abort_flag) break;
       // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
       // two lanes of a row split each 16-column block into 8 + 8 columns.
       {
@@ -674,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
           tc::tmem_ld16(tS + lane_base + cb * 16, yi);
           if (MP == 64) {
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float ho = __shfl_sync(0xffffffffu, yo[j + 8], lane & 15);
               const float hi = __shfl_sync(0xffffffffu, yi[j + 8], lane & 15);
@@ -688,7 +718,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int col0 = cb * 16 + 8 * half;
           if (!mimo) {
             const int u = cb - 2 * wg;
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (t < tv) {
@@ -708,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               const float zv = g.has_z ? zcol[t * HP] : 0.f;
               const float ec = tEc[t];
               float o = 0.f;
-  #pragma unroll
+#pragma unroll
               for (int r = 0; r < kRmax; ++r) {
                 if (r < R) {
                   const int j = (tt << lgR) + r;
@@ -738,17 +768,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    // the state update must finish before the next chunk rewrites the tiles it
-    // reads and issues Yo^T = G Q^T
-    if (!tc::bar_wait(&bars[3], it & 1, kWaitBudget)) abort_flag = 1;
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    if (abort_flag) break;
   }
+  // the last state update
+  if (!abort_flag && it > 0) {
+    if (!tc::bar_wait(&bars[3], (it - 1) & 1, kWaitBudget)) abort_flag = 1;
+    tc::fence_after();
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
   if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
   if (!abort_flag) {
     // final state, cumulative angle and decay of this segment
+    const float* thb = sThBase + (it & 1) * kAngMax;
     if (io.g1) {
       float* g1 = io.g1 + ((int64_t)cta * P + prow) * N;
       for (int c = 16 * wg; c < Npad; c += 32) {
@@ -774,9 +806,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     if (io.th1)
-      for (int i = tid; i < A; i += kThreads) io.th1[(int64_t)cta * A + i] = sThBase[i];
+      for (int i = tid; i < A; i += kThreads) io.th1[(int64_t)cta * A + i] = thb[i];
     if (io.th_last && l1 == L)
-      for (int i = tid; i < A; i += kThreads) io.th_last[(int64_t)bh * A + i] = sThBase[i];
+      for (int i = tid; i < A; i += kThreads) io.th_last[(int64_t)bh * A + i] = thb[i];
     if (io.e1 && tid == 0) io.e1[cta] = expf(esum);
   }
   tc::fence_before();
@@ -784,10 +816,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_free(tbase, 256);
 }
 
+template <int KN, int KA, int KR, int KP>
+struct Shape {};
+
+template <int MP, bool MIMO, int KN, int KA, int KR, int KP>
+cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, const ChunkIO& io,
+                      bool summary, const ChunkLayout& lay, unsigned grid, cudaStream_t s) {
+  auto kernel = summary ? k_scan_chunk<MP, MIMO, true, KN, KA, KR, KP>
+                        : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)lay.bytes);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, io, status);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 bool chunk_supported(const ScanGeom& g) {
-  return (g.R == 1 || g.R == 2 || g.R == 4 || g.R == 8) && g.N <= 128 && g.P <= 128;
+  return (g.R == 1 || g.R == 2 || g.R == 4 || g.R == 8) && g.N <= 128 && g.P <= 128 &&
+         g.A <= kAngMax;
 }
 
 int chunk_rows_per_token(const ScanGeom& g) { return kRows / g.R; }
@@ -797,25 +845,21 @@ cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* st
   const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
   const unsigned grid = (unsigned)(g.B * g.H * io.nseg);
   const bool mimo = a.mimo_o != nullptr;
-  auto run = [&](auto kernel) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)lay.bytes);
-    if (e != cudaSuccess) return e;
-    kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, io, status);
-    return cudaSuccess;
-  };
   cudaError_t e;
-  if (summary) {
-    if (lay.MP == 64)
-      e = mimo ? run(k_scan_chunk<64, true, true>) : run(k_scan_chunk<64, false, true>);
-    else
-      e = mimo ? run(k_scan_chunk<128, true, true>) : run(k_scan_chunk<128, false, true>);
-  } else {
-    if (lay.MP == 64)
-      e = mimo ? run(k_scan_chunk<64, true, false>) : run(k_scan_chunk<64, false, false>);
-    else
-      e = mimo ? run(k_scan_chunk<128, true, false>) : run(k_scan_chunk<128, false, false>);
-  }
+  // shapes with compile-time constants: SISO P64 N128 with A = 32 or 64, MIMO
+  // R4 P64 N64 A32
+  if (!mimo && g.R == 1 && g.P == 64 && g.N == 128 && g.A == 32)
+    e = run_chunk<64, false, 128, 32, 1, 64>(g, a, status, io, summary, lay, grid, s);
+  else if (!mimo && g.R == 1 && g.P == 64 && g.N == 128 && g.A == 64)
+    e = run_chunk<64, false, 128, 64, 1, 64>(g, a, status, io, summary, lay, grid, s);
+  else if (mimo && g.R == 4 && g.P == 64 && g.N == 64 && g.A == 32)
+    e = run_chunk<64, true, 64, 32, 4, 64>(g, a, status, io, summary, lay, grid, s);
+  else if (lay.MP == 64)
+    e = mimo ? run_chunk<64, true, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s)
+             : run_chunk<64, false, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s);
+  else
+    e = mimo ? run_chunk<128, true, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s)
+             : run_chunk<128, false, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
