@@ -53,14 +53,20 @@ constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
 
 struct ChunkLayout {
   int Npad, MP;
-  int q, k, kt, tot, bias, tok, thbase;  // float offsets of the regions
+  int q, k, kt, tot, bias, tok, thbase, th, o;  // float offsets of the regions
   size_t bytes;
 };
 
+// Instances with compile-time N and A (A <= 32, both multiples of 4) stage the
+// C / B rows with cp.async straight into the q / k tile positions; their
+// rotary angles and MIMO norm staging then live in regions of their own.
+__host__ __device__ constexpr bool chunk_async(int KN, int KA) {
+  return KN > 0 && KA > 0 && KA <= 32 && KN % 4 == 0 && KA % 4 == 0;
+}
+
 int imax(int a, int b) { return a > b ? a : b; }
 
-ChunkLayout chunk_layout(int N, int P, int A, int R) {
-  (void)A;
+ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
   ChunkLayout l;
   l.Npad = (N + 15) / 16 * 16;
   l.MP = P <= 64 ? 64 : 128;
@@ -71,9 +77,10 @@ ChunkLayout chunk_layout(int N, int P, int A, int R) {
     off += (floats + 31) / 32 * 32;  // 128-byte aligned regions
     return o;
   };
-  // Q region: q tile [64][Npad]; each warp's 8-row block first holds that
-  // warp's rotary angles; MIMO norm staging [Qt][MP] in the epilogue.
-  l.q = take(imax(kRows * l.Npad, Qt * l.MP));
+  // Q region: q tile [64][Npad]; without cp.async staging each warp's 8-row
+  // block first holds that warp's rotary angles, and the MIMO norm staging
+  // [Qt][MP] uses the region in the epilogue.
+  l.q = take(async ? kRows * l.Npad : imax(kRows * l.Npad, Qt * l.MP));
   // K region: k tile [64][Npad] until S = Q K^T completes, then the masked
   // scores [64][64] followed by the values X^T [MP][64].
   l.k = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
@@ -83,6 +90,8 @@ ChunkLayout chunk_layout(int N, int P, int A, int R) {
   l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
   l.tok = take(4 * kTok);                   // cum, e^cum, gamma, w per token
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
+  l.th = async ? take(kWarps * (8 / R) * (A + 4)) : 0;  // per-warp angles [TPW][A + 4]
+  l.o = (async && mimo) ? take(Qt * l.MP) : 0;          // MIMO norm staging
   l.bytes = (size_t)off * sizeof(float);
   return l;
 }
@@ -170,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int RG = g.G * R;
 
   float* sQ = sm + lay.q;              // [64 rows][Npad] K-major, K = n
-  float* sO = sQ;                      // [Qt][MP]        MIMO epilogue staging
+  constexpr bool kAsync = chunk_async(KN, KA);
+  float* sO = (kAsync && MIMO) ? sm + lay.o : sQ;  // [Qt][MP] MIMO epilogue staging
   float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
   float* sP = sK;                      // [64][64]        masked scores (after S)
   float* sXt = sK + kRows * kRows;     // [MP][64 rows]   values (after S)
@@ -185,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* tW = tGam + kTok;             // gamma_t + scale_{t+1}
   float* sThBase = sm + lay.thbase;    // [2][64] cumulative angle before the chunk
   const int AS = A + 4;                // angle row stride of a warp's angle block
-  float* sTh = sQ + warp * 8 * Npad;   // this warp's angles [TPW][AS] (in its q rows)
+  // this warp's angles [TPW][AS] (without cp.async staging: in its q rows)
+  float* sTh = kAsync ? sm + lay.th + warp * TPW * AS : sQ + warp * 8 * Npad;
 
   if (tid == 0) {
     for (int i = 0; i < 4; ++i) tc::bar_init(&bars[i], 1);
@@ -249,6 +260,71 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc::fence_after();
 
+  // L2 prefetch plan: the blocks of x, z, C, B, dt, adt, trap and angle of a
+  // chunk are contiguous across the heads of a batch row, so the H CTAs of the
+  // row (resident together) each prefetch one 16-byte-aligned slice of every
+  // block; thread i < 8 handles block i.
+  uintptr_t pf_base = 0, pf_bytes = 0, pf_off0 = 0, pf_off1 = 0;
+  if (tid < 8) {
+    const float* base = nullptr;
+    int64_t per_tok = 0;  // floats per token
+    switch (tid) {
+      case 0: base = a.x; per_tok = HP; break;
+      case 1: base = a.z; per_tok = HP; break;
+      case 2: base = a.c; per_tok = (int64_t)RG * N; break;
+      case 3: base = a.b; per_tok = (int64_t)RG * N; break;
+      case 4: base = a.dt; per_tok = H; break;
+      case 5: base = a.adt; per_tok = H; break;
+      case 6: base = a.trap; per_tok = H; break;
+      default: base = a.angle; per_tok = A; break;
+    }
+    if (base && per_tok > 0) {
+      pf_base = reinterpret_cast<uintptr_t>(base);
+      pf_bytes = (uintptr_t)per_tok * sizeof(float);
+      const uintptr_t span = (uintptr_t)Qt * pf_bytes;
+      pf_off0 = span * h / H & ~uintptr_t(15);
+      pf_off1 = span * (h + 1) / H & ~uintptr_t(15);
+    }
+  }
+  // MMA operand descriptors; K step ks adds 16 * ks (256 bytes) to each
+  const uint64_t dQ = tc::kdesc(sQ, Npad, 0), dK = tc::kdesc(sK, Npad, 0);
+  const uint64_t dXt = tc::kdesc(sXt, kRows, 0), dP = tc::kdesc(sP, kRows, 0);
+  const uint64_t dKt = tc::kdesc(sKt, kRows, 0);
+
+  // Row and items of this lane in phase (4): row 8 * warp + l % 8, items
+  // 4 * jb + l / 8.
+  const int rl = lane & 7, jl = lane >> 3;
+  const int rho = 8 * warp + rl;
+  const int t = rho >> lgR, r = rho & (R - 1);
+  // cp.async staging: copies this lane's phase-(4) items of a chunk's C (or B)
+  // rows into the K-major tile positions that phase (4) rewrites in place
+  // (rows past the chunk's valid tokens are zero-filled).
+  auto copy_items = [&](const float* src, float* tile, int64_t tok_first, int tvn) {
+    const bool ok = t < tvn;
+    const float* row = src + (ok ? ((tok_first + t) * RG + (int64_t)grp * R + r) * N : 0);
+    const uint32_t nb = ok ? 16u : 0u;
+    const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
+#pragma unroll
+    for (int jb = 0; jb < QW4; ++jb) {
+      const int j = 4 * jb + jl;
+      if (j >= QW) continue;
+      if (j < PQ) {
+        const int n0 = 4 * j;
+        tc::cp_async16(tile + tc::kmaj(rho, n0, Npad), row + n0, nb);
+        tc::cp_async16(tile + tc::kmaj(rho, n0 + A, Npad), row + n0 + A, nb);
+      } else {
+        const int n0 = 2 * A + 4 * (j - PQ);
+        tc::cp_async16(tile + tc::kmaj(rho, n0, Npad), row + n0, nb);
+      }
+    }
+  };
+  if (kAsync) {
+    const int tv0 = min(Qt, l1 - l0);
+    if (!SUMMARY) copy_items(a.c, sQ, (int64_t)b * L + l0, tv0);
+    copy_items(a.b, sK, (int64_t)b * L + l0, tv0);
+    tc::cp_async_commit();
+  }
+
   TokenPreload pl;
   preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
   float esum = 0.f;  // sum of adt over the segment
@@ -259,31 +335,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t tok0 = (int64_t)b * L + c0;   // first token of the chunk in [B, L]
     const float* thb_cur = sThBase + (it & 1) * kAngMax;
     float* thb_next = sThBase + ((it & 1) ^ 1) * kAngMax;
-    // (0) L2 prefetch of the next chunk's operands. The next chunk's blocks of
-    // x, z, C, B, dt, adt, trap and angle are contiguous across the heads of a
-    // batch row, so the H CTAs of that row (resident together) each prefetch
-    // one 16-byte-aligned slice of every block.
-    if (c0 + Qt < l1 && tid < 8) {
+    // (0) L2 prefetch of the next chunk's operands (slices fixed before the loop)
+    if (pf_bytes && c0 + Qt < l1) {
       const int nv = min(Qt, l1 - c0 - Qt);
-      const int64_t ntok = tok0 + Qt;
-      const float* base = nullptr;
-      int64_t floats = 0;
-      switch (tid) {
-        case 0: base = a.x + ntok * HP; floats = (int64_t)nv * HP; break;
-        case 1: base = a.z + ntok * HP; floats = (int64_t)nv * HP; break;
-        case 2: base = a.c + ntok * RG * N; floats = (int64_t)nv * RG * N; break;
-        case 3: base = a.b + ntok * RG * N; floats = (int64_t)nv * RG * N; break;
-        case 4: base = a.dt + ntok * H; floats = (int64_t)nv * H; break;
-        case 5: base = a.adt + ntok * H; floats = (int64_t)nv * H; break;
-        case 6: base = a.trap + ntok * H; floats = (int64_t)nv * H; break;
-        default: base = a.angle + ntok * A; floats = (int64_t)nv * A; break;
-      }
-      const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
-      const uintptr_t hi = reinterpret_cast<uintptr_t>(base + floats);
-      if (floats > 0 && (lo & 15) == 0 && (hi & 15) == 0) {
-        const uintptr_t span = hi - lo;
-        const uintptr_t s0 = lo + (span * h / H & ~uintptr_t(15));
-        const uintptr_t s1 = (h + 1 == H) ? hi : lo + (span * (h + 1) / H & ~uintptr_t(15));
+      const uintptr_t lo = pf_base + (uintptr_t)(tok0 + Qt) * pf_bytes;
+      const uintptr_t hi = lo + (uintptr_t)nv * pf_bytes;
+      if (((lo | hi) & 15) == 0) {
+        const uintptr_t s0 = lo + pf_off0;
+        const uintptr_t s1 = (h + 1 == H) ? hi : min(lo + pf_off1, hi);
         if (s1 > s0) tc::prefetch_l2(reinterpret_cast<const void*>(s0), (uint32_t)(s1 - s0));
       }
     }
@@ -324,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();  // B1: totals visible; previous chunk's epilogue finished
     if (abort_flag) break;
+    const bool in = t < tv;  // this lane's phase-(4) row holds a valid token
+    const int64_t roff = ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
+    const float* crow = a.c + roff;
+    const float* brow = a.b + roff;
     // (2) per-token coefficients (lane i < TPW) and this warp's angles
     float cend = 0.f, cbase = 0.f;
 #pragma unroll
@@ -367,18 +430,71 @@ __global__ void __launch_bounds__(kThreads, 2)
     // store of the warp lands in a distinct 16-byte slot.
     const bool last_chunk = io.k_last && c0 + tv == L;
     {
-      const int rl = lane & 7, jl = lane >> 3;
-      const int rho = 8 * warp + rl;
-      const int t = rho >> lgR, r = rho & (R - 1);
       const int ti = t - TPW * warp;  // token index within the warp
-      const bool in = t < tv;
       const float omr = __shfl_sync(0xffffffffu, om, ti);
-      const int64_t roff = ((tok0 + t) * RG + (int64_t)grp * R + r) * N;
-      const float* crow = a.c + roff;
-      const float* brow = a.b + roff;
       const float* cb = sBiasC + r * Npad;
       const float* bb = sBiasB + r * Npad;
       float* kl = last_chunk && t == tv - 1 ? io.k_last + ((int64_t)bh * R + r) * N : nullptr;
+      // Rotary item: dims n0..n0+3 and their partners n0+A..n0+A+3.
+      auto pair_item = [&](int n0, float4 cu, float4 cw, float4 bu, float4 bw, float4 th) {
+        float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, k0 = q0, k1 = q0;
+        if (in) {
+          const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
+          const float4 cbw = *reinterpret_cast<const float4*>(cb + n0 + A);
+          const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
+          const float4 bbw = *reinterpret_cast<const float4*>(bb + n0 + A);
+#define M3_ROT(E)                                                            \
+  {                                                                          \
+    float sn, cs;                                                            \
+    sincos_fast(th.E, &sn, &cs);                                             \
+    const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
+    const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
+    q0.E = qu * cs - qw * sn;                                                \
+    q1.E = qu * sn + qw * cs;                                                \
+    k0.E = ku * cs - kw * sn;                                                \
+    k1.E = ku * sn + kw * cs;                                                \
+  }
+          M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
+#undef M3_ROT
+        }
+        if (!SUMMARY) {
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
+        }
+        sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * k0.x);
+        sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * k0.y);
+        sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * k0.z);
+        sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * k0.w);
+        sKt[tc::kmaj(n0 + A, rho, kRows)] = tc::to_tf32(omr * k1.x);
+        sKt[tc::kmaj(n0 + A + 1, rho, kRows)] = tc::to_tf32(omr * k1.y);
+        sKt[tc::kmaj(n0 + A + 2, rho, kRows)] = tc::to_tf32(omr * k1.z);
+        sKt[tc::kmaj(n0 + A + 3, rho, kRows)] = tc::to_tf32(omr * k1.w);
+        if (kl) {
+          *reinterpret_cast<float4*>(kl + n0) = k0;
+          *reinterpret_cast<float4*>(kl + n0 + A) = k1;
+        }
+      };
+      // Plain item: dims n0..n0+3 >= 2A.
+      auto single_item = [&](int n0, float4 cu, float4 bu) {
+        float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv;
+        if (in) {
+          const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
+          const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
+          qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
+          kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
+        }
+        if (!SUMMARY) {
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
+        }
+        sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * kv.x);
+        sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * kv.y);
+        sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * kv.z);
+        sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * kv.w);
+        if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
+      };
       if ((A & 3) == 0 && (N & 3) == 0) {
         // Vector path: an item is 4 consecutive dims n0..n0+3 of one row; for
         // n0 < A it also produces their rotary partners n0+A..n0+A+3.
@@ -393,22 +509,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncwarp();
-#pragma unroll 2
-        for (int jb = 0; jb < QW4; ++jb) {
-          const int j = 4 * jb + jl;
-          if (j >= QW) continue;
-          if (j < PQ) {
-            const int n0 = 4 * j;
-            float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, k0 = q0, k1 = q0;
-            if (in) {
-              const float4 cu = *reinterpret_cast<const float4*>(crow + n0);
-              const float4 cw = *reinterpret_cast<const float4*>(crow + n0 + A);
-              const float4 bu = *reinterpret_cast<const float4*>(brow + n0);
-              const float4 bw = *reinterpret_cast<const float4*>(brow + n0 + A);
-              const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
-              const float4 cbw = *reinterpret_cast<const float4*>(cb + n0 + A);
-              const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
-              const float4 bbw = *reinterpret_cast<const float4*>(bb + n0 + A);
+        if (kAsync) {
+          // operands staged by cp.async in the q / k tile positions
+          tc::cp_async_wait_all();
+#pragma unroll
+          for (int jb = 0; jb < QW4; ++jb) {
+            const int j = 4 * jb + jl;
+            if (j >= QW) continue;
+            if (j < PQ) {
+              const int n0 = 4 * j;
               float4 th;
               switch (jb) {  // registers, not a local array
                 case 0: th = th4[0]; break;
@@ -416,58 +525,40 @@ __global__ void __launch_bounds__(kThreads, 2)
                 case 2: th = th4[2]; break;
                 default: th = th4[3]; break;
               }
-#define M3_ROT(E)                                                            \
-  {                                                                          \
-    float sn, cs;                                                            \
-    sincos_fast(th.E, &sn, &cs);                                             \
-    const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
-    const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
-    q0.E = qu * cs - qw * sn;                                                \
-    q1.E = qu * sn + qw * cs;                                                \
-    k0.E = ku * cs - kw * sn;                                                \
-    k1.E = ku * sn + kw * cs;                                                \
-  }
-              M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
-#undef M3_ROT
+              pair_item(n0, *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0, Npad)),
+                        *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)),
+                        *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad)),
+                        *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0 + A, Npad)), th);
+            } else {
+              const int n0 = 2 * A + 4 * (j - PQ);
+              single_item(n0, *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0, Npad)),
+                          *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad)));
             }
-            if (!SUMMARY) {
-              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
-              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
-              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
-              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
+          }
+        } else {
+#pragma unroll 2
+          for (int jb = 0; jb < QW4; ++jb) {
+            const int j = 4 * jb + jl;
+            if (j >= QW) continue;
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < PQ) {
+              const int n0 = 4 * j;
+              float4 th;
+              switch (jb) {  // registers, not a local array
+                case 0: th = th4[0]; break;
+                case 1: th = th4[1]; break;
+                case 2: th = th4[2]; break;
+                default: th = th4[3]; break;
+              }
+              pair_item(n0, in ? *reinterpret_cast<const float4*>(crow + n0) : z4,
+                        in ? *reinterpret_cast<const float4*>(crow + n0 + A) : z4,
+                        in ? *reinterpret_cast<const float4*>(brow + n0) : z4,
+                        in ? *reinterpret_cast<const float4*>(brow + n0 + A) : z4, th);
+            } else {
+              const int n0 = 2 * A + 4 * (j - PQ);
+              single_item(n0, in ? *reinterpret_cast<const float4*>(crow + n0) : z4,
+                          in ? *reinterpret_cast<const float4*>(brow + n0) : z4);
             }
-            sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * k0.x);
-            sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * k0.y);
-            sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * k0.z);
-            sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * k0.w);
-            sKt[tc::kmaj(n0 + A, rho, kRows)] = tc::to_tf32(omr * k1.x);
-            sKt[tc::kmaj(n0 + A + 1, rho, kRows)] = tc::to_tf32(omr * k1.y);
-            sKt[tc::kmaj(n0 + A + 2, rho, kRows)] = tc::to_tf32(omr * k1.z);
-            sKt[tc::kmaj(n0 + A + 3, rho, kRows)] = tc::to_tf32(omr * k1.w);
-            if (kl) {
-              *reinterpret_cast<float4*>(kl + n0) = k0;
-              *reinterpret_cast<float4*>(kl + n0 + A) = k1;
-            }
-          } else {
-            const int n0 = 2 * A + 4 * (j - PQ);
-            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), kv = qv;
-            if (in) {
-              const float4 cu = *reinterpret_cast<const float4*>(crow + n0);
-              const float4 bu = *reinterpret_cast<const float4*>(brow + n0);
-              const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
-              const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
-              qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
-              kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
-            }
-            if (!SUMMARY) {
-              *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
-              *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
-            }
-            sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * kv.x);
-            sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * kv.y);
-            sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * kv.z);
-            sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * kv.w);
-            if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
           }
         }
       } else {
@@ -545,12 +636,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_after();
     if (abort_flag) break;
     // (5) S = Q K^T and Yo^T = G Q^T
+    // (MMAs issued by one thread run one after another; the two independent
+    // chains come from threads of different warps so that they overlap)
     if (!SUMMARY && tid == 0) {
+#pragma unroll
       for (int ks = 0; ks < Npad / 8; ++ks)
-        tc::mma_ss(tS, tc::kdesc(sQ, Npad, ks), tc::kdesc(sK, Npad, ks), id_S, ks > 0);
+        tc::mma_ss(tS, dQ + 16ull * ks, dK + 16ull * ks, id_S, ks > 0);
       tc::commit(&bars[0]);
+    }
+    if (!SUMMARY && tid == 32) {
+#pragma unroll
       for (int ks = 0; ks < Npad / 8; ++ks)
-        tc::mma_ts(tYo, tG + ks * 8, tc::kdesc(sQ, Npad, ks), id_Y, ks > 0);
+        tc::mma_ts(tYo, tG + ks * 8, dQ + 16ull * ks, id_Y, ks > 0);
       tc::commit(&bars[1]);
     }
     // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
@@ -588,9 +685,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float cum_t = tCum[t];
         const float gam_t = tGam[t];
         const int sh = lane >> 4;
-        for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
-          float v[16];
-          tc::tmem_ld16(tS + lane_base + cb * 16, v);
+        float sv[2][16];
+        tc::tmem_ld16x2(tS + lane_base + 32 * wg, tS + lane_base + 32 * wg + 16, sv[0], sv[1]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cb = 2 * wg + u;
+          const float* v = sv[u];
           float w8[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -641,15 +741,28 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!SUMMARY) {
         if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
         tc::fence_after();
+        // the q tile is free: stage the next chunk's C rows
+        if (kAsync && c0 + Qt < l1) {
+          copy_items(a.c, sQ, tok0 + Qt, min(Qt, l1 - c0 - Qt));
+          tc::cp_async_commit();
+        }
       }
       const float ec = expf(cend);
-      for (int c = 16 * wg; c < Npad; c += 32) {
-        float v[16];
-        tc::tmem_ld16(tG + lane_base + c, v);
+      // two 16-column blocks per pass: one wait per pair of loads, stores
+      // unwaited until the end
+      for (int c = 16 * wg; c < Npad; c += 64) {
+        float v0[16], v1[16];
+        const bool two = c + 32 < Npad;
+        tc::tmem_ld16x2(tG + lane_base + c, tG + lane_base + (two ? c + 32 : c), v0, v1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = tc::to_tf32(v[j] * ec);
-        tc::tmem_st16(tG + lane_base + c, v);
+        for (int j = 0; j < 16; ++j) {
+          v0[j] = tc::to_tf32(v0[j] * ec);
+          v1[j] = tc::to_tf32(v1[j] * ec);
+        }
+        tc::tmem_st16_async(tG + lane_base + c, v0);
+        if (two) tc::tmem_st16_async(tG + lane_base + c + 32, v1);
       }
+      tc::tmem_wait_st();
     }
     tc::fence_async_smem();
     tc::fence_before();
@@ -657,14 +770,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_after();
     if (abort_flag) break;
     // (7) Yi^T = X^T P^T and G += X^T (w K)
-    if (tid == 0) {
-      if (!SUMMARY) {
-        for (int ks = 0; ks < kRows / 8; ++ks)
-          tc::mma_ss(tS, tc::kdesc(sXt, kRows, ks), tc::kdesc(sP, kRows, ks), id_Y, ks > 0);
-        tc::commit(&bars[2]);
-      }
+    // (Yi and the state update come from threads of different warps)
+    if (!SUMMARY && tid == 0) {
+#pragma unroll
       for (int ks = 0; ks < kRows / 8; ++ks)
-        tc::mma_ss(tG, tc::kdesc(sXt, kRows, ks), tc::kdesc(sKt, kRows, ks), id_D, 1);
+        tc::mma_ss(tS, dXt + 16ull * ks, dP + 16ull * ks, id_Y, ks > 0);
+      tc::commit(&bars[2]);
+    }
+    if (tid == 32) {
+#pragma unroll
+      for (int ks = 0; ks < kRows / 8; ++ks)
+        tc::mma_ss(tG, dXt + 16ull * ks, dKt + 16ull * ks, id_D, 1);
       tc::commit(&bars[3]);
     }
     // next chunk's per-token scalars and angles: loads in flight during the
@@ -701,8 +817,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
         for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
           float yo[16], yi[16];
-          tc::tmem_ld16(tYo + lane_base + cb * 16, yo);
-          tc::tmem_ld16(tS + lane_base + cb * 16, yi);
+          tc::tmem_ld16x2(tYo + lane_base + cb * 16, tS + lane_base + cb * 16, yo, yi);
           if (MP == 64) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -768,6 +883,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
+    // once the state update has read the K region: stage the next chunk's B rows
+    if (kAsync && c0 + Qt < l1) {
+      if (!tc::bar_wait(&bars[3], it & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
+      copy_items(a.b, sK, tok0 + Qt, min(Qt, l1 - c0 - Qt));
+      tc::cp_async_commit();
+    }
   }
   // the last state update
   if (!abort_flag && it > 0) {
@@ -816,12 +938,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_free(tbase, 256);
 }
 
-template <int KN, int KA, int KR, int KP>
-struct Shape {};
-
 template <int MP, bool MIMO, int KN, int KA, int KR, int KP>
 cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, const ChunkIO& io,
-                      bool summary, const ChunkLayout& lay, unsigned grid, cudaStream_t s) {
+                      bool summary, unsigned grid, cudaStream_t s) {
+  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R, MIMO, chunk_async(KN, KA));
   auto kernel = summary ? k_scan_chunk<MP, MIMO, true, KN, KA, KR, KP>
                         : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -842,24 +962,23 @@ int chunk_rows_per_token(const ScanGeom& g) { return kRows / g.R; }
 
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
                               const ChunkIO& io, bool summary, cudaStream_t s) {
-  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R);
   const unsigned grid = (unsigned)(g.B * g.H * io.nseg);
   const bool mimo = a.mimo_o != nullptr;
   cudaError_t e;
   // shapes with compile-time constants: SISO P64 N128 with A = 32 or 64, MIMO
   // R4 P64 N64 A32
   if (!mimo && g.R == 1 && g.P == 64 && g.N == 128 && g.A == 32)
-    e = run_chunk<64, false, 128, 32, 1, 64>(g, a, status, io, summary, lay, grid, s);
+    e = run_chunk<64, false, 128, 32, 1, 64>(g, a, status, io, summary, grid, s);
   else if (!mimo && g.R == 1 && g.P == 64 && g.N == 128 && g.A == 64)
-    e = run_chunk<64, false, 128, 64, 1, 64>(g, a, status, io, summary, lay, grid, s);
+    e = run_chunk<64, false, 128, 64, 1, 64>(g, a, status, io, summary, grid, s);
   else if (mimo && g.R == 4 && g.P == 64 && g.N == 64 && g.A == 32)
-    e = run_chunk<64, true, 64, 32, 4, 64>(g, a, status, io, summary, lay, grid, s);
-  else if (lay.MP == 64)
-    e = mimo ? run_chunk<64, true, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s)
-             : run_chunk<64, false, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s);
+    e = run_chunk<64, true, 64, 32, 4, 64>(g, a, status, io, summary, grid, s);
+  else if (g.P <= 64)
+    e = mimo ? run_chunk<64, true, 0, 0, 0, 0>(g, a, status, io, summary, grid, s)
+             : run_chunk<64, false, 0, 0, 0, 0>(g, a, status, io, summary, grid, s);
   else
-    e = mimo ? run_chunk<128, true, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s)
-             : run_chunk<128, false, 0, 0, 0, 0>(g, a, status, io, summary, lay, grid, s);
+    e = mimo ? run_chunk<128, true, 0, 0, 0, 0>(g, a, status, io, summary, grid, s)
+             : run_chunk<128, false, 0, 0, 0, 0>(g, a, status, io, summary, grid, s);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();
