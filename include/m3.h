@@ -206,6 +206,10 @@ int m3_siso_forward_static(const m3_ssm_config* cfg, const float* c, const float
  * A zero state equals the start of a sequence. A rejected call leaves the
  * states untouched ("mutated only after the complete operation has been
  * validated"). Output out [B,1,H,P].
+ * Device-side waits are bounded: if the copy of a (b, h) state row into the
+ * kernel's shared memory does not complete within about a second (a device
+ * fault), that output row is set to NaN and that ssm_state row is left as it
+ * was (the step has no workspace, hence no status word).
  */
 int m3_siso_step(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,
                  const float* z, const float* adt, const float* dt, const float* trap,
