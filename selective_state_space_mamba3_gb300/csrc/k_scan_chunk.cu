@@ -263,12 +263,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   // L2 prefetch plan: the blocks of x, z, C, B, dt, adt, trap and angle of a
   // chunk are contiguous across the heads of a batch row, so the H CTAs of the
   // row (resident together) each prefetch one 16-byte-aligned slice of every
-  // block; thread i < 8 handles block i.
+  // block; lane 0 of warp i handles block i.
   uintptr_t pf_base = 0, pf_bytes = 0, pf_off0 = 0, pf_off1 = 0;
-  if (tid < 8) {
+  if (lane == 0) {
     const float* base = nullptr;
     int64_t per_tok = 0;  // floats per token
-    switch (tid) {
+    switch (warp) {
       case 0: base = a.x; per_tok = HP; break;
       case 1: base = a.z; per_tok = HP; break;
       case 2: base = a.c; per_tok = (int64_t)RG * N; break;
