@@ -146,6 +146,23 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
   }
 }
 
+// Writes w * v, rounded to TF32, into rows n0..n0+3 (n0 % 4 == 0) of column
+// rho of the transposed key tile. Step i stores component (i + rot) & 3: with
+// the phase-(4) lane mapping and rot = 2 * (lane / 16) + (lane / 4) % 2, the
+// 32 lanes' stores of one step land in 32 distinct banks.
+__device__ __forceinline__ void store_kt4(float* kt, int n0, int rho, float4 v, float w, int rot) {
+  const float a0 = tc::to_tf32(w * v.x), a1 = tc::to_tf32(w * v.y);
+  const float a2 = tc::to_tf32(w * v.z), a3 = tc::to_tf32(w * v.w);
+  const bool r1 = rot & 1, r2 = rot & 2;
+  const float s0 = r1 ? a1 : a0, s1 = r1 ? a2 : a1, s2 = r1 ? a3 : a2, s3 = r1 ? a0 : a3;
+  const float t0 = r2 ? s2 : s0, t1 = r2 ? s3 : s1, t2 = r2 ? s0 : s2, t3 = r2 ? s1 : s3;
+  float* base = kt + tc::kmaj(n0, rho, 64);  // row n0 + c is 4 * c floats further
+  base[((rot + 0) & 3) * 4] = t0;
+  base[((rot + 1) & 3) * 4] = t1;
+  base[((rot + 2) & 3) * 4] = t2;
+  base[((rot + 3) & 3) * 4] = t3;
+}
+
 // SiLU with the hardware exp / divide approximations (relative error a few
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
@@ -432,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     {
       const int ti = t - TPW * warp;  // token index within the warp
       const float omr = __shfl_sync(0xffffffffu, om, ti);
+      const int krot = 2 * (lane >> 4) + ((lane >> 2) & 1);  // store order of the Kt rows
       const float* cb = sBiasC + r * Npad;
       const float* bb = sBiasB + r * Npad;
       float* kl = last_chunk && t == tv - 1 ? io.k_last + ((int64_t)bh * R + r) * N : nullptr;
@@ -463,14 +481,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
           *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
         }
-        sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * k0.x);
-        sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * k0.y);
-        sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * k0.z);
-        sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * k0.w);
-        sKt[tc::kmaj(n0 + A, rho, kRows)] = tc::to_tf32(omr * k1.x);
-        sKt[tc::kmaj(n0 + A + 1, rho, kRows)] = tc::to_tf32(omr * k1.y);
-        sKt[tc::kmaj(n0 + A + 2, rho, kRows)] = tc::to_tf32(omr * k1.z);
-        sKt[tc::kmaj(n0 + A + 3, rho, kRows)] = tc::to_tf32(omr * k1.w);
+        store_kt4(sKt, n0, rho, k0, omr, krot);
+        store_kt4(sKt, n0 + A, rho, k1, omr, krot);
         if (kl) {
           *reinterpret_cast<float4*>(kl + n0) = k0;
           *reinterpret_cast<float4*>(kl + n0 + A) = k1;
@@ -489,10 +501,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
           *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
         }
-        sKt[tc::kmaj(n0, rho, kRows)] = tc::to_tf32(omr * kv.x);
-        sKt[tc::kmaj(n0 + 1, rho, kRows)] = tc::to_tf32(omr * kv.y);
-        sKt[tc::kmaj(n0 + 2, rho, kRows)] = tc::to_tf32(omr * kv.z);
-        sKt[tc::kmaj(n0 + 3, rho, kRows)] = tc::to_tf32(omr * kv.w);
+        store_kt4(sKt, n0, rho, kv, omr, krot);
         if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
       };
       if ((A & 3) == 0 && (N & 3) == 0) {
@@ -698,12 +707,31 @@ __global__ void __launch_bounds__(kThreads, 2)
             w8[j] = sh ? hi : v[j];
           }
           const int col0 = cb * 16 + 8 * sh;
+          // coefficients of the 8 key tokens of these columns (vector loads
+          // when a row is a token)
+          float cs[8], ws[8];
+          if (KR == 1) {
+            const float4 c0 = *reinterpret_cast<const float4*>(tCum + col0);
+            const float4 c1 = *reinterpret_cast<const float4*>(tCum + col0 + 4);
+            const float4 w0 = *reinterpret_cast<const float4*>(tW + col0);
+            const float4 w1 = *reinterpret_cast<const float4*>(tW + col0 + 4);
+            cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+            cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+            ws[0] = w0.x; ws[1] = w0.y; ws[2] = w0.z; ws[3] = w0.w;
+            ws[4] = w1.x; ws[5] = w1.y; ws[6] = w1.z; ws[7] = w1.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              cs[j] = tCum[(col0 + j) >> lgR];
+              ws[j] = tW[(col0 + j) >> lgR];
+            }
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int s = (col0 + j) >> lgR;
             float m = 0.f;
             if (s < t)
-              m = __expf(cum_t - tCum[s]) * tW[s];
+              m = __expf(cum_t - cs[j]) * ws[j];
             else if (s == t)
               m = gam_t;
             w8[j] = tc::to_tf32(w8[j] * m);
@@ -833,13 +861,22 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int col0 = cb * 16 + 8 * half;
           if (!mimo) {
             const int u = cb - 2 * wg;
+            float ec[kCols];
+#pragma unroll
+            for (int q = 0; q < kCols / 4; ++q) {
+              const float4 e4 = *reinterpret_cast<const float4*>(tEc + col0 + 4 * q);
+              ec[4 * q] = e4.x;
+              ec[4 * q + 1] = e4.y;
+              ec[4 * q + 2] = e4.z;
+              ec[4 * q + 3] = e4.w;
+            }
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (t < tv) {
                 const float xv = u ? xe[1][j] : xe[0][j];
                 const float zv = u ? ze[1][j] : ze[0][j];
-                float y = tEc[t] * yo[j] + yi[j] + dsk * xv;
+                float y = ec[j] * yo[j] + yi[j] + dsk * xv;
                 if (g.has_z) y *= silu_fast(zv);
                 ocol[t * HP] = y;
               }
