@@ -144,11 +144,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup(args):
+def dist_setup(args=None):
+    """(world size, rank, local rank) from the torchrun environment."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def max_over_ranks(world, values, device):
+    """Maximum over the ranks of each value (timings in ms) by one
+    all_reduce(MAX) on `device` ("cuda" under NCCL, "cpu" under gloo); the
+    values themselves when there is one rank."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(world, tokens_per_rank, steps, ms):
+    """Tokens/s of the whole job: every rank processes `tokens_per_rank` per
+    step (replicas), timed as the slowest rank's `ms` for `steps` steps."""
+    return world * tokens_per_rank * steps / (ms * 1e-3)
 
 
 # --------------------------------------------------------------------- m3 arm
@@ -394,16 +414,12 @@ def run_m3(args):
     launches = m3.launch_count() - n0
     barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(world, [t_start.elapsed_time(t_end)], "cuda")[0]
     pre_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     scan_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
     assert m3.m3_workspace_status(s.ws) == m3.M3_OK
     tokens = w.tokens
-    value = world * tokens * K / (total_ms * 1e-3)
+    value = whole_job_rate(world, tokens, K, total_ms)
 
     # roofline of the dominant kernel (algorithmic bytes / live event time)
     scan_bytes = tokens * bytes_per_token_scan(w)
@@ -424,8 +440,9 @@ def run_m3(args):
     # neighbouring steps overlap on three streams
     KE = max(3, min(K, 10))
     s.e2e(2, 8)
-    e2e_ms = s.e2e(KE, 8)
-    e2e = {"value": round(world * tokens / (e2e_ms * 1e-3), 1), "unit": UNIT,
+    barrier()
+    e2e_ms = max_over_ranks(world, [s.e2e(KE, 8)], "cuda")[0]
+    e2e = {"value": round(whole_job_rate(world, tokens, 1, e2e_ms), 1), "unit": UNIT,
            "h2d_bytes_per_step": s.h_proj.numel() * 4, "d2h_bytes_per_step": s.h_out.numel() * 4,
            "ms_per_step": round(e2e_ms, 4)}
 
