@@ -236,6 +236,18 @@ int m3_mimo_step(const m3_ssm_config* cfg, const float* c, const float* b, const
  */
 int m3_workspace_status(const void* workspace, size_t workspace_bytes, m3_stream_t stream);
 
+/*
+ * m3_selftest_wait_timeout - diagnostic: enqueues one kernel that waits on an
+ * mbarrier nothing completes, with the same bounded wait the scans use, for
+ * about `budget_cycles` SM clock cycles (1 .. 4e9), then records
+ * M3_ERR_TIMEOUT in the workspace status word (first 16 bytes, zeroed first)
+ * and exits normally. m3_workspace_status() then returns M3_ERR_TIMEOUT and
+ * the context stays usable. Checks: workspace non-NULL, >= 16 bytes, 16-byte
+ * aligned.
+ */
+int m3_selftest_wait_timeout(void* workspace, size_t workspace_bytes, int64_t budget_cycles,
+                             m3_stream_t stream);
+
 /* Human-readable description of a status code (static string). */
 const char* m3_status_string(int status);
 

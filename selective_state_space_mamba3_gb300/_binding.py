@@ -28,7 +28,8 @@ EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
             "m3_siso_forward_static", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
-            "m3_workspace_status", "m3_status_string", "m3_launch_count")
+            "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
+            "m3_launch_count")
 
 
 class M3Error(RuntimeError):
@@ -98,6 +99,7 @@ def load_library():
         lib.m3_siso_step.argtypes = [cfgp] + [_vp] * 16 + [_vp]
         lib.m3_mimo_step.argtypes = [cfgp] + [_vp] * 20 + [_vp]
         lib.m3_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
+        lib.m3_selftest_wait_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int64, _vp]
         lib.m3_status_string.argtypes = [ctypes.c_int]
         lib.m3_status_string.restype = ctypes.c_char_p
         lib.m3_launch_count.restype = ctypes.c_uint64
@@ -243,3 +245,9 @@ def m3_mimo_step(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bia
 def m3_workspace_status(workspace, stream=None) -> int:
     wp, wn = _ws(workspace)
     return int(load_library().m3_workspace_status(wp, wn, _stream(stream)))
+
+
+def m3_selftest_wait_timeout(workspace, budget_cycles, stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_selftest_wait_timeout(wp, wn, int(budget_cycles), _stream(stream)),
+           "m3_selftest_wait_timeout")

@@ -147,6 +147,15 @@ def test_workspace_status_rejects_null(lib):
     assert lib.m3_workspace_status(None, 0, None) == m3.M3_ERR_INVALID_ARGUMENT
 
 
+def test_selftest_wait_checks_arguments(lib):
+    """The diagnostic timeout entry point validates before any launch."""
+    assert lib.m3_selftest_wait_timeout(None, 64, 1000, None) == m3.M3_ERR_INVALID_ARGUMENT
+    assert lib.m3_selftest_wait_timeout(FAKE, 8, 1000, None) == m3.M3_ERR_INVALID_ARGUMENT
+    assert lib.m3_selftest_wait_timeout(FAKE, 64, 0, None) == m3.M3_ERR_INVALID_ARGUMENT
+    assert lib.m3_selftest_wait_timeout(FAKE, 64, 5_000_000_000, None) == m3.M3_ERR_INVALID_ARGUMENT
+    assert lib.m3_selftest_wait_timeout(FAKE_ODD, 64, 1000, None) == m3.M3_ERR_UNALIGNED
+
+
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0") or os.path.exists("/dev/nvidiactl"),
                     reason="a GPU is present: fake pointers must never reach a launch")
 def test_failed_launch_is_reported(lib):
