@@ -815,12 +815,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     // MMAs and the epilogue
     if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, TPW, A, H, h, warp, lane);
     if (!SUMMARY) {
-      // SISO epilogue operands x, z of this thread's output column, loaded while
-      // the MMAs run
+      // SISO epilogue gate operand z of this thread's output column, loaded while
+      // the MMAs run (its x comes from the value tile, rounded to TF32 like
+      // every operand of this kernel)
       constexpr int kCols = (MP == 64) ? 8 : 16;
-      float xe[2][kCols], ze[2][kCols];
+      float ze[2][kCols];
       if (!mimo) {
-        const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
         const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -829,7 +829,6 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int j = 0; j < kCols; ++j) {
             const int t = col0 + j;
             const bool ok = pvalid && t < tv;
-            xe[u][j] = ok ? xcol[t * HP] : 0.f;
             ze[u][j] = (ok && g.has_z) ? zcol[t * HP] : 0.f;
           }
         }
@@ -861,7 +860,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int col0 = cb * 16 + 8 * half;
           if (!mimo) {
             const int u = cb - 2 * wg;
-            float ec[kCols];
+            float ec[kCols], xs[kCols];
+#pragma unroll
+            for (int q = 0; q < kCols / 4; ++q) {
+              const float4 x4 = *reinterpret_cast<const float4*>(sXt + tc::kmaj(prow, col0 + 4 * q, kRows));
+              xs[4 * q] = x4.x;
+              xs[4 * q + 1] = x4.y;
+              xs[4 * q + 2] = x4.z;
+              xs[4 * q + 3] = x4.w;
+            }
 #pragma unroll
             for (int q = 0; q < kCols / 4; ++q) {
               const float4 e4 = *reinterpret_cast<const float4*>(tEc + col0 + 4 * q);
@@ -874,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (t < tv) {
-                const float xv = u ? xe[1][j] : xe[0][j];
+                const float xv = xs[j];
                 const float zv = u ? ze[1][j] : ze[0][j];
                 float y = ec[j] * yo[j] + yi[j] + dsk * xv;
                 if (g.has_z) y *= silu_fast(zv);
@@ -920,8 +927,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    // once the state update has read the K region: stage the next chunk's B rows
+    // once the state update has read the K region and every thread has read its
+    // epilogue values out of it: stage the next chunk's B rows
     if (kAsync && c0 + Qt < l1) {
+      if (!SUMMARY) __syncthreads();
       if (!tc::bar_wait(&bars[3], it & 1, kWaitBudget)) abort_flag = 1;
       tc::fence_after();
       copy_items(a.b, sK, tok0 + Qt, min(Qt, l1 - c0 - Qt));
