@@ -819,8 +819,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       // the MMAs run (its x comes from the value tile, rounded to TF32 like
       // every operand of this kernel)
       constexpr int kCols = (MP == 64) ? 8 : 16;
+      // Staged SISO output (P a compile-time multiple of 4, P <= 64): the
+      // pre-gate outputs go through the free score area of shared memory as
+      // [t][P] rows, and the gate and the stores run on float4 rows.
+      constexpr bool kStaged = !MIMO && KP > 0 && KP % 4 == 0 && KP <= 64;
+      constexpr int kQuads = kStaged ? kRows * KP / 4 / kThreads : 1;  // float4 units per thread
+      float4 zq[kQuads > 0 ? kQuads : 1];
       float ze[2][kCols];
-      if (!mimo) {
+      if (kStaged) {
+#pragma unroll
+        for (int k = 0; k < kQuads; ++k) {
+          const int unit = tid + kThreads * k;
+          const int t = unit / (KP / 4), p0 = 4 * (unit % (KP / 4));
+          zq[k] = (t < tv && g.has_z)
+                      ? *reinterpret_cast<const float4*>(a.z + (tok0 + t) * HP + (int64_t)h * P + p0)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      } else if (!mimo) {
         const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -880,10 +895,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
-              if (t < tv) {
-                const float xv = xs[j];
+              if (kStaged) {
+                sP[t * KP + prow] = ec[j] * yo[j] + yi[j] + dsk * xs[j];
+              } else if (t < tv) {
                 const float zv = u ? ze[1][j] : ze[0][j];
-                float y = ec[j] * yo[j] + yi[j] + dsk * xv;
+                float y = ec[j] * yo[j] + yi[j] + dsk * xs[j];
                 if (g.has_z) y *= silu_fast(zv);
                 ocol[t * HP] = y;
               }
@@ -911,6 +927,24 @@ __global__ void __launch_bounds__(kThreads, 2)
               else
                 ocol[t * HP] = o;
             }
+          }
+        }
+      }
+      if (kStaged) {
+        __syncthreads();  // the staged rows are complete
+#pragma unroll
+        for (int k = 0; k < kQuads; ++k) {
+          const int unit = tid + kThreads * k;
+          const int t = unit / (KP / 4), p0 = 4 * (unit % (KP / 4));
+          if (t < tv) {
+            float4 y = *reinterpret_cast<const float4*>(sP + t * KP + p0);
+            if (g.has_z) {
+              y.x *= silu_fast(zq[k].x);
+              y.y *= silu_fast(zq[k].y);
+              y.z *= silu_fast(zq[k].z);
+              y.w *= silu_fast(zq[k].w);
+            }
+            *reinterpret_cast<float4*>(a.out + (tok0 + t) * HP + (int64_t)h * P + p0) = y;
           }
         }
       }
