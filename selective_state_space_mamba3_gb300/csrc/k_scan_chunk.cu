@@ -666,8 +666,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     // first so that their latency overlaps the wait.
     {
       constexpr int kXr = (kRows / 4 + kWarps - 1) / kWarps;  // row blocks per warp
-      float xreg[kXr][MP / 8];
-      {
+      // SISO with P = 64 (compile time): x rows as float4 (warp w: tokens 8w ..
+      // 8w + 7; lane l: token 8w + 4 (k / 2) + l / 8, dims 4 (8 (k % 2) + l % 8) ..)
+      constexpr bool kXVec = !MIMO && KP == 64 && MP == 64;
+      float4 xq[4];
+      float xreg[kXVec ? 1 : kXr][kXVec ? 1 : MP / 8];
+      if (kXVec) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = 8 * warp + 4 * (k >> 1) + (lane >> 3), pq = 8 * (k & 1) + (lane & 7);
+          xq[k] = t < tv ? *reinterpret_cast<const float4*>(a.x + (tok0 + t) * HP + (int64_t)h * P + 4 * pq)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      } else {
         const int pl8 = lane & 7, rl = lane >> 3;
 #pragma unroll
         for (int q = 0; q < kXr; ++q) {
@@ -743,8 +754,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       // values X^T [p][row] (x * mimo_x for MIMO): lane l takes p = 8 * pb +
-      // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores)
-      {
+      // l % 8 and row 4 * rb + l / 8 (conflict-free scalar stores); the float4
+      // rows go out in a lane-rotated component order (conflict-free as well)
+      if (kXVec) {
+        const int rot = (lane >> 1) & 3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = 8 * warp + 4 * (k >> 1) + (lane >> 3), pq = 8 * (k & 1) + (lane & 7);
+          store_kt4(sXt, 4 * pq, t, xq[k], 1.0f, rot);
+        }
+      } else {
         const int pl8 = lane & 7, rl = lane >> 3;
 #pragma unroll
         for (int q = 0; q < kXr; ++q) {
