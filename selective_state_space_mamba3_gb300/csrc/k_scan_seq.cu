@@ -3,8 +3,9 @@
 //
 // The rows p of the [P, N] state evolve independently given the per-token
 // q, k, decay and trapezoid weights, so a block owns one (b, h) and a tile of
-// PT state rows; four lanes share a row, each holding 4 * NPT4 state values in
-// registers (float4-interleaved so that shared-memory reads are conflict-free).
+// PT state rows; LPR lanes share a row, each holding 4 * NPT4 state values in
+// registers (float4-interleaved so that shared-memory reads are broadcasts),
+// and the row's readout is a shuffle reduction over those lanes.
 // Per tile of kT tokens the block stages the coefficients, the cumulative
 // rotary angle, the rotated q/k rows and x/z in shared memory, runs the
 // recurrence over the tile, then writes the gated outputs coalesced. MIMO
@@ -49,7 +50,7 @@ __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
   return l;
 }
 
-template <int NPT4, int RMAX>
+template <int NPT4, int RMAX, int LPR>
 __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay,
                                                   StepState st) {
   extern __shared__ __align__(16) float sm[];
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   const int p0 = (blockIdx.x % ptiles) * PT;
   const int b = bh / H, h = bh % H;
   const int grp = h / (H / g.G);
-  const int pi = tid >> 2, j = tid & 3;
+  const int pi = tid / LPR, j = tid % LPR;
   const int p = p0 + pi;
   const bool row_ok = (pi < PT) && (p < P);
 
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   for (int i = 0; i < NPT4; ++i) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int n = 4 * (j + 4 * i) + e;
+      const int n = 4 * (j + LPR * i) + e;
       hst[4 * i + e] = (hrow && n < N) ? hrow[n] : 0.f;
     }
   }
@@ -184,20 +185,21 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
     for (int t = 0; t < tv; ++t) {
       const float dec = scoef[t * 4 + 0], gam = scoef[t * 4 + 1], sdec = scoef[t * 4 + 2];
       const float xv = row_ok ? sx[t * PT + pi] : 0.f;
-      float cp[RMAX], cc[RMAX], xr[RMAX], acc[RMAX];
+      float cp[RMAX], cc[RMAX], xr[RMAX], acc[RMAX], acc2[RMAX];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         xr[r] = xv * mx[r];
         cp[r] = sdec * xprev[r];
         cc[r] = gam * xr[r];
         acc[r] = 0.f;
+        acc2[r] = 0.f;  // second readout chain (odd groups)
       }
       const float4* kp4 = reinterpret_cast<const float4*>(sk + (size_t)t * R * Npad);
       const float4* kc4 = reinterpret_cast<const float4*>(sk + (size_t)(t + 1) * R * Npad);
       const float4* q4 = reinterpret_cast<const float4*>(sq + (size_t)t * R * Npad);
 #pragma unroll
       for (int i = 0; i < NPT4; ++i) {
-        const int n4 = j + 4 * i;
+        const int n4 = j + LPR * i;
         if (n4 * 4 < Npad) {
           float ux = 0.f, uy = 0.f, uz = 0.f, uw = 0.f;
 #pragma unroll
@@ -220,15 +222,20 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
           for (int r = 0; r < RMAX; ++r) {
             if (r < R) {
               const float4 qq = q4[r * (Npad / 4) + n4];
-              acc[r] += hh[0] * qq.x + hh[1] * qq.y + hh[2] * qq.z + hh[3] * qq.w;
+              const float part = (hh[0] * qq.x + hh[1] * qq.y) + (hh[2] * qq.z + hh[3] * qq.w);
+              if (i & 1)
+                acc2[r] += part;
+              else
+                acc[r] += part;
             }
           }
         }
       }
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
-        acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 1);
-        acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 2);
+        acc[r] += acc2[r];
+#pragma unroll
+        for (int o = 1; o < LPR; o <<= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
         if (r < R && j == 0 && row_ok) sy[(t * R + r) * PT + pi] = acc[r] + dskip * xr[r];
         xprev[r] = xr[r];
       }
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
     for (int i = 0; i < NPT4; ++i) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int n = 4 * (j + 4 * i) + e;
+        const int n = 4 * (j + LPR * i) + e;
         if (hrow && n < N) hrow[n] = hst[4 * i + e];
       }
     }
@@ -300,33 +307,40 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   }
 }
 
-template <int NPT4, int RMAX>
+template <int NPT4, int RMAX, int LPR>
 cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                          cudaStream_t s) {
   // one block per (b, h) for MIMO (block-local output norm) and with state
   // (the per-(b, h) key / angle state is read first and written last)
   const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
   const SeqLayout lay = seq_layout(g.N, PT, g.R, g.A);
-  const int threads = ((PT * 4 + 31) / 32) * 32;
+  const int threads = ((PT * LPR + 31) / 32) * 32;
   const int ptiles = (g.P + PT - 1) / PT;
-  cudaError_t e = cudaFuncSetAttribute(k_scan_seq<NPT4, RMAX>,
+  cudaError_t e = cudaFuncSetAttribute(k_scan_seq<NPT4, RMAX, LPR>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)lay.bytes);
   if (e != cudaSuccess) return e;
-  k_scan_seq<NPT4, RMAX><<<(unsigned)(g.B * g.H * ptiles), threads, lay.bytes, s>>>(g, a, lay,
-                                                                                    st);
+  k_scan_seq<NPT4, RMAX, LPR><<<(unsigned)(g.B * g.H * ptiles), threads, lay.bytes, s>>>(g, a, lay,
+                                                                                         st);
   count_launches(1);
   return cudaGetLastError();
 }
 
+// Lanes per state row: 8 while the block stays within 512 threads, else 4.
 template <int RMAX>
 cudaError_t launch_seq_r(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                          cudaStream_t s) {
-  const int npt4 = ((g.N + 15) / 16);
-  if (npt4 <= 1) return launch_seq_t<1, RMAX>(g, a, st, s);
-  if (npt4 <= 2) return launch_seq_t<2, RMAX>(g, a, st, s);
-  if (npt4 <= 4) return launch_seq_t<4, RMAX>(g, a, st, s);
-  return launch_seq_t<8, RMAX>(g, a, st, s);
+  const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
+  const int groups = (g.N + 15) / 16 * 4;  // float4 groups of a padded row
+  if (PT * 8 <= 512) {
+    if (groups <= 8) return launch_seq_t<1, RMAX, 8>(g, a, st, s);
+    if (groups <= 16) return launch_seq_t<2, RMAX, 8>(g, a, st, s);
+    return launch_seq_t<4, RMAX, 8>(g, a, st, s);
+  }
+  if (groups <= 4) return launch_seq_t<1, RMAX, 4>(g, a, st, s);
+  if (groups <= 8) return launch_seq_t<2, RMAX, 4>(g, a, st, s);
+  if (groups <= 16) return launch_seq_t<4, RMAX, 4>(g, a, st, s);
+  return launch_seq_t<8, RMAX, 4>(g, a, st, s);
 }
 
 }  // namespace
