@@ -6,10 +6,11 @@
 // PT state rows; LPR lanes share a row, each holding 4 * NPT4 state values in
 // registers (float4-interleaved so that shared-memory reads are broadcasts),
 // and the row's readout is a shuffle reduction over those lanes.
-// Per tile of kT tokens the block stages the coefficients, the cumulative
-// rotary angle, the rotated q/k rows and x/z in shared memory, runs the
-// recurrence over the tile, then writes the gated outputs coalesced. MIMO
-// blocks own all P rows so that the output RMS norm is block-local.
+// Per tile of kT tokens (16, or 32 for blocks that own a whole sequence) the
+// block stages the coefficients, the cumulative rotary angle, the rotated q/k
+// rows and x/z in shared memory, runs the recurrence over the tile, then
+// writes the gated outputs coalesced. MIMO blocks own all P rows so that the
+// output RMS norm is block-local.
 //
 // This is the FP32 reference path of the library and the fallback for shapes
 // outside the tensor-core chunked kernels.
@@ -18,19 +19,19 @@
 namespace m3 {
 namespace {
 
-constexpr int kT = 16;  // tokens per staging tile
 
 struct SeqLayout {
-  int Npad, PT, R, A;
+  int Npad, PT, R, A, kT;  // kT: tokens per staging tile
   size_t q, k, coef, theta, cs, xs, zs, ys, os, bytes;
 };
 
-__host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A) {
+__host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int kT) {
   SeqLayout l;
   l.Npad = (N + 15) / 16 * 16;
   l.PT = PT;
   l.R = R;
   l.A = A;
+  l.kT = kT;
   size_t off = 0;
   auto take = [&](size_t floats) {
     size_t o = off;
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int P = g.P, N = g.N, A = g.A, R = g.R, L = g.L, H = g.H;
-  const int Npad = lay.Npad, PT = lay.PT;
+  const int Npad = lay.Npad, PT = lay.PT, kT = lay.kT;
   const int ptiles = (P + PT - 1) / PT;
   const int bh = blockIdx.x / ptiles;
   const int p0 = (blockIdx.x % ptiles) * PT;
@@ -313,7 +314,13 @@ cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& 
   // one block per (b, h) for MIMO (block-local output norm) and with state
   // (the per-(b, h) key / angle state is read first and written last)
   const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
-  const SeqLayout lay = seq_layout(g.N, PT, g.R, g.A);
+  // 16-token staging tiles; 32 for blocks that own a whole (b, h) (one such
+  // block per SM anyway) when they fit in 200 KB of shared memory
+  SeqLayout lay = seq_layout(g.N, PT, g.R, g.A, 16);
+  if (PT == g.P && (RMAX > 1 || a.mimo_o || st.ssm)) {
+    const SeqLayout big = seq_layout(g.N, PT, g.R, g.A, 32);
+    if (big.bytes <= 200 * 1024) lay = big;
+  }
   const int threads = ((PT * LPR + 31) / 32) * 32;
   const int ptiles = (g.P + PT - 1) / PT;
   cudaError_t e = cudaFuncSetAttribute(k_scan_seq<NPT4, RMAX, LPR>,
