@@ -5,7 +5,8 @@
 // HBM-bound streaming: every byte of `projected` is read once and every output
 // byte written once. One 256-thread block handles one row at a time
 // (grid-stride over rows): the z|x slices move as 128-bit streaming loads and
-// stores, each B/C row is owned by one warp whose lanes hold one float4 each
+// stores (four loads in flight per thread before their stores), each B/C row
+// is owned by one warp whose lanes hold one float4 each
 // (N <= 128) and reduce the mean square with shuffles, and the 3H + A scalar
 // columns are mapped by the first threads. Rows whose width or slice offsets
 // are not multiples of 4 floats take the scalar path of the same kernel.
@@ -27,18 +28,30 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
   const int BC = RG * N;
   for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
     const float* p = proj + r * (int64_t)W;
-    // z | x slices (columns [0, 2I)).
+    // z | x slices (columns [0, 2I)): four float4 loads per thread in flight
+    // before their stores (memory-level parallelism of the stream).
     if (VEC) {
       const float4* p4 = reinterpret_cast<const float4*>(p);
-      const int I4 = I >> 2;
+      const int I4 = I >> 2, Z4 = 2 * I4;
       float4* z4 = reinterpret_cast<float4*>(o.z + r * (int64_t)I);
       float4* x4 = reinterpret_cast<float4*>(o.x + r * (int64_t)I);
-      for (int i = tid; i < 2 * I4; i += kThreads) {
-        float4 v = __ldcs(p4 + i);
-        if (i < I4)
-          __stcs(z4 + i, v);
-        else
-          __stcs(x4 + (i - I4), v);
+      for (int base = tid; base < Z4; base += 4 * kThreads) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * kThreads;
+          if (i < Z4) v[u] = __ldcs(p4 + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = base + u * kThreads;
+          if (i < Z4) {
+            if (i < I4)
+              __stcs(z4 + i, v[u]);
+            else
+              __stcs(x4 + (i - I4), v[u]);
+          }
+        }
       }
     } else {
       for (int i = tid; i < 2 * I; i += kThreads) {
