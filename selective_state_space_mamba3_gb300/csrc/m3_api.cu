@@ -88,12 +88,24 @@ static bool use_chunk(const ScanGeom& g) {
   return g.math_mode == M3_MATH_TF32 && chunk_supported(g);
 }
 
-// Sequences per launch below two per SM (GB300: 152 SMs) are split into
-// segments of whole chunks, at least four chunks long: a summary pass, a
-// prefix over segments and the main pass then replace one long serial chain.
+// SMs of the current device (152 on GB300; also the answer when no device can
+// be queried, so that workspace sizes stay defined without a GPU).
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // reset the last-error state the failed query left
+    return 152;
+  }
+  return n;
+}
+
+// Sequences per launch below two per SM are split into segments of whole
+// chunks, at least four chunks long: a summary pass, a prefix over segments
+// and the main pass then replace one long serial chain.
 static int choose_nseg(const ScanGeom& g) {
   const int64_t bh = (int64_t)g.B * g.H;
-  const int64_t target = 2 * 152;
+  const int64_t target = 2 * (int64_t)sm_count();
   if (bh >= target) return 1;
   const int64_t qt = chunk_rows_per_token(g);
   const int64_t max_seg = g.L / (4 * qt);
