@@ -22,7 +22,7 @@ namespace {
 
 struct SeqLayout {
   int Npad, PT, R, A, kT;  // kT: tokens per staging tile
-  size_t q, k, coef, theta, cs, xs, zs, ys, os, bytes;
+  size_t q, k, coef, theta, cs, xs, zs, ys, os, bias, bytes;
 };
 
 __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int kT) {
@@ -47,12 +47,13 @@ __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int
   l.zs = take((size_t)kT * PT);
   l.ys = take((size_t)kT * R * PT);
   l.os = take((size_t)kT * PT);
+  l.bias = take((size_t)2 * R * l.Npad);  // c_bias, b_bias of this head, zero-padded
   l.bytes = off * sizeof(float);
   return l;
 }
 
 template <int NPT4, int RMAX, int LPR>
-__global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay,
+__global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g, ScanArgs a, SeqLayout lay,
                                                   StepState st) {
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
@@ -64,6 +65,8 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   float* sz = sm + lay.zs;
   float* sy = sm + lay.ys;
   float* so = sm + lay.os;
+  float* sbc = sm + lay.bias;          // [R][Npad] c_bias
+  float* sbb = sbc + lay.R * lay.Npad;  // [R][Npad] b_bias
 
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int P = g.P, N = g.N, A = g.A, R = g.R, L = g.L, H = g.H;
@@ -106,6 +109,14 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
   }
   for (int i = tid; i < A; i += nthr)
     sth[(kT - 1) * A + i] = (has_state && st.angle) ? st.angle[(int64_t)bh * A + i] : 0.f;
+  for (int i = tid; i < R * Npad; i += nthr) {
+    const int r = i / Npad, n = i - r * Npad;
+    sbc[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
+    sbb[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
+  }
+  // float4 staging of q/k items and x/z rows when the shapes allow it
+  const bool vec_qk = (A % 4 == 0) && (N % 4 == 0);
+  const bool vec_xz = (P % 4 == 0) && (PT % 4 == 0);
   __syncthreads();
 
   for (int t0 = 0; t0 < L; t0 += kT) {
@@ -138,19 +149,77 @@ __global__ void __launch_bounds__(512) k_scan_seq(ScanGeom g, ScanArgs a, SeqLay
     }
     __syncthreads();
     for (int i = tid; i < tv * A; i += nthr) sincosf(sth[i], &scs[2 * i + 1], &scs[2 * i]);
-    for (int i = tid; i < kT * PT; i += nthr) {
-      const int t = i / PT, pp = i % PT;
-      float xv = 0.f, zv = 0.f;
-      if (t < tv && p0 + pp < P) {
-        const int64_t off = (((int64_t)b * L + t0 + t) * H + h) * P + p0 + pp;
-        xv = a.x[off];
-        zv = a.z[off];
+    if (vec_xz) {
+      const int PT4 = PT / 4;
+      for (int i = tid; i < kT * PT4; i += nthr) {
+        const int t = i / PT4, q4 = i - t * PT4;
+        float4 xv = make_float4(0.f, 0.f, 0.f, 0.f), zv = xv;
+        if (t < tv && p0 + 4 * q4 < P) {
+          const int64_t off = (((int64_t)b * L + t0 + t) * H + h) * P + p0 + 4 * q4;
+          xv = *reinterpret_cast<const float4*>(a.x + off);
+          zv = *reinterpret_cast<const float4*>(a.z + off);
+        }
+        reinterpret_cast<float4*>(sx)[i] = xv;
+        reinterpret_cast<float4*>(sz)[i] = zv;
       }
-      sx[i] = xv;
-      sz[i] = zv;
+    } else {
+      for (int i = tid; i < kT * PT; i += nthr) {
+        const int t = i / PT, pp = i % PT;
+        float xv = 0.f, zv = 0.f;
+        if (t < tv && p0 + pp < P) {
+          const int64_t off = (((int64_t)b * L + t0 + t) * H + h) * P + p0 + pp;
+          xv = a.x[off];
+          zv = a.z[off];
+        }
+        sx[i] = xv;
+        sz[i] = zv;
+      }
     }
     __syncthreads();
     // 2. rotated q/k rows (zero-padded to Npad), k into slots 1..kT
+    if (vec_qk) {
+      // item = 4 dims n0..n0+3 of one (token, rank) row; for n0 < A also their
+      // rotary partners n0+A..n0+A+3; padding dims N..Npad are zero
+      const int PQ = A / 4, QW = PQ + (Npad - 2 * A) / 4;
+      for (int i = tid; i < kT * R * QW; i += nthr) {
+        const int row = i / QW, jq = i - row * QW;
+        const int t = row / R, r = row - t * R;
+        const int n0 = jq < PQ ? 4 * jq : 2 * A + 4 * (jq - PQ);
+        const bool live = t < tv && n0 < N;
+        const int64_t tok = (int64_t)b * L + t0 + t;
+        const int64_t roff = (tok * g.G * R + (int64_t)grp * R + r) * N;
+        const float* csn = scs + 2 * (t * A + n0);  // (cos, sin) pairs of angles n0..n0+3
+        // one operand (C into q, then B into k) at a time: fewer live registers
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const float* src = (which ? a.b : a.c) + roff;
+          const float* bias = (which ? sbb : sbc) + r * Npad;
+          float* dst = which ? sk + (size_t)(R + t * R + r) * Npad : sq + (size_t)(t * R + r) * Npad;
+          float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+          if (live) {
+            const float4 u = *reinterpret_cast<const float4*>(src + n0);
+            const float4 ub = *reinterpret_cast<const float4*>(bias + n0);
+            if (jq < PQ) {
+              const float4 w = *reinterpret_cast<const float4*>(src + n0 + A);
+              const float4 wb = *reinterpret_cast<const float4*>(bias + n0 + A);
+#define M3_SEQ_ROT(E, K)                                                      \
+  {                                                                           \
+    const float cs = csn[2 * K], sn = csn[2 * K + 1];                         \
+    const float uu = u.E + ub.E, ww = w.E + wb.E;                             \
+    v0.E = uu * cs - ww * sn;                                                 \
+    v1.E = uu * sn + ww * cs;                                                 \
+  }
+              M3_SEQ_ROT(x, 0) M3_SEQ_ROT(y, 1) M3_SEQ_ROT(z, 2) M3_SEQ_ROT(w, 3)
+#undef M3_SEQ_ROT
+            } else {
+              v0 = make_float4(u.x + ub.x, u.y + ub.y, u.z + ub.z, u.w + ub.w);
+            }
+          }
+          *reinterpret_cast<float4*>(dst + n0) = v0;
+          if (jq < PQ) *reinterpret_cast<float4*>(dst + n0 + A) = v1;
+        }
+      }
+    } else
     for (int i = tid; i < kT * R * Npad; i += nthr) {
       const int t = i / (R * Npad);
       const int rem = i - t * R * Npad;
