@@ -126,6 +126,12 @@ EDGE = [
     dict(B=1, L=129, H=4, G=2, P=64, N=128, A=16, has_z=0),
     dict(B=1, L=200, H=2, G=1, P=64, N=128, A=16, has_d=0),
     dict(B=1, L=300, H=2, G=1, P=48, N=96, A=20),
+    # compile-time instances (P64 N128 A32 / A64): ragged lengths, gate and D skip off,
+    # a single token
+    dict(B=1, L=65, H=2, G=1, P=64, N=128, A=32, has_z=0),
+    dict(B=1, L=127, H=2, G=1, P=64, N=128, A=32, has_d=0),
+    dict(B=2, L=1, H=2, G=1, P=64, N=128, A=32),
+    dict(B=1, L=90, H=2, G=1, P=64, N=128, A=64),
 ]
 
 
