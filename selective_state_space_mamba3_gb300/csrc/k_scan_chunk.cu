@@ -843,13 +843,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       // [t][P] rows, and the gate and the stores run on float4 rows.
       constexpr bool kStaged = !MIMO && KP > 0 && KP % 4 == 0 && KP <= 64;
       constexpr int kQuads = kStaged ? kRows * KP / 4 / kThreads : 1;  // float4 units per thread
+      constexpr int kRowQ = kStaged ? KP / 4 : 1;                       // float4 units per row
       float4 zq[kQuads > 0 ? kQuads : 1];
       float ze[2][kCols];
       if (kStaged) {
 #pragma unroll
         for (int k = 0; k < kQuads; ++k) {
           const int unit = tid + kThreads * k;
-          const int t = unit / (KP / 4), p0 = 4 * (unit % (KP / 4));
+          const int t = unit / kRowQ, p0 = 4 * (unit % kRowQ);
           zq[k] = (t < tv && g.has_z)
                       ? *reinterpret_cast<const float4*>(a.z + (tok0 + t) * HP + (int64_t)h * P + p0)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -954,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int k = 0; k < kQuads; ++k) {
           const int unit = tid + kThreads * k;
-          const int t = unit / (KP / 4), p0 = 4 * (unit % (KP / 4));
+          const int t = unit / kRowQ, p0 = 4 * (unit % kRowQ);
           if (t < tv) {
             float4 y = *reinterpret_cast<const float4*>(sP + t * KP + p0);
             if (g.has_z) {

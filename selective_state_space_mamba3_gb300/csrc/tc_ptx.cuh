@@ -71,13 +71,16 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
 __device__ __forceinline__ void bar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
+// One wait attempt; the thread may stay suspended for up to about 0.1 ms
+// (suspend-time hint, in ns) unless the phase completes first, so that waiting
+// threads do not spin through issue slots.
 __device__ __forceinline__ bool bar_try(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity));
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u));
   return ok != 0;
 }
 // Bounded wait: false once about `budget` clock cycles have passed.
