@@ -16,11 +16,12 @@
 // Per chunk and (b, h), every contraction is a tcgen05.mma (kind::tf32):
 //   S    = Q K^T               [64 x 64],  K = N     (A, B in shared memory)
 //   Yo^T = G Q^T               [P  x 64],  K = N     (A = state G in TMEM)
-//   Yi^T = X^T (M o S)^T       [P  x 64],  K = 64    (decay/trapezoid mask M)
+//   Yi^T = X^T (M o S + D I)^T [P  x 64],  K = 64    (decay/trapezoid mask M;
+//                                                   the D skip on the diagonal)
 //   G   += X^T (w K)           [P  x N],   K = 64    (after G *= e^{cum_end})
 // The state G [P x N] stays in TMEM for the whole sequence; outputs come out
 // transposed (TMEM lane = p): each output column p is finished by the two
-// lanes that share its TMEM row (D skip, SiLU gate, the MIMO mimo_o
+// lanes that share its TMEM row (e^{cum_t} Yo + Yi, SiLU gate, the MIMO mimo_o
 // contraction over its R rows) and, through shared memory, the MIMO output
 // RMS norm. Every operand is rounded to TF32 (round to nearest).
 //
@@ -50,6 +51,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTok = 72;        // per-token array stride (>= 65)
 constexpr int kAngMax = 64;     // A <= 64
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s)
+// Lazy state scaling: TMEM holds G~ with G = e^{lgE} G~, and G~ is rescaled
+// only when the log decay accumulated since the last rescale would pass
+// -kLazyRange (so |G~| <= e^{kLazyRange} |G|).
+constexpr float kLazyRange = 40.0f;
 
 struct ChunkLayout {
   int Npad, MP;
@@ -146,13 +151,13 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
   }
 }
 
-// Writes w * v, rounded to TF32, into rows n0..n0+3 (n0 % 4 == 0) of column
+// Writes w * v, rounded for the tensor core, into rows n0..n0+3 (n0 % 4 == 0) of column
 // rho of the transposed key tile. Step i stores component (i + rot) & 3: with
 // the phase-(4) lane mapping and rot = 2 * (lane / 16) + (lane / 4) % 2, the
 // 32 lanes' stores of one step land in 32 distinct banks.
 __device__ __forceinline__ void store_kt4(float* kt, int n0, int rho, float4 v, float w, int rot) {
-  const float a0 = tc::to_tf32(w * v.x), a1 = tc::to_tf32(w * v.y);
-  const float a2 = tc::to_tf32(w * v.z), a3 = tc::to_tf32(w * v.w);
+  const float a0 = tc::tf32_feed(w * v.x), a1 = tc::tf32_feed(w * v.y);
+  const float a2 = tc::tf32_feed(w * v.z), a3 = tc::tf32_feed(w * v.w);
   const bool r1 = rot & 1, r2 = rot & 2;
   const float s0 = r1 ? a1 : a0, s1 = r1 ? a2 : a1, s2 = r1 ? a3 : a2, s3 = r1 ? a0 : a3;
   const float t0 = r2 ? s2 : s0, t1 = r2 ? s3 : s1, t2 = r2 ? s0 : s2, t3 = r2 ? s1 : s3;
@@ -260,11 +265,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   constexpr bool mimo = MIMO;
   constexpr int kRmax = MIMO ? 8 : 1;
-  float mxr[kRmax], mzr[kRmax], mor[kRmax];
+  float mzr[kRmax], mor[kRmax];
 #pragma unroll
   for (int r = 0; r < kRmax; ++r) {
     const bool ok = mimo && pvalid && r < R;
-    mxr[r] = ok ? a.mimo_x[((int64_t)h * R + r) * P + prow] : 1.f;
     mzr[r] = ok ? a.mimo_z[((int64_t)h * R + r) * P + prow] : 1.f;
     mor[r] = ok ? a.mimo_o[((int64_t)h * R + r) * P + prow] : 0.f;
   }
@@ -345,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   TokenPreload pl;
   preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
   float esum = 0.f;  // sum of adt over the segment
+  float lgE = 0.f;   // G = e^{lgE} G~ (identical in every thread)
 
   int it = 0;
   for (int c0 = l0; c0 < l1; c0 += Qt, ++it) {
@@ -413,12 +418,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       cend += v;
     }
     esum += cend;
+    // lazy chunk: G~ keeps its scale, e^{-lgE_new} goes into the w-scaled keys
+    // and e^{lgE} into the Yo readout; otherwise G~ *= e^{lgE + cend} below
+    const bool lazy = lgE + cend >= -kLazyRange;
+    const float lg_new = lazy ? lgE + cend : 0.f;
     const float cum = cbase + cl;
     const float wt = gam + __shfl_down_sync(0xffffffffu, scl, 1);
-    const float om = (lane < TPW && tw < tv) ? expf(cend - cum) * wt : 0.f;
+    const float om = (lane < TPW && tw < tv) ? expf(cend - cum - lg_new) * wt : 0.f;
     if (lane < TPW) {
       tCum[tw] = cum;
-      tEc[tw] = expf(cum);
+      tEc[tw] = expf(cum + lgE);
       tGam[tw] = gam;
       tW[tw] = wt;
     }
@@ -476,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #undef M3_ROT
         }
         if (!SUMMARY) {
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(q0);
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(q1);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(k0);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::to_tf32(k1);
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(q0);
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::tf32_feed(q1);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(k0);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::tf32_feed(k1);
         }
         store_kt4(sKt, n0, rho, k0, omr, krot);
         store_kt4(sKt, n0 + A, rho, k1, omr, krot);
@@ -498,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
         }
         if (!SUMMARY) {
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(qv);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::to_tf32(kv);
+          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(qv);
+          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(kv);
         }
         store_kt4(sKt, n0, rho, kv, omr, krot);
         if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
@@ -602,13 +611,13 @@ __global__ void __launch_bounds__(kThreads, 2)
               k1 = ku * sn + kw * cs;
             }
             if (!SUMMARY) {
-              sQ[tc::kmaj(rho, u, Npad)] = tc::to_tf32(q0);
-              sQ[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(q1);
-              sK[tc::kmaj(rho, u, Npad)] = tc::to_tf32(k0);
-              sK[tc::kmaj(rho, u + A, Npad)] = tc::to_tf32(k1);
+              sQ[tc::kmaj(rho, u, Npad)] = tc::tf32_feed(q0);
+              sQ[tc::kmaj(rho, u + A, Npad)] = tc::tf32_feed(q1);
+              sK[tc::kmaj(rho, u, Npad)] = tc::tf32_feed(k0);
+              sK[tc::kmaj(rho, u + A, Npad)] = tc::tf32_feed(k1);
             }
-            sKt[tc::kmaj(u, rho, kRows)] = tc::to_tf32(omr * k0);
-            sKt[tc::kmaj(u + A, rho, kRows)] = tc::to_tf32(omr * k1);
+            sKt[tc::kmaj(u, rho, kRows)] = tc::tf32_feed(omr * k0);
+            sKt[tc::kmaj(u + A, rho, kRows)] = tc::tf32_feed(omr * k1);
             if (kl) {
               kl[u] = k0;
               kl[u + A] = k1;
@@ -621,10 +630,10 @@ __global__ void __launch_bounds__(kThreads, 2)
               kv = brow[n] + bb[n];
             }
             if (!SUMMARY) {
-              sQ[tc::kmaj(rho, n, Npad)] = tc::to_tf32(qv);
-              sK[tc::kmaj(rho, n, Npad)] = tc::to_tf32(kv);
+              sQ[tc::kmaj(rho, n, Npad)] = tc::tf32_feed(qv);
+              sK[tc::kmaj(rho, n, Npad)] = tc::tf32_feed(kv);
             }
-            sKt[tc::kmaj(n, rho, kRows)] = tc::to_tf32(omr * kv);
+            sKt[tc::kmaj(n, rho, kRows)] = tc::tf32_feed(omr * kv);
             if (kl) kl[n] = kv;
           }
         }
@@ -745,7 +754,8 @@ __global__ void __launch_bounds__(kThreads, 2)
               m = __expf(cum_t - cs[j]) * ws[j];
             else if (s == t)
               m = gam_t;
-            w8[j] = tc::to_tf32(w8[j] * m);
+            // the D skip rides on the diagonal: Yi then includes D * x
+            w8[j] = tc::tf32_feed(col0 + j == rho ? fmaf(w8[j], m, dsk) : w8[j] * m);
           }
           *reinterpret_cast<float4*>(sP + tc::kmaj(rho, col0, kRows)) =
               make_float4(w8[0], w8[1], w8[2], w8[3]);
@@ -772,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int rho2 = 4 * rb + rl;
 #pragma unroll
           for (int pb = 0; pb < MP / 8; ++pb)
-            sXt[tc::kmaj(8 * pb + pl8, rho2, kRows)] = tc::to_tf32(xreg[q][pb]);
+            sXt[tc::kmaj(8 * pb + pl8, rho2, kRows)] = tc::tf32_feed(xreg[q][pb]);
         }
       }
       // value of the sequence's last token for the step state (last chunk only)
@@ -784,8 +794,8 @@ __global__ void __launch_bounds__(kThreads, 2)
               mimo ? xrow[p] * a.mimo_x[((int64_t)h * R + r) * P + p] : xrow[p];
         }
       }
-      // G may be rescaled only once Yo^T = G Q^T has read it
-      if (!SUMMARY) {
+      // G~ may be rescaled only once Yo^T = G~ Q^T has read it
+      if (!SUMMARY && !lazy) {
         if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
         tc::fence_after();
         // the q tile is free: stage the next chunk's C rows
@@ -794,17 +804,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           tc::cp_async_commit();
         }
       }
-      const float ec = expf(cend);
+      const float ec = expf(lgE + cend);
       // two 16-column blocks per pass: one wait per pair of loads, stores
       // unwaited until the end
-      for (int c = 16 * wg; c < Npad; c += 64) {
+      if (!lazy) for (int c = 16 * wg; c < Npad; c += 64) {
         float v0[16], v1[16];
         const bool two = c + 32 < Npad;
         tc::tmem_ld16x2(tG + lane_base + c, tG + lane_base + (two ? c + 32 : c), v0, v1);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          v0[j] = tc::to_tf32(v0[j] * ec);
-          v1[j] = tc::to_tf32(v1[j] * ec);
+          v0[j] = tc::tf32_clean(v0[j] * ec);
+          v1[j] = tc::tf32_clean(v1[j] * ec);
         }
         tc::tmem_st16_async(tG + lane_base + c, v0);
         if (two) tc::tmem_st16_async(tG + lane_base + c + 32, v1);
@@ -825,11 +835,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       tc::commit(&bars[2]);
     }
     if (tid == 32) {
+      // a lazy chunk adds to G~ without the rescale pass: the Yo MMAs
+      // (issued by this thread) must have read G~ first
+      bool ok = true;
+      if (!SUMMARY && lazy) {
+        ok = tc::bar_wait(&bars[1], it & 1, kWaitBudget);
+        tc::fence_after();
+      }
+      if (ok) {
 #pragma unroll
-      for (int ks = 0; ks < kRows / 8; ++ks)
-        tc::mma_ss(tG, dXt + 16ull * ks, dKt + 16ull * ks, id_D, 1);
-      tc::commit(&bars[3]);
+        for (int ks = 0; ks < kRows / 8; ++ks)
+          tc::mma_ss(tG, dXt + 16ull * ks, dKt + 16ull * ks, id_D, 1);
+        tc::commit(&bars[3]);
+      } else {
+        abort_flag = 1;
+      }
     }
+    lgE = lg_new;
     // next chunk's per-token scalars and angles: loads in flight during the
     // MMAs and the epilogue
     if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, TPW, A, H, h, warp, lane);
@@ -868,13 +890,22 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-      // the epilogue needs Yi only; the state update runs on under it
+      // a lazy chunk waits for Yo only here; the q tile is then free for the
+      // next chunk's C rows
+      if (lazy) {
+        if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
+        tc::fence_after();
+        if (kAsync && c0 + Qt < l1) {
+          copy_items(a.c, sQ, tok0 + Qt, min(Qt, l1 - c0 - Qt));
+          tc::cp_async_commit();
+        }
+      }
+      // the epilogue needs Yo and Yi; the state update runs on under it
       if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
       tc::fence_after();
       // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
       // two lanes of a row split each 16-column block into 8 + 8 columns.
       {
-        const float* xcol = a.x + tok0 * HP + (int64_t)h * P + prow;
         const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
         float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
         for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
@@ -895,15 +926,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int col0 = cb * 16 + 8 * half;
           if (!mimo) {
             const int u = cb - 2 * wg;
-            float ec[kCols], xs[kCols];
-#pragma unroll
-            for (int q = 0; q < kCols / 4; ++q) {
-              const float4 x4 = *reinterpret_cast<const float4*>(sXt + tc::kmaj(prow, col0 + 4 * q, kRows));
-              xs[4 * q] = x4.x;
-              xs[4 * q + 1] = x4.y;
-              xs[4 * q + 2] = x4.z;
-              xs[4 * q + 3] = x4.w;
-            }
+            float ec[kCols];
 #pragma unroll
             for (int q = 0; q < kCols / 4; ++q) {
               const float4 e4 = *reinterpret_cast<const float4*>(tEc + col0 + 4 * q);
@@ -916,10 +939,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (kStaged) {
-                sP[t * KP + prow] = ec[j] * yo[j] + yi[j] + dsk * xs[j];
+                sP[t * KP + prow] = fmaf(ec[j], yo[j], yi[j]);
               } else if (t < tv) {
                 const float zv = u ? ze[1][j] : ze[0][j];
-                float y = ec[j] * yo[j] + yi[j] + dsk * xs[j];
+                float y = fmaf(ec[j], yo[j], yi[j]);
                 if (g.has_z) y *= silu_fast(zv);
                 ocol[t * HP] = y;
               }
@@ -929,7 +952,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int tt = 0; tt < tpb; ++tt) {
               const int t = (col0 >> lgR) + tt;
               if (t >= tv) break;
-              const float xv = xcol[t * HP];
               const float zv = g.has_z ? zcol[t * HP] : 0.f;
               const float ec = tEc[t];
               float o = 0.f;
@@ -937,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               for (int r = 0; r < kRmax; ++r) {
                 if (r < R) {
                   const int j = (tt << lgR) + r;
-                  float y = ec * yo[j] + yi[j] + dsk * xv * mxr[r];
+                  float y = fmaf(ec, yo[j], yi[j]);
                   if (g.has_z) y *= silu_fast(zv * mzr[r]);
                   o += mor[r] * y;
                 }
@@ -1001,8 +1023,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc::fence_after();
   if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
   if (!abort_flag) {
-    // final state, cumulative angle and decay of this segment
+    // final state (G = e^{lgE} G~), cumulative angle and decay of this segment
     const float* thb = sThBase + (it & 1) * kAngMax;
+    const float gsc = expf(lgE);
     if (io.g1) {
       float* g1 = io.g1 + ((int64_t)cta * P + prow) * N;
       for (int c = 16 * wg; c < Npad; c += 32) {
@@ -1011,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (g_lane) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c + j < N) g1[c + j] = v[j];
+            if (c + j < N) g1[c + j] = v[j] * gsc;
         }
       }
     }
@@ -1023,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (g_lane) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c + j < N) gl[c + j] = v[j];
+            if (c + j < N) gl[c + j] = v[j] * gsc;
         }
       }
     }

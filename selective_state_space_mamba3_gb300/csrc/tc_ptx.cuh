@@ -178,15 +178,21 @@ __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const float* v) 
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// Round-to-nearest conversion to TF32 (the tensor core would otherwise drop
-// the low mantissa bits).
-__device__ __forceinline__ float to_tf32(float v) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-  return __uint_as_float(r);
+// TF32 operand rounding. A kind::tf32 MMA reads the sign, the exponent and the
+// top 10 mantissa bits of each 32-bit element and ignores the low 13 bits, so
+// adding half a TF32 unit in the last place (0x1000) to the bit pattern makes
+// the MMA see the value rounded to nearest (ties away from zero) at the cost of
+// one integer add. tf32_feed is for values that only the tensor core reads;
+// tf32_clean also clears the ignored bits, for values that are read back as
+// FP32 as well. Both turn an infinity into a NaN.
+__device__ __forceinline__ float tf32_feed(float v) {
+  return __uint_as_float(__float_as_uint(v) + 0x1000u);
 }
-__device__ __forceinline__ float4 to_tf32(float4 v) {
-  return make_float4(to_tf32(v.x), to_tf32(v.y), to_tf32(v.z), to_tf32(v.w));
+__device__ __forceinline__ float4 tf32_feed(float4 v) {
+  return make_float4(tf32_feed(v.x), tf32_feed(v.y), tf32_feed(v.z), tf32_feed(v.w));
+}
+__device__ __forceinline__ float tf32_clean(float v) {
+  return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
 }
 
 }  // namespace tc
