@@ -92,56 +92,135 @@ def read_traffic(kernel):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons every 50 ms while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs. Through NVML (libnvidia-ml, read-only queries, every
+    2 ms) when it loads, else through `nvidia-smi -lms 50`; every sample
+    carries a host timestamp, and only those taken between mark_begin() and
+    mark_end() are reported (the nearest one if the region was shorter than
+    the sampling period)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.samples = []          # (time, sm MHz, set of reasons)
+        self.smax = None
+        self.source = None
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+
+    def _nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.gpu).uuid)
+        except Exception:
+            uuid = None
+        ok = False
+        if uuid:
+            ok = nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+            self.smax = float(mx.value)
+        getr = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nv, h, getr
 
     def start(self):
+        import ctypes
+        try:
+            nv, h, getr = self._nvml()
+            self.source = "nvml"
+
+            def run():
+                clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    t = time.perf_counter()
+                    if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                        why = set()
+                        if getr(h, ctypes.byref(rs)) == 0:
+                            why = {n for b, n in self.BITS.items() if rs.value & b}
+                        self.samples.append((t, float(clk.value), why))
+                    time.sleep(0.002)
+            self.t = threading.Thread(target=run, daemon=True)
+            self.t.start()
+            return
+        except (OSError, AttributeError):
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def wait_first(self, timeout=5.0):
+        """Blocks until the first sample arrived (the sampler is running)."""
+        end = time.perf_counter() + timeout
+        while not self.samples and time.perf_counter() < end:
+            time.sleep(0.005)
 
-    def stop(self):
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.t.join(timeout=2)
-        sm, smax, reasons = [], None, set()
+    def mark_begin(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def _read(self):
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.strip().split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
+                sm, self.smax = float(f[1]), float(f[2])
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            why = {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}
+            self.samples.append((time.perf_counter(), sm, why))
+
+    def stop(self):
+        if self.source is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"],
+                    "samples": 0}
+        self._stop.set()
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.t.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        """Median SM clock, max clock and reasons of the samples in the window."""
+        got = list(self.samples)
+        inside = [x for x in got if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        if not inside and got and self.t0 is not None:
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(got, key=lambda x: abs(x[0] - mid))]
+        sm = [x[1] for x in inside]
+        reasons = set().union(*[x[2] for x in inside]) if inside else set()
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": self.smax,
+                "reasons": sorted(reasons), "samples": len(sm), "source": self.source,
+                "window_ms": round(1e3 * (self.t1 - self.t0), 3) if self.t0 is not None else None}
 
 
 def dist_setup(args=None):
@@ -399,9 +478,11 @@ def run_m3(args):
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.wait_first()
     barrier()
     torch.cuda.synchronize()
     n0 = m3.launch_count()
+    clocks.mark_begin()
     t_start.record()
     for k in range(K):
         ev[k][0].record()
@@ -411,6 +492,7 @@ def run_m3(args):
         ev[k][2].record()
     t_end.record()
     torch.cuda.synchronize()
+    clocks.mark_end()
     launches = m3.launch_count() - n0
     barrier()
     clk = clocks.stop()

@@ -39,6 +39,10 @@
 //
 // The kernel is a template over the shape: the generic instance reads N, A, R
 // and P at run time; instances for common shapes have them as constants.
+#include <cuda.h>
+#include <string.h>
+#include <cudaTypedefs.h>
+
 #include "m3_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -58,16 +62,19 @@ constexpr float kLazyRange = 40.0f;
 
 struct ChunkLayout {
   int Npad, MP;
-  int q, k, kt, tot, bias, tok, thbase, th, o;  // float offsets of the regions
+  int q, k, kt, tot, bias, tok, thbase, th, o, p;  // float offsets of the regions
   size_t bytes;
 };
 
-// Instances with compile-time N and A (A <= 32, both multiples of 4) stage the
-// C / B rows with cp.async straight into the q / k tile positions; their
-// rotary angles and MIMO norm staging then live in regions of their own.
+// Instances with compile-time N and A (N a multiple of 32, A <= 32 and a
+// multiple of 4) stage the C / B rows of a chunk by TMA: one 4-D box per
+// 32-column block lands in a 128-byte-swizzled K-major q / k tile, which the
+// threads then rotate in place; their rotary angles and MIMO norm staging live
+// in regions of their own.
 __host__ __device__ constexpr bool chunk_async(int KN, int KA) {
-  return KN > 0 && KA > 0 && KA <= 32 && KN % 4 == 0 && KA % 4 == 0;
+  return KN > 0 && KA > 0 && KA <= 32 && KN % 32 == 0 && KA % 4 == 0;
 }
+constexpr int kTmaThread = 64;  // issues the TMA copies (warp 2, lane 0)
 
 int imax(int a, int b) { return a > b ? a : b; }
 
@@ -87,8 +94,12 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
   // [Qt][MP] uses the region in the epilogue.
   l.q = take(async ? kRows * l.Npad : imax(kRows * l.Npad, Qt * l.MP));
   // K region: k tile [64][Npad] until S = Q K^T completes, then the masked
-  // scores [64][64] followed by the values X^T [MP][64].
-  l.k = take(imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
+  // scores [64][64] followed by the values X^T [MP][64]. With TMA staging and
+  // N <= 64 (split), the values follow the k tile and the scores have a region
+  // of their own, so that the next chunk's B rows can land once S is done.
+  const bool split = async && N <= 64;
+  l.k = take(split ? kRows * l.Npad + l.MP * kRows
+                   : imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
   // Kt region: w-scaled transposed keys [Npad][64] (K-major, K = row).
   l.kt = take(l.Npad * kRows);
   l.tot = take(kWarps * kAngMax + kWarps);  // per-warp angle / log-decay totals
@@ -97,6 +108,7 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
   l.th = async ? take(kWarps * (8 / R) * (A + 4)) : 0;  // per-warp angles [TPW][A + 4]
   l.o = (async && mimo) ? take(Qt * l.MP) : 0;          // MIMO norm staging
+  l.p = split ? take(kRows * kRows) : 0;                 // masked scores (split)
   l.bytes = (size_t)off * sizeof(float);
   return l;
 }
@@ -174,10 +186,15 @@ __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f 
 
 template <int MP, bool MIMO, bool SUMMARY, int KN, int KA, int KR, int KP>
 __global__ void __launch_bounds__(kThreads, 2)
-    k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, ChunkIO io, uint32_t* status) {
-  extern __shared__ __align__(1024) float sm[];
-  // MMA completion barriers: S, Yo, Yi, state update (each completes once per chunk)
-  __shared__ __align__(8) uint64_t bars[4];
+    k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, ChunkIO io, uint32_t* status,
+                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ __align__(1024) float sm_raw[];
+  constexpr bool kAsync = chunk_async(KN, KA);
+  // swizzled tiles start on a 1024-byte boundary (1 KB of slack is allocated)
+  float* sm = kAsync ? sm_raw + ((1024u - (tc::smem_u32(sm_raw) & 1023u)) & 1023u) / 4 : sm_raw;
+  // Completion barriers, each completing once per chunk: MMAs S, Yo, Yi and
+  // state update; TMA copies of the C rows and of the B rows.
+  __shared__ __align__(8) uint64_t bars[6];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -201,11 +218,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int RG = g.G * R;
 
   float* sQ = sm + lay.q;              // [64 rows][Npad] K-major, K = n
-  constexpr bool kAsync = chunk_async(KN, KA);
   float* sO = (kAsync && MIMO) ? sm + lay.o : sQ;  // [Qt][MP] MIMO epilogue staging
   float* sK = sm + lay.k;              // [64 rows][Npad] K-major, K = n
-  float* sP = sK;                      // [64][64]        masked scores (after S)
-  float* sXt = sK + kRows * kRows;     // [MP][64 rows]   values (after S)
+  // With TMA staging the next chunk's B rows are copied as soon as the k tile
+  // is dead (kEarlyB): in the summary pass (no S; the values then use the
+  // unused q tile) right after the tiles are built, and with split regions
+  // (N <= 64) once S = Q K^T completes; otherwise after the state update.
+  constexpr bool kSplitK = kAsync && KN <= 64;
+  constexpr bool kEarlyB = kAsync && (SUMMARY || kSplitK);
+  float* sP = kSplitK ? sm + lay.p : sK;  // [64][64]      masked scores (after S)
+  // [MP][64 rows] values (after S)
+  float* sXt = (kAsync && SUMMARY) ? sQ : sK + (kSplitK ? kRows * Npad : kRows * kRows);
   float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
   float* sTot = sm + lay.tot;          // [8 warps][64]   per-warp angle totals
   float* sTotAdt = sTot + kWarps * kAngMax;  // [8 warps] per-warp log-decay totals
@@ -221,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sTh = kAsync ? sm + lay.th + warp * TPW * AS : sQ + warp * 8 * Npad;
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) tc::bar_init(&bars[i], 1);
+    for (int i = 0; i < 6; ++i) tc::bar_init(&bars[i], 1);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
@@ -308,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   }
   // MMA operand descriptors; K step ks adds 16 * ks (256 bytes) to each
-  const uint64_t dQ = tc::kdesc(sQ, Npad, 0), dK = tc::kdesc(sK, Npad, 0);
+  const uint64_t dQ = kAsync ? tc::swdesc(sQ) : tc::kdesc(sQ, Npad, 0);
+  const uint64_t dK = kAsync ? tc::swdesc(sK) : tc::kdesc(sK, Npad, 0);
   const uint64_t dXt = tc::kdesc(sXt, kRows, 0), dP = tc::kdesc(sP, kRows, 0);
   const uint64_t dKt = tc::kdesc(sKt, kRows, 0);
 
@@ -317,33 +341,27 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int rl = lane & 7, jl = lane >> 3;
   const int rho = 8 * warp + rl;
   const int t = rho >> lgR, r = rho & (R - 1);
-  // cp.async staging: copies this lane's phase-(4) items of a chunk's C (or B)
-  // rows into the K-major tile positions that phase (4) rewrites in place
-  // (rows past the chunk's valid tokens are zero-filled).
-  auto copy_items = [&](const float* src, float* tile, int64_t tok_first, int tvn) {
-    const bool ok = t < tvn;
-    const float* row = src + (ok ? ((tok_first + t) * RG + (int64_t)grp * R + r) * N : 0);
-    const uint32_t nb = ok ? 16u : 0u;
-    const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
+  // Offset of element (row, n) in the q / k tiles, and the descriptor advance
+  // of MMA K step ks over them.
+  auto toff = [&](int row, int n) { return kAsync ? tc::sw128(row, n, kRows) : tc::kmaj(row, n, Npad); };
+  auto qk_step = [&](int ks) -> uint64_t { return kAsync ? tc::swdesc_kstep(ks, kRows) : 16u * ks; };
+  // TMA staging (thread kTmaThread): the C (or B) rows of the chunk starting at
+  // token t_start of the sequence into a q (or k) tile, one box [Qt tokens][R
+  // ranks][32 dims] per column block; rows past the sequence end read zeros.
+  int pendC = -1, pendB = -1;  // chunk whose copy is in flight (issuing thread)
+  auto issue_rows = [&](const CUtensorMap* tm, float* tile, int t_start, uint64_t* bar) {
+    tc::bar_expect_tx(bar, (uint32_t)(kRows * N * 4));
 #pragma unroll
-    for (int jb = 0; jb < QW4; ++jb) {
-      const int j = 4 * jb + jl;
-      if (j >= QW) continue;
-      if (j < PQ) {
-        const int n0 = 4 * j;
-        tc::cp_async16(tile + tc::kmaj(rho, n0, Npad), row + n0, nb);
-        tc::cp_async16(tile + tc::kmaj(rho, n0 + A, Npad), row + n0 + A, nb);
-      } else {
-        const int n0 = 2 * A + 4 * (j - PQ);
-        tc::cp_async16(tile + tc::kmaj(rho, n0, Npad), row + n0, nb);
-      }
-    }
+    for (int cb = 0; cb < (KN > 0 ? KN : 128) / 32; ++cb)
+      tc::tma_load_4d(tile + cb * kRows * 32, tm, 32 * cb, grp * R, t_start, b, bar);
   };
-  if (kAsync) {
-    const int tv0 = min(Qt, l1 - l0);
-    if (!SUMMARY) copy_items(a.c, sQ, (int64_t)b * L + l0, tv0);
-    copy_items(a.b, sK, (int64_t)b * L + l0, tv0);
-    tc::cp_async_commit();
+  if (kAsync && tid == kTmaThread && l0 < l1) {
+    if (!SUMMARY) {
+      issue_rows(&tmC, sQ, l0, &bars[4]);
+      pendC = 0;
+    }
+    issue_rows(&tmB, sK, l0, &bars[5]);
+    pendB = 0;
   }
 
   TokenPreload pl;
@@ -485,10 +503,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #undef M3_ROT
         }
         if (!SUMMARY) {
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(q0);
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)) = tc::tf32_feed(q1);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(k0);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0 + A, Npad)) = tc::tf32_feed(k1);
+          *reinterpret_cast<float4*>(sQ + toff(rho, n0)) = tc::tf32_feed(q0);
+          *reinterpret_cast<float4*>(sQ + toff(rho, n0 + A)) = tc::tf32_feed(q1);
+          *reinterpret_cast<float4*>(sK + toff(rho, n0)) = tc::tf32_feed(k0);
+          *reinterpret_cast<float4*>(sK + toff(rho, n0 + A)) = tc::tf32_feed(k1);
         }
         store_kt4(sKt, n0, rho, k0, omr, krot);
         store_kt4(sKt, n0 + A, rho, k1, omr, krot);
@@ -507,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
         }
         if (!SUMMARY) {
-          *reinterpret_cast<float4*>(sQ + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(qv);
-          *reinterpret_cast<float4*>(sK + tc::kmaj(rho, n0, Npad)) = tc::tf32_feed(kv);
+          *reinterpret_cast<float4*>(sQ + toff(rho, n0)) = tc::tf32_feed(qv);
+          *reinterpret_cast<float4*>(sK + toff(rho, n0)) = tc::tf32_feed(kv);
         }
         store_kt4(sKt, n0, rho, kv, omr, krot);
         if (kl) *reinterpret_cast<float4*>(kl + n0) = kv;
@@ -528,8 +546,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         __syncwarp();
         if (kAsync) {
-          // operands staged by cp.async in the q / k tile positions
-          tc::cp_async_wait_all();
+          // operands staged by TMA in the q / k tile positions
+          bool ok = SUMMARY || tc::bar_wait(&bars[4], it & 1, kWaitBudget);
+          ok = tc::bar_wait(&bars[5], it & 1, kWaitBudget) && ok;
+          if (!ok) abort_flag = 1;
+          if (pendC == it) pendC = -1;
+          if (pendB == it) pendB = -1;
 #pragma unroll
           for (int jb = 0; jb < QW4; ++jb) {
             const int j = 4 * jb + jl;
@@ -543,14 +565,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 case 2: th = th4[2]; break;
                 default: th = th4[3]; break;
               }
-              pair_item(n0, *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0, Npad)),
-                        *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0 + A, Npad)),
-                        *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad)),
-                        *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0 + A, Npad)), th);
+              pair_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
+                        *reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)),
+                        *reinterpret_cast<const float4*>(sK + toff(rho, n0)),
+                        *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)), th);
             } else {
               const int n0 = 2 * A + 4 * (j - PQ);
-              single_item(n0, *reinterpret_cast<const float4*>(sQ + tc::kmaj(rho, n0, Npad)),
-                          *reinterpret_cast<const float4*>(sK + tc::kmaj(rho, n0, Npad)));
+              single_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
+                          *reinterpret_cast<const float4*>(sK + toff(rho, n0)));
             }
           }
         } else {
@@ -653,19 +675,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();  // B2: tiles complete
     tc::fence_after();
     if (abort_flag) break;
+    if (kEarlyB && SUMMARY && tid == kTmaThread && c0 + Qt < l1) {
+      issue_rows(&tmB, sK, c0 + Qt, &bars[5]);
+      pendB = it + 1;
+    }
     // (5) S = Q K^T and Yo^T = G Q^T
     // (MMAs issued by one thread run one after another; the two independent
     // chains come from threads of different warps so that they overlap)
     if (!SUMMARY && tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < Npad / 8; ++ks)
-        tc::mma_ss(tS, dQ + 16ull * ks, dK + 16ull * ks, id_S, ks > 0);
+        tc::mma_ss(tS, dQ + qk_step(ks), dK + qk_step(ks), id_S, ks > 0);
       tc::commit(&bars[0]);
     }
     if (!SUMMARY && tid == 32) {
 #pragma unroll
       for (int ks = 0; ks < Npad / 8; ++ks)
-        tc::mma_ts(tYo, tG + ks * 8, dQ + 16ull * ks, id_Y, ks > 0);
+        tc::mma_ts(tYo, tG + ks * 8, dQ + qk_step(ks), id_Y, ks > 0);
       tc::commit(&bars[1]);
     }
     // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
@@ -707,8 +733,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
       if (!SUMMARY) {
-        if (!tc::bar_wait(&bars[0], it & 1, kWaitBudget)) abort_flag = 1;
+        const bool s_done = tc::bar_wait(&bars[0], it & 1, kWaitBudget);
+        if (!s_done) abort_flag = 1;
         tc::fence_after();
+        // the k tile is dead once S has read it (split regions)
+        if (kEarlyB && s_done && tid == kTmaThread && c0 + Qt < l1) {
+          issue_rows(&tmB, sK, c0 + Qt, &bars[5]);
+          pendB = it + 1;
+        }
         const int rho = 16 * quad + (lane & 15);
         const int t = rho >> lgR;
         const float cum_t = tCum[t];
@@ -799,9 +831,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
         tc::fence_after();
         // the q tile is free: stage the next chunk's C rows
-        if (kAsync && c0 + Qt < l1) {
-          copy_items(a.c, sQ, tok0 + Qt, min(Qt, l1 - c0 - Qt));
-          tc::cp_async_commit();
+        if (kAsync && c0 + Qt < l1 && tid == kTmaThread) {
+          issue_rows(&tmC, sQ, c0 + Qt, &bars[4]);
+          pendC = it + 1;
         }
       }
       const float ec = expf(lgE + cend);
@@ -895,9 +927,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lazy) {
         if (!tc::bar_wait(&bars[1], it & 1, kWaitBudget)) abort_flag = 1;
         tc::fence_after();
-        if (kAsync && c0 + Qt < l1) {
-          copy_items(a.c, sQ, tok0 + Qt, min(Qt, l1 - c0 - Qt));
-          tc::cp_async_commit();
+        if (kAsync && c0 + Qt < l1 && tid == kTmaThread) {
+          issue_rows(&tmC, sQ, c0 + Qt, &bars[4]);
+          pendC = it + 1;
         }
       }
       // the epilogue needs Yo and Yi; the state update runs on under it
@@ -1003,14 +1035,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    // once the state update has read the K region and every thread has read its
-    // epilogue values out of it: stage the next chunk's B rows
-    if (kAsync && c0 + Qt < l1) {
-      if (!SUMMARY) __syncthreads();
-      if (!tc::bar_wait(&bars[3], it & 1, kWaitBudget)) abort_flag = 1;
-      tc::fence_after();
-      copy_items(a.b, sK, tok0 + Qt, min(Qt, l1 - c0 - Qt));
-      tc::cp_async_commit();
+    // once the state update has read the K region and every thread is done with
+    // its scores, values and staged outputs: stage the next chunk's B rows
+    // (the generic-proxy writes of the region are ordered before the TMA's)
+    if (kAsync && !kEarlyB && c0 + Qt < l1) {
+      if (!SUMMARY) {
+        tc::fence_async_smem();
+        __syncthreads();
+      }
+      if (tid == kTmaThread) {
+        if (tc::bar_wait(&bars[3], it & 1, kWaitBudget)) {
+          tc::fence_after();
+          issue_rows(&tmB, sK, c0 + Qt, &bars[5]);
+          pendB = it + 1;
+        } else {
+          abort_flag = 1;
+        }
+      }
     }
   }
   // the last state update
@@ -1022,6 +1063,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   tc::fence_after();
   if (abort_flag && tid == 0) atomicExch(status, kStatusTimeout);
+  // after a timeout: wait (bounded) for TMA copies still in flight, since
+  // shared memory must outlive them
+  if (kAsync && tid == kTmaThread) {
+    if (pendC >= 0) tc::bar_wait(&bars[4], pendC & 1, kWaitBudget);
+    if (pendB >= 0) tc::bar_wait(&bars[5], pendB & 1, kWaitBudget);
+  }
   if (!abort_flag) {
     // final state (G = e^{lgE} G~), cumulative angle and decay of this segment
     const float* thb = sThBase + (it & 1) * kAngMax;
@@ -1061,16 +1108,57 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) tc::tmem_free(tbase, 256);
 }
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of the C or B rows [B, L, G * R, N] for the chunk kernel's TMA
+// staging: dimensions (n, group row, token, batch), box [32 dims][R ranks][Qt
+// tokens][1], 128-byte swizzle, zero fill outside the tensor.
+cudaError_t rows_tensor_map(CUtensorMap* m, const float* base, const ScanGeom& g) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const uint64_t RG = (uint64_t)g.G * g.R, N = (uint64_t)g.N;
+  const cuuint64_t dims[4] = {N, RG, (cuuint64_t)g.L, (cuuint64_t)g.B};
+  const cuuint64_t strides[3] = {N * 4, RG * N * 4, (uint64_t)g.L * RG * N * 4};
+  const cuuint32_t box[4] = {32, (cuuint32_t)g.R, (cuuint32_t)(kRows / g.R), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int MP, bool MIMO, int KN, int KA, int KR, int KP>
 cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, const ChunkIO& io,
                       bool summary, unsigned grid, cudaStream_t s) {
-  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R, MIMO, chunk_async(KN, KA));
+  constexpr bool async = chunk_async(KN, KA);
+  const ChunkLayout lay = chunk_layout(g.N, g.P, g.A, g.R, MIMO, async);
+  const size_t bytes = lay.bytes + (async ? 1024 : 0);
+  CUtensorMap tmC, tmB;
+  memset(&tmC, 0, sizeof(tmC));
+  memset(&tmB, 0, sizeof(tmB));
+  cudaError_t e;
+  if (async) {
+    if ((e = rows_tensor_map(&tmC, a.c, g)) != cudaSuccess) return e;
+    if ((e = rows_tensor_map(&tmB, a.b, g)) != cudaSuccess) return e;
+  }
   auto kernel = summary ? k_scan_chunk<MP, MIMO, true, KN, KA, KR, KP>
                         : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)lay.bytes);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kThreads, lay.bytes, s>>>(g, a, lay, io, status);
+  kernel<<<grid, kThreads, bytes, s>>>(g, a, lay, io, status, tmC, tmB);
   return cudaSuccess;
 }
 

@@ -24,6 +24,15 @@ __device__ __forceinline__ int kmaj(int row, int k, int kext) {
   return (((row >> 3) * (kext >> 2) + (k >> 2)) << 5) + ((row & 7) << 2) + (k & 3);
 }
 
+// Float offset of element (row, k) in a K-major tile with the 128-byte swizzle
+// (the layout a TMA tile copy with CU_TENSOR_MAP_SWIZZLE_128B writes): K is
+// cut into column blocks of 32 elements; a block holds `rows` rows of 128 B,
+// and the 16-byte chunk c of row r sits at chunk position c ^ (r % 8). The
+// tile must start on a 1024-byte boundary.
+__device__ __forceinline__ int sw128(int row, int k, int rows) {
+  return (((k >> 5) * rows + row) << 5) + ((((k & 31) >> 2) ^ (row & 7)) << 2) + (k & 3);
+}
+
 // Shared-memory matrix descriptor (no swizzle, sm_100 descriptor version 1).
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
@@ -33,6 +42,16 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, ui
 // 8 elements (one MMA K step = two core matrices = 256 B).
 __device__ __forceinline__ uint64_t kdesc(const float* tile, int kext, int kstep) {
   return sdesc(smem_u32(tile) + (uint32_t)kstep * 256u, 128u, (uint32_t)kext * 32u);
+}
+// Descriptor of a K-major 128-byte-swizzled tile (layout of sw128): 8-row
+// atoms of 1024 B along M / N (stride-byte offset 1024), swizzle mode 2 in
+// bits 61..63. One MMA K step (8 elements = 32 B) advances the start address
+// by 32 B inside a 128-byte row; the next column block starts rows * 128 B on.
+__device__ __forceinline__ uint64_t swdesc(const float* tile) {
+  return sdesc(smem_u32(tile), 16u, 1024u) | (2ull << 61);
+}
+__host__ __device__ constexpr uint32_t swdesc_kstep(int ks, int rows) {
+  return (uint32_t)(((ks >> 2) * rows * 128 + (ks & 3) * 32) >> 4);  // in descriptor units
 }
 
 // Instruction descriptor: kind::tf32, dense, D = F32, A = B = TF32, A
@@ -134,16 +153,22 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[15])));
 }
 
-// 16-byte asynchronous global -> shared copy (L2 only); src_bytes = 0 fills
-// the 16 bytes with zeros without reading. Completion is per thread:
-// cp_async_commit() closes a group, cp_async_wait_all() waits for all groups.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(src_bytes)
+// TMA: 4-D tiled copy of one box of the tensor map into shared memory,
+// completing `bytes` of transaction count on the mbarrier (coordinates are
+// element indices, innermost first).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                           int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+// Arrives on the mbarrier and raises its expected transaction count.
+__device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Two 32-lane x 16-column loads with a single wait (fewer serialised waits).
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float* va, float* vb) {
