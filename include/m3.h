@@ -44,8 +44,9 @@ enum m3_status {
 
 /* Arithmetic of the scans' dense contractions (an extension of SsmConfig). */
 enum m3_math_mode {
-  M3_MATH_FP32 = 0, /* FP32-exact: FP32 FFMA or 3-pass split-TF32 tensor MMA */
-  M3_MATH_TF32 = 1  /* single-pass TF32 tensor MMA, FP32 accumulate */
+  M3_MATH_FP32 = 0, /* FP32-exact: the token-by-token recurrence in FP32 FFMA */
+  M3_MATH_TF32 = 1  /* chunked form, single-pass TF32 tensor MMA, FP32 accumulate
+                       (shapes the chunked kernel does not take run as FP32) */
 };
 
 typedef struct CUstream_st* m3_stream_t; /* same type as cudaStream_t */

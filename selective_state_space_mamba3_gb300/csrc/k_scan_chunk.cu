@@ -102,9 +102,9 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
                    : imax(kRows * l.Npad, kRows * kRows + l.MP * kRows));
   // Kt region: w-scaled transposed keys [Npad][64] (K-major, K = row).
   l.kt = take(l.Npad * kRows);
-  l.tot = take(kWarps * kAngMax + kWarps);  // per-warp angle / log-decay totals
+  l.tot = take(kWarps * kAngMax + 2 * kWarps);  // per-warp angle, log-decay, |log-decay| totals
   l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
-  l.tok = take(4 * kTok);                   // cum, e^cum, gamma, w per token
+  l.tok = take(6 * kTok);                   // cum, e^{cum + lgE}, gamma, w, e^cum, e^-cum w
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
   l.th = async ? take(kWarps * (8 / R) * (A + 4)) : 0;  // per-warp angles [TPW][A + 4]
   l.o = (async && mimo) ? take(Qt * l.MP) : 0;          // MIMO norm staging
@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // unused q tile) right after the tiles are built, and with split regions
   // (N <= 64) once S = Q K^T completes; otherwise after the state update.
   constexpr bool kSplitK = kAsync && KN <= 64;
+  constexpr bool kFactMask = KR == 1;  // factored decay mask (compile-time SISO)
   constexpr bool kEarlyB = kAsync && (SUMMARY || kSplitK);
   float* sP = kSplitK ? sm + lay.p : sK;  // [64][64]      masked scores (after S)
   // [MP][64 rows] values (after S)
@@ -238,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* tEc = tCum + kTok;            // e^{cum_t}
   float* tGam = tEc + kTok;            // gamma_t
   float* tW = tGam + kTok;             // gamma_t + scale_{t+1}
+  float* tEa = tW + kTok;              // e^{cum_t}            (factored mask)
+  float* tEb = tEa + kTok;             // e^{-cum_t} w_t       (factored mask)
+  float* sAbsAdt = sTotAdt + kWarps;   // [8 warps] per-warp totals of |adt|
   float* sThBase = sm + lay.thbase;    // [2][64] cumulative angle before the chunk
   const int AS = A + 4;                // angle row stride of a warp's angle block
   // this warp's angles [TPW][AS] (without cp.async staging: in its q rows)
@@ -408,6 +412,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const float adt_tot = __shfl_sync(0xffffffffu, cl, TPW - 1);
     if (lane == 0) sTotAdt[warp] = adt_tot;
+    if (kFactMask) {
+      float aab = fabsf(adtv);  // lanes 0 .. TPW - 1 hold the warp's tokens
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) aab += __shfl_xor_sync(0xffffffffu, aab, o);
+      if (lane == 0) sAbsAdt[warp] = aab;
+    }
     float thl[2][8];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -428,13 +438,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float* crow = a.c + roff;
     const float* brow = a.b + roff;
     // (2) per-token coefficients (lane i < TPW) and this warp's angles
-    float cend = 0.f, cbase = 0.f;
+    float cend = 0.f, cbase = 0.f, aabs = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const float v = sTotAdt[w];
       if (w < warp) cbase += v;
       cend += v;
+      if (kFactMask) aabs += sAbsAdt[w];
     }
+    // Factored mask (SISO instances): with sum |adt| <= 85 over the chunk
+    // every |cum_t| <= 85, so e^{cum_t - cum_s} w_s = e^{cum_t} (e^{-cum_s} w_s)
+    // with both factors normal floats, computed once per token instead of once
+    // per (t, s)
+    const bool fact = kFactMask && aabs <= 85.0f;
     esum += cend;
     // lazy chunk: G~ keeps its scale, e^{-lgE_new} goes into the w-scaled keys
     // and e^{lgE} into the Yo readout; otherwise G~ *= e^{lgE + cend} below
@@ -448,6 +464,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       tEc[tw] = expf(cum + lgE);
       tGam[tw] = gam;
       tW[tw] = wt;
+      if (kFactMask) {
+        tEa[tw] = expf(cum);
+        tEb[tw] = expf(-cum) * wt;
+      }
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -745,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int t = rho >> lgR;
         const float cum_t = tCum[t];
         const float gam_t = tGam[t];
+        const float ea_t = kFactMask ? tEa[t] : 0.f;
         const int sh = lane >> 4;
         float sv[2][16];
         tc::tmem_ld16x2(tS + lane_base + 32 * wg, tS + lane_base + 32 * wg + 16, sv[0], sv[1]);
@@ -761,21 +782,25 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int col0 = cb * 16 + 8 * sh;
           // coefficients of the 8 key tokens of these columns (vector loads
           // when a row is a token)
+          // (factored: ws = e^{-cum_s} w_s; otherwise cs = cum_s, ws = w_s)
           float cs[8], ws[8];
+          const float* wsrc = fact ? tEb : tW;
           if (KR == 1) {
-            const float4 c0 = *reinterpret_cast<const float4*>(tCum + col0);
-            const float4 c1 = *reinterpret_cast<const float4*>(tCum + col0 + 4);
-            const float4 w0 = *reinterpret_cast<const float4*>(tW + col0);
-            const float4 w1 = *reinterpret_cast<const float4*>(tW + col0 + 4);
-            cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
-            cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+            const float4 w0 = *reinterpret_cast<const float4*>(wsrc + col0);
+            const float4 w1 = *reinterpret_cast<const float4*>(wsrc + col0 + 4);
             ws[0] = w0.x; ws[1] = w0.y; ws[2] = w0.z; ws[3] = w0.w;
             ws[4] = w1.x; ws[5] = w1.y; ws[6] = w1.z; ws[7] = w1.w;
+            if (!fact) {
+              const float4 c0 = *reinterpret_cast<const float4*>(tCum + col0);
+              const float4 c1 = *reinterpret_cast<const float4*>(tCum + col0 + 4);
+              cs[0] = c0.x; cs[1] = c0.y; cs[2] = c0.z; cs[3] = c0.w;
+              cs[4] = c1.x; cs[5] = c1.y; cs[6] = c1.z; cs[7] = c1.w;
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              cs[j] = tCum[(col0 + j) >> lgR];
-              ws[j] = tW[(col0 + j) >> lgR];
+              ws[j] = wsrc[(col0 + j) >> lgR];
+              if (!fact) cs[j] = tCum[(col0 + j) >> lgR];
             }
           }
 #pragma unroll
@@ -783,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int s = (col0 + j) >> lgR;
             float m = 0.f;
             if (s < t)
-              m = __expf(cum_t - cs[j]) * ws[j];
+              m = fact ? ea_t * ws[j] : __expf(cum_t - cs[j]) * ws[j];
             else if (s == t)
               m = gam_t;
             // the D skip rides on the diagonal: Yi then includes D * x

@@ -163,6 +163,26 @@ def test_siso_full_size(w, mode):
         check_close(got[bsl], ref, TOL[mode])
 
 
+@pytest.mark.parametrize("mode", [FP32, TF32])
+@pytest.mark.parametrize("mimo", [False, True], ids=["siso", "mimo"])
+def test_strong_decay_chunks(mimo, mode):
+    """The log decay adt scaled up along the sequence (x1 at the start, x15 for
+    SISO / x60 for MIMO at the end), so that the chunks' summed |adt| runs from
+    about 3-12 to about 170: the chunked kernel's factored decay mask (SISO,
+    sum <= 85) and its exact-exponential mask both run, and so do its lazy and
+    its rescaling state updates (compile-time P64 N128 A32 and R4 P64 N64 A32)."""
+    shape = (dict(B=1, L=640, H=2, G=1, P=64, N=64, A=32, R=4, norm=1) if mimo
+             else dict(B=1, L=640, H=2, G=1, P=64, N=128, A=32))
+    w, ins = edge_case(**shape, seed=12)
+    top = 60.0 if mimo else 15.0
+    ramp = 1.0 + (top - 1.0) * np.arange(w.sequence_length) / w.sequence_length
+    ins["adt"] = (ins["adt"] * ramp[None, :, None]).astype(np.float32)
+    got = gpu_scan(w.cfg(), ins, mode, mimo=mimo)
+    ref = oracle_scan(w.cfg(), ins, mimo=mimo)
+    tol = MIMO_TF32_NORM_TOL if (mimo and mode == TF32) else TOL[mode]
+    check_close(got, ref, tol)
+
+
 # --------------------------------------------------------------- MIMO scans
 
 MIMO_EDGE = [
