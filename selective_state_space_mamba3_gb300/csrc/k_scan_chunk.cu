@@ -32,10 +32,12 @@
 // tiles), so only three block barriers remain per chunk (after the per-warp
 // totals, before the first and before the second MMA batch). The state update
 // of a chunk runs on under its epilogue and the next chunk's scalar work.
+// The C / B rows of a chunk arrive by TMA (one issuing thread, 4-D boxes into
+// 128-byte-swizzled tiles) a chunk ahead of their use.
 // Waits are bounded: on timeout the kernel records a status word and exits.
-// Shared memory (about 101 KB for P <= 64, N = 128) and TMEM (256 columns)
-// admit two CTAs per SM, and the next chunk's inputs are prefetched into L2
-// while the current chunk runs.
+// Shared memory (about 114 KB for P <= 64, N = 128) and TMEM (256 columns)
+// admit two CTAs per SM, and the next chunk's other inputs are prefetched into
+// L2 while the current chunk runs.
 //
 // The kernel is a template over the shape: the generic instance reads N, A, R
 // and P at run time; instances for common shapes have them as constants.
