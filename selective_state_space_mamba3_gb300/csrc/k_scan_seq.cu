@@ -21,13 +21,17 @@ namespace {
 
 
 struct SeqLayout {
-  int Npad, PT, R, A, kT;  // kT: tokens per staging tile
+  int Npad, RS, PT, R, A, kT;  // kT: tokens per staging tile; RS: q / k row stride
   size_t q, k, coef, theta, cs, xs, zs, ys, os, bias, bytes;
 };
 
-__host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int kT) {
+// RS is the q / k row stride in floats: 4 * NPT4 * LPR of the kernel instance
+// (>= Npad), so that every lane's state groups lie inside a row; the columns
+// Npad .. RS stay zero.
+__host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int kT, int RS) {
   SeqLayout l;
   l.Npad = (N + 15) / 16 * 16;
+  l.RS = RS;
   l.PT = PT;
   l.R = R;
   l.A = A;
@@ -38,8 +42,8 @@ __host__ __device__ inline SeqLayout seq_layout(int N, int PT, int R, int A, int
     off += (floats + 3) / 4 * 4;  // keep 16-byte alignment
     return o;
   };
-  l.q = take((size_t)kT * R * l.Npad);
-  l.k = take((size_t)(kT + 1) * R * l.Npad);
+  l.q = take((size_t)kT * R * RS);
+  l.k = take((size_t)(kT + 1) * R * RS);
   l.coef = take((size_t)kT * 4);
   l.theta = take((size_t)kT * (A > 0 ? A : 1));
   l.cs = take((size_t)2 * kT * (A > 0 ? A : 1));
@@ -71,6 +75,7 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int P = g.P, N = g.N, A = g.A, R = g.R, L = g.L, H = g.H;
   const int Npad = lay.Npad, PT = lay.PT, kT = lay.kT;
+  constexpr int RS = 4 * NPT4 * LPR;  // q / k row stride (the launcher sets lay.RS to it)
   const int ptiles = (P + PT - 1) / PT;
   const int bh = blockIdx.x / ptiles;
   const int p0 = (blockIdx.x % ptiles) * PT;
@@ -101,11 +106,14 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
     xprev[r] = (has_state && r < R && row_ok) ? st.v[((int64_t)bh * R + r) * P + p] : 0.f;
   }
   const float dskip = g.has_d ? a.d[h] : 0.f;
+  // q / k tiles start zeroed (columns Npad .. RS are never written again);
   // previous-token key slot (zero or the state's key); the running angle lives
   // in sth[(kT-1)*A + a]
+  for (int i = tid; i < (2 * kT + 1) * R * RS; i += nthr) sq[i] = 0.f;  // sq, then sk
+  __syncthreads();
   for (int i = tid; i < R * Npad; i += nthr) {
     const int r = i / Npad, n = i - r * Npad;
-    sk[i] = (has_state && n < N) ? st.k[((int64_t)bh * R + r) * N + n] : 0.f;
+    sk[r * RS + n] = (has_state && n < N) ? st.k[((int64_t)bh * R + r) * N + n] : 0.f;
   }
   for (int i = tid; i < A; i += nthr)
     sth[(kT - 1) * A + i] = (has_state && st.angle) ? st.angle[(int64_t)bh * A + i] : 0.f;
@@ -194,7 +202,7 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
         for (int which = 0; which < 2; ++which) {
           const float* src = (which ? a.b : a.c) + roff;
           const float* bias = (which ? sbb : sbc) + r * Npad;
-          float* dst = which ? sk + (size_t)(R + t * R + r) * Npad : sq + (size_t)(t * R + r) * Npad;
+          float* dst = which ? sk + (size_t)(R + t * R + r) * RS : sq + (size_t)(t * R + r) * RS;
           float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
           if (live) {
             const float4 u = *reinterpret_cast<const float4*>(src + n0);
@@ -247,8 +255,8 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
           kv = a.b[row + n] + bb[n];
         }
       }
-      sq[i] = qv;
-      sk[R * Npad + i] = kv;
+      sq[(t * R + r) * RS + n] = qv;
+      sk[(R + t * R + r) * RS + n] = kv;
     }
     __syncthreads();
     // 3. recurrence over the tile
@@ -264,19 +272,19 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
         acc[r] = 0.f;
         acc2[r] = 0.f;  // second readout chain (odd groups)
       }
-      const float4* kp4 = reinterpret_cast<const float4*>(sk + (size_t)t * R * Npad);
-      const float4* kc4 = reinterpret_cast<const float4*>(sk + (size_t)(t + 1) * R * Npad);
-      const float4* q4 = reinterpret_cast<const float4*>(sq + (size_t)t * R * Npad);
+      const float4* kp4 = reinterpret_cast<const float4*>(sk + (size_t)t * R * RS);
+      const float4* kc4 = reinterpret_cast<const float4*>(sk + (size_t)(t + 1) * R * RS);
+      const float4* q4 = reinterpret_cast<const float4*>(sq + (size_t)t * R * RS);
 #pragma unroll
       for (int i = 0; i < NPT4; ++i) {
-        const int n4 = j + LPR * i;
-        if (n4 * 4 < Npad) {
+        const int n4 = j + LPR * i;  // always inside the row (RS = 4 NPT4 LPR)
+        {
           float ux = 0.f, uy = 0.f, uz = 0.f, uw = 0.f;
 #pragma unroll
           for (int r = 0; r < RMAX; ++r) {
             if (r < R) {
-              const float4 kp = kp4[r * (Npad / 4) + n4];
-              const float4 kc = kc4[r * (Npad / 4) + n4];
+              const float4 kp = kp4[r * (RS / 4) + n4];
+              const float4 kc = kc4[r * (RS / 4) + n4];
               ux += cp[r] * kp.x + cc[r] * kc.x;
               uy += cp[r] * kp.y + cc[r] * kc.y;
               uz += cp[r] * kp.z + cc[r] * kc.z;
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
 #pragma unroll
           for (int r = 0; r < RMAX; ++r) {
             if (r < R) {
-              const float4 qq = q4[r * (Npad / 4) + n4];
+              const float4 qq = q4[r * (RS / 4) + n4];
               const float part = (hh[0] * qq.x + hh[1] * qq.y) + (hh[2] * qq.z + hh[3] * qq.w);
               if (i & 1)
                 acc2[r] += part;
@@ -351,7 +359,7 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
       }
     }
     // carry the last token's key into slot 0
-    for (int i = tid; i < R * Npad; i += nthr) sk[i] = sk[(size_t)tv * R * Npad + i];
+    for (int i = tid; i < R * RS; i += nthr) sk[i] = sk[(size_t)tv * R * RS + i];
     __syncthreads();
   }
   if (has_state) {
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
     }
     for (int i = tid; i < R * Npad; i += nthr) {
       const int r = i / Npad, n = i - r * Npad;
-      if (n < N) st.k[((int64_t)bh * R + r) * N + n] = sk[i];
+      if (n < N) st.k[((int64_t)bh * R + r) * N + n] = sk[r * RS + n];
     }
     if (row_ok && j == 0) {
 #pragma unroll
@@ -377,17 +385,26 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
   }
 }
 
+// State rows per block: all P rows (one block per (b, h): the MIMO output norm
+// and the step state need it, and it stages each (b, h)'s q / k once) while
+// 8 lanes per row keep the block within 512 threads; otherwise 32-row tiles.
+int seq_rows_per_block(const ScanGeom& g, const ScanArgs& a, const StepState& st, int rmax) {
+  if (rmax > 1 || a.mimo_o || st.ssm || g.P * 8 <= 512) return g.P;
+  return g.P < 32 ? g.P : 32;
+}
+
 template <int NPT4, int RMAX, int LPR>
 cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                          cudaStream_t s) {
   // one block per (b, h) for MIMO (block-local output norm) and with state
   // (the per-(b, h) key / angle state is read first and written last)
-  const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
+  const int PT = seq_rows_per_block(g, a, st, RMAX);
+  constexpr int RS = 4 * NPT4 * LPR;
   // 16-token staging tiles; 32 for blocks that own a whole (b, h) (one such
   // block per SM anyway) when they fit in 200 KB of shared memory
-  SeqLayout lay = seq_layout(g.N, PT, g.R, g.A, 16);
+  SeqLayout lay = seq_layout(g.N, PT, g.R, g.A, 16, RS);
   if (PT == g.P && (RMAX > 1 || a.mimo_o || st.ssm)) {
-    const SeqLayout big = seq_layout(g.N, PT, g.R, g.A, 32);
+    const SeqLayout big = seq_layout(g.N, PT, g.R, g.A, 32, RS);
     if (big.bytes <= 200 * 1024) lay = big;
   }
   const int threads = ((PT * LPR + 31) / 32) * 32;
@@ -406,7 +423,7 @@ cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& 
 template <int RMAX>
 cudaError_t launch_seq_r(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                          cudaStream_t s) {
-  const int PT = (RMAX > 1 || a.mimo_o || st.ssm) ? g.P : (g.P < 32 ? g.P : 32);
+  const int PT = seq_rows_per_block(g, a, st, RMAX);
   const int groups = (g.N + 15) / 16 * 4;  // float4 groups of a padded row
   if (PT * 8 <= 512) {
     if (groups <= 8) return launch_seq_t<1, RMAX, 8>(g, a, st, s);
