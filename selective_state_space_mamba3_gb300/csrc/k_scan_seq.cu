@@ -259,11 +259,12 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
       sk[(R + t * R + r) * RS + n] = kv;
     }
     __syncthreads();
-    // 3. recurrence over the tile
-    for (int t = 0; t < tv; ++t) {
+    // 3. recurrence over the tile. token_step advances the lane's state groups
+    // by token t and returns the lane's partial readouts per rank.
+    auto token_step = [&](int t, float* acc) {
       const float dec = scoef[t * 4 + 0], gam = scoef[t * 4 + 1], sdec = scoef[t * 4 + 2];
       const float xv = row_ok ? sx[t * PT + pi] : 0.f;
-      float cp[RMAX], cc[RMAX], xr[RMAX], acc[RMAX], acc2[RMAX];
+      float cp[RMAX], cc[RMAX], xr[RMAX], acc2[RMAX];
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         xr[r] = xv * mx[r];
@@ -278,44 +279,87 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
 #pragma unroll
       for (int i = 0; i < NPT4; ++i) {
         const int n4 = j + LPR * i;  // always inside the row (RS = 4 NPT4 LPR)
-        {
-          float ux = 0.f, uy = 0.f, uz = 0.f, uw = 0.f;
+        float ux = 0.f, uy = 0.f, uz = 0.f, uw = 0.f;
 #pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              const float4 kp = kp4[r * (RS / 4) + n4];
-              const float4 kc = kc4[r * (RS / 4) + n4];
-              ux += cp[r] * kp.x + cc[r] * kc.x;
-              uy += cp[r] * kp.y + cc[r] * kc.y;
-              uz += cp[r] * kp.z + cc[r] * kc.z;
-              uw += cp[r] * kp.w + cc[r] * kc.w;
-            }
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            const float4 kp = kp4[r * (RS / 4) + n4];
+            const float4 kc = kc4[r * (RS / 4) + n4];
+            ux += cp[r] * kp.x + cc[r] * kc.x;
+            uy += cp[r] * kp.y + cc[r] * kc.y;
+            uz += cp[r] * kp.z + cc[r] * kc.z;
+            uw += cp[r] * kp.w + cc[r] * kc.w;
           }
-          float* hh = hst + 4 * i;
-          hh[0] = dec * hh[0] + ux;
-          hh[1] = dec * hh[1] + uy;
-          hh[2] = dec * hh[2] + uz;
-          hh[3] = dec * hh[3] + uw;
+        }
+        float* hh = hst + 4 * i;
+        hh[0] = dec * hh[0] + ux;
+        hh[1] = dec * hh[1] + uy;
+        hh[2] = dec * hh[2] + uz;
+        hh[3] = dec * hh[3] + uw;
 #pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              const float4 qq = q4[r * (RS / 4) + n4];
-              const float part = (hh[0] * qq.x + hh[1] * qq.y) + (hh[2] * qq.z + hh[3] * qq.w);
-              if (i & 1)
-                acc2[r] += part;
-              else
-                acc[r] += part;
-            }
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < R) {
+            const float4 qq = q4[r * (RS / 4) + n4];
+            const float part = (hh[0] * qq.x + hh[1] * qq.y) + (hh[2] * qq.z + hh[3] * qq.w);
+            if (i & 1)
+              acc2[r] += part;
+            else
+              acc[r] += part;
           }
         }
       }
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         acc[r] += acc2[r];
-#pragma unroll
-        for (int o = 1; o < LPR; o <<= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-        if (r < R && j == 0 && row_ok) sy[(t * R + r) * PT + pi] = acc[r] + dskip * xr[r];
         xprev[r] = xr[r];
+      }
+    };
+    if constexpr (RMAX <= LPR) {
+      // Batches of TB = LPR / RMAX tokens: each lane keeps its partial readouts
+      // of the batch (value u * RMAX + r for token tb + u, rank r); the LPR
+      // lanes of the row then reduce them together by recursive halving
+      // (LPR - 1 shuffles per batch instead of log2(LPR) per token and rank),
+      // leaving lane j with value j.
+      constexpr int TB = LPR / RMAX;
+      for (int tb = 0; tb < tv; tb += TB) {
+        float part[LPR];
+#pragma unroll
+        for (int u = 0; u < TB; ++u) {
+          float acc[RMAX];
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+          if (tb + u < tv) token_step(tb + u, acc);
+#pragma unroll
+          for (int r = 0; r < RMAX; ++r) part[u * RMAX + r] = acc[r];
+        }
+#pragma unroll
+        for (int o = LPR / 2; o >= 1; o >>= 1) {
+          const bool upper = (j & o) != 0;  // this lane keeps the upper half
+#pragma unroll
+          for (int k = 0; k < o; ++k) {
+            const float send = upper ? part[k] : part[k + o];
+            const float keep = upper ? part[k + o] : part[k];
+            part[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        const int r = j % RMAX, t = tb + j / RMAX;
+        float mxr = 0.f;
+#pragma unroll
+        for (int k = 0; k < RMAX; ++k)
+          if (k == r) mxr = mx[k];
+        if (row_ok && t < tv && r < R)
+          sy[(t * R + r) * PT + pi] = part[0] + dskip * (sx[t * PT + pi] * mxr);
+      }
+    } else {
+      for (int t = 0; t < tv; ++t) {
+        float acc[RMAX];
+        token_step(t, acc);
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+#pragma unroll
+          for (int o = 1; o < LPR; o <<= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+          if (r < R && j == 0 && row_ok) sy[(t * R + r) * PT + pi] = acc[r] + dskip * xprev[r];
+        }
       }
     }
     __syncthreads();
