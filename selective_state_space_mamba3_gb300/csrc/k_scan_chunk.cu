@@ -91,7 +91,7 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
     off += (floats + 31) / 32 * 32;  // 128-byte aligned regions
     return o;
   };
-  // Q region: q tile [64][Npad]; without cp.async staging each warp's 8-row
+  // Q region: q tile [64][Npad]; without TMA staging each warp's 8-row
   // block first holds that warp's rotary angles, and the MIMO norm staging
   // [Qt][MP] uses the region in the epilogue.
   l.q = take(async ? kRows * l.Npad : imax(kRows * l.Npad, Qt * l.MP));
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sAbsAdt = sTotAdt + kWarps;   // [8 warps] per-warp totals of |adt|
   float* sThBase = sm + lay.thbase;    // [2][64] cumulative angle before the chunk
   const int AS = A + 4;                // angle row stride of a warp's angle block
-  // this warp's angles [TPW][AS] (without cp.async staging: in its q rows)
+  // this warp's angles [TPW][AS] (without TMA staging: in its q rows)
   float* sTh = kAsync ? sm + lay.th + warp * TPW * AS : sQ + warp * 8 * Npad;
 
   if (tid == 0) {
