@@ -68,13 +68,18 @@ struct ChunkLayout {
   size_t bytes;
 };
 
-// Instances with compile-time N and A (N a multiple of 32, A <= 32 and a
+// Instances with compile-time N and A (N a multiple of 32, A <= 64 and a
 // multiple of 4) stage the C / B rows of a chunk by TMA: one 4-D box per
 // 32-column block lands in a 128-byte-swizzled K-major q / k tile, which the
-// threads then rotate in place; their rotary angles and MIMO norm staging live
-// in regions of their own.
+// threads then rotate in place. Each warp's rotary angles live in a region of
+// their own for A <= 32; for larger A, which would not fit beside the tiles,
+// in the warp's private part of the transposed key tile (rows 8w .. 8w + 7 of
+// every 8-dim group: 64 contiguous floats per group), which is free from the
+// previous state update until the warp writes its own keys. The MIMO norm
+// staging has a region of its own.
 __host__ __device__ constexpr bool chunk_async(int KN, int KA) {
-  return KN > 0 && KA > 0 && KA <= 32 && KN % 32 == 0 && KA % 4 == 0;
+  return KN > 0 && KA > 0 && KA <= 64 && KN % 32 == 0 && KA % 4 == 0 &&
+         8 * (KA + 4) <= 64 * (KN / 8);  // a warp's angles fit its key-tile part
 }
 constexpr int kTmaThread = 64;  // issues the TMA copies (warp 2, lane 0)
 
@@ -108,7 +113,8 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
   l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
   l.tok = take(6 * kTok);                   // cum, e^{cum + lgE}, gamma, w, e^cum, e^-cum w
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
-  l.th = async ? take(kWarps * (8 / R) * (A + 4)) : 0;  // per-warp angles [TPW][A + 4]
+  // per-warp angles [TPW][A + 4] (TMA staging with A <= 32)
+  l.th = (async && A <= 32) ? take(kWarps * (8 / R) * (A + 4)) : 0;
   l.o = (async && mimo) ? take(Qt * l.MP) : 0;          // MIMO norm staging
   l.p = split ? take(kRows * kRows) : 0;                 // masked scores (split)
   l.bytes = (size_t)off * sizeof(float);
@@ -246,8 +252,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* sAbsAdt = sTotAdt + kWarps;   // [8 warps] per-warp totals of |adt|
   float* sThBase = sm + lay.thbase;    // [2][64] cumulative angle before the chunk
   const int AS = A + 4;                // angle row stride of a warp's angle block
-  // this warp's angles [TPW][AS] (without TMA staging: in its q rows)
+  // this warp's angles [TPW][AS]: element k at thp(k) (TMA staging: in their
+  // own region for A <= 32, else in the warp's part of the transposed key
+  // tile; without TMA staging: in the warp's q rows)
+  constexpr bool kThInKt = kAsync && KA > 32;
   float* sTh = kAsync ? sm + lay.th + warp * TPW * AS : sQ + warp * 8 * Npad;
+  auto thp = [&](int k) -> float* {
+    return kThInKt ? sKt + (((k >> 6) * 16 + 2 * warp) << 5) + (k & 63) : sTh + k;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < 6; ++i) tc::bar_init(&bars[i], 1);
@@ -471,6 +483,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         tEb[tw] = expf(-cum) * wt;
       }
     }
+    // the previous chunk's state update must finish before its tiles are
+    // rewritten and before the next Yo reads G (here already when the angles
+    // go into the transposed key tile)
+    if (kThInKt && it > 0) {
+      if (!tc::bar_wait(&bars[3], (it - 1) & 1, kWaitBudget)) abort_flag = 1;
+      tc::fence_after();
+    }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int aa = lane + 32 * j;
@@ -479,14 +498,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int w = 0; w < warp; ++w) base += sTot[w * kAngMax + aa];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (i < TPW) sTh[i * AS + aa] = base + thl[j][i];
+          if (i < TPW) *thp(i * AS + aa) = base + thl[j][i];
         if (warp == kWarps - 1) thb_next[aa] = base + thl[j][TPW - 1];
       }
     }
     __syncwarp();
-    // the previous chunk's state update must finish before its tiles are
-    // rewritten (and before the next Yo reads G)
-    if (it > 0) {
+    if (!kThInKt && it > 0) {
       if (!tc::bar_wait(&bars[3], (it - 1) & 1, kWaitBudget)) abort_flag = 1;
       tc::fence_after();
     }
@@ -563,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           const int j = 4 * jb + jl;
-          th4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(sTh + ti * AS + 4 * j)
+          th4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(thp(ti * AS + 4 * j))
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncwarp();
@@ -632,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int ub = 0; ub < 16; ++ub) {
           const int u = 4 * ub + jl;
-          thr[ub] = u < A ? sTh[ti * AS + u] : 0.f;
+          thr[ub] = u < A ? *thp(ti * AS + u) : 0.f;
         }
         __syncwarp();
         for (int ub = 0; ub < U4; ++ub) {
