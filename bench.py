@@ -371,19 +371,25 @@ def time_events(torch, fn, reps):
     return ev[0].elapsed_time(ev[1]) / reps
 
 
-def parts_mimo(torch, m3, mode, peak):
-    """Supplementary: MIMO R4 forward at B4 L4096 H32 P64 N64 (device inputs).
-    The workload's stated mode is FP32-exact; TF32 is reported beside it."""
-    w = gen.MIMO_R4
+def parts_scan(torch, m3, w, mode, peak):
+    """Supplementary: one forward of workload w (device inputs): the MIMO R4
+    forward at B4 L4096 H32 P64 N64, the long-context SISO forward at B2
+    L16384 H32 G4 P64 N128 A64. Both workloads are stated FP32-exact; TF32 is
+    reported beside it."""
+    mimo = w.mimo_rank > 1
     ins = gen.scan_inputs(w)
     d = {k: torch.from_numpy(v).cuda() for k, v in ins.items()}
     del ins
     cfg = m3.ssm_config(w.cfg(), mode)
-    ws = torch.empty(max(m3.m3_mimo_forward_workspace(cfg), 16), dtype=torch.uint8, device="cuda")
+    nws = m3.m3_mimo_forward_workspace(cfg) if mimo else m3.m3_siso_forward_workspace(cfg)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
     out = torch.empty_like(d["x"])
-    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d",
-            "mimo_x", "mimo_z", "mimo_o", "norm_weight")
-    fn = lambda: m3.m3_mimo_forward(cfg, *[d[k] for k in keys], out, ws)
+    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d")
+    if mimo:
+        keys += ("mimo_x", "mimo_z", "mimo_o", "norm_weight")
+        fn = lambda: m3.m3_mimo_forward(cfg, *[d[k] for k in keys], out, ws)
+    else:
+        fn = lambda: m3.m3_siso_forward(cfg, *[d[k] for k in keys], out, ws)
     for _ in range(3):
         fn()
     ms = time_events(torch, fn, 10)
@@ -538,10 +544,10 @@ def run_m3(args):
     del s
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_parts:
-        parts["mimo_scan_fp32"] = parts_mimo(torch, m3, m3.M3_MATH_FP32, peak)
-        torch.cuda.empty_cache()
-        parts["mimo_scan_tf32"] = parts_mimo(torch, m3, m3.M3_MATH_TF32, peak)
-        torch.cuda.empty_cache()
+        for key, wl in (("mimo_scan", gen.MIMO_R4), ("siso_long_scan", gen.SISO_LONG)):
+            for mname, mcode in (("fp32", m3.M3_MATH_FP32), ("tf32", m3.M3_MATH_TF32)):
+                parts[f"{key}_{mname}"] = parts_scan(torch, m3, wl, mcode, peak)
+                torch.cuda.empty_cache()
         parts["siso_step"] = parts_step(torch, m3, peak)
 
     cpu = None

@@ -6,7 +6,7 @@
 // PT state rows; LPR lanes share a row, each holding 4 * NPT4 state values in
 // registers (float4-interleaved so that shared-memory reads are broadcasts),
 // and the row's readout is a shuffle reduction over those lanes.
-// Per tile of kT tokens (16, or 32 for blocks that own a whole sequence) the
+// Per tile of kT tokens (16, 32 or 64: the longest that fits) the
 // block stages the coefficients, the cumulative rotary angle, the rotated q/k
 // rows and x/z in shared memory, runs the recurrence over the tile, then
 // writes the gated outputs coalesced. MIMO blocks own all P rows so that the
@@ -429,9 +429,22 @@ __global__ void __launch_bounds__(512, RMAX == 1 ? 2 : 1) k_scan_seq(ScanGeom g,
   }
 }
 
+int device_sm_count() {
+  static const int n = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 152;
+    return v;
+  }();
+  return n;
+}
+
 // State rows per block: all P rows (one block per (b, h): the MIMO output norm
 // and the step state need it, and it stages each (b, h)'s q / k once) while
 // 8 lanes per row keep the block within 512 threads; otherwise 32-row tiles.
+// (Splitting the rows of a few long sequences over more blocks does not help:
+// a block's time is its token loop's latency, not its share of the SM.)
 int seq_rows_per_block(const ScanGeom& g, const ScanArgs& a, const StepState& st, int rmax) {
   if (rmax > 1 || a.mimo_o || st.ssm || g.P * 8 <= 512) return g.P;
   return g.P < 32 ? g.P : 32;
@@ -444,12 +457,21 @@ cudaError_t launch_seq_t(const ScanGeom& g, const ScanArgs& a, const StepState& 
   // (the per-(b, h) key / angle state is read first and written last)
   const int PT = seq_rows_per_block(g, a, st, RMAX);
   constexpr int RS = 4 * NPT4 * LPR;
-  // 16-token staging tiles; 32 for blocks that own a whole (b, h) (one such
-  // block per SM anyway) when they fit in 200 KB of shared memory
+  // Staging tiles as long as they fit (the per-tile staging is a chain of
+  // dependent loads and block barriers, so longer tiles amortise it): 64
+  // tokens in 200 KB when the grid has no more blocks than SMs; 32 tokens in
+  // 200 KB for the one-block-per-SM instances (RMAX > 1, MIMO, step state) or
+  // in 100 KB (two blocks per SM) otherwise; else 16 tokens.
   SeqLayout lay = seq_layout(g.N, PT, g.R, g.A, 16, RS);
-  if (PT == g.P && (RMAX > 1 || a.mimo_o || st.ssm)) {
-    const SeqLayout big = seq_layout(g.N, PT, g.R, g.A, 32, RS);
-    if (big.bytes <= 200 * 1024) lay = big;
+  {
+    const bool one_per_sm = RMAX > 1 || a.mimo_o || st.ssm;
+    const int64_t blocks = (int64_t)g.B * g.H * ((g.P + PT - 1) / PT);
+    const SeqLayout mid = seq_layout(g.N, PT, g.R, g.A, 32, RS);
+    const SeqLayout big = seq_layout(g.N, PT, g.R, g.A, 64, RS);
+    if (blocks <= device_sm_count() && big.bytes <= 200u * 1024u)
+      lay = big;
+    else if (mid.bytes <= (one_per_sm ? 200u : 100u) * 1024u)
+      lay = mid;
   }
   const int threads = ((PT * LPR + 31) / 32) * 32;
   const int ptiles = (g.P + PT - 1) / PT;
