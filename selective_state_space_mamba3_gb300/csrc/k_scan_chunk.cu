@@ -25,19 +25,21 @@
 // contraction over its R rows) and, through shared memory, the MIMO output
 // RMS norm. Every operand is rounded to TF32 (round to nearest).
 //
-// One CTA of 256 threads runs one (b, h) sequence chunk after chunk; thread 0
-// issues the MMAs, and threads wait on mbarriers signalled by tcgen05.commit.
-// Staging is warp-local: warp w owns rows 8w .. 8w + 7 of the chunk (its
-// tokens' scalars, rotary angles and the q / k / w-scaled transposed key
-// tiles), so only three block barriers remain per chunk (after the per-warp
-// totals, before the first and before the second MMA batch). The state update
-// of a chunk runs on under its epilogue and the next chunk's scalar work.
-// The C / B rows of a chunk arrive by TMA (one issuing thread, 4-D boxes into
-// 128-byte-swizzled tiles) a chunk ahead of their use.
+// One CTA of 256 threads runs one (b, h) sequence chunk after chunk; threads 0
+// and 32 issue the MMAs (one independent chain each), and threads wait on
+// mbarriers signalled by tcgen05.commit. Staging is warp-local: warp w owns
+// rows 8w .. 8w + 7 of the chunk (its tokens' scalars, rotary angles and the
+// q / k / w-scaled transposed key tiles), so three block barriers precede the
+// epilogue (after the per-warp totals, before the first and before the second
+// MMA batch); the staged SISO epilogue adds two (its output rows, and before
+// the next chunk's B rows reuse the region). The state update of a chunk runs
+// on under its epilogue and the next chunk's scalar work. The C / B rows of a
+// chunk arrive by TMA (one issuing thread, 4-D boxes into 128-byte-swizzled
+// tiles) a chunk ahead of their use.
 // Waits are bounded: on timeout the kernel records a status word and exits.
-// Shared memory (about 114 KB for P <= 64, N = 128) and TMEM (256 columns)
-// admit two CTAs per SM, and the next chunk's other inputs are prefetched into
-// L2 while the current chunk runs.
+// Shared memory (at most about 114 KB for P <= 64, N = 128) and TMEM (256
+// columns) admit two CTAs per SM, and the next chunk's other inputs are
+// prefetched into L2 while the current chunk runs.
 //
 // The kernel is a template over the shape: the generic instance reads N, A, R
 // and P at run time; instances for common shapes have them as constants.
@@ -733,10 +735,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc::mma_ts(tYo, tG + ks * 8, dQ + qk_step(ks), id_Y, ks > 0);
       tc::commit(&bars[1]);
     }
-    // (6) masked scores P = M o S (S rows: TMEM M = 64 layout, lanes 0..15 of
-    // each quadrant; lane l + 16 takes the upper 8 columns of each 16-column
-    // block of row l) and values X^T, both into the K region once S is done;
-    // then G *= e^{cum_end} once Yo has read G. The value loads are issued
+    // (6) masked scores P = M o S + D I (S rows: TMEM M = 64 layout, lanes
+    // 0..15 of each quadrant; lane l + 16 takes the upper 8 columns of each
+    // 16-column block of row l) and values X^T, both into the K region (or
+    // their own regions) once S is done; then, in a chunk that is not lazy,
+    // G~ *= e^{lgE + cum_end} once Yo has read G~. The value loads are issued
     // first so that their latency overlaps the wait.
     {
       constexpr int kXr = (kRows / 4 + kWarps - 1) / kWarps;  // row blocks per warp
@@ -902,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();  // B3: scores, values and the rescaled state complete
     tc::fence_after();
     if (abort_flag) break;
-    // (7) Yi^T = X^T P^T and G += X^T (w K)
+    // (7) Yi^T = X^T P^T and G~ += X^T (w e^{-lgE} K)
     // (Yi and the state update come from threads of different warps)
     if (!SUMMARY && tid == 0) {
 #pragma unroll
