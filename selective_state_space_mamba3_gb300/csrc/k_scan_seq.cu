@@ -5,7 +5,8 @@
 // q, k, decay and trapezoid weights, so a block owns one (b, h) and a tile of
 // PT state rows; LPR lanes share a row, each holding 4 * NPT4 state values in
 // registers (float4-interleaved so that shared-memory reads are broadcasts),
-// and the row's readout is a shuffle reduction over those lanes.
+// and the row's readouts are reduced across those lanes by shuffles, once per
+// batch of LPR / RMAX tokens (recursive halving) where the ranks allow it.
 // Per tile of kT tokens (16, 32 or 64: the longest that fits) the
 // block stages the coefficients, the cumulative rotary angle, the rotated q/k
 // rows and x/z in shared memory, runs the recurrence over the tile, then
