@@ -107,10 +107,16 @@ def tiny_chain():
 
 @pytest.mark.parametrize("mode", [FP32, TF32])
 def test_tiny_chain(mode):
+    """Tiny workload, preprocess chained into the scan on both sides; the GPU
+    output is also held to the frozen oracle output in tests/golden."""
+    import os
     w, gins, oins = tiny_chain()
     got = gpu_scan(w.cfg(), gins, mode)
     ref = oracle_scan(w.cfg(), oins)
     check_close(got, ref, TOL[mode])
+    golden = np.loadtxt(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                     "tiny_siso_chain.txt")).reshape(got.shape)
+    check_close(got, golden, TOL[mode], label="golden")
 
 
 EDGE = [

@@ -287,3 +287,22 @@ def test_preprocess_softplus_overflow_safe():
     out = oracle.preprocess(proj, np.zeros((1,), np.float32), **kw)
     assert out["dt"][0, 0] == 80.0 and out["dt"][1, 0] == float(np.float32(1e30))
     assert np.all(np.isfinite(out["adt"]))
+
+
+# --- regression fixture: the tiny workload's chained output (tests/golden) ---
+
+def test_tiny_golden_fixture():
+    """The oracle still reproduces tests/golden/tiny_siso_chain.txt, its own
+    output for the tiny SISO workload (preprocess chained into the scan),
+    frozen by tests/golden/make_golden.py: a change to the oracle's arithmetic
+    shows up here and must be justified before the fixture is rewritten."""
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "make_golden.py")
+    spec = importlib.util.spec_from_file_location("make_golden", path)
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    ref = np.loadtxt(mg.FIXTURE)
+    got = np.asarray(mg.tiny_chain_output(), np.float64).ravel()
+    assert ref.shape == got.shape == (2048,)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
