@@ -241,6 +241,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   // [MP][64 rows] values (after S)
   float* sXt = (kAsync && SUMMARY) ? sQ : sK + (kSplitK ? kRows * Npad : kRows * kRows);
   float* sKt = sm + lay.kt;            // [Npad][64 rows] K-major, K = row (w-scaled keys)
+  // Staged SISO epilogue with TMA staging and no early B copy: the output rows
+  // are staged in the transposed key tile, free once the chunk's state update
+  // has read it, so the next chunk's B rows can be copied into the K region as
+  // soon as Yi and the state update are done (start of the epilogue).
+  constexpr bool kStagedEpi = !MIMO && !SUMMARY && KP > 0 && KP % 4 == 0 && KP <= 64;
+  constexpr bool kBAtEpi = kAsync && !kEarlyB && kStagedEpi;
+  float* sStage = kBAtEpi ? sKt : sP;  // [t][P] pre-gate output rows
   float* sTot = sm + lay.tot;          // [8 warps][64]   per-warp angle totals
   float* sTotAdt = sTot + kWarps * kAngMax;  // [8 warps] per-warp log-decay totals
   float* sBiasC = sm + lay.bias;       // [R][Npad]
@@ -982,6 +989,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       // the epilogue needs Yo and Yi; the state update runs on under it
       if (!tc::bar_wait(&bars[2], it & 1, kWaitBudget)) abort_flag = 1;
       tc::fence_after();
+      if (kBAtEpi) {
+        // the staging area (the transposed key tile) is free once the state
+        // update is done; the K region is then free for the next B rows
+        const bool st_done = tc::bar_wait(&bars[3], it & 1, kWaitBudget);
+        if (!st_done) abort_flag = 1;
+        tc::fence_after();
+        if (st_done && c0 + Qt < l1 && tid == kTmaThread) {
+          issue_rows(&tmB, sK, c0 + Qt, &bars[5]);
+          pendB = it + 1;
+        }
+      }
       // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
       // two lanes of a row split each 16-column block into 8 + 8 columns.
       {
@@ -1018,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (kStaged) {
-                sP[t * KP + prow] = fmaf(ec[j], yo[j], yi[j]);
+                sStage[t * KP + prow] = fmaf(ec[j], yo[j], yi[j]);
               } else if (t < tv) {
                 const float zv = u ? ze[1][j] : ze[0][j];
                 float y = fmaf(ec[j], yo[j], yi[j]);
@@ -1058,7 +1076,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int unit = tid + kThreads * k;
           const int t = unit / kRowQ, p0 = 4 * (unit % kRowQ);
           if (t < tv) {
-            float4 y = *reinterpret_cast<const float4*>(sP + t * KP + p0);
+            float4 y = *reinterpret_cast<const float4*>(sStage + t * KP + p0);
             if (g.has_z) {
               y.x *= silu_fast(zq[k].x);
               y.y *= silu_fast(zq[k].y);
@@ -1085,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // once the state update has read the K region and every thread is done with
     // its scores, values and staged outputs: stage the next chunk's B rows
     // (the generic-proxy writes of the region are ordered before the TMA's)
-    if (kAsync && !kEarlyB && c0 + Qt < l1) {
+    if (kAsync && !kEarlyB && !kBAtEpi && c0 + Qt < l1) {
       if (!SUMMARY) {
         tc::fence_async_smem();
         __syncthreads();
