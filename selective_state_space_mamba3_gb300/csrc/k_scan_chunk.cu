@@ -976,6 +976,22 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
+      // MIMO instances with compile-time R: the z values of this lane's tokens
+      // (kTpb per 16-column block), loaded before the waits as well
+      constexpr int kTpb = (MIMO && KR > 0) ? kCols / KR : 0;
+      float zm[2][kTpb > 0 ? kTpb : 1];
+      if (kTpb > 0) {
+        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int col0 = (2 * wg + u) * 16 + 8 * half;
+#pragma unroll
+          for (int tt = 0; tt < (kTpb > 0 ? kTpb : 1); ++tt) {
+            const int t = (col0 >> lgR) + tt;
+            zm[u][tt] = (pvalid && t < tv && g.has_z) ? zcol[t * HP] : 0.f;
+          }
+        }
+      }
       // a lazy chunk waits for Yo only here; the q tile is then free for the
       // next chunk's C rows
       if (lazy) {
@@ -1005,6 +1021,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       {
         const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
         float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
+#pragma unroll
         for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
           float yo[16], yi[16];
           tc::tmem_ld16x2(tYo + lane_base + cb * 16, tS + lane_base + cb * 16, yo, yi);
@@ -1046,10 +1063,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           } else {
             const int tpb = kCols >> lgR;  // whole tokens in this lane's columns
+#pragma unroll
             for (int tt = 0; tt < tpb; ++tt) {
               const int t = (col0 >> lgR) + tt;
               if (t >= tv) break;
-              const float zv = g.has_z ? zcol[t * HP] : 0.f;
+              float zv;
+              if constexpr (kTpb > 0)
+                zv = zm[cb - 2 * wg][tt];
+              else
+                zv = g.has_z ? zcol[t * HP] : 0.f;
               const float ec = tEc[t];
               float o = 0.f;
 #pragma unroll
