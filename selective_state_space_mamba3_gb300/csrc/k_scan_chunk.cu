@@ -115,8 +115,9 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async) {
   l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
   l.tok = take(6 * kTok);                   // cum, e^{cum + lgE}, gamma, w, e^cum, e^-cum w
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
-  // per-warp angles [TPW][A + 4] (TMA staging with A <= 32)
-  l.th = (async && A <= 32) ? take(kWarps * (8 / R) * (A + 4)) : 0;
+  // per-warp angles [TPW][A + 4] (TMA staging with A <= 32); MIMO keeps their
+  // cosines and sines instead (two such blocks per warp)
+  l.th = (async && A <= 32) ? take(kWarps * (8 / R) * (A + 4) * (mimo && R > 1 ? 2 : 1)) : 0;
   l.o = (async && mimo) ? take(Qt * l.MP) : 0;          // MIMO norm staging
   l.p = split ? take(kRows * kRows) : 0;                 // masked scores (split)
   l.bytes = (size_t)off * sizeof(float);
@@ -265,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   // own region for A <= 32, else in the warp's part of the transposed key
   // tile; without TMA staging: in the warp's q rows)
   constexpr bool kThInKt = kAsync && KA > 32;
-  float* sTh = kAsync ? sm + lay.th + warp * TPW * AS : sQ + warp * 8 * Npad;
+  // MIMO with TMA staging: phase (2) stores cos and sin per (token, angle) once,
+  // instead of every one of a token's R rows computing them in phase (4)
+  constexpr bool kCosSin = MIMO && KR > 1 && kAsync && !kThInKt;
+  float* sTh = kAsync ? sm + lay.th + warp * TPW * AS * (kCosSin ? 2 : 1) : sQ + warp * 8 * Npad;
   auto thp = [&](int k) -> float* {
     return kThInKt ? sKt + (((k >> 6) * 16 + 2 * warp) << 5) + (k & 63) : sTh + k;
   };
@@ -507,7 +511,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int w = 0; w < warp; ++w) base += sTot[w * kAngMax + aa];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (i < TPW) *thp(i * AS + aa) = base + thl[j][i];
+          if (i < TPW) {
+            const float th = base + thl[j][i];
+            if constexpr (kCosSin) {
+              float sn, cs;
+              sincos_fast(th, &sn, &cs);
+              sTh[i * AS + aa] = cs;
+              sTh[TPW * AS + i * AS + aa] = sn;
+            } else {
+              *thp(i * AS + aa) = th;
+            }
+          }
         if (warp == kWarps - 1) thb_next[aa] = base + thl[j][TPW - 1];
       }
     }
@@ -529,7 +543,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float* bb = sBiasB + r * Npad;
       float* kl = last_chunk && t == tv - 1 ? io.k_last + ((int64_t)bh * R + r) * N : nullptr;
       // Rotary item: dims n0..n0+3 and their partners n0+A..n0+A+3.
-      auto pair_item = [&](int n0, float4 cu, float4 cw, float4 bu, float4 bw, float4 th) {
+      // th: the four angles (or, with kCosSin, their cosines; sv their sines)
+      auto pair_item = [&](int n0, float4 cu, float4 cw, float4 bu, float4 bw, float4 th,
+                           float4 sv) {
         float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0, k0 = q0, k1 = q0;
         if (in) {
           const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
@@ -539,7 +555,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 #define M3_ROT(E)                                                            \
   {                                                                          \
     float sn, cs;                                                            \
-    sincos_fast(th.E, &sn, &cs);                                             \
+    if constexpr (kCosSin) {                                                 \
+      cs = th.E;                                                             \
+      sn = sv.E;                                                             \
+    } else {                                                                 \
+      sincos_fast(th.E, &sn, &cs);                                           \
+    }                                                                        \
     const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
     const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
     q0.E = qu * cs - qw * sn;                                                \
@@ -585,12 +606,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
         // angles of this lane's rotary items, read before the q rows (which
         // share this warp's angle block) are written
-        float4 th4[4];
+        float4 th4[4], sn4[kCosSin ? 4 : 1];
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           const int j = 4 * jb + jl;
           th4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(thp(ti * AS + 4 * j))
                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (kCosSin)
+            sn4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(sTh + TPW * AS + ti * AS + 4 * j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncwarp();
         if (kAsync) {
@@ -607,16 +631,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (j < PQ) {
               const int n0 = 4 * j;
               float4 th;
+              float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
               switch (jb) {  // registers, not a local array
-                case 0: th = th4[0]; break;
-                case 1: th = th4[1]; break;
-                case 2: th = th4[2]; break;
-                default: th = th4[3]; break;
+                case 0: th = th4[0]; if constexpr (kCosSin) sv = sn4[0]; break;
+                case 1: th = th4[1]; if constexpr (kCosSin) sv = sn4[kCosSin ? 1 : 0]; break;
+                case 2: th = th4[2]; if constexpr (kCosSin) sv = sn4[kCosSin ? 2 : 0]; break;
+                default: th = th4[3]; if constexpr (kCosSin) sv = sn4[kCosSin ? 3 : 0]; break;
               }
               pair_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
                         *reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)),
                         *reinterpret_cast<const float4*>(sK + toff(rho, n0)),
-                        *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)), th);
+                        *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)), th, sv);
             } else {
               const int n0 = 2 * A + 4 * (j - PQ);
               single_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
@@ -641,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               pair_item(n0, in ? *reinterpret_cast<const float4*>(crow + n0) : z4,
                         in ? *reinterpret_cast<const float4*>(crow + n0 + A) : z4,
                         in ? *reinterpret_cast<const float4*>(brow + n0) : z4,
-                        in ? *reinterpret_cast<const float4*>(brow + n0 + A) : z4, th);
+                        in ? *reinterpret_cast<const float4*>(brow + n0 + A) : z4, th, z4);
             } else {
               const int n0 = 2 * A + 4 * (j - PQ);
               single_item(n0, in ? *reinterpret_cast<const float4*>(crow + n0) : z4,
