@@ -148,6 +148,23 @@ def test_step_equals_scan(R):
         assert np.array_equal(out[:, 0], full[:, t])
 
 
+@pytest.mark.parametrize("R", [1, 4])
+def test_split_scan_with_state_equals_whole(R):
+    """Scanning a sequence in two pieces, the second from the ssm / angle / k / v
+    state the first returns, reproduces the one-piece scan exactly (the
+    prefill -> prefill and prefill -> decode hand-off of the state API)."""
+    w, ins = small(B=2, L=20, H=2, G=1, P=4, N=6, A=2, R=R, norm=1 if R > 1 else 0)
+    full = run_scan(w, ins)
+    mimo = {k: ins[k] for k in MIMO_KEYS} if R > 1 else {}
+    state = oracle.zero_state(w.cfg(sequence_length=1))
+    outs = []
+    for t0, t1 in ((0, 7), (7, 20)):
+        part = [np.ascontiguousarray(ins[k][:, t0:t1]) for k in SCAN_KEYS[:8]]
+        outs.append(oracle.scan(w.cfg(sequence_length=t1 - t0), *part, ins["c_bias"],
+                                ins["b_bias"], ins["d"], state=state, **mimo))
+    assert np.array_equal(np.concatenate(outs, axis=1), full)
+
+
 # --- pin 6: rotation only enters through angle differences ------------------
 
 def test_angle_state_offset_invariance():
