@@ -42,7 +42,26 @@
 // prefetched into L2 while the current chunk runs.
 //
 // The kernel is a template over the shape: the generic instance reads N, A, R
-// and P at run time; instances for common shapes have them as constants.
+// and P at run time; instances for common shapes have them as constants. The
+// compile-time shape selects these variants (constexpr flags in the kernel):
+//   kAsync     C / B rows by TMA into swizzled tiles (N % 32 == 0, A <= 64,
+//              A % 4 == 0); otherwise 128-bit loads into unswizzled tiles.
+//   kSplitK    (kAsync, N <= 64) the scores get a region of their own, so the
+//              k tile is dead once S is done.
+//   kEarlyB    the next chunk's B rows are copied as soon as the k tile is
+//              dead: after the tile phase in the summary pass, after S with
+//              kSplitK.
+//   kBAtEpi    (kAsync SISO main pass without kEarlyB) the epilogue stages its
+//              rows in the transposed-key tile and the B copy starts with the
+//              epilogue; otherwise it follows a final block barrier.
+//   kThInKt    (kAsync, A > 32) the rotary angles live in each warp's part of
+//              the transposed-key tile; with kAsync and A <= 32 in their own
+//              region; without kAsync in the warp's q rows.
+//   kCosSin    (kAsync MIMO) the angle slots hold cos and sin per (token,
+//              angle), computed once instead of per rank row.
+//   kFactMask  (SISO) the factored decay mask for chunks with sum |adt| <= 85.
+//   kXVec, kStaged, kTpb: float4 value loads, staged float4 epilogue (SISO),
+//              z preloaded before the epilogue waits (MIMO).
 #include <cuda.h>
 #include <string.h>
 #include <cudaTypedefs.h>
