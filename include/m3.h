@@ -39,7 +39,10 @@ enum m3_status {
   M3_ERR_UNALIGNED = 2,        /* a base pointer is not 16-byte aligned */
   M3_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
   M3_ERR_CUDA = 4,             /* a CUDA launch or runtime call failed */
-  M3_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up */
+  M3_ERR_TIMEOUT = 5,          /* a bounded device-side wait gave up */
+  M3_ERR_DEVICE_STATE = 6      /* a bounded wait gave up and copies still in
+                                  flight did not drain either: the CUDA
+                                  context must be treated as unusable */
 };
 
 /* Arithmetic of the scans' dense contractions (an extension of SsmConfig). */
@@ -186,16 +189,24 @@ int m3_mimo_prefill(const m3_ssm_config* cfg, const float* c, const float* b, co
  * scan needs comes from a fixed 1 MiB array in the library's device image
  * (held by every GPU that loads the library until the process exits); this
  * call allocates nothing. Geometries whose m3_siso_forward_workspace() size
- * exceeds 1 MiB are rejected with M3_ERR_WORKSPACE. The first call on a device
- * looks up the array's device address with cudaGetSymbolAddress (with that
- * device current); make that first call before any stream capture. All calls
- * on a device share the array: calls that overlap on the GPU race and must not
- * be issued; each call clears what must start at zero.
+ * exceeds 1 MiB are rejected with M3_ERR_WORKSPACE. Every call looks up the
+ * array's device address in the current CUDA context (cudaGetSymbolAddress, a
+ * host-side query), so hosts that run their own context get the address valid
+ * there; the first call on a device may load the library's device code, so
+ * make it before any stream capture. All calls on a device share the array
+ * and it keeps the last call's contents: calls that overlap on the GPU race
+ * and must not be issued; each call clears what must start at zero.
+ *
+ * m3_siso_forward_static_status - waits for `stream`, then reads the status
+ * word that the bounded device-side waits of the last m3_siso_forward_static
+ * call on the current device wrote into the array: M3_OK, M3_ERR_TIMEOUT or
+ * M3_ERR_DEVICE_STATE (as m3_workspace_status for a caller workspace).
  */
 int m3_siso_forward_static(const m3_ssm_config* cfg, const float* c, const float* b,
                            const float* x, const float* z, const float* adt, const float* dt,
                            const float* trap, const float* angle, const float* c_bias,
                            const float* b_bias, const float* d, float* out, m3_stream_t stream);
+int m3_siso_forward_static_status(m3_stream_t stream);
 
 /*
  * m3_siso_step - advance one SISO token and update four recurrent states in
@@ -232,8 +243,11 @@ int m3_mimo_step(const m3_ssm_config* cfg, const float* c, const float* b, const
 
 /*
  * m3_workspace_status - waits for `stream`, then reads the device status word
- * that the scans' bounded waits write into `workspace`: M3_OK, or
- * M3_ERR_TIMEOUT if a wait gave up during the last call that used it.
+ * that the scans' bounded waits write into `workspace`: M3_OK, M3_ERR_TIMEOUT
+ * if a wait gave up during the last call that used it, or M3_ERR_DEVICE_STATE
+ * if, after that, the kernel's bounded wait for its own copies still in flight
+ * gave up as well (the kernel then exits with those copies unfinished, and the
+ * context is in an undefined state).
  */
 int m3_workspace_status(const void* workspace, size_t workspace_bytes, m3_stream_t stream);
 

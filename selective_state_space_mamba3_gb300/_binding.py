@@ -21,11 +21,12 @@ M3_ERR_UNALIGNED = 2
 M3_ERR_WORKSPACE = 3
 M3_ERR_CUDA = 4
 M3_ERR_TIMEOUT = 5
+M3_ERR_DEVICE_STATE = 6
 M3_MATH_FP32 = 0
 M3_MATH_TF32 = 1
 
 EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
-            "m3_siso_forward_static", "m3_siso_prefill_workspace", "m3_siso_prefill",
+            "m3_siso_forward_static", "m3_siso_forward_static_status", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
@@ -92,6 +93,7 @@ def load_library():
         lib.m3_siso_forward.argtypes = [cfgp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_forward.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
         lib.m3_siso_forward_static.argtypes = [cfgp] + [_vp] * 12 + [_vp]
+        lib.m3_siso_forward_static_status.argtypes = [_vp]
         lib.m3_siso_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_mimo_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_prefill.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
@@ -184,6 +186,12 @@ def m3_siso_forward_static(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_b
     _check(load_library().m3_siso_forward_static(ctypes.byref(cfg), *[_ptr(t) for t in (
         c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, out)], _stream(stream)),
         "m3_siso_forward_static")
+
+
+def m3_siso_forward_static_status(stream=None) -> int:
+    """Status word of the last m3_siso_forward_static call on the current
+    device (waits for the stream): M3_OK, M3_ERR_TIMEOUT or M3_ERR_DEVICE_STATE."""
+    return int(load_library().m3_siso_forward_static_status(_stream(stream)))
 
 
 def m3_siso_prefill_workspace(cfg: SsmConfig) -> int:
