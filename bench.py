@@ -544,6 +544,8 @@ def run_m3(args):
     del s
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_parts:
+        parts["siso_scan_fp32"] = parts_scan(torch, m3, gen.SISO_1B, m3.M3_MATH_FP32, peak)
+        torch.cuda.empty_cache()
         for key, wl in (("mimo_scan", gen.MIMO_R4), ("siso_long_scan", gen.SISO_LONG)):
             for mname, mcode in (("fp32", m3.M3_MATH_FP32), ("tf32", m3.M3_MATH_TF32)):
                 parts[f"{key}_{mname}"] = parts_scan(torch, m3, wl, mcode, peak)
@@ -606,6 +608,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def relaunch_under_torchrun(n):
+    """`--gpus N` with N > 1 outside torchrun: run this same command as N
+    ranks under torch.distributed.run (one process per GPU) and return its
+    exit status, so that the job never silently runs on one rank."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -617,6 +633,11 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=8)
     args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        sys.exit(relaunch_under_torchrun(args.gpus))
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {world}")
     if args.warmup < 3 and args.impl == "m3":
         args.warmup = 3
     if args.impl == "reference":

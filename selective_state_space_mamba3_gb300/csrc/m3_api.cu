@@ -62,6 +62,7 @@ int resolve_ssm(const m3_ssm_config* cfg, bool mimo, ScanGeom* g) {
   g->has_z = cfg->has_z != 0; g->has_d = cfg->has_d != 0;
   g->has_norm = mimo && cfg->has_output_norm != 0;
   g->math_mode = cfg->math_mode;
+  g->mimo = mimo ? 1 : 0;
   return M3_OK;
 }
 
@@ -81,11 +82,22 @@ int check_angle_ptr(const void* p, int A) {
 
 }  // namespace
 
-// Scan dispatch. TF32 mode runs the tcgen05 chunked kernel where its tiles
-// apply (R in {1,2,4,8}, P, N <= 128); FP32-exact mode and every other shape
-// run the token-sequential FP32 kernel on the CUDA cores.
+// Scan dispatch. The tcgen05 chunked kernel takes R in {1,2,4,8}, P, N <= 128:
+//  - TF32 mode: single-pass TF32 operands, except the MIMO output norm, which
+//    takes the split-operand (3xTF32) flavour. The norm rescales every token to
+//    unit size, so a token's own relative error becomes the normwise error, and
+//    single-pass TF32 rounding reaches a few 1e-3 on some tokens.
+//  - FP32-exact mode: the split-operand flavour where its doubled tiles fit in
+//    shared memory.
+// Every other shape, and FP32-exact shapes the split tiles do not fit, run the
+// token-sequential FP32 kernel on the CUDA cores.
+static bool chunk_split_mode(const ScanGeom& g) {
+  return g.math_mode == M3_MATH_FP32 || g.has_norm;
+}
 static bool use_chunk(const ScanGeom& g) {
-  return g.math_mode == M3_MATH_TF32 && chunk_supported(g);
+  if (!chunk_supported(g)) return false;
+  if (chunk_split_mode(g)) return chunk_split_supported(g);
+  return g.math_mode == M3_MATH_TF32;
 }
 
 // SMs of the current device (152 on GB300; also the answer when no device can
@@ -100,12 +112,13 @@ static int sm_count() {
   return n;
 }
 
-// Sequences per launch below two per SM are split into segments of whole
-// chunks, at least four chunks long: a summary pass, a prefix over segments
-// and the main pass then replace one long serial chain.
+// Sequences per launch below the CTAs the SMs hold at once (two per SM for
+// single-pass TF32, one for the split flavour) are split into segments of
+// whole chunks, at least four chunks long: a summary pass, a prefix over
+// segments and the main pass then replace one long serial chain.
 static int choose_nseg(const ScanGeom& g) {
   const int64_t bh = (int64_t)g.B * g.H;
-  const int64_t target = 2 * (int64_t)sm_count();
+  const int64_t target = (chunk_split_mode(g) ? 1 : 2) * (int64_t)sm_count();
   if (bh >= target) return 1;
   const int64_t qt = chunk_rows_per_token(g);
   const int64_t max_seg = g.L / (4 * qt);
@@ -156,6 +169,7 @@ size_t scan_workspace_bytes(const ScanGeom& g, bool with_state) {
 cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
                         size_t, cudaStream_t s) {
   if (!use_chunk(g)) return launch_scan_seq(g, a, st ? *st : StepState{}, s);
+  const bool split = chunk_split_mode(g);
   const ChunkWs w = chunk_ws(g, st != nullptr);
   char* base = static_cast<char*>(ws);
   auto f = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
@@ -180,7 +194,7 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
       io.g0 = f(w.g0);
       io.th0 = f(w.th0);
     }
-    return launch_scan_chunk(g, a, status, io, false, s);
+    return launch_scan_chunk(g, a, status, io, false, split, s);
   }
   ChunkIO sum{};
   sum.seg_len = w.seg_len;
@@ -188,14 +202,14 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
   sum.g1 = f(w.gsum);
   sum.th1 = f(w.thsum);
   sum.e1 = f(w.esum);
-  e = launch_scan_chunk(g, a, status, sum, true, s);
+  e = launch_scan_chunk(g, a, status, sum, true, split, s);
   if (e != cudaSuccess) return e;
   e = launch_state_prefix(g, w.nseg, st ? f(w.g0) : nullptr, st ? f(w.th0) : nullptr, f(w.gsum),
                           f(w.thsum), f(w.esum), f(w.gentry), f(w.thentry), s);
   if (e != cudaSuccess) return e;
   io.g0 = f(w.gentry);
   io.th0 = f(w.thentry);
-  return launch_scan_chunk(g, a, status, io, false, s);
+  return launch_scan_chunk(g, a, status, io, false, split, s);
 }
 
 }  // namespace m3
@@ -212,6 +226,8 @@ const char* m3_status_string(int status) {
     case M3_ERR_WORKSPACE: return "workspace missing or smaller than required";
     case M3_ERR_CUDA: return "a CUDA launch or runtime call failed";
     case M3_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case M3_ERR_DEVICE_STATE:
+      return "a bounded device-side wait gave up and in-flight copies did not drain: context unusable";
     default: return "unknown status";
   }
 }
@@ -221,6 +237,7 @@ uint64_t m3_launch_count(void) { return g_launches.load(std::memory_order_relaxe
 int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
                   const float* dt_bias, float* x, float* z, float* bh, float* ch, float* dt,
                   float* adt, float* trap, float* angle, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_preprocess");
   if (!cfg) return M3_ERR_INVALID_ARGUMENT;
   const int64_t I = cfg->inner_size, N = cfg->state_size, H = cfg->num_heads;
   const int64_t A = cfg->num_rope_angles, G = cfg->num_groups, R = cfg->mimo_rank;
@@ -294,6 +311,7 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* angle, const float* c_bias, const float* b_bias,
                     const float* d, float* out, void* workspace, size_t workspace_bytes,
                     m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_forward");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              nullptr, nullptr, nullptr, nullptr, out};
   return scan_common(cfg, false, a, nullptr, workspace, workspace_bytes, stream);
@@ -305,6 +323,7 @@ int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* d, const float* mimo_x, const float* mimo_z,
                     const float* mimo_o, const float* norm_weight, float* out,
                     void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_mimo_forward");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              mimo_x, mimo_z, mimo_o, norm_weight, out};
   return scan_common(cfg, true, a, nullptr, workspace, workspace_bytes, stream);
@@ -334,6 +353,7 @@ int m3_siso_prefill(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* d, float* ssm_state, float* angle_state, float* k_state,
                     float* v_state, float* out, void* workspace, size_t workspace_bytes,
                     m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_prefill");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              nullptr, nullptr, nullptr, nullptr, out};
   StepState s{ssm_state, angle_state, k_state, v_state};
@@ -347,6 +367,7 @@ int m3_mimo_prefill(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* mimo_o, const float* norm_weight, float* ssm_state,
                     float* angle_state, float* k_state, float* v_state, float* out,
                     void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_mimo_prefill");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              mimo_x, mimo_z, mimo_o, norm_weight, out};
   StepState s{ssm_state, angle_state, k_state, v_state};
@@ -377,6 +398,7 @@ int m3_siso_step(const m3_ssm_config* cfg, const float* c, const float* b, const
                  const float* angle, const float* c_bias, const float* b_bias, const float* d,
                  float* ssm_state, float* angle_state, float* k_state, float* v_state,
                  float* out, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_step");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              nullptr, nullptr, nullptr, nullptr, out};
   StepState s{ssm_state, angle_state, k_state, v_state};
@@ -389,6 +411,7 @@ int m3_mimo_step(const m3_ssm_config* cfg, const float* c, const float* b, const
                  const float* mimo_x, const float* mimo_z, const float* mimo_o,
                  const float* norm_weight, float* ssm_state, float* angle_state,
                  float* k_state, float* v_state, float* out, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_mimo_step");
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              mimo_x, mimo_z, mimo_o, norm_weight, out};
   StepState s{ssm_state, angle_state, k_state, v_state};
@@ -402,6 +425,7 @@ int m3_workspace_status(const void* workspace, size_t workspace_bytes, m3_stream
   uint32_t word = 0;
   e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return M3_ERR_CUDA;
+  if (word == kStatusUndrained) return M3_ERR_DEVICE_STATE;
   return word == kStatusTimeout ? M3_ERR_TIMEOUT : M3_OK;
 }
 

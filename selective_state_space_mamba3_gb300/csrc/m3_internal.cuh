@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "../../include/m3.h"
@@ -15,6 +16,7 @@ struct ScanGeom {
   int B, L, H, G, P, N, A, R;
   int has_z, has_d, has_norm;
   int math_mode;
+  int mimo;  // the MIMO operation (mimo_x / mimo_z / mimo_o operands)
 };
 
 struct ScanArgs {
@@ -57,6 +59,9 @@ struct ChunkIO {
 
 // Device status word written by bounded waits (lives in the caller's workspace).
 constexpr uint32_t kStatusTimeout = 0x54494d45u;  // "TIME"
+// A wait gave up and the kernel's bounded wait for its own copies still in
+// flight gave up too: it exited with those copies unfinished.
+constexpr uint32_t kStatusUndrained = 0x44524e58u;  // "DRNX"
 
 // Launchers: return cudaSuccess or the launch error. Each increments the
 // library's launch counter by the number of kernels it enqueued.
@@ -74,9 +79,12 @@ cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, const float* g_init
                                 const float* esum, float* g_entry, float* th_entry,
                                 cudaStream_t s);
 bool chunk_supported(const ScanGeom& g);
+// the split-operand (3xTF32) flavour fits the device's shared memory for g
+bool chunk_split_supported(const ScanGeom& g);
 // summary: state-only pass (no outputs), used to split long sequences.
+// split: the split-operand flavour (one CTA per SM) instead of single-pass TF32.
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
-                              const ChunkIO& io, bool summary, cudaStream_t s);
+                              const ChunkIO& io, bool summary, bool split, cudaStream_t s);
 int chunk_rows_per_token(const ScanGeom& g);  // 64 / R: tokens per chunk
 
 // Scan entry chosen by the host: workspace bytes for geometry g (with or
@@ -86,6 +94,15 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
                         size_t ws_bytes, cudaStream_t s);
 
 void count_launches(uint64_t n);
+
+// NVTX range around one C-ABI call (header-only NVTX 3: a no-op unless a
+// profiler injects its tool library), so that timelines show each m3_* call.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // ---------------------------------------------------------------------------
 // Scalar maps of the method, in float32 (overflow-safe softplus as in the

@@ -219,6 +219,10 @@ __device__ __forceinline__ float4 tf32_feed(float4 v) {
 __device__ __forceinline__ float tf32_clean(float v) {
   return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
 }
+// The value as a kind::tf32 MMA reads an unrounded operand (low 13 bits dropped).
+__device__ __forceinline__ float tf32_trunc(float v) {
+  return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+}
 
 }  // namespace tc
 }  // namespace m3

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert m3.status_string(code)
     assert "unknown" in m3.status_string(99)
 
@@ -164,5 +164,25 @@ def test_failed_launch_is_reported(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    assert call_siso(lib, siso_cfg()) == m3.M3_ERR_CUDA
+    # FP32 mode takes the chunked split-operand path here, which needs a
+    # workspace; the fake one is never touched because the first CUDA call fails
+    assert call_siso(lib, siso_cfg(), ws=FAKE, wsn=1 << 20) == m3.M3_ERR_CUDA
     assert lib.m3_preprocess(ctypes.byref(pre_cfg()), 64, *([FAKE] * 10), None) == m3.M3_ERR_CUDA
+
+
+def test_static_entry_rejects_workspace_above_its_array(lib):
+    """m3_siso_forward_static serves only geometries whose workspace fits its
+    fixed 1 MiB device array: the long-context SISO shape in TF32 mode splits
+    its 64 sequences into segments whose summary states need about 16 MiB, so
+    the call is refused with M3_ERR_WORKSPACE before anything is enqueued (the
+    fake pointers are never dereferenced)."""
+    cfg = siso_cfg(batch_size=2, sequence_length=16384, num_heads=32, num_groups=4, head_dim=64,
+                   state_size=128, num_rope_angles=64, math_mode=m3.M3_MATH_TF32)
+    n = ctypes.c_size_t(0)
+    assert lib.m3_siso_forward_workspace(ctypes.byref(cfg), ctypes.byref(n)) == m3.M3_OK
+    assert n.value > (1 << 20)
+    assert lib.m3_siso_forward_static(ctypes.byref(cfg), *([FAKE] * 12), None) == \
+        m3.M3_ERR_WORKSPACE
+    # invalid geometries are still refused as such
+    assert lib.m3_siso_forward_static(ctypes.byref(siso_cfg(head_dim=129)), *([FAKE] * 12),
+                                      None) == m3.M3_ERR_INVALID_ARGUMENT

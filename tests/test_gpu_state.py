@@ -93,8 +93,7 @@ def test_prefill_from_state(mode, mimo):
     state = random_state(w, 5)
     got, fin = gpu_prefill(w, ins, mode, state, mimo=mimo)
     ref, rst = oracle_from_state(w, ins, state, mimo=mimo)
-    tol = TOL[mode] if not (mimo and mode == TF32) else 1e-2
-    check_close(got, ref, tol, "out")
+    check_close(got, ref, TOL[mode], "out")
     compare_states(fin, rst, TOL[mode])
 
 
