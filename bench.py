@@ -1,10 +1,11 @@
 """Benchmark of the Mamba-3 hot path on GB300.
 
-One step = m3_preprocess of the packed projection of a SISO 1B-layer batch
-(B=8, L=2048, H=32, P=64, N=128, A=32, G=1; rows 16384 x width 4480) followed
-by m3_siso_forward over the 16384 tokens it produces, both through the C ABI
-with device-resident inputs. The metric is tokens/s (B*L per step, summed over
-ranks). The JSON line also carries the roofline of the dominant kernel, the
+One step = the SISO scan of the packed input projection of a SISO 1B-layer
+batch (B=8, L=2048, H=32, P=64, N=128, A=32, G=1; rows 16384 x width 4480):
+m3_siso_forward_packed, the preprocess fused into the chunked scan, whose
+output has the bits of m3_preprocess followed by m3_siso_forward (that
+two-call step is timed beside it), through the C ABI with device-resident
+inputs. The metric is tokens/s (B*L per step, summed over ranks). The JSON line also carries the roofline of the dominant kernel, the
 CPU oracle baseline, an end-to-end figure with host buffers, sampled clocks,
 and supplementary timings of the MIMO and decode-step entry points.
 
@@ -41,6 +42,15 @@ def bytes_per_token_scan(w):
     G = w.num_heads if w.num_groups == 0 else w.num_groups
     return 4 * (3 * w.num_heads * w.head_dim + 2 * w.mimo_rank * G * w.state_size +
                 3 * w.num_heads + w.num_rope_angles)
+
+
+def bytes_per_token_packed(w):
+    """Algorithmic HBM bytes of one token of the packed-projection scan: its
+    packed row read once (W floats) and its output row written once (H*P)."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    width = gen.packed_width(w.num_heads * w.head_dim, w.state_size, w.num_heads,
+                             w.num_rope_angles, G, w.mimo_rank)
+    return 4 * (width + w.num_heads * w.head_dim)
 
 
 def bytes_per_row_preprocess(w):
@@ -281,6 +291,13 @@ class Step:
         self.scfg = m3.ssm_config(w.cfg(), mode)
         wsb = m3.m3_siso_forward_workspace(self.scfg)
         self.ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device="cuda")
+        wpb = m3.m3_siso_forward_packed_workspace(self.scfg, self.pcfg)
+        self.ws_packed = torch.empty(max(wpb, 16), dtype=torch.uint8, device="cuda")
+
+    def packed(self):
+        """One step through the fused entry point (packed projection -> out)."""
+        self.m3.m3_siso_forward_packed(self.scfg, self.pcfg, self.proj, self.dt_bias, self.cb,
+                                       self.bb, self.d, self.out, self.ws_packed)
 
     def preprocess(self):
         self.m3.m3_preprocess(self.pcfg, self.rows, self.proj, self.dt_bias, self.x, self.z,
@@ -474,12 +491,13 @@ def run_m3(args):
             torch.distributed.barrier()
 
     for _ in range(args.warmup):
+        s.packed()
         s.preprocess()
         s.scan()
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -492,10 +510,8 @@ def run_m3(args):
     t_start.record()
     for k in range(K):
         ev[k][0].record()
-        s.preprocess()
+        s.packed()
         ev[k][1].record()
-        s.scan()
-        ev[k][2].record()
     t_end.record()
     torch.cuda.synchronize()
     clocks.mark_end()
@@ -503,20 +519,32 @@ def run_m3(args):
     barrier()
     clk = clocks.stop()
     total_ms = max_over_ranks(world, [t_start.elapsed_time(t_end)], "cuda")[0]
-    pre_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    scan_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    assert m3.m3_workspace_status(s.ws) == m3.M3_OK
+    fused_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    assert m3.m3_workspace_status(s.ws_packed) == m3.M3_OK
     tokens = w.tokens
     value = whole_job_rate(world, tokens, K, total_ms)
 
-    # roofline of the dominant kernel (algorithmic bytes / live event time)
+    # the two-call step (preprocess, then scan) and its parts, same workload
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for k in range(K):
+        ev2[k][0].record()
+        s.preprocess()
+        ev2[k][1].record()
+        s.scan()
+        ev2[k][2].record()
+    torch.cuda.synchronize()
+    pre_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev2]))
+    scan_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev2]))
+    assert m3.m3_workspace_status(s.ws) == m3.M3_OK
+
+    # roofline of the dominant kernel (algorithmic bytes / live event time):
+    # the fused scan, one launch per step (the packed rows read once, the
+    # output written once: 4 (W + H P) bytes per token)
     scan_bytes = tokens * bytes_per_token_scan(w)
     pre_bytes = s.rows * bytes_per_row_preprocess(w)
-    scan_kernel = "k_scan_chunk" if mode == m3.M3_MATH_TF32 else "k_scan_seq"
-    if scan_ms >= pre_ms:
-        kname, kms, kbytes = scan_kernel, scan_ms, scan_bytes
-    else:
-        kname, kms, kbytes = "k_preprocess", pre_ms, pre_bytes
+    fused_bytes = tokens * bytes_per_token_packed(w)
+    kname, kms, kbytes = "k_scan_chunk", fused_ms, fused_bytes
     achieved = kbytes / (kms * 1e-3) / 1e9
     roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
@@ -534,7 +562,14 @@ def run_m3(args):
            "h2d_bytes_per_step": s.h_proj.numel() * 4, "d2h_bytes_per_step": s.h_out.numel() * 4,
            "ms_per_step": round(e2e_ms, 4)}
 
-    parts = {"preprocess": {"ms": round(pre_ms, 4), "hbm_gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
+    parts = {"fused_step": {"ms": round(fused_ms, 4), "tokens_per_s": round(tokens / (fused_ms * 1e-3)),
+                            "hbm_gbs": round(achieved, 1), "frac_hbm": round(achieved / peak, 4),
+                            "algorithmic_bytes": fused_bytes,
+                            "entry": "m3_siso_forward_packed"},
+             "two_call_step": {"ms": round(pre_ms + scan_ms, 4),
+                               "tokens_per_s": round(tokens / ((pre_ms + scan_ms) * 1e-3)),
+                               "entry": "m3_preprocess + m3_siso_forward"},
+             "preprocess": {"ms": round(pre_ms, 4), "hbm_gbs": round(pre_bytes / (pre_ms * 1e-3) / 1e9, 1),
                             "frac_hbm": round(pre_bytes / (pre_ms * 1e-3) / 1e9 / peak, 4),
                             "algorithmic_bytes": pre_bytes},
              "siso_scan": {"ms": round(scan_ms, 4), "tokens_per_s": round(tokens / (scan_ms * 1e-3)),
@@ -564,7 +599,8 @@ def run_m3(args):
                 "config": {"workload": w.name, "batch": w.batch_size, "seq_len": w.sequence_length,
                            "heads": w.num_heads, "head_dim": w.head_dim, "state_size": w.state_size,
                            "groups": w.num_groups, "rope_angles": w.num_rope_angles,
-                           "step": "m3_preprocess (16384 x 4480 packed rows) + m3_siso_forward",
+                           "step": "m3_siso_forward_packed: 16384 x 4480 packed rows -> out "
+                                   "(preprocess fused into the scan)",
                            "math_mode": args.mode, "parallelism": f"replicas x{world}",
                            "l2": "inputs larger than L2 (293.6 MB packed projection read per step)"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),

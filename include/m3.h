@@ -10,6 +10,7 @@
  *   m3_mimo_step      - `mamba3_mimo_step`    (one MIMO token, explicit state)
  *   m3_siso_prefill / m3_mimo_prefill - the forward scans from / to an
  *                       explicit step state (prefill -> decode hand-off)
+ *   m3_siso_forward_packed - `mamba3_preprocess` and `mamba3_siso` in one call
  *
  * Conventions for every entry point:
  *  - Every tensor is float32, dense row-major, in device memory owned by the
@@ -127,6 +128,33 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* angle, const float* c_bias, const float* b_bias,
                     const float* d, float* out, void* workspace, size_t workspace_bytes,
                     m3_stream_t stream);
+
+/*
+ * m3_siso_forward_packed - m3_preprocess and m3_siso_forward in one call: the
+ * SISO scan of a packed input projection (`mamba3_preprocess` feeding
+ * `mamba3_siso`; the pages run them as two ops, this entry point fuses them).
+ *
+ * projected [B*L, W] in the m3_preprocess column order, dt_bias [H]; c_bias,
+ * b_bias [H,N]; d [H]; out [B,L,H,P]. pcfg must describe the same layer as
+ * cfg: inner_size = H*P, state_size = N, num_heads = H, num_rope_angles = A,
+ * num_groups = the resolved G, mimo_rank = 1; its epsilon / dt bounds /
+ * a_floor are checked as in m3_preprocess, cfg as in m3_siso_forward.
+ * Where the chunked kernel has a TMA instance for the shape (P = 64, N = 128,
+ * A = 32 or 64) and W is a multiple of 4, the scan reads the packed rows
+ * directly: the B / C rows are RMS-normalised in shared memory in the same
+ * reduction order as m3_preprocess, and dt / adt are formed by the same maps,
+ * so the output has the bits of m3_preprocess followed by m3_siso_forward in
+ * the same math mode. Otherwise the preprocess writes its outputs into the
+ * workspace and the scan reads them from there (the same result).
+ * workspace: at least m3_siso_forward_packed_workspace() bytes, 16-byte
+ * aligned (may be NULL when that size is 0).
+ */
+int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                                     size_t* bytes);
+int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                           const float* projected, const float* dt_bias, const float* c_bias,
+                           const float* b_bias, const float* d, float* out, void* workspace,
+                           size_t workspace_bytes, m3_stream_t stream);
 
 /*
  * m3_mimo_forward - the shared-state Mamba-3 MIMO recurrence (`mamba3_mimo`,

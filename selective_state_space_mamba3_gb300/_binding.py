@@ -26,7 +26,8 @@ M3_MATH_FP32 = 0
 M3_MATH_TF32 = 1
 
 EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
-            "m3_siso_forward_static", "m3_siso_forward_static_status", "m3_siso_prefill_workspace", "m3_siso_prefill",
+            "m3_siso_forward_static", "m3_siso_forward_static_status",
+            "m3_siso_forward_packed_workspace", "m3_siso_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
@@ -94,6 +95,9 @@ def load_library():
         lib.m3_mimo_forward.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
         lib.m3_siso_forward_static.argtypes = [cfgp] + [_vp] * 12 + [_vp]
         lib.m3_siso_forward_static_status.argtypes = [_vp]
+        pcfgp = ctypes.POINTER(PreprocessConfig)
+        lib.m3_siso_forward_packed_workspace.argtypes = [cfgp, pcfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_siso_forward_packed.argtypes = [cfgp, pcfgp] + [_vp] * 7 + [ctypes.c_size_t, _vp]
         lib.m3_siso_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_mimo_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_prefill.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
@@ -186,6 +190,24 @@ def m3_siso_forward_static(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_b
     _check(load_library().m3_siso_forward_static(ctypes.byref(cfg), *[_ptr(t) for t in (
         c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, out)], _stream(stream)),
         "m3_siso_forward_static")
+
+
+def m3_siso_forward_packed_workspace(cfg: SsmConfig, pcfg: PreprocessConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_siso_forward_packed_workspace(ctypes.byref(cfg), ctypes.byref(pcfg),
+                                                            ctypes.byref(n)),
+           "m3_siso_forward_packed_workspace")
+    return n.value
+
+
+def m3_siso_forward_packed(cfg: SsmConfig, pcfg: PreprocessConfig, projected, dt_bias, c_bias,
+                           b_bias, d, out, workspace=None, stream=None):
+    """m3_preprocess and m3_siso_forward in one call (packed projection in,
+    scan output out)."""
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_siso_forward_packed(ctypes.byref(cfg), ctypes.byref(pcfg), *[
+        _ptr(t) for t in (projected, dt_bias, c_bias, b_bias, d, out)], wp, wn, _stream(stream)),
+        "m3_siso_forward_packed")
 
 
 def m3_siso_forward_static_status(stream=None) -> int:

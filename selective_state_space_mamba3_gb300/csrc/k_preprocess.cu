@@ -71,11 +71,14 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
         const int N4 = N >> 2;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (lane < N4) v = __ldcs(reinterpret_cast<const float4*>(src) + lane);
-        float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-        const float inv = 1.0f / sqrtf(ss / (float)N + g.eps);
+        // (the fused packed-projection scan reduces in this same order: lane
+        // = float4 group, then the 16-8-4-2-1 butterfly)
+        const float ss = warp_sum(sumsq4(v));
+        const float inv = rms_inv(ss, N, g.eps);
         if (lane < N4)
           __stcs(reinterpret_cast<float4*>(dst) + lane,
-                 make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv));
+                 make_float4(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv), __fmul_rn(v.z, inv),
+                             __fmul_rn(v.w, inv)));
       } else {
         float ss = 0.f;
         for (int n = lane; n < N; n += 32) {
@@ -83,18 +86,16 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
           ss += v * v;
         }
         ss = warp_sum(ss);
-        const float inv = 1.0f / sqrtf(ss / (float)N + g.eps);
+        const float inv = rms_inv(ss, N, g.eps);
         for (int n = lane; n < N; n += 32) __stcs(dst + n, src[n] * inv);
       }
     }
     // dt_raw | a_raw | trap (H each) | angle (A).
     const float* s = p + 2 * I + 2 * BC;
     for (int h = tid; h < H; h += kThreads) {
-      float d = softplus_f(__ldcs(s + h) + __ldg(dt_bias + h));
-      d = fminf(fmaxf(d, g.dt_min), g.dt_max);
-      const float a_mag = fmaxf(softplus_f(__ldcs(s + H + h)), g.a_floor);
+      const float d = pre_dt(__ldcs(s + h), __ldg(dt_bias + h), g.dt_min, g.dt_max);
       __stcs(o.dt + r * (int64_t)H + h, d);
-      __stcs(o.adt + r * (int64_t)H + h, -a_mag * d);
+      __stcs(o.adt + r * (int64_t)H + h, pre_adt(__ldcs(s + H + h), g.a_floor, d));
       __stcs(o.trap + r * (int64_t)H + h, __ldcs(s + 2 * H + h));
     }
     for (int a = tid; a < A; a += kThreads) __stcs(o.angle + r * (int64_t)A + a, __ldcs(s + 3 * H + a));

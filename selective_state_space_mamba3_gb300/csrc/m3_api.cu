@@ -166,9 +166,15 @@ size_t scan_workspace_bytes(const ScanGeom& g, bool with_state) {
   return use_chunk(g) ? chunk_ws(g, with_state).bytes : 0;
 }
 
-cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
-                        size_t, cudaStream_t s) {
-  if (!use_chunk(g)) return launch_scan_seq(g, a, st ? *st : StepState{}, s);
+namespace {
+using ChunkLauncher = cudaError_t (*)(const ScanGeom&, const ScanArgs&, uint32_t*,
+                                      const ChunkIO&, bool, bool, cudaStream_t);
+
+// The chunked scan: status word cleared, the step state converted into the
+// kernel's entry state (prefill), then one main pass, or for split sequences a
+// summary pass, the prefix over segments and the main pass.
+cudaError_t run_chunked(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
+                        cudaStream_t s, ChunkLauncher launch_scan_chunk) {
   const bool split = chunk_split_mode(g);
   const ChunkWs w = chunk_ws(g, st != nullptr);
   char* base = static_cast<char*>(ws);
@@ -211,6 +217,68 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
   io.th0 = f(w.thentry);
   return launch_scan_chunk(g, a, status, io, false, split, s);
 }
+}  // namespace
+
+cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
+                        size_t, cudaStream_t s) {
+  if (!use_chunk(g)) return launch_scan_seq(g, a, st ? *st : StepState{}, s);
+  return run_chunked(g, a, st, ws, s, launch_scan_chunk);
+}
+
+// ---------------------------------------------------------------------------
+// SISO scan of a packed projection: fused where the chunked kernel has a TMA
+// instance for the shape and the packed rows are 16-byte aligned column by
+// column, otherwise m3_preprocess into the workspace followed by the scan.
+namespace {
+struct PackedPlan {
+  bool fused;
+  size_t pre_bytes;  // fallback: x, z, bh, ch, dt, adt, trap, angle at the workspace start
+  size_t off[8];
+  size_t bytes;
+};
+
+PackedPlan packed_plan(const ScanGeom& g, const PreGeom& p) {
+  PackedPlan pl{};
+  pl.fused = use_chunk(g) && chunk_packed_supported(g) && p.W % 4 == 0;
+  if (pl.fused) {
+    pl.bytes = scan_workspace_bytes(g, false);
+    return pl;
+  }
+  const size_t rows = (size_t)p.rows;
+  const size_t bc = (size_t)p.G * p.R * p.N;
+  const size_t cols[8] = {(size_t)p.I, (size_t)p.I, bc, bc, (size_t)p.H, (size_t)p.H,
+                          (size_t)p.H, (size_t)p.A};
+  size_t o = 0;
+  for (int i = 0; i < 8; ++i) {
+    pl.off[i] = o;
+    o += (rows * cols[i] * 4 + 255) / 256 * 256;
+  }
+  pl.pre_bytes = o;
+  pl.bytes = o + scan_workspace_bytes(g, false);
+  return pl;
+}
+
+// Geometry of the packed scan: the SsmConfig rules, and a preprocess config
+// that describes the same layer (inner = H * P, the same N, H, A and groups,
+// rank 1).
+int resolve_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg, ScanGeom* g,
+                   PreGeom* p) {
+  int st = resolve_ssm(cfg, false, g);
+  if (st != M3_OK) return st;
+  if (!pcfg) return M3_ERR_INVALID_ARGUMENT;
+  st = resolve_pre(pcfg, (int64_t)g->B * g->L, p);
+  if (st != M3_OK) return st;
+  if (p->I != g->H * g->P || p->N != g->N || p->H != g->H || p->A != g->A || p->G != g->G ||
+      p->R != 1)
+    return M3_ERR_INVALID_ARGUMENT;
+  g->W = p->W;
+  g->eps = p->eps;
+  g->dt_min = p->dt_min;
+  g->dt_max = p->dt_max;
+  g->a_floor = p->a_floor;
+  return M3_OK;
+}
+}  // namespace
 
 }  // namespace m3
 
@@ -238,6 +306,21 @@ int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* pr
                   const float* dt_bias, float* x, float* z, float* bh, float* ch, float* dt,
                   float* adt, float* trap, float* angle, m3_stream_t stream) {
   NvtxRange nvtx_range("m3_preprocess");
+  PreGeom g;
+  int st = resolve_pre(cfg, rows, &g);
+  if (st != M3_OK) return st;
+  st = check_ptrs({projected, dt_bias, x, z, bh, ch, dt, adt, trap});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(angle, g.A)) != M3_OK) return st;
+  PreOut o{x, z, bh, ch, dt, adt, trap, angle};
+  return cuda_status(launch_preprocess(g, projected, dt_bias, o, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+namespace m3 {
+// `PreprocessGeometry::resolve` rules; fills g.
+int resolve_pre(const m3_preprocess_config* cfg, int64_t rows, PreGeom* out) {
   if (!cfg) return M3_ERR_INVALID_ARGUMENT;
   const int64_t I = cfg->inner_size, N = cfg->state_size, H = cfg->num_heads;
   const int64_t A = cfg->num_rope_angles, G = cfg->num_groups, R = cfg->mimo_rank;
@@ -254,16 +337,15 @@ int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* pr
   if (!count_below_u32({W}) || !count_below_u32({rows, W}) || !count_below_u32({rows, I}) ||
       !count_below_u32({rows, bc}) || !count_below_u32({rows, H}) || !count_below_u32({rows, A}))
     return M3_ERR_INVALID_ARGUMENT;
-  int st = check_ptrs({projected, dt_bias, x, z, bh, ch, dt, adt, trap});
-  if (st != M3_OK) return st;
-  if ((st = check_angle_ptr(angle, (int)A)) != M3_OK) return st;
-  PreGeom g;
+  PreGeom& g = *out;
   g.rows = rows; g.I = (int)I; g.N = (int)N; g.H = (int)H; g.A = (int)A; g.G = (int)G;
   g.R = (int)R; g.W = (int)W;
   g.eps = eps; g.dt_min = lo; g.dt_max = hi; g.a_floor = fl;
-  PreOut o{x, z, bh, ch, dt, adt, trap, angle};
-  return cuda_status(launch_preprocess(g, projected, dt_bias, o, (cudaStream_t)stream));
+  return M3_OK;
 }
+}  // namespace m3
+
+extern "C" {
 
 int m3_siso_forward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
   ScanGeom g;
@@ -315,6 +397,51 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
   ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
              nullptr, nullptr, nullptr, nullptr, out};
   return scan_common(cfg, false, a, nullptr, workspace, workspace_bytes, stream);
+}
+
+int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                                     size_t* bytes) {
+  ScanGeom g;
+  PreGeom p;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  const int st = resolve_packed(cfg, pcfg, &g, &p);
+  if (st != M3_OK) return st;
+  *bytes = packed_plan(g, p).bytes;
+  return M3_OK;
+}
+
+int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                           const float* projected, const float* dt_bias, const float* c_bias,
+                           const float* b_bias, const float* d, float* out, void* workspace,
+                           size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_forward_packed");
+  ScanGeom g;
+  PreGeom p;
+  int st = resolve_packed(cfg, pcfg, &g, &p);
+  if (st != M3_OK) return st;
+  if ((st = check_ptrs({projected, dt_bias, c_bias, b_bias, d, out})) != M3_OK) return st;
+  const PackedPlan pl = packed_plan(g, p);
+  if (pl.bytes > 0 && (!workspace || workspace_bytes < pl.bytes)) return M3_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return M3_ERR_UNALIGNED;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if (pl.fused) {
+    // x, z and the scalar columns of the packed rows; C / B through tensor maps
+    const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.N;
+    ScanArgs a{projected, projected, projected + I, projected, projected + o_s + p.H,
+               projected + o_s, projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias,
+               b_bias, d, nullptr, nullptr, nullptr, nullptr, out, dt_bias};
+    return cuda_status(run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed));
+  }
+  char* w = static_cast<char*>(workspace);
+  float* f[8];
+  for (int i = 0; i < 8; ++i) f[i] = reinterpret_cast<float*>(w + pl.off[i]);
+  PreOut o{f[0], f[1], f[2], f[3], f[4], f[5], f[6], g.A ? f[7] : nullptr};
+  cudaError_t e = launch_preprocess(p, projected, dt_bias, o, s);
+  if (e != cudaSuccess) return M3_ERR_CUDA;
+  ScanArgs a{o.ch, o.bh, o.x, o.z, o.adt, o.dt, o.trap, o.angle, c_bias, b_bias, d,
+             nullptr, nullptr, nullptr, nullptr, out};
+  return cuda_status(launch_scan(g, a, nullptr, w + pl.pre_bytes, workspace_bytes - pl.pre_bytes,
+                                 s));
 }
 
 int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,

@@ -17,12 +17,21 @@ struct ScanGeom {
   int has_z, has_d, has_norm;
   int math_mode;
   int mimo;  // the MIMO operation (mimo_x / mimo_z / mimo_o operands)
+  // packed-projection scan only: width W of a packed row and the preprocess
+  // settings (`Mamba3PreprocessConfig`)
+  int W;
+  float eps, dt_min, dt_max, a_floor;
 };
 
+// Scan operands. For the packed-projection scan, x and z point at their
+// columns of the packed rows, dt / adt / trap / angle at the dt_raw / a_raw /
+// trap / angle columns (row stride W), c and b are unused (the C and B rows
+// are read through tensor maps of the packed rows) and dt_bias is set.
 struct ScanArgs {
   const float *c, *b, *x, *z, *adt, *dt, *trap, *angle, *c_bias, *b_bias, *d;
   const float *mimo_x, *mimo_z, *mimo_o, *norm_weight;  // null for SISO
   float* out;
+  const float* dt_bias;  // packed-projection scan only
 };
 
 struct StepState {
@@ -86,6 +95,13 @@ bool chunk_split_supported(const ScanGeom& g);
 cudaError_t launch_scan_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
                               const ChunkIO& io, bool summary, bool split, cudaStream_t s);
 int chunk_rows_per_token(const ScanGeom& g);  // 64 / R: tokens per chunk
+// the SISO scan of a packed projection (ScanArgs as described above)
+bool chunk_packed_supported(const ScanGeom& g);
+cudaError_t launch_scan_chunk_packed(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
+                                     const ChunkIO& io, bool summary, bool split,
+                                     cudaStream_t s);
+// `PreprocessGeometry::resolve` rules for `rows` packed rows; fills g
+int resolve_pre(const m3_preprocess_config* cfg, int64_t rows, PreGeom* g);
 
 // Scan entry chosen by the host: workspace bytes for geometry g (with or
 // without a recurrent state), then launch (st null: zero state).
@@ -112,6 +128,24 @@ __device__ __forceinline__ float softplus_f(float v) {
 }
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + expf(-v)); }
 __device__ __forceinline__ float silu_f(float v) { return v * sigmoid_f(v); }
+
+// Preprocess maps (`mamba3_preprocess`), shared by the preprocess kernel and
+// the fused packed-projection scan so that both produce the same bits: the
+// clamped dt, the floored negative log decay adt, the sum of squares of four
+// B/C values (a fixed FMA chain), and the inverse RMS of a row from its sum of
+// squares (IEEE division and square root).
+__device__ __forceinline__ float pre_dt(float raw, float bias, float lo, float hi) {
+  return fminf(fmaxf(softplus_f(__fadd_rn(raw, bias)), lo), hi);
+}
+__device__ __forceinline__ float pre_adt(float a_raw, float a_floor, float dt) {
+  return __fmul_rn(-fmaxf(softplus_f(a_raw), a_floor), dt);
+}
+__device__ __forceinline__ float sumsq4(float4 v) {
+  return __fmaf_rn(v.w, v.w, __fmaf_rn(v.z, v.z, __fmaf_rn(v.y, v.y, __fmul_rn(v.x, v.x))));
+}
+__device__ __forceinline__ float rms_inv(float ss, int n, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)n), eps)));
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -185,24 +185,34 @@ struct TokenPreload {
   float ang[16];
 };
 
-__device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs& a, int64_t tok,
-                                               int cn, int L, int TPW, int A, int H, int h,
-                                               int warp, int lane) {
+// Packed projection (PACKED): the columns dt_raw / a_raw / trap / angle of the
+// packed rows (row stride W), with dt and adt formed by the preprocess maps.
+template <bool PACKED>
+__device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs& a,
+                                               const ScanGeom& g, int64_t tok, int cn, int L,
+                                               int TPW, int A, int H, int h, int warp, int lane) {
   pl.dt = pl.adt = pl.trap = 0.f;
   const int tw = TPW * warp + lane;
+  const int64_t rs = PACKED ? (int64_t)g.W : (int64_t)H;  // row stride of the scalar columns
   if (lane <= TPW && cn + tw < L) {
-    const int64_t sc = (tok + tw) * H + h;
-    pl.dt = a.dt[sc];
-    pl.adt = a.adt[sc];
+    const int64_t sc = (tok + tw) * rs + h;
+    if constexpr (PACKED) {
+      pl.dt = pre_dt(a.dt[sc], a.dt_bias[h], g.dt_min, g.dt_max);
+      pl.adt = pre_adt(a.adt[sc], g.a_floor, pl.dt);
+    } else {
+      pl.dt = a.dt[sc];
+      pl.adt = a.adt[sc];
+    }
     pl.trap = a.trap[sc];
   }
+  const int64_t ars = PACKED ? (int64_t)g.W : (int64_t)A;  // row stride of the angle columns
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int t = TPW * warp + i, aa = lane + 32 * j;
       pl.ang[2 * i + j] =
-          (i < TPW && aa < A && cn + t < L) ? a.angle[(tok + t) * A + aa] : 0.f;
+          (i < TPW && aa < A && cn + t < L) ? a.angle[(tok + t) * ars + aa] : 0.f;
     }
   }
 }
@@ -274,7 +284,8 @@ __device__ __forceinline__ void put4(float* dst, int LO, float4 v) {
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
-template <int MP, bool MIMO, bool SUMMARY, int KN, int KA, int KR, int KP, bool SPLIT>
+template <int MP, bool MIMO, bool SUMMARY, int KN, int KA, int KR, int KP, bool SPLIT,
+          bool PACKED>
 __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     k_scan_chunk(ScanGeom g, ScanArgs a, ChunkLayout lay, ChunkIO io, uint32_t* status,
                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB) {
@@ -417,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   const uint32_t id_Y = tc::idesc_tf32(MP, 64);
   const uint32_t id_D = tc::idesc_tf32(MP, Npad);
   const int64_t HP = (int64_t)H * P;
+  // row stride of the x and z rows: H * P in their own tensors, W in the
+  // packed projection (PACKED: x and z are column slices of the packed rows)
+  const int64_t XS = PACKED ? (int64_t)g.W : HP;
+  static_assert(!PACKED || kAsync, "the packed projection is read by TMA instances only");
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -429,7 +444,13 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   if (lane == 0) {
     const float* base = nullptr;
     int64_t per_tok = 0;  // floats per token
-    switch (warp) {
+    if (PACKED) {
+      // the packed rows of a chunk are contiguous: warp 0 takes this head's slice
+      if (warp == 0) {
+        base = a.z;
+        per_tok = g.W;
+      }
+    } else switch (warp) {
       case 0: base = a.x; per_tok = HP; break;
       case 1: base = a.z; per_tok = HP; break;
       case 2: base = a.c; per_tok = (int64_t)RG * N; break;
@@ -488,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   }
 
   TokenPreload pl;
-  preload_tokens(pl, a, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
+  preload_tokens<PACKED>(pl, a, g, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
   float esum = 0.f;  // sum of adt over the segment
   float lgE = 0.f;   // G = e^{lgE} G~ (identical in every thread)
 
@@ -734,6 +755,55 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           if (!ok) abort_flag = 1;
           if (pendC == it) pendC = -1;
           if (pendB == it) pendB = -1;
+          // Packed projection: the B / C rows arrive raw and are RMS-normalised
+          // here. The row's float4 groups q = 0 .. N/4 - 1 are spread over the
+          // four lanes of the row (lane jl holds the groups q = jl + 4m), and
+          // their sums of squares are added in the order of the preprocess
+          // kernel's butterfly over q (bits 4, 3, 2 of q here, then bits 1 and
+          // 0 across the lanes), so that the normalised rows have its bits.
+          float inv_c = 1.f, inv_b = 1.f;
+          if constexpr (PACKED) {
+            static_assert(KA % 16 == 0 && KN <= 128, "group classes need A % 16 == 0");
+            float sc[8], sb[8];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) sc[m] = sb[m] = 0.f;
+#pragma unroll
+            for (int jb = 0; jb < QW4; ++jb) {
+              if (jb < PQ / 4) {  // rotary item: groups j and j + A/4 (m = jb, jb + A/16)
+                const int n0 = 16 * jb + 4 * jl;
+                if (!SUMMARY) {
+                  sc[jb] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)));
+                  sc[jb + KA / 16] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)));
+                }
+                sb[jb] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0)));
+                sb[jb + KA / 16] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)));
+              } else {            // plain item: group A/4 + j (m = A/16 + jb)
+                const int n0 = KA + 16 * jb + 4 * jl;
+                if (!SUMMARY)
+                  sc[KA / 16 + jb] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)));
+                sb[KA / 16 + jb] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0)));
+              }
+            }
+            auto tree = [](const float* v) {
+              return __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[4]), __fadd_rn(v[2], v[6])),
+                               __fadd_rn(__fadd_rn(v[1], v[5]), __fadd_rn(v[3], v[7])));
+            };
+            float tcs = tree(sc), tbs = tree(sb);
+            tcs = __fadd_rn(tcs, __shfl_xor_sync(0xffffffffu, tcs, 16));
+            tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 16));
+            tcs = __fadd_rn(tcs, __shfl_xor_sync(0xffffffffu, tcs, 8));
+            tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 8));
+            inv_c = rms_inv(tcs, N, g.eps);
+            inv_b = rms_inv(tbs, N, g.eps);
+          }
+          // (the raw row times its inverse RMS, as the preprocess writes it)
+          auto nrm = [&](float4 v, float inv) -> float4 {
+            if constexpr (PACKED)
+              return make_float4(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv), __fmul_rn(v.z, inv),
+                                 __fmul_rn(v.w, inv));
+            else
+              return v;
+          };
 #pragma unroll
           for (int jb = 0; jb < QW4; ++jb) {
             const int j = 4 * jb + jl;
@@ -748,14 +818,15 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
                 case 2: th = th4[2]; if constexpr (kCosSin) sv = sn4[kCosSin ? 2 : 0]; break;
                 default: th = th4[3]; if constexpr (kCosSin) sv = sn4[kCosSin ? 3 : 0]; break;
               }
-              pair_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
-                        *reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)),
-                        *reinterpret_cast<const float4*>(sK + toff(rho, n0)),
-                        *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)), th, sv);
+              pair_item(n0, nrm(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)), inv_c),
+                        nrm(*reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)), inv_c),
+                        nrm(*reinterpret_cast<const float4*>(sK + toff(rho, n0)), inv_b),
+                        nrm(*reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)), inv_b), th,
+                        sv);
             } else {
               const int n0 = 2 * A + 4 * (j - PQ);
-              single_item(n0, *reinterpret_cast<const float4*>(sQ + toff(rho, n0)),
-                          *reinterpret_cast<const float4*>(sK + toff(rho, n0)));
+              single_item(n0, nrm(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)), inv_c),
+                          nrm(*reinterpret_cast<const float4*>(sK + toff(rho, n0)), inv_b));
             }
           }
         } else {
@@ -910,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int t = 8 * warp + 4 * (k >> 1) + (lane >> 3), pq = 8 * (k & 1) + (lane & 7);
-          xq[k] = t < tv ? *reinterpret_cast<const float4*>(a.x + (tok0 + t) * HP + (int64_t)h * P + 4 * pq)
+          xq[k] = t < tv ? *reinterpret_cast<const float4*>(a.x + (tok0 + t) * XS + (int64_t)h * P + 4 * pq)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       } else {
@@ -921,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           const int rho2 = 4 * rb + rl;
           const int t2 = rho2 >> lgR, r2 = rho2 & (R - 1);
           const bool in = rb < kRows / 4 && t2 < tv;
-          const float* xrow = a.x + (tok0 + t2) * HP + (int64_t)h * P;
+          const float* xrow = a.x + (tok0 + t2) * XS + (int64_t)h * P;
           const float* mx = mimo ? a.mimo_x + ((int64_t)h * R + r2) * P : nullptr;
 #pragma unroll
           for (int pb = 0; pb < MP / 8; ++pb) {
@@ -1023,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       }
       // value of the sequence's last token for the step state (last chunk only)
       if (io.v_last && c0 + tv == L) {
-        const float* xrow = a.x + (tok0 + tv - 1) * HP + (int64_t)h * P;
+        const float* xrow = a.x + (tok0 + tv - 1) * XS + (int64_t)h * P;
         for (int i = tid; i < R * P; i += kThreads) {
           const int r = i / P, p = i - r * P;
           io.v_last[((int64_t)bh * R + r) * P + p] =
@@ -1102,7 +1173,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     lgE = lg_new;
     // next chunk's per-token scalars and angles: loads in flight during the
     // MMAs and the epilogue
-    if (c0 + Qt < l1) preload_tokens(pl, a, tok0 + Qt, c0 + Qt, L, TPW, A, H, h, warp, lane);
+    if (c0 + Qt < l1)
+      preload_tokens<PACKED>(pl, a, g, tok0 + Qt, c0 + Qt, L, TPW, A, H, h, warp, lane);
     if (!SUMMARY) {
       // SISO epilogue gate operand z of this thread's output column, loaded while
       // the MMAs run (its x comes from the value tile, rounded to TF32 like
@@ -1122,11 +1194,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           const int unit = tid + kThreads * k;
           const int t = unit / kRowQ, p0 = 4 * (unit % kRowQ);
           zq[k] = (t < tv && g.has_z)
-                      ? *reinterpret_cast<const float4*>(a.z + (tok0 + t) * HP + (int64_t)h * P + p0)
+                      ? *reinterpret_cast<const float4*>(a.z + (tok0 + t) * XS + (int64_t)h * P + p0)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       } else if (!mimo) {
-        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+        const float* zcol = a.z + tok0 * XS + (int64_t)h * P + prow;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int col0 = (2 * wg + u) * 16 + 8 * half;
@@ -1134,7 +1206,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           for (int j = 0; j < kCols; ++j) {
             const int t = col0 + j;
             const bool ok = pvalid && t < tv;
-            ze[u][j] = (ok && g.has_z) ? zcol[t * HP] : 0.f;
+            ze[u][j] = (ok && g.has_z) ? zcol[t * XS] : 0.f;
           }
         }
       }
@@ -1143,14 +1215,14 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       constexpr int kTpb = (MIMO && KR > 0) ? kCols / KR : 0;
       float zm[2][kTpb > 0 ? kTpb : 1];
       if (kTpb > 0) {
-        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+        const float* zcol = a.z + tok0 * XS + (int64_t)h * P + prow;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int col0 = (2 * wg + u) * 16 + 8 * half;
 #pragma unroll
           for (int tt = 0; tt < (kTpb > 0 ? kTpb : 1); ++tt) {
             const int t = (col0 >> lgR) + tt;
-            zm[u][tt] = (pvalid && t < tv && g.has_z) ? zcol[t * HP] : 0.f;
+            zm[u][tt] = (pvalid && t < tv && g.has_z) ? zcol[t * XS] : 0.f;
           }
         }
       }
@@ -1181,7 +1253,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       // (8) epilogue: output column p of this chunk's tokens. With MP = 64 the
       // two lanes of a row split each 16-column block into 8 + 8 columns.
       {
-        const float* zcol = a.z + tok0 * HP + (int64_t)h * P + prow;
+        const float* zcol = a.z + tok0 * XS + (int64_t)h * P + prow;
         float* ocol = a.out + tok0 * HP + (int64_t)h * P + prow;
 #pragma unroll
         for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
@@ -1233,7 +1305,7 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
               if constexpr (kTpb > 0)
                 zv = zm[cb - 2 * wg][tt];
               else
-                zv = g.has_z ? zcol[t * HP] : 0.f;
+                zv = g.has_z ? zcol[t * XS] : 0.f;
               const float ec = tEc[t];
               float o = 0.f;
 #pragma unroll
@@ -1376,13 +1448,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Tensor map of the C or B rows [B, L, G * R, N] for the chunk kernel's TMA
 // staging: dimensions (n, group row, token, batch), box [32 dims][R ranks][Qt
-// tokens][1], 128-byte swizzle, zero fill outside the tensor.
-cudaError_t rows_tensor_map(CUtensorMap* m, const float* base, const ScanGeom& g) {
+// tokens][1], 128-byte swizzle, zero fill outside the tensor. tok_stride is
+// the distance in floats between consecutive tokens' rows: G * R * N in the
+// C / B tensors, the packed width W when they are column slices of the packed
+// projection.
+cudaError_t rows_tensor_map(CUtensorMap* m, const float* base, const ScanGeom& g,
+                            uint64_t tok_stride) {
   const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
   const uint64_t RG = (uint64_t)g.G * g.R, N = (uint64_t)g.N;
   const cuuint64_t dims[4] = {N, RG, (cuuint64_t)g.L, (cuuint64_t)g.B};
-  const cuuint64_t strides[3] = {N * 4, RG * N * 4, (uint64_t)g.L * RG * N * 4};
+  const cuuint64_t strides[3] = {N * 4, tok_stride * 4, (uint64_t)g.L * tok_stride * 4};
   const cuuint32_t box[4] = {32, (cuuint32_t)g.R, (cuuint32_t)(kRows / g.R), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims,
@@ -1401,7 +1477,7 @@ size_t chunk_smem_bytes(const ChunkLayout& lay, bool async, bool split) {
   return b;
 }
 
-template <int MP, bool MIMO, int KN, int KA, int KR, int KP, bool SPLIT>
+template <int MP, bool MIMO, int KN, int KA, int KR, int KP, bool SPLIT, bool PACKED = false>
 cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, const ChunkIO& io,
                       bool summary, unsigned grid, cudaStream_t s) {
   constexpr bool async = chunk_async(KN, KA);
@@ -1411,12 +1487,20 @@ cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, co
   memset(&tmC, 0, sizeof(tmC));
   memset(&tmB, 0, sizeof(tmB));
   cudaError_t e;
-  if (async) {
-    if ((e = rows_tensor_map(&tmC, a.c, g)) != cudaSuccess) return e;
-    if ((e = rows_tensor_map(&tmB, a.b, g)) != cudaSuccess) return e;
+  if (PACKED) {
+    // B rows at columns [2I, 2I + GRN), C rows at [2I + GRN, 2I + 2GRN) of the
+    // packed rows, which start at a.z (z is the first slice)
+    const float* rows_b = a.z + 2 * (int64_t)g.H * g.P;
+    const float* rows_c = rows_b + (int64_t)g.G * g.R * g.N;
+    if ((e = rows_tensor_map(&tmC, rows_c, g, (uint64_t)g.W)) != cudaSuccess) return e;
+    if ((e = rows_tensor_map(&tmB, rows_b, g, (uint64_t)g.W)) != cudaSuccess) return e;
+  } else if (async) {
+    const uint64_t rgn = (uint64_t)g.G * g.R * g.N;
+    if ((e = rows_tensor_map(&tmC, a.c, g, rgn)) != cudaSuccess) return e;
+    if ((e = rows_tensor_map(&tmB, a.b, g, rgn)) != cudaSuccess) return e;
   }
-  auto kernel = summary ? k_scan_chunk<MP, MIMO, true, KN, KA, KR, KP, SPLIT>
-                        : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP, SPLIT>;
+  auto kernel = summary ? k_scan_chunk<MP, MIMO, true, KN, KA, KR, KP, SPLIT, PACKED>
+                        : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP, SPLIT, PACKED>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, bytes, s>>>(g, a, lay, io, status, tmC, tmB);
@@ -1444,6 +1528,27 @@ cudaError_t dispatch_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* statu
   else
     e = mimo ? run_chunk<128, true, 0, 0, 0, 0, SPLIT>(g, a, status, io, summary, grid, s)
              : run_chunk<128, false, 0, 0, 0, 0, SPLIT>(g, a, status, io, summary, grid, s);
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+// The SISO scan reading the packed projection directly (compile-time TMA
+// shapes P64 N128 with A = 32 or 64 only; the host routes every other shape
+// through the preprocess kernel and a workspace instead).
+bool packed_instance(const ScanGeom& g) {
+  return !g.mimo && g.R == 1 && g.P == 64 && g.N == 128 && (g.A == 32 || g.A == 64);
+}
+template <bool SPLIT>
+cudaError_t dispatch_chunk_packed(const ScanGeom& g, const ScanArgs& a, uint32_t* status,
+                                  const ChunkIO& io, bool summary, cudaStream_t s) {
+  const unsigned grid = (unsigned)(g.B * g.H * io.nseg);
+  cudaError_t e;
+  if (!packed_instance(g)) return cudaErrorInvalidValue;
+  if (g.A == 32)
+    e = run_chunk<64, false, 128, 32, 1, 64, SPLIT, true>(g, a, status, io, summary, grid, s);
+  else
+    e = run_chunk<64, false, 128, 64, 1, 64, SPLIT, true>(g, a, status, io, summary, grid, s);
   if (e != cudaSuccess) return e;
   count_launches(1);
   return cudaGetLastError();

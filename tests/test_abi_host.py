@@ -186,3 +186,30 @@ def test_static_entry_rejects_workspace_above_its_array(lib):
     # invalid geometries are still refused as such
     assert lib.m3_siso_forward_static(ctypes.byref(siso_cfg(head_dim=129)), *([FAKE] * 12),
                                       None) == m3.M3_ERR_INVALID_ARGUMENT
+
+
+def test_packed_entry_checks_both_configs(lib):
+    """m3_siso_forward_packed validates the SsmConfig as m3_siso_forward does
+    and requires a preprocess config that describes the same layer."""
+    cfg = siso_cfg(head_dim=16, state_size=32, num_heads=4, num_groups=2, num_rope_angles=8)
+    good = dict(inner_size=64, state_size=32, num_heads=4, num_rope_angles=8, num_groups=2,
+                mimo_rank=1, epsilon=1e-6, dt_min=1e-3, dt_max=0.1, a_floor=1e-4)
+    n = ctypes.c_size_t(0)
+    pc = m3.preprocess_config(**good)
+    assert lib.m3_siso_forward_packed_workspace(ctypes.byref(cfg), ctypes.byref(pc),
+                                                ctypes.byref(n)) == m3.M3_OK
+    call = lambda c, p, ws=FAKE, wsn=1 << 30: lib.m3_siso_forward_packed(
+        ctypes.byref(c), p, *([FAKE] * 6), ws, wsn, None)
+    assert call(cfg, None) == m3.M3_ERR_INVALID_ARGUMENT
+    for bad in (dict(inner_size=32), dict(state_size=16), dict(num_heads=2),
+                dict(num_rope_angles=4), dict(num_groups=4), dict(mimo_rank=2),
+                dict(epsilon=0.0), dict(dt_min=0.5)):
+        assert call(cfg, ctypes.byref(m3.preprocess_config(**dict(good, **bad)))) == \
+            m3.M3_ERR_INVALID_ARGUMENT, bad
+    assert call(siso_cfg(head_dim=129), ctypes.byref(pc)) == m3.M3_ERR_INVALID_ARGUMENT
+    # a workspace is required (the preprocess outputs live there for this shape)
+    assert n.value > 0
+    assert call(cfg, ctypes.byref(pc), ws=None, wsn=0) == m3.M3_ERR_WORKSPACE
+    assert call(cfg, ctypes.byref(pc), wsn=n.value - 1) == m3.M3_ERR_WORKSPACE
+    assert lib.m3_siso_forward_packed(ctypes.byref(cfg), ctypes.byref(pc), *([FAKE_ODD] * 6),
+                                      FAKE, 1 << 30, None) == m3.M3_ERR_UNALIGNED
