@@ -82,22 +82,42 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+# Sources that make up each kernel the bench reports a roofline for (the
+# traffic figure of a capture is valid only while all of them are unchanged).
+KERNEL_SOURCES = {
+    "k_scan_chunk": ["scan_chunk.cuh", "k_scan_chunk_packed.cu", "tc_ptx.cuh", "m3_internal.cuh"],
+    "k_preprocess": ["k_preprocess.cu", "m3_internal.cuh"],
+    "k_step_bulk": ["k_step.cu", "tc_ptx.cuh", "m3_internal.cuh"],
+}
+
+
+def kernel_source_sha(kernel):
+    """sha1[:12] of the concatenated sources of `kernel` (None if unknown)."""
+    import hashlib
+    files = KERNEL_SOURCES.get(kernel)
+    if not files:
+        return None
+    h = hashlib.sha1()
+    for f in files:
+        path = os.path.join(ROOT, "selective_state_space_mamba3_gb300", "csrc", f)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:12]
+
+
 def read_traffic(kernel):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary
     (profiles/traffic.txt: `<kernel> <source sha1> <bytes per launch> <workload>`),
-    or None when absent or when the kernel's source has changed since."""
-    import hashlib
+    or None when absent or when the kernel's sources have changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
+    sha = kernel_source_sha(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
-            src = os.path.join(ROOT, "selective_state_space_mamba3_gb300", "csrc", parts[0] + ".cu")
-            if not os.path.exists(src):
-                return None
-            sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
-            return float(parts[2]) if sha == parts[1] else None
+            return float(parts[2]) if sha is not None and sha == parts[1] else None
     return None
 
 
@@ -416,23 +436,31 @@ def parts_scan(torch, m3, w, mode, peak):
             "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4)}
 
 
-def parts_step(torch, m3, peak):
-    """Supplementary: decode step at B256 H32 P64 N128 A32, 512 single-token
+def parts_step(torch, m3, peak, mimo=False):
+    """Supplementary: decode step at B256 H32 P64 N128 A32 (SISO), or the MIMO
+    step at B256 H32 P64 N64 A32 R4 with the output norm, 512 single-token
     calls cycling over 32 distinct token inputs, states resident on the device."""
     w = gen.DECODE_STEP
+    if mimo:
+        w = w.with_(name="MIMO decode step B256 H32 G1 P64 N64 A32 R4 norm x512", state_size=64,
+                    mimo_rank=4, has_output_norm=1)
     ins = gen.decode_inputs(w, steps=32)
     seq = {k: torch.from_numpy(ins[k]).cuda() for k in ("c", "b", "x", "z", "adt", "dt", "trap", "angle")}
     toks = [[seq[k][:, t:t + 1].contiguous() for k in ("c", "b", "x", "z", "adt", "dt", "trap", "angle")]
             for t in range(32)]
-    par = [torch.from_numpy(ins[k]).cuda() for k in ("c_bias", "b_bias", "d")]
-    B, H, P, N, A = w.batch_size, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
-    st = [torch.zeros(s, device="cuda") for s in ((B, H, P, N), (B, H, A), (B, H, N), (B, H, P))]
+    pkeys = ("c_bias", "b_bias", "d") + (("mimo_x", "mimo_z", "mimo_o", "norm_weight") if mimo else ())
+    par = [torch.from_numpy(ins[k]).cuda() for k in pkeys]
+    B, H, P, N, A, R = (w.batch_size, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles,
+                        w.mimo_rank)
+    st = [torch.zeros(s, device="cuda") for s in ((B, H, P, N), (B, H, A), (B, H, R, N),
+                                                  (B, H, R, P))]
     out = torch.empty(B, 1, H, P, device="cuda")
     cfg = m3.ssm_config(w.cfg(sequence_length=1))
+    step = m3.m3_mimo_step if mimo else m3.m3_siso_step
     i = [0]
 
     def fn():
-        m3.m3_siso_step(cfg, *toks[i[0] % 32], *par, *st, out)
+        step(cfg, *toks[i[0] % 32], *par, *st, out)
         i[0] += 1
     for _ in range(5):
         fn()
@@ -441,6 +469,31 @@ def parts_step(torch, m3, peak):
     return {"workload": w.name, "ms_per_call": round(ms, 4),
             "tokens_per_s": round(B / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
             "frac_hbm": round(gbs / peak, 4)}
+
+
+def parts_prefill(torch, m3, w, peak):
+    """Supplementary: m3_siso_prefill over the 1B-layer workload in TF32 mode,
+    from a zero step state, writing the final ssm / angle / k / v states (the
+    prefill -> decode hand-off). Algorithmic bytes: the scan's, plus the four
+    states written once (and read once as the entry state)."""
+    ins = gen.scan_inputs(w)
+    d = {k: torch.from_numpy(v).cuda() for k, v in ins.items()}
+    del ins
+    B, H, P, N, A = w.batch_size, w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    cfg = m3.ssm_config(w.cfg(), m3.M3_MATH_TF32)
+    ws = torch.empty(max(m3.m3_siso_prefill_workspace(cfg), 16), dtype=torch.uint8, device="cuda")
+    st = [torch.zeros(s, device="cuda") for s in ((B, H, P, N), (B, H, A), (B, H, N), (B, H, P))]
+    out = torch.empty_like(d["x"])
+    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d")
+    fn = lambda: m3.m3_siso_prefill(cfg, *[d[k] for k in keys], *st, out, ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 10)
+    nbytes = w.tokens * bytes_per_token_scan(w) + 2 * 4 * B * H * (P * N + A + N + P)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name + " prefill", "mode": "tf32", "ms": round(ms, 4),
+            "tokens_per_s": round(w.tokens / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4), "algorithmic_bytes": nbytes}
 
 
 def cpu_baseline_oracle(w, batch_rows):
@@ -586,6 +639,8 @@ def run_m3(args):
                 parts[f"{key}_{mname}"] = parts_scan(torch, m3, wl, mcode, peak)
                 torch.cuda.empty_cache()
         parts["siso_step"] = parts_step(torch, m3, peak)
+        parts["mimo_step"] = parts_step(torch, m3, peak, mimo=True)
+        parts["siso_prefill_tf32"] = parts_prefill(torch, m3, gen.SISO_1B, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -221,12 +221,28 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
 // rho of the transposed key tile. Step i stores component (i + rot) & 3: with
 // the phase-(4) lane mapping and rot = 2 * (lane / 16) + (lane / 4) % 2, the
 // 32 lanes' stores of one step land in 32 distinct banks.
+// Paired FP32 arithmetic (FADD2 / FMUL2 / FFMA2: two IEEE single-precision
+// operations per instruction) on the (x, y) and (z, w) halves of float4s.
+__device__ __forceinline__ float4 cat4(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return cat4(__fadd2_rn(lo2(a), lo2(b)), __fadd2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+  return cat4(__fmul2_rn(lo2(a), lo2(b)), __fmul2_rn(hi2(a), hi2(b)));
+}
+__device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
+  return cat4(__ffma2_rn(lo2(a), lo2(b), lo2(c)), __ffma2_rn(hi2(a), hi2(b), hi2(c)));
+}
+
 // Split operands: the low part (the rounded remainder) of each value goes to
 // the same position LO floats further on.
 template <bool SPLIT>
 __device__ __forceinline__ void store_kt4(float* kt, int LO, int n0, int rho, float4 v, float w,
                                           int rot) {
-  const float p0 = w * v.x, p1 = w * v.y, p2 = w * v.z, p3 = w * v.w;
+  const float4 pw = mul4(v, make_float4(w, w, w, w));
+  const float p0 = pw.x, p1 = pw.y, p2 = pw.z, p3 = pw.w;
   const float a0 = SPLIT ? tc::tf32_clean(p0) : tc::tf32_feed(p0);
   const float a1 = SPLIT ? tc::tf32_clean(p1) : tc::tf32_feed(p1);
   const float a2 = SPLIT ? tc::tf32_clean(p2) : tc::tf32_feed(p2);
@@ -283,6 +299,28 @@ __device__ __forceinline__ void put4(float* dst, int LO, float4 v) {
 // SiLU with the hardware exp / divide approximations (relative error a few
 // float32 ulps, far inside the scan tolerances).
 __device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+// SFU base-2 exponential and reciprocal (PTX ex2.approx / rcp.approx).
+__device__ __forceinline__ float ex2_sfu(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float rcp_sfu(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+// y * silu(z) = y z / (1 + 2^(-z log2 e)) for four values: the exponential
+// and the reciprocal on the SFU, the rest as paired FP32 operations (relative
+// error a few float32 units, like the scalar silu_fast).
+__device__ __forceinline__ float4 gate4(float4 y, float4 z) {
+  const float l2e = -1.4426950408889634f;
+  const float4 a = mul4(z, make_float4(l2e, l2e, l2e, l2e));
+  const float4 e = make_float4(ex2_sfu(a.x), ex2_sfu(a.y), ex2_sfu(a.z), ex2_sfu(a.w));
+  const float4 d = add4(e, make_float4(1.f, 1.f, 1.f, 1.f));
+  const float4 r = make_float4(rcp_sfu(d.x), rcp_sfu(d.y), rcp_sfu(d.z), rcp_sfu(d.w));
+  return mul4(y, mul4(z, r));
+}
 
 template <int MP, bool MIMO, bool SUMMARY, int KN, int KA, int KR, int KP, bool SPLIT,
           bool PACKED>
@@ -342,6 +380,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   constexpr bool kStagedEpi = !MIMO && !SUMMARY && KP > 0 && KP % 4 == 0 && KP <= 64;
   constexpr bool kBAtEpi = kAsync && !kEarlyB && kStagedEpi;
   float* sStage = kBAtEpi ? sKt : sP;  // [t][P] pre-gate output rows
+  // Row t starts at t * P + 16 (t / 8) (in the transposed key tile, which has
+  // room): lanes l and l + 16 stage tokens t and t + 8 of the same column, and
+  // the extra 16 floats per group of 8 rows put their stores in different
+  // banks while keeping the rows disjoint and 16-byte aligned.
+  constexpr int kStageSkew = kBAtEpi ? 16 : 0;
   float* sTot = sm + lay.tot;          // [8 warps][64]   per-warp angle totals
   float* sTotAdt = sTot + kWarps * kAngMax;  // [8 warps] per-warp log-decay totals
   float* sBiasC = sm + lay.bias;       // [R][Npad]
@@ -536,7 +579,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     const int tw = TPW * warp + lane;
     float dtv = 0.f, adtv = 0.f, gam = 0.f, scl = 0.f;
     if (lane <= TPW) {
-      const float lam = sigmoid_f(pl.trap);
+      // (single pass: SFU exponential and division; split: the accurate ones)
+      const float lam = SPLIT ? sigmoid_f(pl.trap) : __fdividef(1.0f, 1.0f + __expf(-pl.trap));
       if (c0 + tw < L) scl = (1.0f - lam) * pl.dt;
       if (tw < tv && lane < TPW) {
         dtv = pl.dt;
@@ -558,14 +602,15 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       for (int o = 1; o < 8; o <<= 1) aab += __shfl_xor_sync(0xffffffffu, aab, o);
       if (lane == 0) sAbsAdt[warp] = aab;
     }
-    float thl[2][8];
+    float thl[2][8], dsh[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dsh[i] = __shfl_sync(0xffffffffu, dtv, i);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       float s = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float d = __shfl_sync(0xffffffffu, dtv, i);
-        if (i < TPW) s = fmaf(d, pl.ang[2 * i + j], s);
+        if (i < TPW && 32 * j < A) s = fmaf(dsh[i], pl.ang[2 * i + j], s);
         thl[j][i] = s;
       }
       const int aa = lane + 32 * j;
@@ -598,15 +643,16 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     const float lg_new = lazy ? lgE + cend : 0.f;
     const float cum = cbase + cl;
     const float wt = gam + __shfl_down_sync(0xffffffffu, scl, 1);
-    const float om = (lane < TPW && tw < tv) ? expf(cend - cum - lg_new) * wt : 0.f;
+    auto xpf = [](float v) { return SPLIT ? expf(v) : __expf(v); };
+    const float om = (lane < TPW && tw < tv) ? xpf(cend - cum - lg_new) * wt : 0.f;
     if (lane < TPW) {
       tCum[tw] = cum;
-      tEc[tw] = expf(cum + lgE);
+      tEc[tw] = xpf(cum + lgE);
       tGam[tw] = gam;
       tW[tw] = wt;
       if (kFactMask) {
-        tEa[tw] = expf(cum);
-        tEb[tw] = expf(-cum) * wt;
+        tEa[tw] = xpf(cum);
+        tEb[tw] = xpf(-cum) * wt;
       }
     }
     // the previous chunk's state update must finish before its tiles are
@@ -647,7 +693,21 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       // low part of the state for this chunk's Yo: G - trunc(G), rounded (the
       // MMA reads G itself truncated to TF32 as the high part); made visible
       // to the MMAs by the block barrier that precedes them
-      for (int c = 16 * wg; c < Npad; c += 64) {
+      if (MP == 64 && 32 * wg < Npad) {
+        float v0[16], v1[16];
+        const bool two = 32 * wg + 64 < Npad;
+        tc::tmem_ld_m64_16(tG + lane_base + 32 * wg, v0);
+        if (two) tc::tmem_ld_m64_16(tG + lane_base + 32 * wg + 64, v1);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v0[j] = tc::tf32_feed(v0[j] - tc::tf32_trunc(v0[j]));
+          v1[j] = tc::tf32_feed(v1[j] - tc::tf32_trunc(v1[j]));
+        }
+        tc::tmem_st_m64_16(tGl + lane_base + 32 * wg, v0);
+        if (two) tc::tmem_st_m64_16(tGl + lane_base + 32 * wg + 64, v1);
+      }
+      if (MP == 128) for (int c = 16 * wg; c < Npad; c += 64) {
         float v0[16], v1[16];
         const bool two = c + 32 < Npad;
         tc::tmem_ld16x2(tG + lane_base + c, tG + lane_base + (two ? c + 32 : c), v0, v1);
@@ -683,24 +743,25 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           const float4 cbw = *reinterpret_cast<const float4*>(cb + n0 + A);
           const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
           const float4 bbw = *reinterpret_cast<const float4*>(bb + n0 + A);
-#define M3_ROT(E)                                                            \
-  {                                                                          \
-    float sn, cs;                                                            \
-    if constexpr (kCosSin) {                                                 \
-      cs = th.E;                                                             \
-      sn = sv.E;                                                             \
-    } else {                                                                 \
-      sincos_fast(th.E, &sn, &cs);                                           \
-    }                                                                        \
-    const float qu = cu.E + cbu.E, qw = cw.E + cbw.E;                        \
-    const float ku = bu.E + bbu.E, kw = bw.E + bbw.E;                        \
-    q0.E = qu * cs - qw * sn;                                                \
-    q1.E = qu * sn + qw * cs;                                                \
-    k0.E = ku * cs - kw * sn;                                                \
-    k1.E = ku * sn + kw * cs;                                                \
-  }
-          M3_ROT(x) M3_ROT(y) M3_ROT(z) M3_ROT(w)
-#undef M3_ROT
+          float4 cs4, sn4;
+          if constexpr (kCosSin) {
+            cs4 = th;
+            sn4 = sv;
+          } else {
+            sincos_fast(th.x, &sn4.x, &cs4.x);
+            sincos_fast(th.y, &sn4.y, &cs4.y);
+            sincos_fast(th.z, &sn4.z, &cs4.z);
+            sincos_fast(th.w, &sn4.w, &cs4.w);
+          }
+          const float4 nsn4 = make_float4(-sn4.x, -sn4.y, -sn4.z, -sn4.w);
+          // biased pair (u, w) = (C + c_bias, its partner); rotated:
+          // (u cos - w sin, u sin + w cos), likewise for the key
+          const float4 qu = add4(cu, cbu), qw = add4(cw, cbw);
+          const float4 ku = add4(bu, bbu), kw = add4(bw, bbw);
+          q0 = fma4(qu, cs4, mul4(qw, nsn4));
+          q1 = fma4(qu, sn4, mul4(qw, cs4));
+          k0 = fma4(ku, cs4, mul4(kw, nsn4));
+          k1 = fma4(ku, sn4, mul4(kw, cs4));
         }
         if (!SUMMARY) {
           put4<SPLIT>(sQ + toff(rho, n0), LO, q0);
@@ -721,8 +782,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
         if (in) {
           const float4 cbu = *reinterpret_cast<const float4*>(cb + n0);
           const float4 bbu = *reinterpret_cast<const float4*>(bb + n0);
-          qv = make_float4(cu.x + cbu.x, cu.y + cbu.y, cu.z + cbu.z, cu.w + cbu.w);
-          kv = make_float4(bu.x + bbu.x, bu.y + bbu.y, bu.z + bbu.z, bu.w + bbu.w);
+          qv = add4(cu, cbu);
+          kv = add4(bu, bbu);
         }
         if (!SUMMARY) {
           put4<SPLIT>(sQ + toff(rho, n0), LO, qv);
@@ -764,24 +825,38 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           float inv_c = 1.f, inv_b = 1.f;
           if constexpr (PACKED) {
             static_assert(KA % 16 == 0 && KN <= 128, "group classes need A % 16 == 0");
+            // sums of squares of the lane's groups (C and B rows in the two
+            // halves of each paired FMA chain: per lane the preprocess's chain)
             float sc[8], sb[8];
 #pragma unroll
             for (int m = 0; m < 8; ++m) sc[m] = sb[m] = 0.f;
+            auto sumsq2 = [](float4 u, float4 v, float& su, float& sv) {
+              float2 r = __fmul2_rn(make_float2(u.x, v.x), make_float2(u.x, v.x));
+              r = __ffma2_rn(make_float2(u.y, v.y), make_float2(u.y, v.y), r);
+              r = __ffma2_rn(make_float2(u.z, v.z), make_float2(u.z, v.z), r);
+              r = __ffma2_rn(make_float2(u.w, v.w), make_float2(u.w, v.w), r);
+              su = r.x;
+              sv = r.y;
+            };
 #pragma unroll
             for (int jb = 0; jb < QW4; ++jb) {
               if (jb < PQ / 4) {  // rotary item: groups j and j + A/4 (m = jb, jb + A/16)
                 const int n0 = 16 * jb + 4 * jl;
+                const float4 bu = *reinterpret_cast<const float4*>(sK + toff(rho, n0));
+                const float4 bw = *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A));
                 if (!SUMMARY) {
-                  sc[jb] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)));
-                  sc[jb + KA / 16] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A)));
+                  const float4 cu = *reinterpret_cast<const float4*>(sQ + toff(rho, n0));
+                  const float4 cw = *reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A));
+                  sumsq2(cu, bu, sc[jb], sb[jb]);
+                  sumsq2(cw, bw, sc[jb + KA / 16], sb[jb + KA / 16]);
+                } else {
+                  sumsq2(bu, bw, sb[jb], sb[jb + KA / 16]);
                 }
-                sb[jb] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0)));
-                sb[jb + KA / 16] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0 + A)));
               } else {            // plain item: group A/4 + j (m = A/16 + jb)
                 const int n0 = KA + 16 * jb + 4 * jl;
-                if (!SUMMARY)
-                  sc[KA / 16 + jb] = sumsq4(*reinterpret_cast<const float4*>(sQ + toff(rho, n0)));
-                sb[KA / 16 + jb] = sumsq4(*reinterpret_cast<const float4*>(sK + toff(rho, n0)));
+                const float4 bu = *reinterpret_cast<const float4*>(sK + toff(rho, n0));
+                const float4 cu = SUMMARY ? bu : *reinterpret_cast<const float4*>(sQ + toff(rho, n0));
+                sumsq2(cu, bu, sc[KA / 16 + jb], sb[KA / 16 + jb]);
               }
             }
             auto tree = [](const float* v) {
@@ -793,10 +868,16 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
             tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 16));
             tcs = __fadd_rn(tcs, __shfl_xor_sync(0xffffffffu, tcs, 8));
             tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 8));
-            inv_c = rms_inv(tcs, N, g.eps);
-            inv_b = rms_inv(tbs, N, g.eps);
+            // the four lanes of a row hold both totals: lanes with an even jl
+            // invert the C total, odd ones the B total, and exchange
+            const float r = rms_inv((jl & 1) ? tbs : tcs, N, g.eps);
+            inv_c = __shfl_sync(0xffffffffu, r, lane & ~8);
+            inv_b = __shfl_sync(0xffffffffu, r, lane | 8);
           }
           // (the raw row times its inverse RMS, as the preprocess writes it)
+          // (scalar __fmul_rn: never merged with the bias add that follows, so
+          // the normalised value is rounded on its own, as the preprocess
+          // stores it)
           auto nrm = [&](float4 v, float inv) -> float4 {
             if constexpr (PACKED)
               return make_float4(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv), __fmul_rn(v.z, inv),
@@ -1018,18 +1099,15 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
         const float gam_t = tGam[t];
         const float ea_t = kFactMask ? tEa[t] : 0.f;
         const int sh = lane >> 4;
-        float sv[2][16];
-        tc::tmem_ld16x2(tS + lane_base + 32 * wg, tS + lane_base + 32 * wg + 16, sv[0], sv[1]);
+        // lane l and l + 16 share row rho: columns cb * 16 + 8 * sh .. + 8
+        float sv[2][8];
+        tc::tmem_ld_m64_8x2(tS + lane_base + 32 * wg, tS + lane_base + 32 * wg + 16, sv[0], sv[1]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int cb = 2 * wg + u;
-          const float* v = sv[u];
           float w8[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float hi = __shfl_sync(0xffffffffu, v[j + 8], lane & 15);
-            w8[j] = sh ? hi : v[j];
-          }
+          for (int j = 0; j < 8; ++j) w8[j] = sv[u][j];
           const int col0 = cb * 16 + 8 * sh;
           // coefficients of the 8 key tokens of these columns (vector loads
           // when a row is a token)
@@ -1054,16 +1132,39 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
               if (!fact) cs[j] = tCum[(col0 + j) >> lgR];
             }
           }
+          if constexpr (KR == 1) {
+            // a row is a token: columns before the diagonal position kd take
+            // S e^{cum_t - cum_s} w_s, the diagonal gamma_t S + D (the D skip
+            // rides on the diagonal: Yi then includes D * x), later ones zero
+            const int kd = rho - col0;
+            float pr[8];
+            if (fact) {
+              const float4 e4 = make_float4(ea_t, ea_t, ea_t, ea_t);
+              const float4 m0 = mul4(make_float4(ws[0], ws[1], ws[2], ws[3]), e4);
+              const float4 m1 = mul4(make_float4(ws[4], ws[5], ws[6], ws[7]), e4);
+              const float4 p0 = mul4(make_float4(w8[0], w8[1], w8[2], w8[3]), m0);
+              const float4 p1 = mul4(make_float4(w8[4], w8[5], w8[6], w8[7]), m1);
+              pr[0] = p0.x; pr[1] = p0.y; pr[2] = p0.z; pr[3] = p0.w;
+              pr[4] = p1.x; pr[5] = p1.y; pr[6] = p1.z; pr[7] = p1.w;
+            } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int s = (col0 + j) >> lgR;
-            float m = 0.f;
-            if (s < t)
-              m = fact ? ea_t * ws[j] : __expf(cum_t - cs[j]) * ws[j];
-            else if (s == t)
-              m = gam_t;
-            // the D skip rides on the diagonal: Yi then includes D * x
-            w8[j] = col0 + j == rho ? fmaf(w8[j], m, dsk) : w8[j] * m;
+              for (int j = 0; j < 8; ++j) pr[j] = w8[j] * (__expf(cum_t - cs[j]) * ws[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              w8[j] = j < kd ? pr[j] : (j == kd ? fmaf(w8[j], gam_t, dsk) : 0.f);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int s = (col0 + j) >> lgR;
+              float m = 0.f;
+              if (s < t)
+                m = fact ? ea_t * ws[j] : __expf(cum_t - cs[j]) * ws[j];
+              else if (s == t)
+                m = gam_t;
+              // the D skip rides on the diagonal: Yi then includes D * x
+              w8[j] = col0 + j == rho ? fmaf(w8[j], m, dsk) : w8[j] * m;
+            }
           }
           put4<SPLIT>(sP + tc::kmaj(rho, col0, kRows), LO, make_float4(w8[0], w8[1], w8[2], w8[3]));
           put4<SPLIT>(sP + tc::kmaj(rho, col0 + 4, kRows), LO,
@@ -1112,9 +1213,25 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
         }
       }
       const float ec = expf(lgE + cend);
-      // two 16-column blocks per pass: one wait per pair of loads, stores
-      // unwaited until the end
-      if (!lazy) for (int c = 16 * wg; c < Npad; c += 64) {
+      // M = 64 state (P <= 64): the half-split loads give each thread 16 useful
+      // columns of its row; warp group wg takes the 32-column blocks 32 wg and
+      // 32 wg + 64. M = 128: two 16-column blocks per pass. One wait per pair
+      // of loads, stores unwaited until the end.
+      if (!lazy && MP == 64 && 32 * wg < Npad) {
+        float v0[16], v1[16];
+        const bool two = 32 * wg + 64 < Npad;
+        tc::tmem_ld_m64_16(tG + lane_base + 32 * wg, v0);
+        if (two) tc::tmem_ld_m64_16(tG + lane_base + 32 * wg + 64, v1);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          v0[j] = SPLIT ? v0[j] * ec : tc::tf32_clean(v0[j] * ec);
+          v1[j] = SPLIT ? v1[j] * ec : tc::tf32_clean(v1[j] * ec);
+        }
+        tc::tmem_st_m64_16(tG + lane_base + 32 * wg, v0);
+        if (two) tc::tmem_st_m64_16(tG + lane_base + 32 * wg + 64, v1);
+      }
+      if (!lazy && MP == 128) for (int c = 16 * wg; c < Npad; c += 64) {
         float v0[16], v1[16];
         const bool two = c + 32 < Npad;
         tc::tmem_ld16x2(tG + lane_base + c, tG + lane_base + (two ? c + 32 : c), v0, v1);
@@ -1258,18 +1375,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
 #pragma unroll
         for (int cb = 2 * wg; cb < 2 * wg + 2; ++cb) {
           float yo[16], yi[16];
-          tc::tmem_ld16x2(tYo + lane_base + cb * 16, tS + lane_base + cb * 16, yo, yi);
-          if (MP == 64) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float ho = __shfl_sync(0xffffffffu, yo[j + 8], lane & 15);
-              const float hi = __shfl_sync(0xffffffffu, yi[j + 8], lane & 15);
-              if (half) {
-                yo[j] = ho;
-                yi[j] = hi;
-              }
-            }
-          }
+          if constexpr (MP == 64)  // lane l + 16: the upper 8 columns of row l's block
+            tc::tmem_ld_m64_8x2(tYo + lane_base + cb * 16, tS + lane_base + cb * 16, yo, yi);
+          else
+            tc::tmem_ld16x2(tYo + lane_base + cb * 16, tS + lane_base + cb * 16, yo, yi);
           if (!pvalid) continue;
           const int col0 = cb * 16 + 8 * half;
           if (!mimo) {
@@ -1283,14 +1392,22 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
               ec[4 * q + 2] = e4.z;
               ec[4 * q + 3] = e4.w;
             }
+            float yv[kCols];
+#pragma unroll
+            for (int j = 0; j < kCols; j += 2) {
+              const float2 r = __ffma2_rn(make_float2(ec[j], ec[j + 1]), make_float2(yo[j], yo[j + 1]),
+                                          make_float2(yi[j], yi[j + 1]));
+              yv[j] = r.x;
+              yv[j + 1] = r.y;
+            }
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int t = col0 + j;
               if (kStaged) {
-                sStage[t * KP + prow] = fmaf(ec[j], yo[j], yi[j]);
+                sStage[t * KP + prow + kStageSkew * (t >> 3)] = yv[j];
               } else if (t < tv) {
                 const float zv = u ? ze[1][j] : ze[0][j];
-                float y = fmaf(ec[j], yo[j], yi[j]);
+                float y = yv[j];
                 if (g.has_z) y *= silu_fast(zv);
                 ocol[t * HP] = y;
               }
@@ -1332,13 +1449,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           const int unit = tid + kThreads * k;
           const int t = unit / kRowQ, p0 = 4 * (unit % kRowQ);
           if (t < tv) {
-            float4 y = *reinterpret_cast<const float4*>(sStage + t * KP + p0);
-            if (g.has_z) {
-              y.x *= silu_fast(zq[k].x);
-              y.y *= silu_fast(zq[k].y);
-              y.z *= silu_fast(zq[k].z);
-              y.w *= silu_fast(zq[k].w);
-            }
+            float4 y = *reinterpret_cast<const float4*>(sStage + t * KP + kStageSkew * (t >> 3) + p0);
+            if (g.has_z) y = gate4(y, zq[k]);
             *reinterpret_cast<float4*>(a.out + (tok0 + t) * HP + (int64_t)h * P + p0) = y;
           }
         }
