@@ -10,7 +10,10 @@ CPU oracle baseline, an end-to-end figure with host buffers, sampled clocks,
 and supplementary timings of the MIMO and decode-step entry points.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
-                [--mode fp32|tf32] [--no-parts]
+                [--mode fp32|tf32] [--no-parts] [--part NAME]
+--part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
+mimo_scan_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
+mimo_step, siso_prefill_tf32) and prints its JSON, for profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -523,6 +526,35 @@ def cpu_baseline_oracle(w, batch_rows):
             "seconds": round(dt, 3)}
 
 
+def part_by_name(torch, m3, name, peak):
+    """One supplementary part, by its key in the JSON line's `parts`."""
+    table = {
+        "siso_scan_fp32": lambda: parts_scan(torch, m3, gen.SISO_1B, m3.M3_MATH_FP32, peak),
+        "mimo_scan_fp32": lambda: parts_scan(torch, m3, gen.MIMO_R4, m3.M3_MATH_FP32, peak),
+        "mimo_scan_tf32": lambda: parts_scan(torch, m3, gen.MIMO_R4, m3.M3_MATH_TF32, peak),
+        "siso_long_scan_fp32": lambda: parts_scan(torch, m3, gen.SISO_LONG, m3.M3_MATH_FP32, peak),
+        "siso_long_scan_tf32": lambda: parts_scan(torch, m3, gen.SISO_LONG, m3.M3_MATH_TF32, peak),
+        "siso_step": lambda: parts_step(torch, m3, peak),
+        "mimo_step": lambda: parts_step(torch, m3, peak, mimo=True),
+        "siso_prefill_tf32": lambda: parts_prefill(torch, m3, gen.SISO_1B, peak),
+    }
+    if name not in table:
+        raise SystemExit(f"bench.py: unknown part {name!r}; one of {sorted(table)}")
+    return table[name]()
+
+
+def run_part(args):
+    """--part NAME: one supplementary part alone (for profiling it)."""
+    import torch
+    import selective_state_space_mamba3_gb300 as m3
+    from selective_state_space_mamba3_gb300 import build as m3build
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    m3build.build()
+    m3.load_library()
+    peak, _ = load_peaks()
+    print(json.dumps({"part": args.part, **part_by_name(torch, m3, args.part, peak)}), flush=True)
+
+
 def run_m3(args):
     import torch
     import selective_state_space_mamba3_gb300 as m3
@@ -632,15 +664,10 @@ def run_m3(args):
     del s
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_parts:
-        parts["siso_scan_fp32"] = parts_scan(torch, m3, gen.SISO_1B, m3.M3_MATH_FP32, peak)
-        torch.cuda.empty_cache()
-        for key, wl in (("mimo_scan", gen.MIMO_R4), ("siso_long_scan", gen.SISO_LONG)):
-            for mname, mcode in (("fp32", m3.M3_MATH_FP32), ("tf32", m3.M3_MATH_TF32)):
-                parts[f"{key}_{mname}"] = parts_scan(torch, m3, wl, mcode, peak)
-                torch.cuda.empty_cache()
-        parts["siso_step"] = parts_step(torch, m3, peak)
-        parts["mimo_step"] = parts_step(torch, m3, peak, mimo=True)
-        parts["siso_prefill_tf32"] = parts_prefill(torch, m3, gen.SISO_1B, peak)
+        for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "siso_long_scan_fp32",
+                     "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32"):
+            parts[name] = part_by_name(torch, m3, name, peak)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -723,6 +750,7 @@ def main():
     ap.add_argument("--no-parts", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=8)
+    ap.add_argument("--part", default=None)
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if "WORLD_SIZE" not in os.environ and args.gpus > 1:
@@ -733,6 +761,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.part:
+        run_part(args)
     else:
         run_m3(args)
 

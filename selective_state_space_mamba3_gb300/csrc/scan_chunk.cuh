@@ -146,7 +146,7 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async, bool
   l.lo = split_ops ? (off + 255) / 256 * 256 : 0;
   if (split_ops) off = 2 * l.lo;
   l.tot = take(kWarps * kAngMax + 2 * kWarps);  // per-warp angle, log-decay, |log-decay| totals
-  l.bias = take(2 * R * l.Npad);            // c_bias, b_bias of this head, zero-padded
+  l.bias = take(2 * R * (l.Npad + 4));      // c_bias, b_bias of this head, zero-padded rows
   l.tok = take(6 * kTok);                   // cum, e^{cum + lgE}, gamma, w, e^cum, e^-cum w
   l.thbase = take(2 * kAngMax);             // cumulative angle at the chunk start (x2)
   // per-warp angles [TPW][A + 4] (TMA staging with A <= 32); MIMO keeps their
@@ -387,8 +387,11 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   constexpr int kStageSkew = kBAtEpi ? 16 : 0;
   float* sTot = sm + lay.tot;          // [8 warps][64]   per-warp angle totals
   float* sTotAdt = sTot + kWarps * kAngMax;  // [8 warps] per-warp log-decay totals
-  float* sBiasC = sm + lay.bias;       // [R][Npad]
-  float* sBiasB = sBiasC + R * Npad;   // [R][Npad]
+  // bias rows of Npad + 4 floats: the ranks of a row block read the same
+  // columns at once, and the extra 16 bytes per row put them on different banks
+  const int BS = Npad + 4;
+  float* sBiasC = sm + lay.bias;       // [R][BS]
+  float* sBiasB = sBiasC + R * BS;     // [R][BS]
   float* tCum = sm + lay.tok;          // local cumulative log decay
   float* tEc = tCum + kTok;            // e^{cum_t}
   float* tGam = tEc + kTok;            // gamma_t
@@ -420,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   constexpr uint32_t kTmemCols = SPLIT ? 512 : 256;
   if (warp == 0) tc::tmem_alloc(&tmem_slot, kTmemCols);
   for (int i = tid; i < A; i += kThreads) sThBase[i] = io.th0 ? io.th0[(int64_t)cta * A + i] : 0.f;
-  for (int i = tid; i < R * Npad; i += kThreads) {
-    const int r = i / Npad, n = i - r * Npad;
+  for (int i = tid; i < R * BS; i += kThreads) {
+    const int r = i / BS, n = i - r * BS;
     sBiasC[i] = n < N ? a.c_bias[((int64_t)h * R + r) * N + n] : 0.f;
     sBiasB[i] = n < N ? a.b_bias[((int64_t)h * R + r) * N + n] : 0.f;
   }
@@ -730,8 +733,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       const int ti = t - TPW * warp;  // token index within the warp
       const float omr = __shfl_sync(0xffffffffu, om, ti);
       const int krot = 2 * (lane >> 4) + ((lane >> 2) & 1);  // store order of the Kt rows
-      const float* cb = sBiasC + r * Npad;
-      const float* bb = sBiasB + r * Npad;
+      const float* cb = sBiasC + r * BS;
+      const float* bb = sBiasB + r * BS;
       float* kl = last_chunk && t == tv - 1 ? io.k_last + ((int64_t)bh * R + r) * N : nullptr;
       // Rotary item: dims n0..n0+3 and their partners n0+A..n0+A+3.
       // th: the four angles (or, with kCosSin, their cosines; sv their sines)
@@ -798,15 +801,23 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
         const int PQ = A >> 2, QW = PQ + ((N - 2 * A) >> 2), QW4 = (QW + 3) >> 2;
         // angles of this lane's rotary items, read before the q rows (which
         // share this warp's angle block) are written
+        // Compile-time shapes with A a multiple of 16 and N of 4: item step jb
+        // holds rotary pairs exactly when jb < A / 16 and real dims when
+        // jb < QW / 4, whatever the lane, so the item kind is known per step.
+        constexpr bool kStaticItems = KA > 0 && KA % 16 == 0 && KN > 0 && KN % 4 == 0;
+        constexpr int kPairSteps = kStaticItems ? KA / 16 : 0;
+        constexpr int kSteps = kStaticItems ? (KA / 4 + (KN - 2 * KA) / 4) / 4 : 0;
+        auto is_pair = [&](int jb, int j) { return kStaticItems ? jb < kPairSteps : j < PQ; };
+        auto is_item = [&](int jb, int j) { return kStaticItems ? jb < kSteps : j < QW; };
         float4 th4[4], sn4[kCosSin ? 4 : 1];
 #pragma unroll
         for (int jb = 0; jb < 4; ++jb) {
           const int j = 4 * jb + jl;
-          th4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(thp(ti * AS + 4 * j))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+          th4[jb] = is_pair(jb, j) ? *reinterpret_cast<const float4*>(thp(ti * AS + 4 * j))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
           if constexpr (kCosSin)
-            sn4[jb] = (j < PQ) ? *reinterpret_cast<const float4*>(sTh + TPW * AS + ti * AS + 4 * j)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            sn4[jb] = is_pair(jb, j) ? *reinterpret_cast<const float4*>(sTh + TPW * AS + ti * AS + 4 * j)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         __syncwarp();
         if (kAsync) {
@@ -888,8 +899,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
 #pragma unroll
           for (int jb = 0; jb < QW4; ++jb) {
             const int j = 4 * jb + jl;
-            if (j >= QW) continue;
-            if (j < PQ) {
+            if (!is_item(jb, j)) continue;
+            if (is_pair(jb, j)) {
               const int n0 = 4 * j;
               float4 th;
               float4 sv = make_float4(0.f, 0.f, 0.f, 0.f);
