@@ -67,7 +67,7 @@ __device__ __forceinline__ void stage_step(StepSmem<RMAX>& sm, const ScanGeom& g
         const float ku = a.b[row + n] + bb[n], kv = a.b[row + n + A] + bb[n + A];
         if (r == 0) sm.theta[n] = th;
         float sn, cs;
-        sincosf(th, &sn, &cs);
+        sincos_fast(th, &sn, &cs);
         sm.q[r * N + n] = qu * cs - qv * sn;
         sm.q[r * N + n + A] = qu * sn + qv * cs;
         sm.k[r * N + n] = ku * cs - kv * sn;
@@ -147,7 +147,7 @@ __device__ __forceinline__ void step_output(StepSmem<RMAX>& sm, const ScanGeom& 
 // cp.async.bulk transfers of P * N * 4 bytes (a multiple of 16; the state base
 // is 16-byte aligned by the host checks).
 template <int RMAX>
-__global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : 4) k_step_bulk(ScanGeom g, ScanArgs a, StepState st) {
+__global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : (RMAX == 4 ? 5 : 4)) k_step_bulk(ScanGeom g, ScanArgs a, StepState st) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   StepSmem<RMAX>& sm = *reinterpret_cast<StepSmem<RMAX>*>(smem_raw);
   float* hsm = reinterpret_cast<float*>(smem_raw + step_smem_head<RMAX>());
@@ -191,40 +191,66 @@ __global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : 4) k_step_bulk(ScanG
     return;
   }
   const int N4 = N >> 2;
-  for (int p = warp; p < P; p += kWarps) {
-    float acc[RMAX];
+  // Row p of the state: h = decay * h + sum_r (sdec v_prev[r][p] k_prev[r] +
+  // gamma v[r][p] k[r]) over the lane's float4 of columns, then the readouts
+  // h . q_r as lane partial sums.
+  auto row_update = [&](int p, int l, float* acc) {
+    float4* hp = reinterpret_cast<float4*>(hsm + p * N) + l;
+    float4 hv = *hp;
+    float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-    if (lane < N4) {
-      float4* hp = reinterpret_cast<float4*>(hsm + p * N) + lane;
-      float4 hv = *hp;
-      float4 upd = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-          const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
-          const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[lane];
-          const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[lane];
-          upd.x += cp * kp4.x + cc * k4.x;
-          upd.y += cp * kp4.y + cc * k4.y;
-          upd.z += cp * kp4.z + cc * k4.z;
-          upd.w += cp * kp4.w + cc * k4.w;
-        }
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const float cp = sdec * sm.vp[r * P + p], cc = gam * sm.v[r * P + p];
+        const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[l];
+        const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[l];
+        upd.x += cp * kp4.x + cc * k4.x;
+        upd.y += cp * kp4.y + cc * k4.y;
+        upd.z += cp * kp4.z + cc * k4.z;
+        upd.w += cp * kp4.w + cc * k4.w;
       }
-      hv.x = decay * hv.x + upd.x;
-      hv.y = decay * hv.y + upd.y;
-      hv.z = decay * hv.z + upd.z;
-      hv.w = decay * hv.w + upd.w;
-      *hp = hv;
+    }
+    hv.x = decay * hv.x + upd.x;
+    hv.y = decay * hv.y + upd.y;
+    hv.z = decay * hv.z + upd.z;
+    hv.w = decay * hv.w + upd.w;
+    *hp = hv;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[l];
+        acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
+      }
+    }
+  };
+  if (N4 <= 16) {
+    // rows of at most 16 float4: each half warp takes a row (rows p and
+    // p + 8 per step) and reduces its readouts within the half
+    const int hw = lane >> 4, hl = lane & 15;
+    for (int p0 = warp; p0 < P; p0 += 2 * kWarps) {
+      const int p = p0 + hw * kWarps;
+      float acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+      if (p < P && hl < N4) row_update(p, hl, acc);
 #pragma unroll
       for (int r = 0; r < RMAX; ++r) {
         if (r < R) {
-          const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[lane];
-          acc[r] = hv.x * q4.x + hv.y * q4.y + hv.z * q4.z + hv.w * q4.w;
+          float v = acc[r];
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (hl == 0 && p < P) sm.y[r * P + p] = v + dskip * sm.v[r * P + p];
         }
       }
     }
-    finish_row<RMAX>(sm, R, P, p, dskip, acc);
+  } else {
+    for (int p = warp; p < P; p += kWarps) {
+      float acc[RMAX];
+#pragma unroll
+      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
+      if (lane < N4) row_update(p, lane, acc);
+      finish_row<RMAX>(sm, R, P, p, dskip, acc);
+    }
   }
   // generic-proxy writes of the updated rows -> visible to the bulk store
   tc::fence_async_smem();
@@ -304,7 +330,9 @@ cudaError_t launch_step_r(const ScanGeom& g, const ScanArgs& a, const StepState&
 
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                         cudaStream_t s) {
-  return g.R == 1 ? launch_step_r<1>(g, a, st, s) : launch_step_r<8>(g, a, st, s);
+  if (g.R == 1) return launch_step_r<1>(g, a, st, s);
+  if (g.R <= 4) return launch_step_r<4>(g, a, st, s);
+  return launch_step_r<8>(g, a, st, s);
 }
 
 }  // namespace m3

@@ -147,6 +147,21 @@ __device__ __forceinline__ float rms_inv(float ss, int n, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)n), eps)));
 }
 
+// sin and cos of v: Cody-Waite reduction by 2 pi (2 pi split into its float
+// value and the float remainder), then the SFU sine / cosine on [-pi, pi]
+// (absolute error about 2^-21). Arguments beyond 2^15 take sincosf.
+__device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
+  if (fabsf(v) > 32768.0f) {
+    sincosf(v, s, c);
+    return;
+  }
+  const float k = rintf(v * 0.159154943f);
+  float r = fmaf(-k, 6.28318548f, v);
+  r = fmaf(-k, -1.74845553e-7f, r);
+  *s = __sinf(r);
+  *c = __cosf(r);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

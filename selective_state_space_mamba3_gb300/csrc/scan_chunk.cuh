@@ -159,21 +159,6 @@ ChunkLayout chunk_layout(int N, int P, int A, int R, bool mimo, bool async, bool
 
 __host__ __device__ constexpr int ilog2c(int v) { return v <= 1 ? 0 : 1 + ilog2c(v >> 1); }
 
-// sin and cos of v: Cody-Waite reduction by 2 pi (2 pi split into its float
-// value and the float remainder), then the SFU sine / cosine on [-pi, pi]
-// (absolute error about 2^-21). Arguments beyond 2^15 take sincosf.
-__device__ __forceinline__ void sincos_fast(float v, float* s, float* c) {
-  if (fabsf(v) > 32768.0f) {
-    sincosf(v, s, c);
-    return;
-  }
-  const float k = rintf(v * 0.159154943f);
-  float r = fmaf(-k, 6.28318548f, v);
-  r = fmaf(-k, -1.74845553e-7f, r);
-  *s = __sinf(r);
-  *c = __cosf(r);
-}
-
 // Per-token scalars and angle increments of one chunk, loaded into registers
 // one chunk ahead. Warp w owns tokens TPW * w .. TPW * w + TPW - 1 (TPW = 8 /
 // R); lane i <= TPW holds the dt / adt / trap of token TPW * w + i (lane TPW:
@@ -234,6 +219,17 @@ __device__ __forceinline__ float4 mul4(float4 a, float4 b) {
 }
 __device__ __forceinline__ float4 fma4(float4 a, float4 b, float4 c) {
   return cat4(__ffma2_rn(lo2(a), lo2(b), lo2(c)), __ffma2_rn(hi2(a), hi2(b), hi2(c)));
+}
+// Paired multiply in inline PTX: the compiler cannot merge it with a
+// following add into a fused multiply-add, so each product is rounded on its
+// own (as a separately stored product would be).
+__device__ __forceinline__ float2 mul2_sep(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ta, tb, td;\n\tmov.b64 ta, {%2, %3};\n\tmov.b64 tb, {%4, %5};\n\t"
+      "mul.rn.f32x2 td, ta, tb;\n\tmov.b64 {%0, %1}, td;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
 }
 
 // Split operands: the low part (the rounded remainder) of each value goes to
@@ -886,13 +882,12 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
             inv_b = __shfl_sync(0xffffffffu, r, lane | 8);
           }
           // (the raw row times its inverse RMS, as the preprocess writes it)
-          // (scalar __fmul_rn: never merged with the bias add that follows, so
-          // the normalised value is rounded on its own, as the preprocess
-          // stores it)
+          // (never merged with the bias add that follows, so the normalised
+          // value is rounded on its own, as the preprocess stores it)
           auto nrm = [&](float4 v, float inv) -> float4 {
             if constexpr (PACKED)
-              return make_float4(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv), __fmul_rn(v.z, inv),
-                                 __fmul_rn(v.w, inv));
+              return cat4(mul2_sep(lo2(v), make_float2(inv, inv)),
+                          mul2_sep(hi2(v), make_float2(inv, inv)));
             else
               return v;
           };
