@@ -12,7 +12,7 @@ and supplementary timings of the MIMO and decode-step entry points.
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
                 [--mode fp32|tf32] [--no-parts] [--part NAME]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
-mimo_scan_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
+mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
 mimo_step, siso_prefill_tf32) and prints its JSON, for profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
@@ -499,6 +499,38 @@ def parts_prefill(torch, m3, w, peak):
             "frac_hbm": round(gbs / peak, 4), "algorithmic_bytes": nbytes}
 
 
+def parts_packed_mimo(torch, m3, w, mode, peak):
+    """Supplementary: m3_mimo_forward_packed over the MIMO R4 workload (B4 L4096
+    H32 P64 N64 A32 R4 with the output norm): packed projection rows in, output
+    out (the preprocess kernel into the workspace, then the MIMO scan).
+    Algorithmic bytes: each packed row read once, the output written once."""
+    H, P, N, A = w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    G = H if w.num_groups == 0 else w.num_groups
+    proj = gen.layer_projection(w)
+    par = gen.scan_params(w)
+    dp = torch.from_numpy(proj["projected"]).cuda()
+    db = torch.from_numpy(proj["dt_bias"]).cuda()
+    keys = ("c_bias", "b_bias", "d", "mimo_x", "mimo_z", "mimo_o", "norm_weight")
+    pv = [torch.from_numpy(par[k]).cuda() for k in keys]
+    del proj
+    cfg = m3.ssm_config(w.cfg(), mode)
+    pcfg = m3.preprocess_config(inner_size=H * P, state_size=N, num_heads=H, num_rope_angles=A,
+                                num_groups=G, mimo_rank=w.mimo_rank, **gen.PRE_DEFAULT)
+    nws = m3.m3_mimo_forward_packed_workspace(cfg, pcfg)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+    out = torch.empty(w.batch_size, w.sequence_length, H, P, device="cuda")
+    fn = lambda: m3.m3_mimo_forward_packed(cfg, pcfg, dp, db, *pv, out, ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 10)
+    nbytes = w.tokens * bytes_per_token_packed(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name + " packed", "mode": "tf32" if mode == m3.M3_MATH_TF32 else "fp32",
+            "entry": "m3_mimo_forward_packed", "ms": round(ms, 4),
+            "tokens_per_s": round(w.tokens / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4), "algorithmic_bytes": nbytes}
+
+
 def cpu_baseline_oracle(w, batch_rows):
     """The CPU oracle (as it stands) on a bounded sample of the workload: the
     first `batch_rows` batch rows, preprocess + SISO scan, all host threads."""
@@ -532,6 +564,7 @@ def part_by_name(torch, m3, name, peak):
         "siso_scan_fp32": lambda: parts_scan(torch, m3, gen.SISO_1B, m3.M3_MATH_FP32, peak),
         "mimo_scan_fp32": lambda: parts_scan(torch, m3, gen.MIMO_R4, m3.M3_MATH_FP32, peak),
         "mimo_scan_tf32": lambda: parts_scan(torch, m3, gen.MIMO_R4, m3.M3_MATH_TF32, peak),
+        "mimo_packed_tf32": lambda: parts_packed_mimo(torch, m3, gen.MIMO_R4, m3.M3_MATH_TF32, peak),
         "siso_long_scan_fp32": lambda: parts_scan(torch, m3, gen.SISO_LONG, m3.M3_MATH_FP32, peak),
         "siso_long_scan_tf32": lambda: parts_scan(torch, m3, gen.SISO_LONG, m3.M3_MATH_TF32, peak),
         "siso_step": lambda: parts_step(torch, m3, peak),
@@ -664,7 +697,8 @@ def run_m3(args):
     del s
     torch.cuda.empty_cache()
     if rank == 0 and not args.no_parts:
-        for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "siso_long_scan_fp32",
+        for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "mimo_packed_tf32",
+                     "siso_long_scan_fp32",
                      "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()

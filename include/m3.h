@@ -10,7 +10,8 @@
  *   m3_mimo_step      - `mamba3_mimo_step`    (one MIMO token, explicit state)
  *   m3_siso_prefill / m3_mimo_prefill - the forward scans from / to an
  *                       explicit step state (prefill -> decode hand-off)
- *   m3_siso_forward_packed - `mamba3_preprocess` and `mamba3_siso` in one call
+ *   m3_siso_forward_packed / m3_mimo_forward_packed - `mamba3_preprocess` and
+ *                       `mamba3_siso` / `mamba3_mimo` in one call
  *
  * Conventions for every entry point:
  *  - Every tensor is float32, dense row-major, in device memory owned by the
@@ -155,6 +156,27 @@ int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config*
                            const float* projected, const float* dt_bias, const float* c_bias,
                            const float* b_bias, const float* d, float* out, void* workspace,
                            size_t workspace_bytes, m3_stream_t stream);
+
+/*
+ * m3_mimo_forward_packed - m3_preprocess and m3_mimo_forward in one call
+ * (`mamba3_preprocess` feeding `mamba3_mimo`). As m3_siso_forward_packed, with
+ * the MIMO operands and checks of m3_mimo_forward: pcfg->mimo_rank = R (the
+ * packed rows hold G*R B / C rows), c_bias / b_bias [H,R,N], mimo_x / mimo_z /
+ * mimo_o [H,R,P], norm_weight [H,P]. Every shape runs the preprocess into the
+ * workspace and then the MIMO scan (the MIMO scan kernel is bound by its
+ * per-chunk latency, and the per-head RMS of R rank rows that reading the
+ * packed rows directly adds to it costs more than the preprocess pass), so
+ * the output is that of m3_preprocess followed by m3_mimo_forward in the same
+ * math mode.
+ */
+int m3_mimo_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                                     size_t* bytes);
+int m3_mimo_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                           const float* projected, const float* dt_bias, const float* c_bias,
+                           const float* b_bias, const float* d, const float* mimo_x,
+                           const float* mimo_z, const float* mimo_o, const float* norm_weight,
+                           float* out, void* workspace, size_t workspace_bytes,
+                           m3_stream_t stream);
 
 /*
  * m3_mimo_forward - the shared-state Mamba-3 MIMO recurrence (`mamba3_mimo`,

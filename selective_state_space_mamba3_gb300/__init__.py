@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     ssm_config, preprocess_config, load_library, status_string, launch_count, m3_preprocess,
     m3_siso_forward_workspace, m3_siso_forward, m3_siso_forward_static,
     m3_siso_forward_static_status, m3_siso_forward_packed_workspace, m3_siso_forward_packed,
+    m3_mimo_forward_packed_workspace, m3_mimo_forward_packed,
     m3_mimo_forward_workspace, m3_mimo_forward,
     m3_siso_step, m3_mimo_step, m3_workspace_status, LIB_PATH, m3_siso_prefill_workspace,
     m3_mimo_prefill_workspace, m3_siso_prefill, m3_mimo_prefill, m3_selftest_wait_timeout)

@@ -27,7 +27,8 @@ M3_MATH_TF32 = 1
 
 EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
             "m3_siso_forward_static", "m3_siso_forward_static_status",
-            "m3_siso_forward_packed_workspace", "m3_siso_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
+            "m3_siso_forward_packed_workspace", "m3_siso_forward_packed",
+            "m3_mimo_forward_packed_workspace", "m3_mimo_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
@@ -98,6 +99,8 @@ def load_library():
         pcfgp = ctypes.POINTER(PreprocessConfig)
         lib.m3_siso_forward_packed_workspace.argtypes = [cfgp, pcfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_forward_packed.argtypes = [cfgp, pcfgp] + [_vp] * 7 + [ctypes.c_size_t, _vp]
+        lib.m3_mimo_forward_packed_workspace.argtypes = [cfgp, pcfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_mimo_forward_packed.argtypes = [cfgp, pcfgp] + [_vp] * 11 + [ctypes.c_size_t, _vp]
         lib.m3_siso_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_mimo_prefill_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_prefill.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
@@ -208,6 +211,24 @@ def m3_siso_forward_packed(cfg: SsmConfig, pcfg: PreprocessConfig, projected, dt
     _check(load_library().m3_siso_forward_packed(ctypes.byref(cfg), ctypes.byref(pcfg), *[
         _ptr(t) for t in (projected, dt_bias, c_bias, b_bias, d, out)], wp, wn, _stream(stream)),
         "m3_siso_forward_packed")
+
+
+def m3_mimo_forward_packed_workspace(cfg: SsmConfig, pcfg: PreprocessConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_mimo_forward_packed_workspace(ctypes.byref(cfg), ctypes.byref(pcfg),
+                                                            ctypes.byref(n)),
+           "m3_mimo_forward_packed_workspace")
+    return n.value
+
+
+def m3_mimo_forward_packed(cfg: SsmConfig, pcfg: PreprocessConfig, projected, dt_bias, c_bias,
+                           b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, workspace=None,
+                           stream=None):
+    """m3_preprocess and m3_mimo_forward in one call."""
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_mimo_forward_packed(ctypes.byref(cfg), ctypes.byref(pcfg), *[
+        _ptr(t) for t in (projected, dt_bias, c_bias, b_bias, d, mimo_x, mimo_z, mimo_o,
+                          norm_weight, out)], wp, wn, _stream(stream)), "m3_mimo_forward_packed")
 
 
 def m3_siso_forward_static_status(stream=None) -> int:

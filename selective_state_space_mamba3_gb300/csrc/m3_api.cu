@@ -226,9 +226,11 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
 }
 
 // ---------------------------------------------------------------------------
-// SISO scan of a packed projection: fused where the chunked kernel has a TMA
+// Scans of a packed projection. SISO: fused where the chunked kernel has a TMA
 // instance for the shape and the packed rows are 16-byte aligned column by
 // column, otherwise m3_preprocess into the workspace followed by the scan.
+// MIMO: always the preprocess and then the scan (measured faster than reading
+// the packed rows in the latency-bound MIMO kernel).
 namespace {
 struct PackedPlan {
   bool fused;
@@ -239,13 +241,13 @@ struct PackedPlan {
 
 PackedPlan packed_plan(const ScanGeom& g, const PreGeom& p) {
   PackedPlan pl{};
-  pl.fused = use_chunk(g) && chunk_packed_supported(g) && p.W % 4 == 0;
+  pl.fused = !g.mimo && use_chunk(g) && chunk_packed_supported(g) && p.W % 4 == 0;
   if (pl.fused) {
     pl.bytes = scan_workspace_bytes(g, false);
     return pl;
   }
   const size_t rows = (size_t)p.rows;
-  const size_t bc = (size_t)p.G * p.R * p.N;
+  const size_t bc = (size_t)p.G * p.R * p.N;  // B / C rows per packed row
   const size_t cols[8] = {(size_t)p.I, (size_t)p.I, bc, bc, (size_t)p.H, (size_t)p.H,
                           (size_t)p.H, (size_t)p.A};
   size_t o = 0;
@@ -258,18 +260,18 @@ PackedPlan packed_plan(const ScanGeom& g, const PreGeom& p) {
   return pl;
 }
 
-// Geometry of the packed scan: the SsmConfig rules, and a preprocess config
-// that describes the same layer (inner = H * P, the same N, H, A and groups,
-// rank 1).
-int resolve_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg, ScanGeom* g,
-                   PreGeom* p) {
-  int st = resolve_ssm(cfg, false, g);
+// Geometry of the packed scan: the SsmConfig rules (SISO or MIMO), and a
+// preprocess config that describes the same layer (inner = H * P, the same N,
+// H, A, groups and rank).
+int resolve_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg, bool mimo,
+                   ScanGeom* g, PreGeom* p) {
+  int st = resolve_ssm(cfg, mimo, g);
   if (st != M3_OK) return st;
   if (!pcfg) return M3_ERR_INVALID_ARGUMENT;
   st = resolve_pre(pcfg, (int64_t)g->B * g->L, p);
   if (st != M3_OK) return st;
   if (p->I != g->H * g->P || p->N != g->N || p->H != g->H || p->A != g->A || p->G != g->G ||
-      p->R != 1)
+      p->R != g->R)
     return M3_ERR_INVALID_ARGUMENT;
   g->W = p->W;
   g->eps = p->eps;
@@ -399,37 +401,40 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
   return scan_common(cfg, false, a, nullptr, workspace, workspace_bytes, stream);
 }
 
-int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
-                                     size_t* bytes) {
+static int packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                            bool mimo, size_t* bytes) {
   ScanGeom g;
   PreGeom p;
   if (!bytes) return M3_ERR_INVALID_ARGUMENT;
-  const int st = resolve_packed(cfg, pcfg, &g, &p);
+  const int st = resolve_packed(cfg, pcfg, mimo, &g, &p);
   if (st != M3_OK) return st;
   *bytes = packed_plan(g, p).bytes;
   return M3_OK;
 }
 
-int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
-                           const float* projected, const float* dt_bias, const float* c_bias,
-                           const float* b_bias, const float* d, float* out, void* workspace,
-                           size_t workspace_bytes, m3_stream_t stream) {
-  NvtxRange nvtx_range("m3_siso_forward_packed");
+// The packed-projection scan, SISO (mimo operands null) or MIMO.
+static int packed_common(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg, bool mimo,
+                         const float* projected, const float* dt_bias, const float* c_bias,
+                         const float* b_bias, const float* d, const float* mimo_x,
+                         const float* mimo_z, const float* mimo_o, const float* norm_weight,
+                         float* out, void* workspace, size_t workspace_bytes,
+                         m3_stream_t stream) {
   ScanGeom g;
   PreGeom p;
-  int st = resolve_packed(cfg, pcfg, &g, &p);
+  int st = resolve_packed(cfg, pcfg, mimo, &g, &p);
   if (st != M3_OK) return st;
   if ((st = check_ptrs({projected, dt_bias, c_bias, b_bias, d, out})) != M3_OK) return st;
+  if (mimo && (st = check_ptrs({mimo_x, mimo_z, mimo_o, norm_weight})) != M3_OK) return st;
   const PackedPlan pl = packed_plan(g, p);
   if (pl.bytes > 0 && (!workspace || workspace_bytes < pl.bytes)) return M3_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return M3_ERR_UNALIGNED;
   const cudaStream_t s = (cudaStream_t)stream;
   if (pl.fused) {
     // x, z and the scalar columns of the packed rows; C / B through tensor maps
-    const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.N;
+    const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.R * p.N;
     ScanArgs a{projected, projected, projected + I, projected, projected + o_s + p.H,
                projected + o_s, projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias,
-               b_bias, d, nullptr, nullptr, nullptr, nullptr, out, dt_bias};
+               b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias};
     return cuda_status(run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed));
   }
   char* w = static_cast<char*>(workspace);
@@ -439,9 +444,39 @@ int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config*
   cudaError_t e = launch_preprocess(p, projected, dt_bias, o, s);
   if (e != cudaSuccess) return M3_ERR_CUDA;
   ScanArgs a{o.ch, o.bh, o.x, o.z, o.adt, o.dt, o.trap, o.angle, c_bias, b_bias, d,
-             nullptr, nullptr, nullptr, nullptr, out};
+             mimo_x, mimo_z, mimo_o, norm_weight, out};
   return cuda_status(launch_scan(g, a, nullptr, w + pl.pre_bytes, workspace_bytes - pl.pre_bytes,
                                  s));
+}
+
+int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                                     size_t* bytes) {
+  return packed_workspace(cfg, pcfg, false, bytes);
+}
+
+int m3_siso_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                           const float* projected, const float* dt_bias, const float* c_bias,
+                           const float* b_bias, const float* d, float* out, void* workspace,
+                           size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_forward_packed");
+  return packed_common(cfg, pcfg, false, projected, dt_bias, c_bias, b_bias, d, nullptr, nullptr,
+                       nullptr, nullptr, out, workspace, workspace_bytes, stream);
+}
+
+int m3_mimo_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                                     size_t* bytes) {
+  return packed_workspace(cfg, pcfg, true, bytes);
+}
+
+int m3_mimo_forward_packed(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
+                           const float* projected, const float* dt_bias, const float* c_bias,
+                           const float* b_bias, const float* d, const float* mimo_x,
+                           const float* mimo_z, const float* mimo_o, const float* norm_weight,
+                           float* out, void* workspace, size_t workspace_bytes,
+                           m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_mimo_forward_packed");
+  return packed_common(cfg, pcfg, true, projected, dt_bias, c_bias, b_bias, d, mimo_x, mimo_z,
+                       mimo_o, norm_weight, out, workspace, workspace_bytes, stream);
 }
 
 int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, const float* x,

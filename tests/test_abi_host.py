@@ -213,3 +213,22 @@ def test_packed_entry_checks_both_configs(lib):
     assert call(cfg, ctypes.byref(pc), wsn=n.value - 1) == m3.M3_ERR_WORKSPACE
     assert lib.m3_siso_forward_packed(ctypes.byref(cfg), ctypes.byref(pc), *([FAKE_ODD] * 6),
                                       FAKE, 1 << 30, None) == m3.M3_ERR_UNALIGNED
+
+
+def test_mimo_packed_entry_checks_rank(lib):
+    """m3_mimo_forward_packed takes the MIMO geometry rules and a preprocess
+    config whose mimo_rank matches the scan's rank."""
+    cfg = siso_cfg(head_dim=16, state_size=32, num_heads=4, num_groups=2, num_rope_angles=8,
+                   mimo_rank=4, has_output_norm=1)
+    good = dict(inner_size=64, state_size=32, num_heads=4, num_rope_angles=8, num_groups=2,
+                mimo_rank=4, epsilon=1e-6, dt_min=1e-3, dt_max=0.1, a_floor=1e-4)
+    n = ctypes.c_size_t(0)
+    pc = m3.preprocess_config(**good)
+    assert lib.m3_mimo_forward_packed_workspace(ctypes.byref(cfg), ctypes.byref(pc),
+                                                ctypes.byref(n)) == m3.M3_OK and n.value > 0
+    call = lambda c, p, ptr=FAKE: lib.m3_mimo_forward_packed(ctypes.byref(c), p, *([ptr] * 10),
+                                                             FAKE, 1 << 30, None)
+    assert call(cfg, ctypes.byref(m3.preprocess_config(**dict(good, mimo_rank=1)))) == \
+        m3.M3_ERR_INVALID_ARGUMENT
+    assert call(siso_cfg(mimo_rank=9), ctypes.byref(pc)) == m3.M3_ERR_INVALID_ARGUMENT
+    assert call(cfg, ctypes.byref(pc), ptr=None) == m3.M3_ERR_INVALID_ARGUMENT

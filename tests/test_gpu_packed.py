@@ -1,11 +1,12 @@
-"""GPU parity of m3_siso_forward_packed: the SISO scan of a packed input
-projection (oarust mamba3.rs `mamba3_preprocess` feeding `mamba3_siso`).
+"""GPU parity of m3_siso_forward_packed / m3_mimo_forward_packed: the scans of a
+packed input projection (oarust mamba3.rs `mamba3_preprocess` feeding
+`mamba3_siso` / `mamba3_mimo`).
 
-Where the chunked kernel reads the packed rows itself (P = 64, N = 128,
+Where the chunked kernel reads the packed rows itself (SISO P = 64, N = 128,
 A = 32 or 64, W a multiple of 4), its output must have the bits of
-m3_preprocess followed by m3_siso_forward in the same math mode; every other
-shape goes through the preprocess kernel and a workspace, with the same
-result. Both are also held to the oracle's preprocess -> scan chain at the
+m3_preprocess followed by the scan in the same math mode; every other SISO
+shape, and every MIMO shape, goes through the preprocess kernel and a
+workspace, with the same result. Both are also held to the oracle's preprocess -> scan chain at the
 mode's bar (FP32-exact 1e-5, TF32 2e-3), on the first and last batch rows."""
 import numpy as np
 import pytest
@@ -27,37 +28,56 @@ def _built():
     oracle.build()
 
 
+MIMO_PAR = ("mimo_x", "mimo_z", "mimo_o", "norm_weight")
+
+
 def pre_kw(w, pre):
     G = w.num_heads if w.num_groups == 0 else w.num_groups
     return dict(inner_size=w.num_heads * w.head_dim, state_size=w.state_size,
                 num_heads=w.num_heads, num_rope_angles=w.num_rope_angles, num_groups=G,
-                mimo_rank=1, **pre)
+                mimo_rank=w.mimo_rank, **pre)
+
+
+def is_mimo(w):
+    return w.mimo_rank > 1 or w.has_output_norm
 
 
 def run_both(w, proj, dt_bias, par, mode, pre):
-    """(packed entry output, m3_preprocess + m3_siso_forward output)."""
+    """(packed entry output, m3_preprocess + scan output)."""
     import torch
-    B, L, H, P, N, A = (w.batch_size, w.sequence_length, w.num_heads, w.head_dim,
-                        w.state_size, w.num_rope_angles)
+    B, L, H, P, N, A, R = (w.batch_size, w.sequence_length, w.num_heads, w.head_dim,
+                           w.state_size, w.num_rope_angles, w.mimo_rank)
     G = H if w.num_groups == 0 else w.num_groups
+    mimo = is_mimo(w)
     cfg = m3.ssm_config(w.cfg(), mode)
     pcfg = m3.preprocess_config(**pre_kw(w, pre))
     dp, db = dev(proj), dev(dt_bias)
     cb, bb, d = dev(par["c_bias"]), dev(par["b_bias"]), dev(par["d"])
+    mp = [dev(par[k]) for k in MIMO_PAR] if mimo else []
     out = torch.full((B, L, H, P), float("nan"), device="cuda")
-    nws = m3.m3_siso_forward_packed_workspace(cfg, pcfg)
-    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
-    m3.m3_siso_forward_packed(cfg, pcfg, dp, db, cb, bb, d, out, ws)
+    if mimo:
+        nws = m3.m3_mimo_forward_packed_workspace(cfg, pcfg)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+        m3.m3_mimo_forward_packed(cfg, pcfg, dp, db, cb, bb, d, *mp, out, ws)
+    else:
+        nws = m3.m3_siso_forward_packed_workspace(cfg, pcfg)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+        m3.m3_siso_forward_packed(cfg, pcfg, dp, db, cb, bb, d, out, ws)
     e = lambda *s: torch.empty(*s, device="cuda")
     x, z = e(B, L, H, P), e(B, L, H, P)
-    bh, ch = e(B, L, G, N), e(B, L, G, N)
+    bh, ch = e(B, L, G * R, N), e(B, L, G * R, N)
     dt, adt, trap = e(B, L, H), e(B, L, H), e(B, L, H)
     ang = e(B, L, A) if A else None
     m3.m3_preprocess(pcfg, B * L, dp, db, x, z, bh, ch, dt, adt, trap, ang)
     out2 = torch.full_like(out, float("nan"))
-    nws2 = m3.m3_siso_forward_workspace(cfg)
-    ws2 = torch.empty(max(nws2, 16), dtype=torch.uint8, device="cuda")
-    m3.m3_siso_forward(cfg, ch, bh, x, z, adt, dt, trap, ang, cb, bb, d, out2, ws2)
+    if mimo:
+        nws2 = m3.m3_mimo_forward_workspace(cfg)
+        ws2 = torch.empty(max(nws2, 16), dtype=torch.uint8, device="cuda")
+        m3.m3_mimo_forward(cfg, ch, bh, x, z, adt, dt, trap, ang, cb, bb, d, *mp, out2, ws2)
+    else:
+        nws2 = m3.m3_siso_forward_workspace(cfg)
+        ws2 = torch.empty(max(nws2, 16), dtype=torch.uint8, device="cuda")
+        m3.m3_siso_forward(cfg, ch, bh, x, z, adt, dt, trap, ang, cb, bb, d, out2, ws2)
     torch.cuda.synchronize()
     assert m3.m3_workspace_status(ws) == m3.M3_OK
     return out.cpu().numpy(), out2.cpu().numpy()
@@ -65,17 +85,18 @@ def run_both(w, proj, dt_bias, par, mode, pre):
 
 def oracle_chain(w, proj, dt_bias, par, pre, bsl):
     """The oracle's preprocess of batch rows `bsl`, then its scan."""
-    L, H, P, N, A = (w.sequence_length, w.num_heads, w.head_dim, w.state_size,
-                     w.num_rope_angles)
+    L, H, P, N, A, R = (w.sequence_length, w.num_heads, w.head_dim, w.state_size,
+                        w.num_rope_angles, w.mimo_rank)
     G = H if w.num_groups == 0 else w.num_groups
     nb = bsl.stop - bsl.start
     rows = proj.reshape(w.batch_size, L, -1)[bsl].reshape(nb * L, -1)
     o = oracle.preprocess(rows, dt_bias, **pre_kw(w, pre))
     f = lambda k, *s: o[k].astype(np.float32).reshape(nb, L, *s)
-    return oracle.scan(w.cfg(batch_size=nb), f("ch", G, N), f("bh", G, N), f("x", H, P),
+    extra = {k: par[k] for k in MIMO_PAR} if is_mimo(w) else {}
+    return oracle.scan(w.cfg(batch_size=nb), f("ch", G * R, N), f("bh", G * R, N), f("x", H, P),
                        f("z", H, P), f("adt", H), f("dt", H), f("trap", H),
                        f("angle", A) if A else np.zeros((nb, L, 0), np.float32),
-                       par["c_bias"], par["b_bias"], par["d"])
+                       par["c_bias"], par["b_bias"], par["d"], **extra)
 
 
 CASES = {
@@ -89,6 +110,11 @@ CASES = {
                      dict(epsilon=1e-5, dt_min=2e-3, dt_max=0.2, a_floor=0.5)),
     # preprocess + scan through the workspace: W = 110 is not a multiple of 4
     "workspace_tiny": (gen.TINY_SISO, gen.TINY_PRE),
+    # MIMO: the R4 workload's shape with two batch rows and 1,000 tokens
+    "mimo_r4": (gen.MIMO_R4.with_(batch_size=2, sequence_length=1000), gen.PRE_DEFAULT),
+    # MIMO: rank 2, no compile-time instance of the scan
+    "mimo_r2": (gen.Workload("packed MIMO R2", 1, 300, 4, 2, 32, 32, 8, mimo_rank=2,
+                                       has_output_norm=1, seed_index=52), gen.PRE_DEFAULT),
 }
 
 
