@@ -44,8 +44,10 @@ __global__ void __launch_bounds__(kThreads) k_state_init(ScanGeom g, ScanArgs a,
     th0[(int64_t)bh * A + i] = st.angle ? st.angle[(int64_t)bh * A + i] : 0.f;
 }
 
-// One block per (b, h). Thread-owned units: rotary pair (p, a) for a < A, or
-// single column (p, n >= 2A). Segments are walked in order.
+// Grid (b * H + h, unit block): one thread per unit, a unit being a rotary
+// pair (p, a) for a < A or a single column (p, n >= 2A); each thread walks
+// the segments in order (the units are independent, so the walks of all units
+// of all sequences overlap).
 __global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg,
                                                             const float* g_init,
                                                             const float* th_init,
@@ -57,7 +59,8 @@ __global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg,
   const int P = g.P, N = g.N, A = g.A;
   const int U = N - A;
   const int64_t PN = (int64_t)P * N;
-  for (int i = threadIdx.x; i < P * U; i += kThreads) {
+  const int i = blockIdx.y * kThreads + threadIdx.x;
+  if (i < P * U) {
     const int p = i / U, u = i - p * U;
     const int n0 = u < A ? u : u + A;  // first column of the unit
     const bool pair = u < A;
@@ -105,8 +108,10 @@ cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, const float* g_init
                                 const float* th_init, const float* gsum, const float* thsum,
                                 const float* esum, float* g_entry, float* th_entry,
                                 cudaStream_t s) {
-  k_state_prefix<<<(unsigned)(g.B * g.H), kThreads, 0, s>>>(g, nseg, g_init, th_init, gsum,
-                                                            thsum, esum, g_entry, th_entry);
+  const dim3 grid((unsigned)(g.B * g.H),
+                  (unsigned)max(1, (g.P * (g.N - g.A) + kThreads - 1) / kThreads));
+  k_state_prefix<<<grid, kThreads, 0, s>>>(g, nseg, g_init, th_init, gsum, thsum, esum, g_entry,
+                                           th_entry);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -134,11 +134,19 @@ __device__ __forceinline__ float silu_f(float v) { return v * sigmoid_f(v); }
 // clamped dt, the floored negative log decay adt, the sum of squares of four
 // B/C values (a fixed FMA chain), and the inverse RMS of a row from its sum of
 // squares (IEEE division and square root).
+// (pre_dt_sp / pre_adt_sp take the softplus already formed, for callers that
+// compute the two softplus maps in different lanes)
+__device__ __forceinline__ float pre_dt_sp(float sp, float lo, float hi) {
+  return fminf(fmaxf(sp, lo), hi);
+}
+__device__ __forceinline__ float pre_adt_sp(float sp_a, float a_floor, float dt) {
+  return __fmul_rn(-fmaxf(sp_a, a_floor), dt);
+}
 __device__ __forceinline__ float pre_dt(float raw, float bias, float lo, float hi) {
-  return fminf(fmaxf(softplus_f(__fadd_rn(raw, bias)), lo), hi);
+  return pre_dt_sp(softplus_f(__fadd_rn(raw, bias)), lo, hi);
 }
 __device__ __forceinline__ float pre_adt(float a_raw, float a_floor, float dt) {
-  return __fmul_rn(-fmaxf(softplus_f(a_raw), a_floor), dt);
+  return pre_adt_sp(softplus_f(a_raw), a_floor, dt);
 }
 __device__ __forceinline__ float sumsq4(float4 v) {
   return __fmaf_rn(v.w, v.w, __fmaf_rn(v.z, v.z, __fmaf_rn(v.y, v.y, __fmul_rn(v.x, v.x))));

@@ -179,11 +179,24 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
   pl.dt = pl.adt = pl.trap = 0.f;
   const int tw = TPW * warp + lane;
   const int64_t rs = PACKED ? (int64_t)g.W : (int64_t)H;  // row stride of the scalar columns
+  // packed: one softplus per lane, lanes 0 .. TPW on dt_raw + dt_bias and
+  // lanes 16 .. 16 + TPW on a_raw of the same tokens
+  float sp_a = 0.f, sp_dt = 0.f;
+  if constexpr (PACKED) {
+    const int li = lane & 15, twl = TPW * warp + li;
+    float sp = 0.f;
+    if (li <= TPW && cn + twl < L) {
+      const int64_t sc = (tok + twl) * rs + h;
+      sp = softplus_f(lane < 16 ? __fadd_rn(a.dt[sc], a.dt_bias[h]) : a.adt[sc]);
+    }
+    sp_dt = sp;
+    sp_a = __shfl_down_sync(0xffffffffu, sp, 16);
+  }
   if (lane <= TPW && cn + tw < L) {
     const int64_t sc = (tok + tw) * rs + h;
     if constexpr (PACKED) {
-      pl.dt = pre_dt(a.dt[sc], a.dt_bias[h], g.dt_min, g.dt_max);
-      pl.adt = pre_adt(a.adt[sc], g.a_floor, pl.dt);
+      pl.dt = pre_dt_sp(sp_dt, g.dt_min, g.dt_max);
+      pl.adt = pre_adt_sp(sp_a, g.a_floor, pl.dt);
     } else {
       pl.dt = a.dt[sc];
       pl.adt = a.adt[sc];
