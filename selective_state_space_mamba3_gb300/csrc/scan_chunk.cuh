@@ -479,6 +479,16 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     mor[r] = ok ? a.mimo_o[((int64_t)h * R + r) * P + prow] : 0.f;
   }
   const float dsk = g.has_d ? a.d[h] : 0.f;
+  // MIMO with compile-time R <= 4: the value rows 4 rb + l / 8 of this lane all
+  // have rank (l / 8) mod R, so its mimo_x factors (columns 8 pb + l % 8) are
+  // loaded once and applied when the values are stored
+  constexpr bool kMxPre = MIMO && KR > 0 && KR <= 4;
+  float mxr[kMxPre ? MP / 8 : 1];
+#pragma unroll
+  for (int pb = 0; pb < (kMxPre ? MP / 8 : 1); ++pb) {
+    const int p = 8 * pb + (lane & 7), r2 = (lane >> 3) & (R - 1);
+    mxr[pb] = (kMxPre && p < P) ? a.mimo_x[((int64_t)h * R + r2) * P + p] : 1.f;
+  }
   const uint32_t id_S = tc::idesc_tf32(64, 64);
   const uint32_t id_Y = tc::idesc_tf32(MP, 64);
   const uint32_t id_D = tc::idesc_tf32(MP, Npad);
@@ -1042,6 +1052,10 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     // chains come from threads of different warps so that they overlap)
     // (split: three MMAs per K step, hi * hi + hi * lo + lo * hi; the state's
     // high part is the MMA's own truncation of G, its low part sits at tGl)
+    // (an issuing thread's warp waits about a hundred cycles per MMA: in the
+    // MIMO instances, whose values come from scalar loads, the issue comes
+    // after the warp's value loads are in flight)
+    auto issue_s_yo = [&] {
     if (!SUMMARY && tid == 0) {
 #pragma unroll
       for (int ks = 0; ks < Npad / 8; ++ks) {
@@ -1064,6 +1078,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
       }
       tc::commit(&bars[1]);
     }
+    };
+    if constexpr (!kMxPre) issue_s_yo();
     // (6) masked scores P = M o S + D I (S rows: TMEM M = 64 layout, lanes
     // 0..15 of each quadrant; lane l + 16 takes the upper 8 columns of each
     // 16-column block of row l) and values X^T, both into the K region (or
@@ -1098,11 +1114,12 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           for (int pb = 0; pb < MP / 8; ++pb) {
             const int p = 8 * pb + pl8;
             float xv = (in && p < P) ? xrow[p] : 0.f;
-            if (mimo && in && p < P) xv *= mx[p];
+            if (!kMxPre && mimo && in && p < P) xv *= mx[p];
             xreg[q][pb] = xv;
           }
         }
       }
+      if constexpr (kMxPre) issue_s_yo();
       if (!SUMMARY) {
         const bool s_done = tc::bar_wait(&bars[0], it & 1, kWaitBudget);
         if (!s_done) abort_flag = 1;
@@ -1209,7 +1226,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           const int rho2 = 4 * rb + rl;
 #pragma unroll
           for (int pb = 0; pb < MP / 8; ++pb)
-            put1<SPLIT>(sXt + tc::kmaj(8 * pb + pl8, rho2, kRows), LO, xreg[q][pb]);
+            put1<SPLIT>(sXt + tc::kmaj(8 * pb + pl8, rho2, kRows), LO,
+                        kMxPre ? xreg[q][pb] * mxr[pb] : xreg[q][pb]);
         }
       }
       // value of the sequence's last token for the step state (last chunk only)
