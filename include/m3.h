@@ -141,14 +141,16 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
  * num_groups = the resolved G, mimo_rank = 1; its epsilon / dt bounds /
  * a_floor are checked as in m3_preprocess, cfg as in m3_siso_forward.
  * Where the chunked kernel has a TMA instance for the shape (P = 64, N = 128,
- * A = 32 or 64) and W is a multiple of 4, the scan reads the packed rows
- * directly: the B / C rows are RMS-normalised in shared memory in the same
- * reduction order as m3_preprocess, and dt / adt are formed by the same maps,
- * so the output has the bits of m3_preprocess followed by m3_siso_forward in
- * the same math mode. Otherwise the preprocess writes its outputs into the
- * workspace and the scan reads them from there (the same result).
- * workspace: at least m3_siso_forward_packed_workspace() bytes, 16-byte
- * aligned (may be NULL when that size is 0).
+ * A = 32 or 64) and W is a multiple of 4, a short pass writes the inverse
+ * RMS of every B / C row into the workspace (computed exactly as m3_preprocess
+ * computes it) and the scan reads the packed rows directly, scaling the B / C
+ * rows in shared memory and forming dt / adt by the same maps, so the output
+ * has the bits of m3_preprocess followed by m3_siso_forward in the same math
+ * mode. Otherwise the preprocess writes its outputs into the workspace and the
+ * scan reads them from there (the same result).
+ * workspace: at least m3_siso_forward_packed_workspace() bytes (never 0),
+ * 16-byte aligned; its first word is the scan's status word, read by
+ * m3_workspace_status.
  */
 int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
                                      size_t* bytes);

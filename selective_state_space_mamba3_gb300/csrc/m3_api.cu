@@ -6,6 +6,7 @@
 // state-shape checks, and `shader_u32` (every element count below 2^32).
 // Every check runs before anything is enqueued, so a rejected call changes no
 // buffer (the step docstring: states are mutated only after validation).
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -232,31 +233,36 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
 // MIMO: always the preprocess and then the scan (measured faster than reading
 // the packed rows in the latency-bound MIMO kernel).
 namespace {
+// Workspace: the scan's own workspace first (its status word at offset 0, where
+// m3_workspace_status reads it), then, fused, the rows' B / C inverse RMS at
+// scan_bytes, or, otherwise, the preprocess outputs at scan_bytes + off[i].
 struct PackedPlan {
   bool fused;
-  size_t pre_bytes;  // fallback: x, z, bh, ch, dt, adt, trap, angle at the workspace start
-  size_t off[8];
+  size_t scan_bytes;
+  size_t off[8];  // fallback: x, z, bh, ch, dt, adt, trap, angle
   size_t bytes;
 };
 
 PackedPlan packed_plan(const ScanGeom& g, const PreGeom& p) {
   PackedPlan pl{};
   pl.fused = !g.mimo && use_chunk(g) && chunk_packed_supported(g) && p.W % 4 == 0;
+  // (at least the 256 bytes of the status word, which the token-sequential
+  // scan does not use but which is cleared for m3_workspace_status)
+  pl.scan_bytes = std::max<size_t>(256, (scan_workspace_bytes(g, false) + 255) / 256 * 256);
   if (pl.fused) {
-    pl.bytes = scan_workspace_bytes(g, false);
+    pl.bytes = pl.scan_bytes + ((size_t)p.rows * 2 * p.G * p.R * 4 + 255) / 256 * 256;
     return pl;
   }
   const size_t rows = (size_t)p.rows;
   const size_t bc = (size_t)p.G * p.R * p.N;  // B / C rows per packed row
   const size_t cols[8] = {(size_t)p.I, (size_t)p.I, bc, bc, (size_t)p.H, (size_t)p.H,
                           (size_t)p.H, (size_t)p.A};
-  size_t o = 0;
+  size_t o = pl.scan_bytes;
   for (int i = 0; i < 8; ++i) {
     pl.off[i] = o;
     o += (rows * cols[i] * 4 + 255) / 256 * 256;
   }
-  pl.pre_bytes = o;
-  pl.bytes = o + scan_workspace_bytes(g, false);
+  pl.bytes = o;
   return pl;
 }
 
@@ -430,14 +436,18 @@ static int packed_common(const m3_ssm_config* cfg, const m3_preprocess_config* p
   if (workspace && !aligned16(workspace)) return M3_ERR_UNALIGNED;
   const cudaStream_t s = (cudaStream_t)stream;
   if (pl.fused) {
-    // x, z and the scalar columns of the packed rows; C / B through tensor maps
+    // the rows' B / C inverse RMS, then the scan: x, z and the scalar columns
+    // of the packed rows, C / B through tensor maps
+    float* inv = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.scan_bytes);
+    if (launch_row_rms(p, projected, inv, s) != cudaSuccess) return M3_ERR_CUDA;
     const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.R * p.N;
     ScanArgs a{projected, projected, projected + I, projected, projected + o_s + p.H,
                projected + o_s, projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias,
-               b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias};
+               b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias, inv};
     return cuda_status(run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed));
   }
   char* w = static_cast<char*>(workspace);
+  if (!use_chunk(g) && cudaMemsetAsync(w, 0, 16, s) != cudaSuccess) return M3_ERR_CUDA;
   float* f[8];
   for (int i = 0; i < 8; ++i) f[i] = reinterpret_cast<float*>(w + pl.off[i]);
   PreOut o{f[0], f[1], f[2], f[3], f[4], f[5], f[6], g.A ? f[7] : nullptr};
@@ -445,8 +455,7 @@ static int packed_common(const m3_ssm_config* cfg, const m3_preprocess_config* p
   if (e != cudaSuccess) return M3_ERR_CUDA;
   ScanArgs a{o.ch, o.bh, o.x, o.z, o.adt, o.dt, o.trap, o.angle, c_bias, b_bias, d,
              mimo_x, mimo_z, mimo_o, norm_weight, out};
-  return cuda_status(launch_scan(g, a, nullptr, w + pl.pre_bytes, workspace_bytes - pl.pre_bytes,
-                                 s));
+  return cuda_status(launch_scan(g, a, nullptr, w, pl.scan_bytes, s));
 }
 
 int m3_siso_forward_packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,

@@ -26,12 +26,15 @@ struct ScanGeom {
 // Scan operands. For the packed-projection scan, x and z point at their
 // columns of the packed rows, dt / adt / trap / angle at the dt_raw / a_raw /
 // trap / angle columns (row stride W), c and b are unused (the C and B rows
-// are read through tensor maps of the packed rows) and dt_bias is set.
+// are read through tensor maps of the packed rows), dt_bias is set and
+// row_inv holds the inverse RMS of every B and C row ([rows][2 G R]: the G R
+// B rows, then the G R C rows, as launch_row_rms writes them).
 struct ScanArgs {
   const float *c, *b, *x, *z, *adt, *dt, *trap, *angle, *c_bias, *b_bias, *d;
   const float *mimo_x, *mimo_z, *mimo_o, *norm_weight;  // null for SISO
   float* out;
   const float* dt_bias;  // packed-projection scan only
+  const float* row_inv;  // packed-projection scan only
 };
 
 struct StepState {
@@ -74,6 +77,10 @@ constexpr uint32_t kStatusUndrained = 0x44524e58u;  // "DRNX"
 
 // Launchers: return cudaSuccess or the launch error. Each increments the
 // library's launch counter by the number of kernels it enqueued.
+// Inverse RMS of every B and C row of the packed projection (W, I, N
+// multiples of 4 and N <= 128), computed exactly as the preprocess computes it
+// before scaling the row: inv[row][j] for the j-th of the 2 G R rows.
+cudaError_t launch_row_rms(const PreGeom& g, const float* projected, float* inv, cudaStream_t s);
 cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const float* dt_bias,
                               const PreOut& o, cudaStream_t s);
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,

@@ -167,6 +167,7 @@ __host__ __device__ constexpr int ilog2c(int v) { return v <= 1 ? 0 : 1 + ilog2c
 // warp's token i.
 struct TokenPreload {
   float dt, adt, trap;
+  float inv_b, inv_c;  // packed projection: inverse RMS of the token's B / C row
   float ang[16];
 };
 
@@ -177,6 +178,7 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
                                                const ScanGeom& g, int64_t tok, int cn, int L,
                                                int TPW, int A, int H, int h, int warp, int lane) {
   pl.dt = pl.adt = pl.trap = 0.f;
+  pl.inv_b = pl.inv_c = 1.f;
   const int tw = TPW * warp + lane;
   const int64_t rs = PACKED ? (int64_t)g.W : (int64_t)H;  // row stride of the scalar columns
   // packed: one softplus per lane, lanes 0 .. TPW on dt_raw + dt_bias and
@@ -197,6 +199,11 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
     if constexpr (PACKED) {
       pl.dt = pre_dt_sp(sp_dt, g.dt_min, g.dt_max);
       pl.adt = pre_adt_sp(sp_a, g.a_floor, pl.dt);
+      // (SISO: one B and one C row per group)
+      const int grp = h / (H / g.G);
+      const float* ri = a.row_inv + (tok + tw) * 2 * g.G;
+      pl.inv_b = ri[grp];
+      pl.inv_c = ri[g.G + grp];
     } else {
       pl.dt = a.dt[sc];
       pl.adt = a.adt[sc];
@@ -846,63 +853,15 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
           if (!ok) abort_flag = 1;
           if (pendC == it) pendC = -1;
           if (pendB == it) pendB = -1;
-          // Packed projection: the B / C rows arrive raw and are RMS-normalised
-          // here. The row's float4 groups q = 0 .. N/4 - 1 are spread over the
-          // four lanes of the row (lane jl holds the groups q = jl + 4m), and
-          // their sums of squares are added in the order of the preprocess
-          // kernel's butterfly over q (bits 4, 3, 2 of q here, then bits 1 and
-          // 0 across the lanes), so that the normalised rows have its bits.
+          // Packed projection: the B / C rows arrive raw and are scaled here by
+          // their inverse RMS, which a pass over the packed rows has computed
+          // exactly as the preprocess does (this row's token is the warp's
+          // token ti, whose preloaded scalars sit in lane ti)
           float inv_c = 1.f, inv_b = 1.f;
           if constexpr (PACKED) {
-            static_assert(KA % 16 == 0 && KN <= 128, "group classes need A % 16 == 0");
-            // sums of squares of the lane's groups (C and B rows in the two
-            // halves of each paired FMA chain: per lane the preprocess's chain)
-            float sc[8], sb[8];
-#pragma unroll
-            for (int m = 0; m < 8; ++m) sc[m] = sb[m] = 0.f;
-            auto sumsq2 = [](float4 u, float4 v, float& su, float& sv) {
-              float2 r = __fmul2_rn(make_float2(u.x, v.x), make_float2(u.x, v.x));
-              r = __ffma2_rn(make_float2(u.y, v.y), make_float2(u.y, v.y), r);
-              r = __ffma2_rn(make_float2(u.z, v.z), make_float2(u.z, v.z), r);
-              r = __ffma2_rn(make_float2(u.w, v.w), make_float2(u.w, v.w), r);
-              su = r.x;
-              sv = r.y;
-            };
-#pragma unroll
-            for (int jb = 0; jb < QW4; ++jb) {
-              if (jb < PQ / 4) {  // rotary item: groups j and j + A/4 (m = jb, jb + A/16)
-                const int n0 = 16 * jb + 4 * jl;
-                const float4 bu = *reinterpret_cast<const float4*>(sK + toff(rho, n0));
-                const float4 bw = *reinterpret_cast<const float4*>(sK + toff(rho, n0 + A));
-                if (!SUMMARY) {
-                  const float4 cu = *reinterpret_cast<const float4*>(sQ + toff(rho, n0));
-                  const float4 cw = *reinterpret_cast<const float4*>(sQ + toff(rho, n0 + A));
-                  sumsq2(cu, bu, sc[jb], sb[jb]);
-                  sumsq2(cw, bw, sc[jb + KA / 16], sb[jb + KA / 16]);
-                } else {
-                  sumsq2(bu, bw, sb[jb], sb[jb + KA / 16]);
-                }
-              } else {            // plain item: group A/4 + j (m = A/16 + jb)
-                const int n0 = KA + 16 * jb + 4 * jl;
-                const float4 bu = *reinterpret_cast<const float4*>(sK + toff(rho, n0));
-                const float4 cu = SUMMARY ? bu : *reinterpret_cast<const float4*>(sQ + toff(rho, n0));
-                sumsq2(cu, bu, sc[KA / 16 + jb], sb[KA / 16 + jb]);
-              }
-            }
-            auto tree = [](const float* v) {
-              return __fadd_rn(__fadd_rn(__fadd_rn(v[0], v[4]), __fadd_rn(v[2], v[6])),
-                               __fadd_rn(__fadd_rn(v[1], v[5]), __fadd_rn(v[3], v[7])));
-            };
-            float tcs = tree(sc), tbs = tree(sb);
-            tcs = __fadd_rn(tcs, __shfl_xor_sync(0xffffffffu, tcs, 16));
-            tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 16));
-            tcs = __fadd_rn(tcs, __shfl_xor_sync(0xffffffffu, tcs, 8));
-            tbs = __fadd_rn(tbs, __shfl_xor_sync(0xffffffffu, tbs, 8));
-            // the four lanes of a row hold both totals: lanes with an even jl
-            // invert the C total, odd ones the B total, and exchange
-            const float r = rms_inv((jl & 1) ? tbs : tcs, N, g.eps);
-            inv_c = __shfl_sync(0xffffffffu, r, lane & ~8);
-            inv_b = __shfl_sync(0xffffffffu, r, lane | 8);
+            static_assert(KR == 1, "the packed projection is read by SISO instances only");
+            inv_c = __shfl_sync(0xffffffffu, pl.inv_c, ti);
+            inv_b = __shfl_sync(0xffffffffu, pl.inv_b, ti);
           }
           // (the raw row times its inverse RMS, as the preprocess writes it)
           // (never merged with the bias add that follows, so the normalised
