@@ -102,28 +102,44 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
   }
 }
 
-// One warp per (row, B/C row): the row's float4 groups in lanes 0 .. N/4 - 1,
-// the same sum of squares, butterfly and inverse as k_preprocess<true>.
+// One warp per kRmsUnits (row, B/C row) units, their loads issued together:
+// each unit's float4 groups in lanes 0 .. N/4 - 1, the same sum of squares,
+// butterfly and inverse as k_preprocess<true>.
+constexpr int kRmsUnits = 4;
 __global__ void __launch_bounds__(kThreads) k_row_rms(PreGeom g, const float* __restrict__ proj,
                                                       float* __restrict__ inv) {
+  // the packed scan that follows may start its prologue now (it waits for
+  // this grid's results before reading them)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int RG2 = 2 * g.G * g.R;
-  const int64_t unit = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-  if (unit >= g.rows * RG2) return;
-  const int64_t r = unit / RG2;
-  const int j = (int)(unit - r * RG2);
-  const float* src = proj + r * (int64_t)g.W + 2 * (int64_t)g.I + (int64_t)j * g.N;
-  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (lane < (g.N >> 2)) v = __ldcs(reinterpret_cast<const float4*>(src) + lane);
-  const float ss = warp_sum(sumsq4(v));
-  if (lane == 0) inv[unit] = rms_inv(ss, g.N, g.eps);
+  const int64_t units = g.rows * RG2;
+  const int64_t u0 = ((int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5)) * kRmsUnits;
+  float4 v[kRmsUnits];
+#pragma unroll
+  for (int k = 0; k < kRmsUnits; ++k) {
+    const int64_t unit = u0 + k;
+    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (unit < units && lane < (g.N >> 2)) {
+      const int64_t r = unit / RG2;
+      const int j = (int)(unit - r * RG2);
+      const float* src = proj + r * (int64_t)g.W + 2 * (int64_t)g.I + (int64_t)j * g.N;
+      v[k] = __ldcs(reinterpret_cast<const float4*>(src) + lane);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kRmsUnits; ++k) {
+    const float ss = warp_sum(sumsq4(v[k]));
+    if (lane == 0 && u0 + k < units) inv[u0 + k] = rms_inv(ss, g.N, g.eps);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_row_rms(const PreGeom& g, const float* projected, float* inv, cudaStream_t s) {
   const int64_t units = g.rows * 2 * g.G * g.R;
-  const int64_t blocks = (units + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t per_block = (int64_t)(kThreads / 32) * kRmsUnits;
+  const int64_t blocks = (units + per_block - 1) / per_block;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
   k_row_rms<<<(unsigned)blocks, kThreads, 0, s>>>(g, projected, inv);
   count_launches(1);

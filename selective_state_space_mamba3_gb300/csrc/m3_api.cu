@@ -174,14 +174,18 @@ using ChunkLauncher = cudaError_t (*)(const ScanGeom&, const ScanArgs&, uint32_t
 // The chunked scan: status word cleared, the step state converted into the
 // kernel's entry state (prefill), then one main pass, or for split sequences a
 // summary pass, the prefix over segments and the main pass.
+// after_kernel: the caller has cleared the status word and launched, just
+// before, a kernel whose outputs the scan reads (the packed scan's row norms):
+// the first scan launch then follows it as a programmatic dependent launch.
 cudaError_t run_chunked(const ScanGeom& g, const ScanArgs& a, const StepState* st, void* ws,
-                        cudaStream_t s, ChunkLauncher launch_scan_chunk) {
+                        cudaStream_t s, ChunkLauncher launch_scan_chunk,
+                        bool after_kernel = false) {
   const bool split = chunk_split_mode(g);
   const ChunkWs w = chunk_ws(g, st != nullptr);
   char* base = static_cast<char*>(ws);
   auto f = [&](size_t off) { return reinterpret_cast<float*>(base + off); };
   uint32_t* status = reinterpret_cast<uint32_t*>(base + w.status);
-  cudaError_t e = cudaMemsetAsync(status, 0, 16, s);
+  cudaError_t e = after_kernel ? cudaSuccess : cudaMemsetAsync(status, 0, 16, s);
   if (e != cudaSuccess) return e;
   if (st) {
     e = launch_state_init(g, a, *st, f(w.g0), f(w.th0), s);
@@ -190,6 +194,7 @@ cudaError_t run_chunked(const ScanGeom& g, const ScanArgs& a, const StepState* s
   ChunkIO io{};
   io.seg_len = w.seg_len;
   io.nseg = w.nseg;
+  io.pdl = after_kernel && w.nseg == 1;
   if (st) {
     io.g_last = st->ssm;
     io.th_last = st->angle;
@@ -206,6 +211,7 @@ cudaError_t run_chunked(const ScanGeom& g, const ScanArgs& a, const StepState* s
   ChunkIO sum{};
   sum.seg_len = w.seg_len;
   sum.nseg = w.nseg;
+  sum.pdl = after_kernel;
   sum.g1 = f(w.gsum);
   sum.th1 = f(w.thsum);
   sum.e1 = f(w.esum);
@@ -439,12 +445,16 @@ static int packed_common(const m3_ssm_config* cfg, const m3_preprocess_config* p
     // the rows' B / C inverse RMS, then the scan: x, z and the scalar columns
     // of the packed rows, C / B through tensor maps
     float* inv = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.scan_bytes);
+    // (the status word is cleared first, so that the scan directly follows the
+    // row-norm pass in the stream)
+    if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return M3_ERR_CUDA;
     if (launch_row_rms(p, projected, inv, s) != cudaSuccess) return M3_ERR_CUDA;
     const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.R * p.N;
     ScanArgs a{projected, projected, projected + I, projected, projected + o_s + p.H,
                projected + o_s, projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias,
                b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias, inv};
-    return cuda_status(run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed));
+    return cuda_status(
+        run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed, /*after_kernel=*/true));
   }
   char* w = static_cast<char*>(workspace);
   if (!use_chunk(g) && cudaMemsetAsync(w, 0, 16, s) != cudaSuccess) return M3_ERR_CUDA;

@@ -57,6 +57,10 @@ struct PreOut {
 // [cta][P][N] with cta = bh * nseg + seg; angles [cta][A].
 struct ChunkIO {
   int seg_len, nseg;
+  // launched as a programmatic dependent of the kernel just before it in the
+  // stream (the packed scan after its row-norm pass): wait for that kernel's
+  // results before the first token preload
+  int pdl;
   const float* g0;   // initial state per CTA (null: zero)
   const float* th0;  // initial cumulative angle per CTA (null: zero)
   float* g1;         // final state per CTA (null: not written)

@@ -581,6 +581,12 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   }
 
   TokenPreload pl;
+  // a programmatic dependent launch runs the prologue above (and the first C /
+  // B row copies) under the tail of the kernel before it; its results (the row
+  // norms the preload reads) are waited for here
+  if constexpr (PACKED) {
+    if (io.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");
+  }
   preload_tokens<PACKED>(pl, a, g, (int64_t)b * L + l0, l0, L, TPW, A, H, h, warp, lane);
   float esum = 0.f;  // sum of adt over the segment
   float lgE = 0.f;   // G = e^{lgE} G~ (identical in every thread)
@@ -1611,6 +1617,19 @@ cudaError_t run_chunk(const ScanGeom& g, const ScanArgs& a, uint32_t* status, co
                         : k_scan_chunk<MP, MIMO, false, KN, KA, KR, KP, SPLIT, PACKED>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
+  if (PACKED && io.pdl) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, g, a, lay, io, status, tmC, tmB);
+  }
   kernel<<<grid, kThreads, bytes, s>>>(g, a, lay, io, status, tmC, tmB);
   return cudaSuccess;
 }
