@@ -102,15 +102,31 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
   }
 }
 
-// One warp per kRmsUnits (row, B/C row) units, their loads issued together:
-// each unit's float4 groups in lanes 0 .. N/4 - 1, the same sum of squares,
-// butterfly and inverse as k_preprocess<true>.
+// Per-row scalars of the packed scan, computed exactly as k_preprocess<true>
+// computes them: blocks [0, nb_rms) give one warp kRmsUnits (row, B/C row)
+// units with their loads issued together (each unit's float4 groups in lanes
+// 0 .. N/4 - 1, the same sum of squares, butterfly and inverse); the other
+// blocks give one thread per (row, head) its dt and adt.
 constexpr int kRmsUnits = 4;
-__global__ void __launch_bounds__(kThreads) k_row_rms(PreGeom g, const float* __restrict__ proj,
-                                                      float* __restrict__ inv) {
+__global__ void __launch_bounds__(kThreads) k_row_pre(PreGeom g, const float* __restrict__ proj,
+                                                      const float* __restrict__ dt_bias,
+                                                      float* __restrict__ inv,
+                                                      float* __restrict__ dt,
+                                                      float* __restrict__ adt, int nb_rms) {
   // the packed scan that follows may start its prologue now (it waits for
   // this grid's results before reading them)
   asm volatile("griddepcontrol.launch_dependents;");
+  if ((int)blockIdx.x >= nb_rms) {
+    const int64_t u = (int64_t)(blockIdx.x - nb_rms) * kThreads + threadIdx.x;
+    if (u >= g.rows * g.H) return;
+    const int64_t r = u / g.H;
+    const int h = (int)(u - r * g.H);
+    const float* s = proj + r * (int64_t)g.W + 2 * (int64_t)g.I + 2 * (int64_t)g.G * g.R * g.N;
+    const float d = pre_dt(__ldcs(s + h), __ldg(dt_bias + h), g.dt_min, g.dt_max);
+    dt[u] = d;
+    adt[u] = pre_adt(__ldcs(s + g.H + h), g.a_floor, d);
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int RG2 = 2 * g.G * g.R;
   const int64_t units = g.rows * RG2;
@@ -136,12 +152,15 @@ __global__ void __launch_bounds__(kThreads) k_row_rms(PreGeom g, const float* __
 
 }  // namespace
 
-cudaError_t launch_row_rms(const PreGeom& g, const float* projected, float* inv, cudaStream_t s) {
+cudaError_t launch_row_pre(const PreGeom& g, const float* projected, const float* dt_bias,
+                           float* inv, float* dt, float* adt, cudaStream_t s) {
   const int64_t units = g.rows * 2 * g.G * g.R;
   const int64_t per_block = (int64_t)(kThreads / 32) * kRmsUnits;
-  const int64_t blocks = (units + per_block - 1) / per_block;
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  k_row_rms<<<(unsigned)blocks, kThreads, 0, s>>>(g, projected, inv);
+  const int64_t nb_rms = (units + per_block - 1) / per_block;
+  const int64_t nb_dt = (g.rows * g.H + kThreads - 1) / kThreads;
+  if (nb_rms + nb_dt > 0x7fffffff) return cudaErrorInvalidValue;
+  k_row_pre<<<(unsigned)(nb_rms + nb_dt), kThreads, 0, s>>>(g, projected, dt_bias, inv, dt, adt,
+                                                            (int)nb_rms);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -240,8 +240,9 @@ cudaError_t launch_scan(const ScanGeom& g, const ScanArgs& a, const StepState* s
 // the packed rows in the latency-bound MIMO kernel).
 namespace {
 // Workspace: the scan's own workspace first (its status word at offset 0, where
-// m3_workspace_status reads it), then, fused, the rows' B / C inverse RMS at
-// scan_bytes, or, otherwise, the preprocess outputs at scan_bytes + off[i].
+// m3_workspace_status reads it), then, fused, the row pass's outputs (B / C
+// inverse RMS, dt, adt) at off[0..2], or, otherwise, the preprocess outputs at
+// off[0..7].
 struct PackedPlan {
   bool fused;
   size_t scan_bytes;
@@ -256,7 +257,11 @@ PackedPlan packed_plan(const ScanGeom& g, const PreGeom& p) {
   // scan does not use but which is cleared for m3_workspace_status)
   pl.scan_bytes = std::max<size_t>(256, (scan_workspace_bytes(g, false) + 255) / 256 * 256);
   if (pl.fused) {
-    pl.bytes = pl.scan_bytes + ((size_t)p.rows * 2 * p.G * p.R * 4 + 255) / 256 * 256;
+    // the row pass's outputs: B / C inverse RMS, then dt and adt
+    pl.off[0] = pl.scan_bytes;
+    pl.off[1] = pl.off[0] + ((size_t)p.rows * 2 * p.G * p.R * 4 + 255) / 256 * 256;
+    pl.off[2] = pl.off[1] + ((size_t)p.rows * p.H * 4 + 255) / 256 * 256;
+    pl.bytes = pl.off[2] + ((size_t)p.rows * p.H * 4 + 255) / 256 * 256;
     return pl;
   }
   const size_t rows = (size_t)p.rows;
@@ -444,15 +449,18 @@ static int packed_common(const m3_ssm_config* cfg, const m3_preprocess_config* p
   if (pl.fused) {
     // the rows' B / C inverse RMS, then the scan: x, z and the scalar columns
     // of the packed rows, C / B through tensor maps
-    float* inv = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.scan_bytes);
+    char* wb = static_cast<char*>(workspace);
+    float* inv = reinterpret_cast<float*>(wb + pl.off[0]);
+    float* dt = reinterpret_cast<float*>(wb + pl.off[1]);
+    float* adt = reinterpret_cast<float*>(wb + pl.off[2]);
     // (the status word is cleared first, so that the scan directly follows the
-    // row-norm pass in the stream)
+    // row pass in the stream)
     if (cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return M3_ERR_CUDA;
-    if (launch_row_rms(p, projected, inv, s) != cudaSuccess) return M3_ERR_CUDA;
+    if (launch_row_pre(p, projected, dt_bias, inv, dt, adt, s) != cudaSuccess) return M3_ERR_CUDA;
     const int64_t I = p.I, o_s = 2 * I + 2 * (int64_t)p.G * p.R * p.N;
-    ScanArgs a{projected, projected, projected + I, projected, projected + o_s + p.H,
-               projected + o_s, projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias,
-               b_bias, d, mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias, inv};
+    ScanArgs a{projected, projected, projected + I, projected, adt, dt,
+               projected + o_s + 2 * p.H, projected + o_s + 3 * p.H, c_bias, b_bias, d,
+               mimo_x, mimo_z, mimo_o, norm_weight, out, dt_bias, inv};
     return cuda_status(
         run_chunked(g, a, nullptr, workspace, s, launch_scan_chunk_packed, /*after_kernel=*/true));
   }

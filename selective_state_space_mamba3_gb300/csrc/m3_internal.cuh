@@ -24,11 +24,11 @@ struct ScanGeom {
 };
 
 // Scan operands. For the packed-projection scan, x and z point at their
-// columns of the packed rows, dt / adt / trap / angle at the dt_raw / a_raw /
-// trap / angle columns (row stride W), c and b are unused (the C and B rows
-// are read through tensor maps of the packed rows), dt_bias is set and
+// columns of the packed rows, trap / angle at the trap / angle columns (row
+// stride W), dt / adt at the row pass's [rows][H] arrays, c and b are unused
+// (the C and B rows are read through tensor maps of the packed rows) and
 // row_inv holds the inverse RMS of every B and C row ([rows][2 G R]: the G R
-// B rows, then the G R C rows, as launch_row_rms writes them).
+// B rows, then the G R C rows, as launch_row_pre writes them).
 struct ScanArgs {
   const float *c, *b, *x, *z, *adt, *dt, *trap, *angle, *c_bias, *b_bias, *d;
   const float *mimo_x, *mimo_z, *mimo_o, *norm_weight;  // null for SISO
@@ -81,10 +81,12 @@ constexpr uint32_t kStatusUndrained = 0x44524e58u;  // "DRNX"
 
 // Launchers: return cudaSuccess or the launch error. Each increments the
 // library's launch counter by the number of kernels it enqueued.
-// Inverse RMS of every B and C row of the packed projection (W, I, N
-// multiples of 4 and N <= 128), computed exactly as the preprocess computes it
-// before scaling the row: inv[row][j] for the j-th of the 2 G R rows.
-cudaError_t launch_row_rms(const PreGeom& g, const float* projected, float* inv, cudaStream_t s);
+// Per-row scalars of the packed scan, computed exactly as the preprocess
+// computes them (W, I, N multiples of 4 and N <= 128): the inverse RMS of
+// every B and C row, inv[row][j] for the j-th of the 2 G R rows, and the
+// clamped dt and floored adt, dt[row][h] and adt[row][h].
+cudaError_t launch_row_pre(const PreGeom& g, const float* projected, const float* dt_bias,
+                           float* inv, float* dt, float* adt, cudaStream_t s);
 cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const float* dt_bias,
                               const PreOut& o, cudaStream_t s);
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
@@ -145,19 +147,11 @@ __device__ __forceinline__ float silu_f(float v) { return v * sigmoid_f(v); }
 // clamped dt, the floored negative log decay adt, the sum of squares of four
 // B/C values (a fixed FMA chain), and the inverse RMS of a row from its sum of
 // squares (IEEE division and square root).
-// (pre_dt_sp / pre_adt_sp take the softplus already formed, for callers that
-// compute the two softplus maps in different lanes)
-__device__ __forceinline__ float pre_dt_sp(float sp, float lo, float hi) {
-  return fminf(fmaxf(sp, lo), hi);
-}
-__device__ __forceinline__ float pre_adt_sp(float sp_a, float a_floor, float dt) {
-  return __fmul_rn(-fmaxf(sp_a, a_floor), dt);
-}
 __device__ __forceinline__ float pre_dt(float raw, float bias, float lo, float hi) {
-  return pre_dt_sp(softplus_f(__fadd_rn(raw, bias)), lo, hi);
+  return fminf(fmaxf(softplus_f(__fadd_rn(raw, bias)), lo), hi);
 }
 __device__ __forceinline__ float pre_adt(float a_raw, float a_floor, float dt) {
-  return pre_adt_sp(softplus_f(a_raw), a_floor, dt);
+  return __fmul_rn(-fmaxf(softplus_f(a_raw), a_floor), dt);
 }
 __device__ __forceinline__ float sumsq4(float4 v) {
   return __fmaf_rn(v.w, v.w, __fmaf_rn(v.z, v.z, __fmaf_rn(v.y, v.y, __fmul_rn(v.x, v.x))));

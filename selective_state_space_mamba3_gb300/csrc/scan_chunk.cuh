@@ -171,8 +171,8 @@ struct TokenPreload {
   float ang[16];
 };
 
-// Packed projection (PACKED): the columns dt_raw / a_raw / trap / angle of the
-// packed rows (row stride W), with dt and adt formed by the preprocess maps.
+// Packed projection (PACKED): trap and angle from their columns of the packed
+// rows (row stride W), dt / adt and the B / C inverse RMS from the row pass.
 template <bool PACKED>
 __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs& a,
                                                const ScanGeom& g, int64_t tok, int cn, int L,
@@ -180,35 +180,19 @@ __device__ __forceinline__ void preload_tokens(TokenPreload& pl, const ScanArgs&
   pl.dt = pl.adt = pl.trap = 0.f;
   pl.inv_b = pl.inv_c = 1.f;
   const int tw = TPW * warp + lane;
-  const int64_t rs = PACKED ? (int64_t)g.W : (int64_t)H;  // row stride of the scalar columns
-  // packed: one softplus per lane, lanes 0 .. TPW on dt_raw + dt_bias and
-  // lanes 16 .. 16 + TPW on a_raw of the same tokens
-  float sp_a = 0.f, sp_dt = 0.f;
-  if constexpr (PACKED) {
-    const int li = lane & 15, twl = TPW * warp + li;
-    float sp = 0.f;
-    if (li <= TPW && cn + twl < L) {
-      const int64_t sc = (tok + twl) * rs + h;
-      sp = softplus_f(lane < 16 ? __fadd_rn(a.dt[sc], a.dt_bias[h]) : a.adt[sc]);
-    }
-    sp_dt = sp;
-    sp_a = __shfl_down_sync(0xffffffffu, sp, 16);
-  }
+  const int64_t rs = PACKED ? (int64_t)g.W : (int64_t)H;  // row stride of the trap column
   if (lane <= TPW && cn + tw < L) {
-    const int64_t sc = (tok + tw) * rs + h;
+    const int64_t sc = (tok + tw) * H + h;
+    pl.dt = a.dt[sc];
+    pl.adt = a.adt[sc];
+    pl.trap = a.trap[(tok + tw) * rs + h];
     if constexpr (PACKED) {
-      pl.dt = pre_dt_sp(sp_dt, g.dt_min, g.dt_max);
-      pl.adt = pre_adt_sp(sp_a, g.a_floor, pl.dt);
       // (SISO: one B and one C row per group)
       const int grp = h / (H / g.G);
       const float* ri = a.row_inv + (tok + tw) * 2 * g.G;
       pl.inv_b = ri[grp];
       pl.inv_c = ri[g.G + grp];
-    } else {
-      pl.dt = a.dt[sc];
-      pl.adt = a.adt[sc];
     }
-    pl.trap = a.trap[sc];
   }
   const int64_t ars = PACKED ? (int64_t)g.W : (int64_t)A;  // row stride of the angle columns
 #pragma unroll
