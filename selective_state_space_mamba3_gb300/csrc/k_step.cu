@@ -122,9 +122,30 @@ __device__ __forceinline__ void step_output(StepSmem<RMAX>& sm, const ScanGeom& 
     }
     return;
   }
+  // (row p, rank r) of thread 4 p + r when R <= 4 and P <= 64: the gated rank
+  // values of a row in four neighbouring lanes, summed in rank order by the
+  // rank-0 lane; otherwise thread p loops over the ranks
+  const bool quad = RMAX == 4 && P <= kThreads / 4;
+  const int p = quad ? tid >> 2 : tid;
+  const int r0 = quad ? tid & 3 : 0;
   float ov = 0.f;
-  const int p = tid;
-  if (p < P) {
+  if (quad) {
+    float term = 0.f;
+    if (p < P && r0 < R) {
+      float yv = sm.y[r0 * P + p];
+      if (g.has_z) yv *= silu_f(sm.zz[p] * a.mimo_z[((int64_t)h * R + r0) * P + p]);
+      term = a.mimo_o[((int64_t)h * R + r0) * P + p] * yv;
+    }
+    // ov = ((t0 + t1) + t2) + t3 in the rank-0 lane, as the loop below adds
+    const float t1 = __shfl_down_sync(0xffffffffu, term, 1);
+    const float t2 = __shfl_down_sync(0xffffffffu, term, 2);
+    const float t3 = __shfl_down_sync(0xffffffffu, term, 3);
+    ov = term;
+    if (R > 1) ov += t1;
+    if (R > 2) ov += t2;
+    if (R > 3) ov += t3;
+    if (r0 != 0) ov = 0.f;
+  } else if (p < P) {
     for (int r = 0; r < R; ++r) {
       float yv = sm.y[r * P + p];
       if (g.has_z) yv *= silu_f(sm.zz[p] * a.mimo_z[((int64_t)h * R + r) * P + p]);
@@ -140,7 +161,7 @@ __device__ __forceinline__ void step_output(StepSmem<RMAX>& sm, const ScanGeom& 
     const float inv = 1.0f / sqrtf(tot / (float)P + 1.0e-5f);
     if (p < P) ov = ov * inv * a.norm_weight[(int64_t)h * P + p];
   }
-  if (p < P) outp[p] = ov;
+  if (p < P && r0 == 0) outp[p] = ov;
 }
 
 // Bulk-copy path (N % 4 == 0): the state travels HBM -> shared -> HBM as two
@@ -223,23 +244,94 @@ __global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : (RMAX == 4 ? 5 : 4))
       }
     }
   };
+  // rows pa and pb together (each with row_update's arithmetic), the key and
+  // query float4s loaded once for both
+  auto row_update2 = [&](int pa, int pb, int l, float* acc_a, float* acc_b) {
+    float4* hpa = reinterpret_cast<float4*>(hsm + pa * N) + l;
+    float4* hpb = reinterpret_cast<float4*>(hsm + pb * N) + l;
+    float4 ha = *hpa, hb = *hpb;
+    float4 ua = make_float4(0.f, 0.f, 0.f, 0.f), ub = ua;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const float cpa = sdec * sm.vp[r * P + pa], cca = gam * sm.v[r * P + pa];
+        const float cpb = sdec * sm.vp[r * P + pb], ccb = gam * sm.v[r * P + pb];
+        const float4 kp4 = reinterpret_cast<const float4*>(sm.kp + r * N)[l];
+        const float4 k4 = reinterpret_cast<const float4*>(sm.k + r * N)[l];
+        ua.x += cpa * kp4.x + cca * k4.x;
+        ua.y += cpa * kp4.y + cca * k4.y;
+        ua.z += cpa * kp4.z + cca * k4.z;
+        ua.w += cpa * kp4.w + cca * k4.w;
+        ub.x += cpb * kp4.x + ccb * k4.x;
+        ub.y += cpb * kp4.y + ccb * k4.y;
+        ub.z += cpb * kp4.z + ccb * k4.z;
+        ub.w += cpb * kp4.w + ccb * k4.w;
+      }
+    }
+    ha.x = decay * ha.x + ua.x;
+    ha.y = decay * ha.y + ua.y;
+    ha.z = decay * ha.z + ua.z;
+    ha.w = decay * ha.w + ua.w;
+    hb.x = decay * hb.x + ub.x;
+    hb.y = decay * hb.y + ub.y;
+    hb.z = decay * hb.z + ub.z;
+    hb.w = decay * hb.w + ub.w;
+    *hpa = ha;
+    *hpb = hb;
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) {
+      if (r < R) {
+        const float4 q4 = reinterpret_cast<const float4*>(sm.q + r * N)[l];
+        acc_a[r] = ha.x * q4.x + ha.y * q4.y + ha.z * q4.z + ha.w * q4.w;
+        acc_b[r] = hb.x * q4.x + hb.y * q4.y + hb.z * q4.z + hb.w * q4.w;
+      }
+    }
+  };
   if (N4 <= 16) {
-    // rows of at most 16 float4: each half warp takes a row (rows p and
-    // p + 8 per step) and reduces its readouts within the half
+    // rows of at most 16 float4: each half warp takes two rows per step (rows
+    // p and p + 16 of the step's 32; p + 8 in the other half), so that the
+    // key and query loads serve both
     const int hw = lane >> 4, hl = lane & 15;
-    for (int p0 = warp; p0 < P; p0 += 2 * kWarps) {
-      const int p = p0 + hw * kWarps;
-      float acc[RMAX];
+    for (int p0 = warp; p0 < P; p0 += 4 * kWarps) {
+      const int pa = p0 + hw * kWarps, pb = pa + 2 * kWarps;
+      float acc[2][RMAX];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-      if (p < P && hl < N4) row_update(p, hl, acc);
+      for (int r = 0; r < RMAX; ++r) acc[0][r] = acc[1][r] = 0.f;
+      if (hl < N4) {
+        if (pb < P)
+          row_update2(pa, pb, hl, acc[0], acc[1]);
+        else if (pa < P)
+          row_update(pa, hl, acc[0]);
+      }
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-          float v = acc[r];
+      for (int i = 0; i < 2; ++i) {
+        const int p = i ? pb : pa;
+        if constexpr (RMAX == 4) {
+          // the four rank sums over the half warp by recursive halving: lanes
+          // with bit 3 keep ranks 2, 3 and send 0, 1 (and the other way
+          // round), then bit 2 picks one rank; each rank's sum is the tree
+          // of the 8-4-2-1 butterfly
+          const bool b3 = (hl >> 3) & 1, b2 = (hl >> 2) & 1;
+          float k0 = b3 ? acc[i][2] : acc[i][0], k1 = b3 ? acc[i][3] : acc[i][1];
+          const float s0 = b3 ? acc[i][0] : acc[i][2], s1 = b3 ? acc[i][1] : acc[i][3];
+          k0 += __shfl_xor_sync(0xffffffffu, s0, 8);
+          k1 += __shfl_xor_sync(0xffffffffu, s1, 8);
+          float v = b2 ? k1 : k0;
+          v += __shfl_xor_sync(0xffffffffu, b2 ? k0 : k1, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          const int r = hl >> 2;
+          if ((hl & 3) == 0 && r < R && p < P) sm.y[r * P + p] = v + dskip * sm.v[r * P + p];
+        } else {
 #pragma unroll
-          for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-          if (hl == 0 && p < P) sm.y[r * P + p] = v + dskip * sm.v[r * P + p];
+          for (int r = 0; r < RMAX; ++r) {
+            if (r < R) {
+              float v = acc[i][r];
+#pragma unroll
+              for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+              if (hl == 0 && p < P) sm.y[r * P + p] = v + dskip * sm.v[r * P + p];
+            }
+          }
         }
       }
     }
