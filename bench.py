@@ -668,7 +668,7 @@ def run_m3(args):
     roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "algorithmic_bytes": kbytes, "ms": round(kms, 4),
-            "timed_with": "k_row_rms (the packed step's row-norm pass, same call)",
+            "timed_with": "k_row_pre (the packed step's row pass, same call)",
             "traffic": read_traffic(kname)}
 
     # end to end through the public API with host buffers (pinned), rank-local:
