@@ -336,12 +336,21 @@ __global__ void __launch_bounds__(kThreads, RMAX == 1 ? 5 : (RMAX == 4 ? 5 : 4))
       }
     }
   } else {
-    for (int p = warp; p < P; p += kWarps) {
-      float acc[RMAX];
+    // a warp per row, two rows (p and p + 8) per step sharing the key and
+    // query loads
+    for (int p = warp; p < P; p += 2 * kWarps) {
+      const int pb = p + kWarps;
+      float acc[2][RMAX];
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) acc[r] = 0.f;
-      if (lane < N4) row_update(p, lane, acc);
-      finish_row<RMAX>(sm, R, P, p, dskip, acc);
+      for (int r = 0; r < RMAX; ++r) acc[0][r] = acc[1][r] = 0.f;
+      if (lane < N4) {
+        if (pb < P)
+          row_update2(p, pb, lane, acc[0], acc[1]);
+        else
+          row_update(p, lane, acc[0]);
+      }
+      finish_row<RMAX>(sm, R, P, p, dskip, acc[0]);
+      if (pb < P) finish_row<RMAX>(sm, R, P, pb, dskip, acc[1]);
     }
   }
   // generic-proxy writes of the updated rows -> visible to the bulk store
