@@ -22,11 +22,16 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Grid (b * H + h, block of 16 state rows): one thread per float4 of the rows
+// when N % 4 == 0 (every state base is 16-byte aligned by the host checks),
+// else per element; the rank sum in rank order.
+constexpr int kInitRows = 16;
 __global__ void __launch_bounds__(kThreads) k_state_init(ScanGeom g, ScanArgs a, StepState st,
                                                           float* g0, float* th0) {
   const int bh = blockIdx.x;
   const int b = bh / g.H, h = bh % g.H;
   const int P = g.P, N = g.N, A = g.A, R = g.R;
+  const int p0 = blockIdx.y * kInitRows, p1 = min(P, p0 + kInitRows);
   const int64_t sc = (int64_t)b * g.L * g.H + h;  // token 0 of batch row b
   const float lam = sigmoid_f(a.trap[sc]);
   const float s0 = (1.0f - lam) * a.dt[sc];
@@ -34,14 +39,34 @@ __global__ void __launch_bounds__(kThreads) k_state_init(ScanGeom g, ScanArgs a,
   const float* kp = st.k + (int64_t)bh * R * N;
   const float* vp = st.v + (int64_t)bh * R * P;
   float* gd = g0 + (int64_t)bh * P * N;
-  for (int i = threadIdx.x; i < P * N; i += kThreads) {
-    const int p = i / N, n = i - p * N;
-    float acc = 0.f;
-    for (int r = 0; r < R; ++r) acc += vp[r * P + p] * kp[r * N + n];
-    gd[i] = hs[i] + s0 * acc;
+  if (N % 4 == 0) {
+    const int N4 = N >> 2;
+    for (int i = p0 * N4 + threadIdx.x; i < p1 * N4; i += kThreads) {
+      const int p = i / N4, n4 = i - p * N4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < R; ++r) {
+        const float v = vp[r * P + p];
+        const float4 k = reinterpret_cast<const float4*>(kp + r * N)[n4];
+        acc.x += v * k.x;
+        acc.y += v * k.y;
+        acc.z += v * k.z;
+        acc.w += v * k.w;
+      }
+      const float4 hv = reinterpret_cast<const float4*>(hs)[i];
+      reinterpret_cast<float4*>(gd)[i] =
+          make_float4(hv.x + s0 * acc.x, hv.y + s0 * acc.y, hv.z + s0 * acc.z, hv.w + s0 * acc.w);
+    }
+  } else {
+    for (int i = p0 * N + threadIdx.x; i < p1 * N; i += kThreads) {
+      const int p = i / N, n = i - p * N;
+      float acc = 0.f;
+      for (int r = 0; r < R; ++r) acc += vp[r * P + p] * kp[r * N + n];
+      gd[i] = hs[i] + s0 * acc;
+    }
   }
-  for (int i = threadIdx.x; i < A; i += kThreads)
-    th0[(int64_t)bh * A + i] = st.angle ? st.angle[(int64_t)bh * A + i] : 0.f;
+  if (blockIdx.y == 0)
+    for (int i = threadIdx.x; i < A; i += kThreads)
+      th0[(int64_t)bh * A + i] = st.angle ? st.angle[(int64_t)bh * A + i] : 0.f;
 }
 
 // Grid (b * H + h, unit block): one thread per unit, a unit being a rotary
@@ -99,7 +124,8 @@ __global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg,
 
 cudaError_t launch_state_init(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                               float* g0, float* th0, cudaStream_t s) {
-  k_state_init<<<(unsigned)(g.B * g.H), kThreads, 0, s>>>(g, a, st, g0, th0);
+  const dim3 grid((unsigned)(g.B * g.H), (unsigned)((g.P + kInitRows - 1) / kInitRows));
+  k_state_init<<<grid, kThreads, 0, s>>>(g, a, st, g0, th0);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -453,10 +453,26 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   {
     // initial state G (zero, or this segment's entry state)
     const float* g0 = io.g0 ? io.g0 + ((int64_t)cta * P + prow) * N : nullptr;
+    // (N % 16 == 0: a 16-column block is wholly inside the row or wholly past
+    // it, and the row bases are 16-byte aligned, so it moves as four float4s)
+    const bool vec16 = N % 16 == 0;
     for (int c = 16 * wg; c < Npad; c += 32) {
       float v[16];
+      if (vec16) {
+        const bool on = g0 && g_lane && c < N;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = (g0 && g_lane && c + j < N) ? g0[c + j] : 0.f;
+        for (int q = 0; q < 4; ++q) {
+          const float4 u = on ? reinterpret_cast<const float4*>(g0 + c)[q]
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[4 * q] = u.x;
+          v[4 * q + 1] = u.y;
+          v[4 * q + 2] = u.z;
+          v[4 * q + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = (g0 && g_lane && c + j < N) ? g0[c + j] : 0.f;
+      }
       tc::tmem_st16(tG + lane_base + c, v);
     }
   }
@@ -1495,30 +1511,30 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
     // final state (G = e^{lgE} G~), cumulative angle and decay of this segment
     const float* thb = sThBase + (it & 1) * kAngMax;
     const float gsc = expf(lgE);
-    if (io.g1) {
-      float* g1 = io.g1 + ((int64_t)cta * P + prow) * N;
+    // this thread's state row (G = e^{lgE} G~) into dst, 16 columns per load
+    // (as four float4s when N % 16 == 0, the row bases then 16-byte aligned)
+    auto store_state = [&](float* dst) {
       for (int c = 16 * wg; c < Npad; c += 32) {
         float v[16];
         tc::tmem_ld16(tG + lane_base + c, v);
-        if (g_lane) {
+        if (!g_lane) continue;
+        if (N % 16 == 0) {
+          if (c < N) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              reinterpret_cast<float4*>(dst + c)[q] =
+                  make_float4(v[4 * q] * gsc, v[4 * q + 1] * gsc, v[4 * q + 2] * gsc,
+                              v[4 * q + 3] * gsc);
+          }
+        } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c + j < N) g1[c + j] = v[j] * gsc;
+            if (c + j < N) dst[c + j] = v[j] * gsc;
         }
       }
-    }
-    if (io.g_last && l1 == L) {
-      float* gl = io.g_last + ((int64_t)bh * P + prow) * N;
-      for (int c = 16 * wg; c < Npad; c += 32) {
-        float v[16];
-        tc::tmem_ld16(tG + lane_base + c, v);
-        if (g_lane) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c + j < N) gl[c + j] = v[j] * gsc;
-        }
-      }
-    }
+    };
+    if (io.g1) store_state(io.g1 + ((int64_t)cta * P + prow) * N);
+    if (io.g_last && l1 == L) store_state(io.g_last + ((int64_t)bh * P + prow) * N);
     if (io.th1)
       for (int i = tid; i < A; i += kThreads) io.th1[(int64_t)cta * A + i] = thb[i];
     if (io.th_last && l1 == L)
