@@ -85,6 +85,26 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def tf32_peak():
+    """Dense TF32 tensor peak in TFLOP/s: the measured BF16 GEMM peak times the
+    nominal TF32 / BF16 ratio (1.1 / 2.25 PFLOP/s), else the fallback's."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        if "bf16_tflops" in p:
+            return float(p["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 x nominal 1.1/2.25"
+    return 1900.0 * 1.1 / 2.25, "fallback bf16 x nominal 1.1/2.25"
+
+
+def mma_flops_per_token_chunked(w, q=64):
+    """FLOPs the chunked scan's MMAs execute per token (single pass, Q tokens per
+    chunk): S = Q K^T and Yo = G Q^T (2 Q N each per token and head), Yi = X P^T
+    (2 Q P) and the state update (2 P N), i.e. 2 (Q (N + P) + 2 P N) per head."""
+    P, N, H = w.head_dim, w.state_size, w.num_heads
+    return 2 * (q * (N + P) + 2 * P * N) * H
+
+
 # Sources that make up each kernel the bench reports a roofline for (the
 # traffic figure of a capture is valid only while all of them are unchanged).
 KERNEL_SOURCES = {
@@ -670,6 +690,16 @@ def run_m3(args):
             "algorithmic_bytes": kbytes, "ms": round(kms, 4),
             "timed_with": "k_row_pre (the packed step's row pass, same call)",
             "traffic": read_traffic(kname)}
+    # the other roofline term: the MMA flops the kernel executes against the
+    # TF32 tensor peak (the larger of the two terms' times is the bound)
+    tpeak, tkind = tf32_peak()
+    mma_flops = tokens * mma_flops_per_token_chunked(w)
+    roof["hbm_us_at_peak"] = round(kbytes / (peak * 1e9) * 1e6, 1)
+    roof["tensor_term"] = {"executed_mma_flops": mma_flops, "peak_tflops": round(tpeak, 1),
+                           "peak_kind": tkind,
+                           "us_at_peak": round(mma_flops / (tpeak * 1e12) * 1e6, 1),
+                           "achieved_tflops": round(mma_flops / (kms * 1e-3) / 1e12, 1),
+                           "frac": round(mma_flops / (kms * 1e-3) / (tpeak * 1e12), 4)}
 
     # end to end through the public API with host buffers (pinned), rank-local:
     # every step copies its inputs in and its output out; copies and compute of

@@ -32,3 +32,17 @@ def test_no_source_reports_nothing():
     import bench
     r = bench.ClockSampler(0).stop()
     assert r["sm_mhz"] is None and r["samples"] == 0
+
+
+def test_roofline_terms_of_the_1b_workload():
+    """The two roofline terms of the 1B-layer step: 26,112 algorithmic bytes per
+    token (the packed row once, the output once) and the chunked scan's MMA work
+    2 (Q (N + P) + 2 P N) H = 1.835 MFLOP per token at Q = 64."""
+    import bench
+    from selective_state_space_mamba3_gb300 import inputs as gen
+    w = gen.SISO_1B
+    assert bench.bytes_per_token_packed(w) == 26112
+    assert bench.mma_flops_per_token_chunked(w) == 2 * (64 * (128 + 64) + 2 * 64 * 128) * 32
+    assert bench.mma_flops_per_token_chunked(w) == 1835008
+    peak, kind = bench.tf32_peak()
+    assert 400.0 < peak < 1200.0 and "1.1/2.25" in kind
