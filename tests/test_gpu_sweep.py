@@ -121,3 +121,19 @@ def test_packed_sweep(w, mode):
     assert np.array_equal(got, two_step), np.max(np.abs(got - two_step))
     ref = oracle_chain(w, p["projected"], p["dt_bias"], par, gen.PRE_DEFAULT, slice(0, 1))
     check_close(got[0:1], ref, TOL[mode], "packed " + _id(w))
+
+
+STEPS = [w.with_(sequence_length=min(w.sequence_length, 24)) for w in SISO[:12]] + \
+        [w.with_(sequence_length=min(w.sequence_length, 24)) for w in MIMO[:8]]
+
+
+@pytest.mark.parametrize("w", STEPS, ids=_id)
+def test_step_sweep(w):
+    """Single-token steps from zero states over up to 24 tokens against the
+    oracle's scan of the same tokens (FP32-exact bar)."""
+    from test_gpu_parity import run_gpu_steps
+    mimo = w.name.startswith("mimo")
+    ins = gen.scan_inputs(w)
+    got, _ = run_gpu_steps(w, ins, w.sequence_length, mimo=mimo)
+    ref = oracle_scan(w.cfg(), ins, mimo=mimo)
+    check_close(got, ref, TOL[FP32], "step " + _id(w))
