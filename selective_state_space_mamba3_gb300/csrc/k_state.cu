@@ -72,8 +72,10 @@ __global__ void __launch_bounds__(kThreads) k_state_init(ScanGeom g, ScanArgs a,
 // Grid (b * H + h, unit block): one thread per unit, a unit being a rotary
 // pair (p, a) for a < A or a single column (p, n >= 2A); each thread walks
 // the segments in order (the units are independent, so the walks of all units
-// of all sequences overlap).
-__global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg,
+// of all sequences overlap), writing each segment's entry state and folding in
+// the summaries of its `pieces` pieces (summary index (bh * nseg + s) * pieces
+// + k for piece k of segment s).
+__global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg, int pieces,
                                                             const float* g_init,
                                                             const float* th_init,
                                                             const float* gsum,
@@ -104,17 +106,20 @@ __global__ void __launch_bounds__(kThreads) k_state_prefix(ScanGeom g, int nseg,
       if (pair) ge[n0 + A] = x1;
       if (p == 0 && pair) th_entry[cs * A + u] = th;
       if (s + 1 == nseg) break;
-      const float e = esum[cs];
-      const float* gs = gsum + cs * PN + row;
-      if (pair) {
-        float sn, c;
-        sincosf(th, &sn, &c);
-        const float y0 = gs[n0], y1 = gs[n0 + A];
-        x0 = e * x0 + (y0 * c - y1 * sn);
-        x1 = e * x1 + (y0 * sn + y1 * c);
-        th += thsum[cs * A + u];
-      } else {
-        x0 = e * x0 + gs[n0];
+      for (int k = 0; k < pieces; ++k) {
+        const int64_t cp = cs * pieces + k;
+        const float e = esum[cp];
+        const float* gs = gsum + cp * PN + row;
+        if (pair) {
+          float sn, c;
+          sincosf(th, &sn, &c);
+          const float y0 = gs[n0], y1 = gs[n0 + A];
+          x0 = e * x0 + (y0 * c - y1 * sn);
+          x1 = e * x1 + (y0 * sn + y1 * c);
+          th += thsum[cp * A + u];
+        } else {
+          x0 = e * x0 + gs[n0];
+        }
       }
     }
   }
@@ -130,13 +135,13 @@ cudaError_t launch_state_init(const ScanGeom& g, const ScanArgs& a, const StepSt
   return cudaGetLastError();
 }
 
-cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, const float* g_init,
+cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, int pieces, const float* g_init,
                                 const float* th_init, const float* gsum, const float* thsum,
                                 const float* esum, float* g_entry, float* th_entry,
                                 cudaStream_t s) {
   const dim3 grid((unsigned)(g.B * g.H),
                   (unsigned)max(1, (g.P * (g.N - g.A) + kThreads - 1) / kThreads));
-  k_state_prefix<<<grid, kThreads, 0, s>>>(g, nseg, g_init, th_init, gsum, thsum, esum, g_entry,
+  k_state_prefix<<<grid, kThreads, 0, s>>>(g, nseg, pieces, g_init, th_init, gsum, thsum, esum, g_entry,
                                            th_entry);
   count_launches(1);
   return cudaGetLastError();

@@ -129,11 +129,29 @@ static int choose_nseg(const ScanGeom& g) {
   return n < 1 ? 1 : (int)n;
 }
 
+// Relative time of a pass of C CTAs that each walk c chunks, for SMs holding
+// `slots` CTAs at once: each SM takes ceil(C / SMs) CTAs in turns of `slots`;
+// a chunk of a CTA that shares its SM takes kShared times as long as one that
+// runs alone (the chunk chain is latency-bound, so two CTAs on an SM run each
+// at about 0.7 of the lone speed).
+static double pass_cost(int64_t C, int64_t c, int slots, int sms) {
+  constexpr double kShared = 1.4;
+  const int64_t k = (C + sms - 1) / sms;
+  const int64_t turns = k / slots, rem = k % slots;
+  const double t_full = slots == 1 ? 1.0 : kShared;
+  return (double)c * ((double)turns * t_full + (rem == 0 ? 0.0 : rem == 1 ? 1.0 : kShared));
+}
+
 namespace {
 // Workspace layout of the chunked path (byte offsets, 256-byte aligned).
+// Split sequences: nseg segments of seg_len tokens; the summary pass runs
+// over `pieces` equal pieces of each segment (pieces * nseg CTAs per
+// sequence, the last segment's pieces skipped), so that its short chains
+// fill the SMs that the main pass's nseg CTAs per sequence leave idle; the
+// prefix folds the pieces of a segment into the next segment's entry state.
 struct ChunkWs {
   size_t status, gsum, thsum, esum, gentry, thentry, g0, th0, bytes;
-  int nseg, seg_len;
+  int nseg, seg_len, pieces;
 };
 
 ChunkWs chunk_ws(const ScanGeom& g, bool with_state) {
@@ -143,6 +161,29 @@ ChunkWs chunk_ws(const ScanGeom& g, bool with_state) {
   const int qt = chunk_rows_per_token(g);
   const int per = (g.L + w.nseg - 1) / w.nseg;
   w.seg_len = (per + qt - 1) / qt * qt;
+  w.pieces = 1;
+  if (w.nseg > 1) {
+    // pieces per segment: the least modelled time of summary + main pass over
+    // 1..4 pieces of at least two chunks (a segment then holds a whole number
+    // of pieces, so it may grow by up to pieces - 1 chunks)
+    const int sms = sm_count(), slots = chunk_split_mode(g) ? 1 : 2;
+    const int64_t seg_chunks = w.seg_len / qt, L_chunks = ((int64_t)g.L + qt - 1) / qt;
+    double best = 0.0;
+    for (int m = 1; m <= 4; ++m) {
+      const int64_t pc = (seg_chunks + m - 1) / m;
+      if (m > 1 && pc < 2) break;
+      const int64_t sc = pc * m, ns = (L_chunks + sc - 1) / sc;
+      if (ns < 2) continue;
+      const double t = pass_cost((int64_t)bh * (ns - 1) * m, pc, slots, sms) +
+                       pass_cost((int64_t)bh * ns, sc, slots, sms);
+      if (m == 1 || t < best) {
+        best = t;
+        w.pieces = m;
+        w.seg_len = (int)(sc * qt);
+        w.nseg = (int)ns;
+      }
+    }
+  }
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -150,10 +191,10 @@ ChunkWs chunk_ws(const ScanGeom& g, bool with_state) {
     return o;
   };
   w.status = take(256);
-  const size_t ns = w.nseg > 1 ? bh * (size_t)w.nseg : 0;
-  w.gsum = take(ns * pn * 4);
-  w.thsum = take(ns * A * 4);
-  w.esum = take(ns * 4);
+  const size_t ns = w.nseg > 1 ? bh * (size_t)w.nseg : 0, np = ns * (size_t)w.pieces;
+  w.gsum = take(np * pn * 4);
+  w.thsum = take(np * A * 4);
+  w.esum = take(np * 4);
   w.gentry = take(ns * pn * 4);
   w.thentry = take(ns * A * 4);
   w.g0 = take(with_state ? bh * pn * 4 : 0);
@@ -209,15 +250,16 @@ cudaError_t run_chunked(const ScanGeom& g, const ScanArgs& a, const StepState* s
     return launch_scan_chunk(g, a, status, io, false, split, s);
   }
   ChunkIO sum{};
-  sum.seg_len = w.seg_len;
-  sum.nseg = w.nseg;
+  sum.seg_len = w.seg_len / w.pieces;
+  sum.nseg = w.nseg * w.pieces;
+  sum.sum_skip = w.pieces;
   sum.pdl = after_kernel;
   sum.g1 = f(w.gsum);
   sum.th1 = f(w.thsum);
   sum.e1 = f(w.esum);
   e = launch_scan_chunk(g, a, status, sum, true, split, s);
   if (e != cudaSuccess) return e;
-  e = launch_state_prefix(g, w.nseg, st ? f(w.g0) : nullptr, st ? f(w.th0) : nullptr, f(w.gsum),
+  e = launch_state_prefix(g, w.nseg, w.pieces, st ? f(w.g0) : nullptr, st ? f(w.th0) : nullptr, f(w.gsum),
                           f(w.thsum), f(w.esum), f(w.gentry), f(w.thentry), s);
   if (e != cudaSuccess) return e;
   io.g0 = f(w.gentry);

@@ -61,6 +61,9 @@ struct ChunkIO {
   // stream (the packed scan after its row-norm pass): wait for that kernel's
   // results before the first token preload
   int pdl;
+  // summary pass: its last sum_skip segments (the pieces of the main pass's
+  // last segment) have no use and return at once
+  int sum_skip;
   const float* g0;   // initial state per CTA (null: zero)
   const float* th0;  // initial cumulative angle per CTA (null: zero)
   float* g1;         // final state per CTA (null: not written)
@@ -96,7 +99,7 @@ cudaError_t launch_scan_seq(const ScanGeom& g, const ScanArgs& a, const StepStat
                             cudaStream_t s);
 cudaError_t launch_state_init(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                               float* g0, float* th0, cudaStream_t s);
-cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, const float* g_init,
+cudaError_t launch_state_prefix(const ScanGeom& g, int nseg, int pieces, const float* g_init,
                                 const float* th_init, const float* gsum, const float* thsum,
                                 const float* esum, float* g_entry, float* th_entry,
                                 cudaStream_t s);

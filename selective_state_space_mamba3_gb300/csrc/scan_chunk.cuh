@@ -351,8 +351,8 @@ __global__ void __launch_bounds__(kThreads, SPLIT ? 1 : 2)
   const int bh = cta / io.nseg, seg = cta - bh * io.nseg;
   const int b = bh / H, h = bh % H;
   const int l0 = seg * io.seg_len, l1 = min(L, l0 + io.seg_len);
-  // the summary of the last segment is never used
-  if (SUMMARY && seg == io.nseg - 1) return;
+  // the summaries of the main pass's last segment are never used
+  if (SUMMARY && seg >= io.nseg - io.sum_skip) return;
   const int grp = h / (H / g.G);
   const int RG = g.G * R;
 

@@ -51,12 +51,13 @@ def test_static_scratch_entry_matches_workspace_entry(mode):
 
 
 def test_static_scratch_segmented_sequences():
-    """B1 H2 L1500: two sequences cannot fill the GPU, so the TF32 path splits
-    each into segments; their summary states, angles and decays and the entry
-    states derived from them (about 0.66 MB) all live in the shared array. A
+    """B1 H2 L1000: two sequences cannot fill the GPU, so the TF32 path splits
+    each into three segments of two-chunk summary pieces; their summary states,
+    angles and decays and the entry states derived from them (about 0.59 MB)
+    all live in the shared array. A
     call at another geometry runs first, then two calls in a row; each is held
     to the oracle and to m3_siso_forward."""
-    w = gen.Workload("no-alloc segmented", 1, 1500, 2, 1, 64, 128, 32, seed_index=22)
+    w = gen.Workload("no-alloc segmented", 1, 1000, 2, 1, 64, 128, 32, seed_index=22)
     mode = m3.M3_MATH_TF32
     need = m3.m3_siso_forward_workspace(m3.ssm_config(w.cfg(), mode))
     assert 256 < need <= (1 << 20), need     # segmented, and within the array
