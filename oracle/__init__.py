@@ -10,7 +10,8 @@ the independent O(L^2) unrolled form used to pin it. The readings taken where
 the source pages are silent are listed at the top of `m3_oracle.cpp`.
 
 Pinned functions (see tests/test_oracle_pins.py): preprocess, SISO scan, SISO
-step (as the scan with explicit state), MIMO scan, MIMO step.
+step (as the scan with explicit state), MIMO scan, MIMO step; SISO adjoints
+(tests/test_oracle_backward_pins.py: central differences of the scan).
 """
 from __future__ import annotations
 
@@ -51,6 +52,9 @@ def _load():
             lib.m3o_preprocess.argtypes = [_i64] * 7 + [_f64] * 4 + [_ptr] * 10 + [ctypes.c_int]
             lib.m3o_scan.restype = ctypes.c_int
             lib.m3o_scan.argtypes = [_i64] * 8 + [ctypes.c_int] * 3 + [_ptr] * 20 + [ctypes.c_int]
+            lib.m3o_siso_backward.restype = ctypes.c_int
+            lib.m3o_siso_backward.argtypes = ([_i64] * 7 + [ctypes.c_int] * 2 + [_ptr] * 23 +
+                                              [ctypes.c_int])
             _lib = lib
     return _lib
 
@@ -133,3 +137,30 @@ def step(cfg, *args, state, **kw):
     if cfg["sequence_length"] != 1:
         raise ValueError("step requires sequence_length == 1")
     return scan(cfg, *args, state=state, **kw)
+
+
+GRAD_NAMES = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d")
+
+
+def siso_backward(cfg, dout, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, threads=None):
+    """The eleven SISO adjoints (`mamba3_siso_backward`) of the scan from a zero
+    state, given dout [B,L,H,P], the gradient of its output. Returns a dict of
+    float64 arrays keyed by GRAD_NAMES, each in its forward operand's layout:
+    c/b [B,L,G,N], x/z [B,L,H,P], adt/dt/trap [B,L,H], angle [B,L,A],
+    c_bias/b_bias [H,N], d [H]."""
+    B, L, H = cfg["batch_size"], cfg["sequence_length"], cfg["num_heads"]
+    P, N, A = cfg["head_dim"], cfg["state_size"], cfg["num_rope_angles"]
+    G = cfg["num_groups"] or H
+    if cfg.get("mimo_rank", 1) != 1 or cfg.get("has_output_norm", 0):
+        raise ValueError("oracle siso_backward: SISO only")
+    arrs = [_f32(a) for a in (dout, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d)]
+    shapes = dict(c=(B, L, G, N), b=(B, L, G, N), x=(B, L, H, P), z=(B, L, H, P),
+                  adt=(B, L, H), dt=(B, L, H), trap=(B, L, H), angle=(B, L, A),
+                  c_bias=(H, N), b_bias=(H, N), d=(H,))
+    g = {k: np.zeros(shapes[k]) for k in GRAD_NAMES}
+    rc = _load().m3o_siso_backward(B, L, H, cfg["num_groups"], P, N, A, int(cfg["has_z"]),
+                                   int(cfg["has_d"]), *[_p(a) for a in arrs],
+                                   *[_p(g[k]) for k in GRAD_NAMES], threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle siso_backward: invalid geometry")
+    return g

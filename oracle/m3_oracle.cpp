@@ -281,4 +281,203 @@ int m3o_scan(i64 B, i64 L, i64 H, i64 num_groups, i64 P, i64 N, i64 A, i64 R, in
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// SISO adjoints: reverse-mode differentiation of the token loop of m3o_scan
+// (R = 1, zero initial state), returning the eleven gradients of `SsmBackward`
+// in mamba3.rs (`mamba3_siso_backward`: c, b, x, z, adt, dt, trap, angle,
+// c_bias, b_bias, d) in the layouts of the forward operands: c/b [B,L,G,N],
+// x/z [B,L,H,P], adt/dt/trap [B,L,H], angle [B,L,A], c_bias/b_bias [H,N],
+// d [H]. dout [B,L,H,P] is the gradient of the scan's output.
+//
+// The forward pass of each (b, h) is re-run and every state h_t kept; the
+// reverse pass then walks t = L-1 .. 0 and takes the adjoint of each forward
+// statement in reverse order (the chain rule written out, nothing fused):
+//   out_t = y_t * silu(z_t):  dy_t = dout_t silu(z_t),  dz_t = dout_t y_t silu'(z_t)
+//   y_t = h_t q_t + D v_t:    Lam_t += dy_t q_t^T,  dq_t = h_t^T dy_t,
+//                             dD += dy_t . v_t,  dv_t += D dy_t
+//   h_t = a_t h_{t-1} + s_t a_t v_{t-1} k_{t-1}^T + g_t v_t k_t^T:
+//       da_t = <Lam_t, h_{t-1} + s_t v_{t-1} k_{t-1}^T>,
+//       ds_t = a_t <Lam_t, v_{t-1} k_{t-1}^T>,  dg_t = <Lam_t, v_t k_t^T>,
+//       dv_t += g_t Lam_t k_t,  dk_t += g_t Lam_t^T v_t,
+//       dv_{t-1} += s_t a_t Lam_t k_{t-1},  dk_{t-1} += s_t a_t Lam_t^T v_{t-1},
+//       Lam_{t-1} = a_t Lam_t
+//   a_t = exp(adt_t), g_t = sigmoid(trap_t) dt_t, s_t = (1 - sigmoid(trap_t)) dt_t
+//   q_t = Rot(theta_t)(C_t + c_bias), k_t = Rot(theta_t)(B_t + b_bias):
+//       d(C_t + c_bias) = Rot(theta_t)^T dq_t, and d theta_t[a] from both pairs
+//   theta_t = theta_{t-1} + dt_t angle_t: the running adjoint of theta carries
+//       back, adding to d dt_t and d angle_t.
+// Sums over heads (c, b within a group; angle over all heads) and over batch
+// and tokens (c_bias, b_bias, d) are taken after the parallel part, in a fixed
+// order. Returns 0, or 1 for an invalid geometry.
+int m3o_siso_backward(i64 B, i64 L, i64 H, i64 num_groups, i64 P, i64 N, i64 A, int has_z,
+                      int has_d, const float* dout, const float* c, const float* b,
+                      const float* x, const float* z, const float* adt, const float* dt,
+                      const float* trap, const float* angle, const float* c_bias,
+                      const float* b_bias, const float* d, double* gc, double* gb, double* gx,
+                      double* gz, double* gadt, double* gdt, double* gtrap, double* gangle,
+                      double* gc_bias, double* gb_bias, double* gd, int threads) {
+  const i64 G = num_groups == 0 ? H : num_groups;
+  if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || H % G != 0 || P <= 0 || N <= 0 || A < 0 ||
+      2 * A > N)
+    return 1;
+  const i64 hpg = H / G;
+  // per-head parts, summed below
+  std::vector<double> pc(B * L * H * N), pb(B * L * H * N), pang(B * L * H * A);
+  std::vector<double> pcb(B * H * N), pbb(B * H * N), pd(B * H);
+  parallel_for(B * H, threads, [&](i64 bh) {
+    const i64 bb = bh / H, h = bh % H, g = h / hpg;
+    const double dd = has_d ? (double)d[h] : 0.0;
+    // forward, keeping every state and per-token quantity
+    std::vector<double> hs((L + 1) * P * N, 0.0);  // hs[t + 1] = h_t, hs[0] = 0
+    std::vector<double> q(L * N), k(L * N), ch(L * N), bhat(L * N), th(L * A), v(L * P);
+    std::vector<double> al(L), ga(L), sc(L), lam(L), y(L * P);
+    std::vector<double> theta(A, 0.0), tmp(N);
+    for (i64 t = 0; t < L; ++t) {
+      const i64 tok = bb * L + t, s = tok * H + h;
+      const double l = sigmoid((double)trap[s]);
+      lam[t] = l;
+      al[t] = std::exp((double)adt[s]);
+      ga[t] = l * (double)dt[s];
+      sc[t] = (1.0 - l) * (double)dt[s];
+      for (i64 a = 0; a < A; ++a) theta[a] += (double)dt[s] * (double)angle[tok * A + a];
+      for (i64 a = 0; a < A; ++a) th[t * A + a] = theta[a];
+      for (i64 n = 0; n < N; ++n) tmp[n] = (double)c[(tok * G + g) * N + n] + (double)c_bias[h * N + n];
+      for (i64 n = 0; n < N; ++n) ch[t * N + n] = tmp[n];
+      rotate(tmp, theta, A);
+      for (i64 n = 0; n < N; ++n) q[t * N + n] = tmp[n];
+      for (i64 n = 0; n < N; ++n) tmp[n] = (double)b[(tok * G + g) * N + n] + (double)b_bias[h * N + n];
+      for (i64 n = 0; n < N; ++n) bhat[t * N + n] = tmp[n];
+      rotate(tmp, theta, A);
+      for (i64 n = 0; n < N; ++n) k[t * N + n] = tmp[n];
+      for (i64 p = 0; p < P; ++p) v[t * P + p] = (double)x[s * P + p];
+      const double* hp = &hs[t * P * N];
+      double* hc = &hs[(t + 1) * P * N];
+      for (i64 p = 0; p < P; ++p)
+        for (i64 n = 0; n < N; ++n) {
+          const double prev = t > 0 ? v[(t - 1) * P + p] * k[(t - 1) * N + n] : 0.0;
+          hc[p * N + n] = al[t] * hp[p * N + n] + sc[t] * al[t] * prev +
+                          ga[t] * v[t * P + p] * k[t * N + n];
+        }
+      for (i64 p = 0; p < P; ++p) {
+        double acc = 0.0;
+        for (i64 n = 0; n < N; ++n) acc += hc[p * N + n] * q[t * N + n];
+        y[t * P + p] = acc + dd * v[t * P + p];
+      }
+    }
+    // reverse
+    std::vector<double> Lam(P * N, 0.0), dv(L * P, 0.0), dk(L * N, 0.0), dq(N), dy(P);
+    std::vector<double> gth(A, 0.0);  // running adjoint of theta
+    double dsum = 0.0;
+    for (i64 t = L - 1; t >= 0; --t) {
+      const i64 tok = bb * L + t, s = tok * H + h;
+      // out_t = y_t * silu(z_t)
+      for (i64 p = 0; p < P; ++p) {
+        const double go = (double)dout[s * P + p];
+        if (has_z) {
+          const double zv = (double)z[s * P + p], sg = sigmoid(zv);
+          dy[p] = go * zv * sg;
+          gz[s * P + p] = go * y[t * P + p] * (sg + zv * sg * (1.0 - sg));
+        } else {
+          dy[p] = go;
+          gz[s * P + p] = 0.0;
+        }
+      }
+      // y_t = h_t q_t + D v_t
+      const double* hc = &hs[(t + 1) * P * N];
+      for (i64 n = 0; n < N; ++n) dq[n] = 0.0;
+      for (i64 p = 0; p < P; ++p) {
+        for (i64 n = 0; n < N; ++n) {
+          Lam[p * N + n] += dy[p] * q[t * N + n];
+          dq[n] += hc[p * N + n] * dy[p];
+        }
+        dsum += dy[p] * v[t * P + p];
+        dv[t * P + p] += dd * dy[p];
+      }
+      // h_t = a h_{t-1} + s a v_{t-1} k_{t-1}^T + g v_t k_t^T
+      const double* hp = &hs[t * P * N];
+      double da = 0.0, ds = 0.0, dg = 0.0;
+      for (i64 p = 0; p < P; ++p)
+        for (i64 n = 0; n < N; ++n) {
+          const double lm = Lam[p * N + n];
+          const double prev = t > 0 ? v[(t - 1) * P + p] * k[(t - 1) * N + n] : 0.0;
+          da += lm * (hp[p * N + n] + sc[t] * prev);
+          ds += al[t] * lm * prev;
+          dg += lm * v[t * P + p] * k[t * N + n];
+          dv[t * P + p] += ga[t] * lm * k[t * N + n];
+          dk[t * N + n] += ga[t] * lm * v[t * P + p];
+          if (t > 0) {
+            dv[(t - 1) * P + p] += sc[t] * al[t] * lm * k[(t - 1) * N + n];
+            dk[(t - 1) * N + n] += sc[t] * al[t] * lm * v[(t - 1) * P + p];
+          }
+        }
+      for (i64 i = 0; i < P * N; ++i) Lam[i] *= al[t];
+      // a = exp(adt), g = sigmoid(trap) dt, s = (1 - sigmoid(trap)) dt
+      gadt[s] = da * al[t];
+      double gdt_t = dg * lam[t] + ds * (1.0 - lam[t]);
+      gtrap[s] = (dg - ds) * (double)dt[s] * lam[t] * (1.0 - lam[t]);
+      for (i64 p = 0; p < P; ++p) gx[s * P + p] = dv[t * P + p];
+      // rotations: q = Rot(theta)(chat), k = Rot(theta)(bhat)
+      std::vector<double> dth(A, 0.0);
+      for (int which = 0; which < 2; ++which) {
+        const double* gr = which == 0 ? dq.data() : &dk[t * N];
+        const double* rv = which == 0 ? &q[t * N] : &k[t * N];
+        double* dst = which == 0 ? &pc[(tok * H + h) * N] : &pb[(tok * H + h) * N];
+        double* bias = which == 0 ? &pcb[bh * N] : &pbb[bh * N];
+        for (i64 n = 0; n < N; ++n) dst[n] = gr[n];  // the dims >= 2A pass through
+        for (i64 a = 0; a < A; ++a) {
+          const double cs = std::cos(th[t * A + a]), sn = std::sin(th[t * A + a]);
+          const double g0 = gr[a], g1 = gr[a + A];
+          // (u, w) -> (u cs - w sn, u sn + w cs); its transpose on the adjoint
+          dst[a] = g0 * cs + g1 * sn;
+          dst[a + A] = -g0 * sn + g1 * cs;
+          // d/dtheta of the rotated pair (r0, r1) is (-r1, r0)
+          dth[a] += -g0 * rv[a + A] + g1 * rv[a];
+        }
+        for (i64 n = 0; n < N; ++n) bias[n] += dst[n];
+      }
+      // theta_t = theta_{t-1} + dt_t angle_t
+      for (i64 a = 0; a < A; ++a) {
+        gth[a] += dth[a];
+        gdt_t += gth[a] * (double)angle[tok * A + a];
+        pang[(tok * H + h) * A + a] = gth[a] * (double)dt[s];
+      }
+      gdt[s] = gdt_t;
+    }
+    pd[bh] = dsum;
+  });
+  // sums over heads, batch and tokens, in index order
+  for (i64 tok = 0; tok < B * L; ++tok) {
+    for (i64 g = 0; g < G; ++g)
+      for (i64 n = 0; n < N; ++n) {
+        double sc_ = 0.0, sb_ = 0.0;
+        for (i64 j = 0; j < hpg; ++j) {
+          sc_ += pc[(tok * H + g * hpg + j) * N + n];
+          sb_ += pb[(tok * H + g * hpg + j) * N + n];
+        }
+        gc[(tok * G + g) * N + n] = sc_;
+        gb[(tok * G + g) * N + n] = sb_;
+      }
+    for (i64 a = 0; a < A; ++a) {
+      double sa = 0.0;
+      for (i64 h = 0; h < H; ++h) sa += pang[(tok * H + h) * A + a];
+      gangle[tok * A + a] = sa;
+    }
+  }
+  for (i64 h = 0; h < H; ++h) {
+    for (i64 n = 0; n < N; ++n) {
+      double sc_ = 0.0, sb_ = 0.0;
+      for (i64 bb = 0; bb < B; ++bb) {
+        sc_ += pcb[(bb * H + h) * N + n];
+        sb_ += pbb[(bb * H + h) * N + n];
+      }
+      gc_bias[h * N + n] = sc_;
+      gb_bias[h * N + n] = sb_;
+    }
+    double sd = 0.0;
+    for (i64 bb = 0; bb < B; ++bb) sd += pd[bb * H + h];
+    gd[h] = has_d ? sd : 0.0;
+  }
+  return 0;
+}
+
 }  // extern "C"

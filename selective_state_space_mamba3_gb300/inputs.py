@@ -197,3 +197,11 @@ def scan_params(w: Workload, salt: int = 0):
         out["mimo_o"] = _normal(rng, (H, R, P), s)
         out["norm_weight"] = (1.0 + _normal(rng, (H, P), 0.02)).astype(np.float32)
     return out
+
+
+def output_gradient(w: Workload, salt: int = 0, *, length=None):
+    """The gradient of the scan output fed to the SISO backward: dout ~ N(0,1)
+    in the output layout [B, L, H, P]."""
+    rng = rng_for(w, 500 + salt)
+    L = length or w.sequence_length
+    return _normal(rng, (w.batch_size, L, w.num_heads, w.head_dim))
