@@ -12,6 +12,7 @@
  *                       explicit step state (prefill -> decode hand-off)
  *   m3_siso_forward_packed / m3_mimo_forward_packed - `mamba3_preprocess` and
  *                       `mamba3_siso` / `mamba3_mimo` in one call
+ *   m3_siso_backward  - `mamba3_siso_backward` (the eleven SISO adjoints)
  *
  * Conventions for every entry point:
  *  - Every tensor is float32, dense row-major, in device memory owned by the
@@ -197,6 +198,36 @@ int m3_mimo_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
                     const float* d, const float* mimo_x, const float* mimo_z,
                     const float* mimo_o, const float* norm_weight, float* out,
                     void* workspace, size_t workspace_bytes, m3_stream_t stream);
+
+/*
+ * m3_siso_backward - the eleven adjoints of m3_siso_forward
+ * (`mamba3_siso_backward`, the fields of `SsmBackward`): given grad_out
+ * [B,L,H,P], the gradient of a loss with respect to the scan's output, and the
+ * forward operands, writes the gradient with respect to each operand in that
+ * operand's layout: grad_c, grad_b [B,L,G,N] (summed over the heads that share
+ * a group's rows); grad_x, grad_z [B,L,H,P]; grad_adt, grad_dt, grad_trap
+ * [B,L,H]; grad_angle [B,L,A] (summed over the heads; may be NULL when
+ * A == 0); grad_c_bias, grad_b_bias [H,N] (summed over batch and tokens);
+ * grad_d [H]. grad_z is zero without has_z, grad_d zero without has_d. The
+ * scan starts from a zero state, as in m3_siso_forward.
+ * Arithmetic: FP32 on the CUDA cores whatever cfg->math_mode says (two
+ * token-sequential sweeps per (b, h) and a reduction in a fixed order, so
+ * that repeated calls give the same bits). Checks: those of m3_siso_forward,
+ * plus B*L*H*N and B*L*H*A below 2^32; every pointer but angle / grad_angle
+ * (when A == 0) non-NULL and 16-byte aligned.
+ * workspace: at least m3_siso_backward_workspace() bytes (never 0), 16-byte
+ * aligned, used only during the call's kernels. Outputs must not overlap the
+ * inputs or the workspace.
+ */
+int m3_siso_backward_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_siso_backward(const m3_ssm_config* cfg, const float* grad_out, const float* c,
+                     const float* b, const float* x, const float* z, const float* adt,
+                     const float* dt, const float* trap, const float* angle,
+                     const float* c_bias, const float* b_bias, const float* d, float* grad_c,
+                     float* grad_b, float* grad_x, float* grad_z, float* grad_adt,
+                     float* grad_dt, float* grad_trap, float* grad_angle, float* grad_c_bias,
+                     float* grad_b_bias, float* grad_d, void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream);
 
 /*
  * m3_siso_prefill / m3_mimo_prefill - the scan of m3_siso_forward /

@@ -30,6 +30,7 @@ EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
             "m3_siso_forward_packed_workspace", "m3_siso_forward_packed",
             "m3_mimo_forward_packed_workspace", "m3_mimo_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
+            "m3_siso_backward_workspace", "m3_siso_backward",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
             "m3_launch_count")
@@ -106,6 +107,8 @@ def load_library():
         lib.m3_siso_prefill.argtypes = [cfgp] + [_vp] * 17 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_prefill.argtypes = [cfgp] + [_vp] * 21 + [ctypes.c_size_t, _vp]
         lib.m3_siso_step.argtypes = [cfgp] + [_vp] * 16 + [_vp]
+        lib.m3_siso_backward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_siso_backward.argtypes = [cfgp] + [_vp] * 24 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_step.argtypes = [cfgp] + [_vp] * 20 + [_vp]
         lib.m3_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
         lib.m3_selftest_wait_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int64, _vp]
@@ -257,6 +260,23 @@ def m3_siso_prefill(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_
     _check(load_library().m3_siso_prefill(ctypes.byref(cfg), *[_ptr(t) for t in (
         c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, ssm_state, angle_state, k_state,
         v_state, out)], wp, wn, _stream(stream)), "m3_siso_prefill")
+
+
+def m3_siso_backward_workspace(cfg: SsmConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_siso_backward_workspace(ctypes.byref(cfg), ctypes.byref(n)),
+           "m3_siso_backward_workspace")
+    return n.value
+
+
+def m3_siso_backward(cfg: SsmConfig, grad_out, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias,
+                     d, grad_c, grad_b, grad_x, grad_z, grad_adt, grad_dt, grad_trap, grad_angle,
+                     grad_c_bias, grad_b_bias, grad_d, workspace=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_siso_backward(ctypes.byref(cfg), *[_ptr(t) for t in (
+        grad_out, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, grad_c, grad_b, grad_x,
+        grad_z, grad_adt, grad_dt, grad_trap, grad_angle, grad_c_bias, grad_b_bias, grad_d)],
+        wp, wn, _stream(stream)), "m3_siso_backward")
 
 
 def m3_mimo_prefill(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,

@@ -460,6 +460,52 @@ int m3_siso_forward(const m3_ssm_config* cfg, const float* c, const float* b, co
   return scan_common(cfg, false, a, nullptr, workspace, workspace_bytes, stream);
 }
 
+// `mamba3_siso_backward`: the SISO geometry rules, plus the backward's
+// workspace arrays ([B,L,H,N] per-head C / B parts, [B,H,L,A] angles) below
+// 2^32 elements.
+static int resolve_backward(const m3_ssm_config* cfg, ScanGeom* g) {
+  const int st = resolve_ssm(cfg, false, g);
+  if (st != M3_OK) return st;
+  if (!count_below_u32({g->B, g->L, g->H, g->N}) || !count_below_u32({g->B, g->L, g->H, g->A}))
+    return M3_ERR_INVALID_ARGUMENT;
+  return M3_OK;
+}
+
+int m3_siso_backward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  const int st = resolve_backward(cfg, &g);
+  if (st != M3_OK) return st;
+  *bytes = backward_workspace_bytes(g);
+  return M3_OK;
+}
+
+int m3_siso_backward(const m3_ssm_config* cfg, const float* dout, const float* c, const float* b,
+                     const float* x, const float* z, const float* adt, const float* dt,
+                     const float* trap, const float* angle, const float* c_bias,
+                     const float* b_bias, const float* d, float* grad_c, float* grad_b,
+                     float* grad_x, float* grad_z, float* grad_adt, float* grad_dt,
+                     float* grad_trap, float* grad_angle, float* grad_c_bias, float* grad_b_bias,
+                     float* grad_d, void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_siso_backward");
+  ScanGeom g;
+  int st = resolve_backward(cfg, &g);
+  if (st != M3_OK) return st;
+  st = check_ptrs({dout, c, b, x, z, adt, dt, trap, c_bias, b_bias, d, grad_c, grad_b, grad_x,
+                   grad_z, grad_adt, grad_dt, grad_trap, grad_c_bias, grad_b_bias, grad_d});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(angle, g.A)) != M3_OK) return st;
+  if ((st = check_angle_ptr(grad_angle, g.A)) != M3_OK) return st;
+  const size_t need = backward_workspace_bytes(g);
+  if (!workspace || workspace_bytes < need) return M3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return M3_ERR_UNALIGNED;
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             nullptr, nullptr, nullptr, nullptr, nullptr};
+  BwdArgs o{dout, grad_c, grad_b, grad_x, grad_z, grad_adt, grad_dt, grad_trap, grad_angle,
+            grad_c_bias, grad_b_bias, grad_d};
+  return cuda_status(launch_siso_backward(g, a, o, workspace, (cudaStream_t)stream));
+}
+
 static int packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
                             bool mimo, size_t* bytes) {
   ScanGeom g;

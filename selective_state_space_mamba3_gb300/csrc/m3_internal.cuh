@@ -119,6 +119,16 @@ cudaError_t launch_scan_chunk_packed(const ScanGeom& g, const ScanArgs& a, uint3
 // `PreprocessGeometry::resolve` rules for `rows` packed rows; fills g
 int resolve_pre(const m3_preprocess_config* cfg, int64_t rows, PreGeom* g);
 
+// SISO adjoints (`mamba3_siso_backward`): the gradient of the scan output and
+// the eleven gradient outputs, each in its forward operand's layout.
+struct BwdArgs {
+  const float* dout;
+  float *gc, *gb, *gx, *gz, *gadt, *gdt, *gtrap, *gangle, *gc_bias, *gb_bias, *gd;
+};
+size_t backward_workspace_bytes(const ScanGeom& g);
+cudaError_t launch_siso_backward(const ScanGeom& g, const ScanArgs& a, const BwdArgs& o,
+                                 void* ws, cudaStream_t s);
+
 // Scan entry chosen by the host: workspace bytes for geometry g (with or
 // without a recurrent state), then launch (st null: zero state).
 size_t scan_workspace_bytes(const ScanGeom& g, bool with_state);
