@@ -13,7 +13,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
                 [--mode fp32|tf32] [--no-parts] [--part NAME]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
 mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
-mimo_step, siso_prefill_tf32) and prints its JSON, for profiling it alone.
+mimo_step, siso_prefill_tf32, siso_backward_fp32) and prints its JSON, for profiling it
+alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -74,6 +75,38 @@ def bytes_per_step_call(w):
     state = 2 * B * H * (P * N + R * N + R * P + A)
     tok = B * (3 * H * P + 2 * R * G * N + 3 * H + A)
     return 4 * (state + tok)
+
+
+def bytes_per_token_backward(w):
+    """Algorithmic HBM bytes of one token of the SISO backward: the forward
+    operands and the output gradient read once (dout, x, z [H,P]; B, C rows
+    [G,N]; adt, dt, trap [H]; angle [A]) and their gradients written once
+    (dx, dz; dB, dC; d adt, d dt, d trap; d angle)."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    H, P, N, A = w.num_heads, w.head_dim, w.state_size, w.num_rope_angles
+    return 4 * ((3 * H * P + 2 * G * N + 3 * H + A) + (2 * H * P + 2 * G * N + 3 * H + A))
+
+
+def flops_per_token_backward(w):
+    """FP32 CUDA-core flops of the two sweeps per token: per state element the
+    forward sweep's state update (3 FMA), readout (1 FMA) and dq (1 FMA), and
+    the reverse sweep's decay (1 MUL), M k, M^T v and adjoint update (3 FMA);
+    an FMA is 2 flops: 17 H P N."""
+    return 17 * w.num_heads * w.head_dim * w.state_size
+
+
+def fp32_alu_peak():
+    """FP32 CUDA-core peak in TFLOP/s: 152 SMs x 128 FP32 lanes x 2 flops per
+    FMA x the maximum SM clock (MEASURED_PEAKS.json's sm_max_mhz, else the
+    nominal 2070 MHz)."""
+    mhz, how = 2070.0, "nominal 2070 MHz"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        if "sm_max_mhz" in p:
+            mhz, how = float(p["sm_max_mhz"]), "measured sm_max_mhz"
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12, f"152 SMs x 128 FP32 lanes x 2 x {how}"
 
 
 def load_peaks():
@@ -578,6 +611,34 @@ def cpu_baseline_oracle(w, batch_rows):
             "seconds": round(dt, 3)}
 
 
+def parts_backward(torch, m3, w, peak):
+    """Supplementary: m3_siso_backward (the eleven SISO adjoints, FP32) of
+    workload w with device-resident operands and output gradient. Bound: the
+    FP32 CUDA-core rate of the two token-sequential sweeps (alu), with the HBM
+    fraction beside it."""
+    ins = gen.scan_inputs(w)
+    d = {k: torch.from_numpy(v).cuda() for k, v in ins.items()}
+    go = torch.from_numpy(gen.output_gradient(w)).cuda()
+    del ins
+    cfg = m3.ssm_config(w.cfg(), m3.M3_MATH_FP32)
+    ws = torch.empty(m3.m3_siso_backward_workspace(cfg), dtype=torch.uint8, device="cuda")
+    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d")
+    g = {k: torch.empty_like(d[k]) for k in keys}
+    fn = lambda: m3.m3_siso_backward(cfg, go, *[d[k] for k in keys], *[g[k] for k in keys], ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 5)
+    gbs = w.tokens * bytes_per_token_backward(w) / (ms * 1e-3) / 1e9
+    tflops = w.tokens * flops_per_token_backward(w) / (ms * 1e-3) / 1e12
+    alu, how = fp32_alu_peak()
+    return {"workload": w.name, "mode": "fp32", "ms": round(ms, 4),
+            "tokens_per_s": round(w.tokens / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4), "alu_tflops": round(tflops, 2),
+            "alu_peak_tflops": round(alu, 1), "alu_peak": how, "frac_alu": round(tflops / alu, 4),
+            "algorithmic_bytes": w.tokens * bytes_per_token_backward(w),
+            "flops": w.tokens * flops_per_token_backward(w)}
+
+
 def part_by_name(torch, m3, name, peak):
     """One supplementary part, by its key in the JSON line's `parts`."""
     table = {
@@ -590,6 +651,7 @@ def part_by_name(torch, m3, name, peak):
         "siso_step": lambda: parts_step(torch, m3, peak),
         "mimo_step": lambda: parts_step(torch, m3, peak, mimo=True),
         "siso_prefill_tf32": lambda: parts_prefill(torch, m3, gen.SISO_1B, peak),
+        "siso_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_1B, peak),
     }
     if name not in table:
         raise SystemExit(f"bench.py: unknown part {name!r}; one of {sorted(table)}")
@@ -731,7 +793,8 @@ def run_m3(args):
     if rank == 0 and not args.no_parts:
         for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "mimo_packed_tf32",
                      "siso_long_scan_fp32",
-                     "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32"):
+                     "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32",
+                     "siso_backward_fp32"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()
 
