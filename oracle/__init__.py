@@ -10,8 +10,8 @@ the independent O(L^2) unrolled form used to pin it. The readings taken where
 the source pages are silent are listed at the top of `m3_oracle.cpp`.
 
 Pinned functions (see tests/test_oracle_pins.py): preprocess, SISO scan, SISO
-step (as the scan with explicit state), MIMO scan, MIMO step; SISO adjoints
-(tests/test_oracle_backward_pins.py: central differences of the scan).
+step (as the scan with explicit state), MIMO scan, MIMO step; SISO and MIMO
+adjoints (tests/test_oracle_backward_pins.py: central differences of the scans).
 """
 from __future__ import annotations
 
@@ -54,6 +54,9 @@ def _load():
             lib.m3o_scan.argtypes = [_i64] * 8 + [ctypes.c_int] * 3 + [_ptr] * 20 + [ctypes.c_int]
             lib.m3o_siso_backward.restype = ctypes.c_int
             lib.m3o_siso_backward.argtypes = ([_i64] * 7 + [ctypes.c_int] * 2 + [_ptr] * 23 +
+                                              [ctypes.c_int])
+            lib.m3o_mimo_backward.restype = ctypes.c_int
+            lib.m3o_mimo_backward.argtypes = ([_i64] * 8 + [ctypes.c_int] * 3 + [_ptr] * 31 +
                                               [ctypes.c_int])
             _lib = lib
     return _lib
@@ -163,4 +166,33 @@ def siso_backward(cfg, dout, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d
                                    *[_p(g[k]) for k in GRAD_NAMES], threads or default_threads())
     if rc != 0:
         raise ValueError("oracle siso_backward: invalid geometry")
+    return g
+
+
+MIMO_GRAD_NAMES = GRAD_NAMES + ("mimo_x", "mimo_z", "mimo_o", "norm_weight")
+
+
+def mimo_backward(cfg, dout, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x, mimo_z,
+                  mimo_o, norm_weight, threads=None):
+    """The fifteen MIMO adjoints (`mamba3_mimo_backward`) of the scan from a
+    zero state, given dout [B,L,H,P]. Returns a dict of float64 arrays keyed by
+    MIMO_GRAD_NAMES in the forward operands' layouts: c/b [B,L,R*G,N], x/z
+    [B,L,H,P], adt/dt/trap [B,L,H], angle [B,L,A], c_bias/b_bias [H,R,N],
+    d [H], mimo_x/z/o [H,R,P], norm_weight [H,P]."""
+    B, L, H = cfg["batch_size"], cfg["sequence_length"], cfg["num_heads"]
+    P, N, A, R = cfg["head_dim"], cfg["state_size"], cfg["num_rope_angles"], cfg["mimo_rank"]
+    G = cfg["num_groups"] or H
+    arrs = [_f32(a) for a in (dout, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,
+                               mimo_z, mimo_o, norm_weight)]
+    shapes = dict(c=(B, L, R * G, N), b=(B, L, R * G, N), x=(B, L, H, P), z=(B, L, H, P),
+                  adt=(B, L, H), dt=(B, L, H), trap=(B, L, H), angle=(B, L, A),
+                  c_bias=(H, R, N), b_bias=(H, R, N), d=(H,), mimo_x=(H, R, P),
+                  mimo_z=(H, R, P), mimo_o=(H, R, P), norm_weight=(H, P))
+    g = {k: np.zeros(shapes[k]) for k in MIMO_GRAD_NAMES}
+    rc = _load().m3o_mimo_backward(B, L, H, cfg["num_groups"], P, N, A, R, int(cfg["has_z"]),
+                                   int(cfg["has_d"]), int(cfg.get("has_output_norm", 0)),
+                                   *[_p(a) for a in arrs], *[_p(g[k]) for k in MIMO_GRAD_NAMES],
+                                   threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle mimo_backward: invalid geometry")
     return g

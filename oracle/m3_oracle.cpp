@@ -480,4 +480,270 @@ int m3o_siso_backward(i64 B, i64 L, i64 H, i64 num_groups, i64 P, i64 N, i64 A, 
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// MIMO adjoints: reverse-mode differentiation of the MIMO token loop of
+// m3o_scan (rank R, zero initial state), returning the fifteen gradients of
+// `Mamba3MimoBackward` in mamba3.rs (`mamba3_mimo_backward`): c, b
+// [B,L,R*G,N], x, z [B,L,H,P], adt, dt, trap [B,L,H], angle [B,L,A], c_bias,
+// b_bias [H,R,N], d [H], mimo_x, mimo_z, mimo_o [H,R,P], norm_weight [H,P].
+// As for the SISO adjoints, every state is kept and each forward statement's
+// adjoint is taken in reverse order; the MIMO statements add:
+//   out_t = o_t rho_t w (has_norm), rho_t = (mean_p o_t^2 + 1e-5)^(-1/2):
+//       d w += dout o rho,  d o = rho w dout - rho^3 o (1/P) sum_j dout_j w_j o_j
+//   o_t = sum_r mimo_o[r] y_{t,r} silu(z_t mimo_z[r])   (no gate without has_z):
+//       d y_{t,r} = d o mimo_o[r] silu(.),  d mimo_o[r] += d o y_{t,r} silu(.),
+//       d z_t += d o mimo_o[r] y_{t,r} silu'(.) mimo_z[r],  d mimo_z[r] += ... z_t
+//   v_{t,r} = x_t mimo_x[r]:  d x_t += d v_{t,r} mimo_x[r],  d mimo_x[r] += d v_{t,r} x_t
+// and the state terms sum their rank products. Returns 0, or 1 for an invalid
+// geometry.
+int m3o_mimo_backward(i64 B, i64 L, i64 H, i64 num_groups, i64 P, i64 N, i64 A, i64 R,
+                      int has_z, int has_d, int has_norm, const float* dout, const float* c,
+                      const float* b, const float* x, const float* z, const float* adt,
+                      const float* dt, const float* trap, const float* angle,
+                      const float* c_bias, const float* b_bias, const float* d,
+                      const float* mimo_x, const float* mimo_z, const float* mimo_o,
+                      const float* norm_weight, double* gc, double* gb, double* gx, double* gz,
+                      double* gadt, double* gdt, double* gtrap, double* gangle, double* gc_bias,
+                      double* gb_bias, double* gd, double* gmx, double* gmz, double* gmo,
+                      double* gnw, int threads) {
+  const i64 G = num_groups == 0 ? H : num_groups;
+  if (B <= 0 || L <= 0 || H <= 0 || G <= 0 || H % G != 0 || P <= 0 || N <= 0 || A < 0 ||
+      2 * A > N || R <= 0)
+    return 1;
+  const i64 hpg = H / G, RG = R * G;
+  // per-(b, h) parts, summed below
+  std::vector<double> pc(B * L * H * R * N), pb(B * L * H * R * N), pang(B * L * H * A);
+  std::vector<double> pcb(B * H * R * N), pbb(B * H * R * N), pd(B * H);
+  std::vector<double> pmx(B * H * R * P), pmz(B * H * R * P), pmo(B * H * R * P), pnw(B * H * P);
+  parallel_for(B * H, threads, [&](i64 bh) {
+    const i64 bb = bh / H, h = bh % H, g = h / hpg;
+    const double dd = has_d ? (double)d[h] : 0.0;
+    const float* mx = mimo_x + h * R * P;
+    const float* mz = mimo_z + h * R * P;
+    const float* mo = mimo_o + h * R * P;
+    // forward, keeping every state and per-token quantity
+    std::vector<double> hs((L + 1) * P * N, 0.0);
+    std::vector<double> q(L * R * N), k(L * R * N), th(L * A), v(L * R * P), y(L * R * P);
+    std::vector<double> o(L * P), rho(L, 1.0), al(L), ga(L), sc(L), lam(L);
+    std::vector<double> theta(A, 0.0), tmp(N);
+    for (i64 t = 0; t < L; ++t) {
+      const i64 tok = bb * L + t, s = tok * H + h;
+      const double l = sigmoid((double)trap[s]);
+      lam[t] = l;
+      al[t] = std::exp((double)adt[s]);
+      ga[t] = l * (double)dt[s];
+      sc[t] = (1.0 - l) * (double)dt[s];
+      for (i64 a = 0; a < A; ++a) theta[a] += (double)dt[s] * (double)angle[tok * A + a];
+      for (i64 a = 0; a < A; ++a) th[t * A + a] = theta[a];
+      for (i64 r = 0; r < R; ++r) {
+        const i64 row = tok * RG + g * R + r;
+        for (i64 n = 0; n < N; ++n) tmp[n] = (double)c[row * N + n] + (double)c_bias[(h * R + r) * N + n];
+        rotate(tmp, theta, A);
+        for (i64 n = 0; n < N; ++n) q[(t * R + r) * N + n] = tmp[n];
+        for (i64 n = 0; n < N; ++n) tmp[n] = (double)b[row * N + n] + (double)b_bias[(h * R + r) * N + n];
+        rotate(tmp, theta, A);
+        for (i64 n = 0; n < N; ++n) k[(t * R + r) * N + n] = tmp[n];
+        for (i64 p = 0; p < P; ++p) v[(t * R + r) * P + p] = (double)x[s * P + p] * (double)mx[r * P + p];
+      }
+      const double* hp = &hs[t * P * N];
+      double* hc = &hs[(t + 1) * P * N];
+      for (i64 p = 0; p < P; ++p)
+        for (i64 n = 0; n < N; ++n) {
+          double prev = 0.0, cur = 0.0;
+          for (i64 r = 0; r < R; ++r) {
+            if (t > 0) prev += v[((t - 1) * R + r) * P + p] * k[((t - 1) * R + r) * N + n];
+            cur += v[(t * R + r) * P + p] * k[(t * R + r) * N + n];
+          }
+          hc[p * N + n] = al[t] * hp[p * N + n] + sc[t] * al[t] * prev + ga[t] * cur;
+        }
+      for (i64 r = 0; r < R; ++r)
+        for (i64 p = 0; p < P; ++p) {
+          double acc = 0.0;
+          for (i64 n = 0; n < N; ++n) acc += hc[p * N + n] * q[(t * R + r) * N + n];
+          y[(t * R + r) * P + p] = acc + dd * v[(t * R + r) * P + p];
+        }
+      double ms = 0.0;
+      for (i64 p = 0; p < P; ++p) {
+        double acc = 0.0;
+        for (i64 r = 0; r < R; ++r) {
+          double val = y[(t * R + r) * P + p];
+          if (has_z) val *= silu((double)z[s * P + p] * (double)mz[r * P + p]);
+          acc += (double)mo[r * P + p] * val;
+        }
+        o[t * P + p] = acc;
+        ms += acc * acc;
+      }
+      if (has_norm) rho[t] = 1.0 / std::sqrt(ms / (double)P + 1.0e-5);
+    }
+    // reverse
+    std::vector<double> Lam(P * N, 0.0), dv(L * R * P, 0.0), dk(L * R * N, 0.0);
+    std::vector<double> dq(R * N), dy(R * P), dob(P), gth(A, 0.0);
+    double dsum = 0.0;
+    for (i64 t = L - 1; t >= 0; --t) {
+      const i64 tok = bb * L + t, s = tok * H + h;
+      // out_t = o_t rho_t w (or o_t)
+      const float* go = dout + s * P;
+      if (has_norm) {
+        const float* w = norm_weight + h * P;
+        double cdot = 0.0;
+        for (i64 p = 0; p < P; ++p) cdot += (double)go[p] * (double)w[p] * o[t * P + p];
+        cdot /= (double)P;
+        const double r3 = rho[t] * rho[t] * rho[t];
+        for (i64 p = 0; p < P; ++p) {
+          pnw[bh * P + p] += (double)go[p] * o[t * P + p] * rho[t];
+          dob[p] = rho[t] * (double)w[p] * (double)go[p] - r3 * o[t * P + p] * cdot;
+        }
+      } else {
+        for (i64 p = 0; p < P; ++p) dob[p] = (double)go[p];
+      }
+      // o_t = sum_r mimo_o[r] y_{t,r} silu(z_t mimo_z[r])
+      for (i64 p = 0; p < P; ++p) {
+        double gzp = 0.0;
+        for (i64 r = 0; r < R; ++r) {
+          const double yv = y[(t * R + r) * P + p], mov = (double)mo[r * P + p];
+          double gate = 1.0, dgate = 0.0, arg = 0.0;
+          if (has_z) {
+            arg = (double)z[s * P + p] * (double)mz[r * P + p];
+            const double sg = sigmoid(arg);
+            gate = arg * sg;
+            dgate = sg + arg * sg * (1.0 - sg);
+          }
+          dy[r * P + p] = dob[p] * mov * gate;
+          pmo[(bh * R + r) * P + p] += dob[p] * yv * gate;
+          if (has_z) {
+            const double da = dob[p] * mov * yv * dgate;
+            gzp += da * (double)mz[r * P + p];
+            pmz[(bh * R + r) * P + p] += da * (double)z[s * P + p];
+          }
+        }
+        gz[s * P + p] = gzp;
+      }
+      // y_{t,r} = h_t q_{t,r} + D v_{t,r}
+      const double* hc = &hs[(t + 1) * P * N];
+      for (i64 i = 0; i < R * N; ++i) dq[i] = 0.0;
+      for (i64 r = 0; r < R; ++r)
+        for (i64 p = 0; p < P; ++p) {
+          const double dyv = dy[r * P + p];
+          for (i64 n = 0; n < N; ++n) {
+            Lam[p * N + n] += dyv * q[(t * R + r) * N + n];
+            dq[r * N + n] += hc[p * N + n] * dyv;
+          }
+          dsum += dyv * v[(t * R + r) * P + p];
+          dv[(t * R + r) * P + p] += dd * dyv;
+        }
+      // h_t = a h_{t-1} + s a sum_r v_{t-1,r} k_{t-1,r}^T + g sum_r v_{t,r} k_{t,r}^T
+      const double* hp = &hs[t * P * N];
+      double da = 0.0, ds = 0.0, dg = 0.0;
+      for (i64 p = 0; p < P; ++p)
+        for (i64 n = 0; n < N; ++n) {
+          const double lm = Lam[p * N + n];
+          double prev = 0.0, cur = 0.0;
+          for (i64 r = 0; r < R; ++r) {
+            if (t > 0) prev += v[((t - 1) * R + r) * P + p] * k[((t - 1) * R + r) * N + n];
+            cur += v[(t * R + r) * P + p] * k[(t * R + r) * N + n];
+          }
+          da += lm * (hp[p * N + n] + sc[t] * prev);
+          ds += al[t] * lm * prev;
+          dg += lm * cur;
+          for (i64 r = 0; r < R; ++r) {
+            dv[(t * R + r) * P + p] += ga[t] * lm * k[(t * R + r) * N + n];
+            dk[(t * R + r) * N + n] += ga[t] * lm * v[(t * R + r) * P + p];
+            if (t > 0) {
+              dv[((t - 1) * R + r) * P + p] += sc[t] * al[t] * lm * k[((t - 1) * R + r) * N + n];
+              dk[((t - 1) * R + r) * N + n] += sc[t] * al[t] * lm * v[((t - 1) * R + r) * P + p];
+            }
+          }
+        }
+      for (i64 i = 0; i < P * N; ++i) Lam[i] *= al[t];
+      gadt[s] = da * al[t];
+      double gdt_t = dg * lam[t] + ds * (1.0 - lam[t]);
+      gtrap[s] = (dg - ds) * (double)dt[s] * lam[t] * (1.0 - lam[t]);
+      // v_{t,r} = x_t mimo_x[r]
+      for (i64 p = 0; p < P; ++p) {
+        double acc = 0.0;
+        for (i64 r = 0; r < R; ++r) {
+          acc += dv[(t * R + r) * P + p] * (double)mx[r * P + p];
+          pmx[(bh * R + r) * P + p] += dv[(t * R + r) * P + p] * (double)x[s * P + p];
+        }
+        gx[s * P + p] = acc;
+      }
+      // rotations of every rank's q and k
+      std::vector<double> dth(A, 0.0);
+      for (i64 r = 0; r < R; ++r)
+        for (int which = 0; which < 2; ++which) {
+          const double* gr = which == 0 ? &dq[r * N] : &dk[(t * R + r) * N];
+          const double* rv = which == 0 ? &q[(t * R + r) * N] : &k[(t * R + r) * N];
+          double* dst = (which == 0 ? &pc[0] : &pb[0]) + ((tok * H + h) * R + r) * N;
+          double* bias = (which == 0 ? &pcb[0] : &pbb[0]) + (bh * R + r) * N;
+          for (i64 n = 0; n < N; ++n) dst[n] = gr[n];
+          for (i64 a = 0; a < A; ++a) {
+            const double cs = std::cos(th[t * A + a]), sn = std::sin(th[t * A + a]);
+            const double g0 = gr[a], g1 = gr[a + A];
+            dst[a] = g0 * cs + g1 * sn;
+            dst[a + A] = -g0 * sn + g1 * cs;
+            dth[a] += -g0 * rv[a + A] + g1 * rv[a];
+          }
+          for (i64 n = 0; n < N; ++n) bias[n] += dst[n];
+        }
+      for (i64 a = 0; a < A; ++a) {
+        gth[a] += dth[a];
+        gdt_t += gth[a] * (double)angle[tok * A + a];
+        pang[(tok * H + h) * A + a] = gth[a] * (double)dt[s];
+      }
+      gdt[s] = gdt_t;
+    }
+    pd[bh] = dsum;
+  });
+  // sums over heads, batch and tokens, in index order
+  for (i64 tok = 0; tok < B * L; ++tok) {
+    for (i64 g = 0; g < G; ++g)
+      for (i64 r = 0; r < R; ++r)
+        for (i64 n = 0; n < N; ++n) {
+          double sc_ = 0.0, sb_ = 0.0;
+          for (i64 j = 0; j < hpg; ++j) {
+            sc_ += pc[((tok * H + g * hpg + j) * R + r) * N + n];
+            sb_ += pb[((tok * H + g * hpg + j) * R + r) * N + n];
+          }
+          gc[(tok * RG + g * R + r) * N + n] = sc_;
+          gb[(tok * RG + g * R + r) * N + n] = sb_;
+        }
+    for (i64 a = 0; a < A; ++a) {
+      double sa = 0.0;
+      for (i64 h = 0; h < H; ++h) sa += pang[(tok * H + h) * A + a];
+      gangle[tok * A + a] = sa;
+    }
+  }
+  for (i64 h = 0; h < H; ++h) {
+    for (i64 i = 0; i < R * N; ++i) {
+      double sc_ = 0.0, sb_ = 0.0;
+      for (i64 bb = 0; bb < B; ++bb) {
+        sc_ += pcb[(bb * H + h) * R * N + i];
+        sb_ += pbb[(bb * H + h) * R * N + i];
+      }
+      gc_bias[h * R * N + i] = sc_;
+      gb_bias[h * R * N + i] = sb_;
+    }
+    for (i64 i = 0; i < R * P; ++i) {
+      double sx = 0.0, sz = 0.0, so = 0.0;
+      for (i64 bb = 0; bb < B; ++bb) {
+        sx += pmx[(bb * H + h) * R * P + i];
+        sz += pmz[(bb * H + h) * R * P + i];
+        so += pmo[(bb * H + h) * R * P + i];
+      }
+      gmx[h * R * P + i] = sx;
+      gmz[h * R * P + i] = has_z ? sz : 0.0;
+      gmo[h * R * P + i] = so;
+    }
+    for (i64 p = 0; p < P; ++p) {
+      double sw = 0.0;
+      for (i64 bb = 0; bb < B; ++bb) sw += pnw[(bb * H + h) * P + p];
+      gnw[h * P + p] = has_norm ? sw : 0.0;
+    }
+    double sd = 0.0;
+    for (i64 bb = 0; bb < B; ++bb) sd += pd[bb * H + h];
+    gd[h] = has_d ? sd : 0.0;
+  }
+  return 0;
+}
+
 }  // extern "C"
