@@ -13,8 +13,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
                 [--mode fp32|tf32] [--no-parts] [--part NAME]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
 mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
-mimo_step, siso_prefill_tf32, siso_backward_fp32) and prints its JSON, for profiling it
-alone.
+mimo_step, siso_prefill_tf32, siso_backward_fp32, mimo_backward_fp32) and prints its
+JSON, for profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -93,6 +93,24 @@ def flops_per_token_backward(w):
     the reverse sweep's decay (1 MUL), M k, M^T v and adjoint update (3 FMA);
     an FMA is 2 flops: 17 H P N."""
     return 17 * w.num_heads * w.head_dim * w.state_size
+
+
+def bytes_per_token_backward_mimo(w):
+    """Algorithmic HBM bytes of one token of the MIMO backward: dout, x, z
+    [H,P]; B, C rows [R*G,N]; adt, dt, trap [H]; angle [A] read once, and the
+    gradients of x, z, B, C, adt, dt, trap and angle written once."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    H, P, N, A, R = w.num_heads, w.head_dim, w.state_size, w.num_rope_angles, w.mimo_rank
+    return 4 * ((3 * H * P + 2 * R * G * N + 3 * H + A) + (2 * H * P + 2 * R * G * N + 3 * H + A))
+
+
+def flops_per_token_backward_mimo(w):
+    """FP32 flops of the MIMO adjoints per token: per state element the state
+    update (a decay multiply and 2R FMA), the y and dq readouts (R FMA each)
+    and the reverse sweep (a multiply and 3R FMA): (2 + 14 R) H P N. The second
+    forward sweep that the output norm's row-wide adjoint requires is not
+    counted."""
+    return (2 + 14 * w.mimo_rank) * w.num_heads * w.head_dim * w.state_size
 
 
 def fp32_alu_peak():
@@ -639,6 +657,33 @@ def parts_backward(torch, m3, w, peak):
             "flops": w.tokens * flops_per_token_backward(w)}
 
 
+def parts_backward_mimo(torch, m3, w, peak):
+    """Supplementary: m3_mimo_backward (the fifteen MIMO adjoints, FP32) of
+    workload w with device-resident operands and output gradient."""
+    ins = gen.scan_inputs(w)
+    d = {k: torch.from_numpy(v).cuda() for k, v in ins.items()}
+    go = torch.from_numpy(gen.output_gradient(w)).cuda()
+    del ins
+    cfg = m3.ssm_config(w.cfg(), m3.M3_MATH_FP32)
+    ws = torch.empty(m3.m3_mimo_backward_workspace(cfg), dtype=torch.uint8, device="cuda")
+    keys = ("c", "b", "x", "z", "adt", "dt", "trap", "angle", "c_bias", "b_bias", "d", "mimo_x",
+            "mimo_z", "mimo_o", "norm_weight")
+    g = {k: torch.empty_like(d[k]) for k in keys}
+    fn = lambda: m3.m3_mimo_backward(cfg, go, *[d[k] for k in keys], *[g[k] for k in keys], ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 5)
+    gbs = w.tokens * bytes_per_token_backward_mimo(w) / (ms * 1e-3) / 1e9
+    tflops = w.tokens * flops_per_token_backward_mimo(w) / (ms * 1e-3) / 1e12
+    alu, how = fp32_alu_peak()
+    return {"workload": w.name, "mode": "fp32", "ms": round(ms, 4),
+            "tokens_per_s": round(w.tokens / (ms * 1e-3)), "hbm_gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4), "alu_tflops": round(tflops, 2),
+            "alu_peak_tflops": round(alu, 1), "alu_peak": how, "frac_alu": round(tflops / alu, 4),
+            "algorithmic_bytes": w.tokens * bytes_per_token_backward_mimo(w),
+            "flops": w.tokens * flops_per_token_backward_mimo(w)}
+
+
 def part_by_name(torch, m3, name, peak):
     """One supplementary part, by its key in the JSON line's `parts`."""
     table = {
@@ -652,6 +697,7 @@ def part_by_name(torch, m3, name, peak):
         "mimo_step": lambda: parts_step(torch, m3, peak, mimo=True),
         "siso_prefill_tf32": lambda: parts_prefill(torch, m3, gen.SISO_1B, peak),
         "siso_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_1B, peak),
+        "mimo_backward_fp32": lambda: parts_backward_mimo(torch, m3, gen.MIMO_R4, peak),
     }
     if name not in table:
         raise SystemExit(f"bench.py: unknown part {name!r}; one of {sorted(table)}")
@@ -794,7 +840,7 @@ def run_m3(args):
         for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "mimo_packed_tf32",
                      "siso_long_scan_fp32",
                      "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32",
-                     "siso_backward_fp32"):
+                     "siso_backward_fp32", "mimo_backward_fp32"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()
 

@@ -13,6 +13,7 @@
  *   m3_siso_forward_packed / m3_mimo_forward_packed - `mamba3_preprocess` and
  *                       `mamba3_siso` / `mamba3_mimo` in one call
  *   m3_siso_backward  - `mamba3_siso_backward` (the eleven SISO adjoints)
+ *   m3_mimo_backward  - `mamba3_mimo_backward` (the fifteen MIMO adjoints)
  *
  * Conventions for every entry point:
  *  - Every tensor is float32, dense row-major, in device memory owned by the
@@ -227,6 +228,39 @@ int m3_siso_backward(const m3_ssm_config* cfg, const float* grad_out, const floa
                      float* grad_b, float* grad_x, float* grad_z, float* grad_adt,
                      float* grad_dt, float* grad_trap, float* grad_angle, float* grad_c_bias,
                      float* grad_b_bias, float* grad_d, void* workspace, size_t workspace_bytes,
+                     m3_stream_t stream);
+
+/*
+ * m3_mimo_backward - the fifteen adjoints of m3_mimo_forward
+ * (`mamba3_mimo_backward`, the fields of `Mamba3MimoBackward`): given grad_out
+ * [B,L,H,P] and the forward operands, writes grad_c, grad_b [B,L,R*G,N] (summed
+ * over the heads sharing a group's rows); grad_x, grad_z [B,L,H,P]; grad_adt,
+ * grad_dt, grad_trap [B,L,H]; grad_angle [B,L,A] (summed over heads; may be
+ * NULL when A == 0); grad_c_bias, grad_b_bias [H,R,N]; grad_d [H];
+ * grad_mimo_x, grad_mimo_z, grad_mimo_o [H,R,P]; grad_norm_weight [H,P] (the
+ * batch and token sums). grad_z and grad_mimo_z are zero without has_z,
+ * grad_d without has_d, grad_norm_weight without has_output_norm. The scan
+ * starts from a zero state.
+ * Arithmetic: FP32 on the CUDA cores whatever cfg->math_mode says: a forward
+ * sweep for the readouts y_{t,r}, a per-token pass for the norm, gate and
+ * mimo_o adjoints, a second forward sweep for the query gradients, a reverse
+ * sweep and a reduction in a fixed order (repeated calls give the same bits).
+ * Checks: those of m3_mimo_forward, plus B*L*H*R*N, B*L*H*R*P and B*L*H*A
+ * below 2^32; every pointer but angle / grad_angle (when A == 0) non-NULL and
+ * 16-byte aligned. workspace: at least m3_mimo_backward_workspace() bytes,
+ * 16-byte aligned. Outputs must not overlap the inputs or the workspace.
+ */
+int m3_mimo_backward_workspace(const m3_ssm_config* cfg, size_t* bytes);
+int m3_mimo_backward(const m3_ssm_config* cfg, const float* grad_out, const float* c,
+                     const float* b, const float* x, const float* z, const float* adt,
+                     const float* dt, const float* trap, const float* angle,
+                     const float* c_bias, const float* b_bias, const float* d,
+                     const float* mimo_x, const float* mimo_z, const float* mimo_o,
+                     const float* norm_weight, float* grad_c, float* grad_b, float* grad_x,
+                     float* grad_z, float* grad_adt, float* grad_dt, float* grad_trap,
+                     float* grad_angle, float* grad_c_bias, float* grad_b_bias, float* grad_d,
+                     float* grad_mimo_x, float* grad_mimo_z, float* grad_mimo_o,
+                     float* grad_norm_weight, void* workspace, size_t workspace_bytes,
                      m3_stream_t stream);
 
 /*

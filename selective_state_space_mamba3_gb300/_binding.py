@@ -31,6 +31,7 @@ EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
             "m3_mimo_forward_packed_workspace", "m3_mimo_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
             "m3_mimo_prefill_workspace", "m3_mimo_prefill",
             "m3_siso_backward_workspace", "m3_siso_backward",
+            "m3_mimo_backward_workspace", "m3_mimo_backward",
             "m3_mimo_forward_workspace", "m3_mimo_forward", "m3_siso_step", "m3_mimo_step",
             "m3_workspace_status", "m3_selftest_wait_timeout", "m3_status_string",
             "m3_launch_count")
@@ -109,6 +110,8 @@ def load_library():
         lib.m3_siso_step.argtypes = [cfgp] + [_vp] * 16 + [_vp]
         lib.m3_siso_backward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_backward.argtypes = [cfgp] + [_vp] * 24 + [ctypes.c_size_t, _vp]
+        lib.m3_mimo_backward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_mimo_backward.argtypes = [cfgp] + [_vp] * 32 + [ctypes.c_size_t, _vp]
         lib.m3_mimo_step.argtypes = [cfgp] + [_vp] * 20 + [_vp]
         lib.m3_workspace_status.argtypes = [_vp, ctypes.c_size_t, _vp]
         lib.m3_selftest_wait_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_int64, _vp]
@@ -277,6 +280,26 @@ def m3_siso_backward(cfg: SsmConfig, grad_out, c, b, x, z, adt, dt, trap, angle,
         grad_out, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, grad_c, grad_b, grad_x,
         grad_z, grad_adt, grad_dt, grad_trap, grad_angle, grad_c_bias, grad_b_bias, grad_d)],
         wp, wn, _stream(stream)), "m3_siso_backward")
+
+
+def m3_mimo_backward_workspace(cfg: SsmConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_mimo_backward_workspace(ctypes.byref(cfg), ctypes.byref(n)),
+           "m3_mimo_backward_workspace")
+    return n.value
+
+
+def m3_mimo_backward(cfg: SsmConfig, grad_out, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias,
+                     d, mimo_x, mimo_z, mimo_o, norm_weight, grad_c, grad_b, grad_x, grad_z,
+                     grad_adt, grad_dt, grad_trap, grad_angle, grad_c_bias, grad_b_bias, grad_d,
+                     grad_mimo_x, grad_mimo_z, grad_mimo_o, grad_norm_weight, workspace=None,
+                     stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_mimo_backward(ctypes.byref(cfg), *[_ptr(t) for t in (
+        grad_out, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x, mimo_z, mimo_o,
+        norm_weight, grad_c, grad_b, grad_x, grad_z, grad_adt, grad_dt, grad_trap, grad_angle,
+        grad_c_bias, grad_b_bias, grad_d, grad_mimo_x, grad_mimo_z, grad_mimo_o,
+        grad_norm_weight)], wp, wn, _stream(stream)), "m3_mimo_backward")
 
 
 def m3_mimo_prefill(cfg: SsmConfig, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x,

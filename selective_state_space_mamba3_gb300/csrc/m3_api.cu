@@ -506,6 +506,58 @@ int m3_siso_backward(const m3_ssm_config* cfg, const float* dout, const float* c
   return cuda_status(launch_siso_backward(g, a, o, workspace, (cudaStream_t)stream));
 }
 
+// `mamba3_mimo_backward`: the MIMO geometry rules, plus the workspace arrays
+// ([B,L,H,R,N] per-head C / B parts, [B,H,L,R,P] readouts) below 2^32 elements.
+static int resolve_mimo_backward(const m3_ssm_config* cfg, ScanGeom* g) {
+  const int st = resolve_ssm(cfg, true, g);
+  if (st != M3_OK) return st;
+  if (!count_below_u32({g->B, g->L, g->H, g->R, g->N}) ||
+      !count_below_u32({g->B, g->L, g->H, g->R, g->P}) || !count_below_u32({g->B, g->L, g->H, g->A}))
+    return M3_ERR_INVALID_ARGUMENT;
+  return M3_OK;
+}
+
+int m3_mimo_backward_workspace(const m3_ssm_config* cfg, size_t* bytes) {
+  ScanGeom g;
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  const int st = resolve_mimo_backward(cfg, &g);
+  if (st != M3_OK) return st;
+  *bytes = mimo_backward_workspace_bytes(g);
+  return M3_OK;
+}
+
+int m3_mimo_backward(const m3_ssm_config* cfg, const float* dout, const float* c, const float* b,
+                     const float* x, const float* z, const float* adt, const float* dt,
+                     const float* trap, const float* angle, const float* c_bias,
+                     const float* b_bias, const float* d, const float* mimo_x,
+                     const float* mimo_z, const float* mimo_o, const float* norm_weight,
+                     float* grad_c, float* grad_b, float* grad_x, float* grad_z, float* grad_adt,
+                     float* grad_dt, float* grad_trap, float* grad_angle, float* grad_c_bias,
+                     float* grad_b_bias, float* grad_d, float* grad_mimo_x, float* grad_mimo_z,
+                     float* grad_mimo_o, float* grad_norm_weight, void* workspace,
+                     size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_mimo_backward");
+  ScanGeom g;
+  int st = resolve_mimo_backward(cfg, &g);
+  if (st != M3_OK) return st;
+  st = check_ptrs({dout, c, b, x, z, adt, dt, trap, c_bias, b_bias, d, mimo_x, mimo_z, mimo_o,
+                   norm_weight, grad_c, grad_b, grad_x, grad_z, grad_adt, grad_dt, grad_trap,
+                   grad_c_bias, grad_b_bias, grad_d, grad_mimo_x, grad_mimo_z, grad_mimo_o,
+                   grad_norm_weight});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(angle, g.A)) != M3_OK) return st;
+  if ((st = check_angle_ptr(grad_angle, g.A)) != M3_OK) return st;
+  const size_t need = mimo_backward_workspace_bytes(g);
+  if (!workspace || workspace_bytes < need) return M3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return M3_ERR_UNALIGNED;
+  ScanArgs a{c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d,
+             mimo_x, mimo_z, mimo_o, norm_weight, nullptr};
+  MBwdArgs o{{dout, grad_c, grad_b, grad_x, grad_z, grad_adt, grad_dt, grad_trap, grad_angle,
+              grad_c_bias, grad_b_bias, grad_d},
+             grad_mimo_x, grad_mimo_z, grad_mimo_o, grad_norm_weight};
+  return cuda_status(launch_mimo_backward(g, a, o, workspace, (cudaStream_t)stream));
+}
+
 static int packed_workspace(const m3_ssm_config* cfg, const m3_preprocess_config* pcfg,
                             bool mimo, size_t* bytes) {
   ScanGeom g;

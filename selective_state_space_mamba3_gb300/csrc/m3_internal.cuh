@@ -126,6 +126,15 @@ struct BwdArgs {
   float *gc, *gb, *gx, *gz, *gadt, *gdt, *gtrap, *gangle, *gc_bias, *gb_bias, *gd;
 };
 size_t backward_workspace_bytes(const ScanGeom& g);
+// MIMO adjoints (`mamba3_mimo_backward`): the eleven of the SISO set plus the
+// gradients of mimo_x, mimo_z, mimo_o [H,R,P] and norm_weight [H,P].
+struct MBwdArgs {
+  BwdArgs g;
+  float *gmx, *gmz, *gmo, *gnw;
+};
+size_t mimo_backward_workspace_bytes(const ScanGeom& g);
+cudaError_t launch_mimo_backward(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
+                                 void* ws, cudaStream_t s);
 cudaError_t launch_siso_backward(const ScanGeom& g, const ScanArgs& a, const BwdArgs& o,
                                  void* ws, cudaStream_t s);
 

@@ -7,7 +7,7 @@ Bar: the FP32 bar of the forward, 1e-5 normwise (max|gpu - oracle| / max|oracle|
 per gradient), for all eleven gradients. A gradient that vanishes in exact
 arithmetic (with one token, the angle adjoint: q_t . k_t does not depend on
 theta_t) is compared against a floor of 1e-3 times the call's largest
-gradient instead of its own rounding residue. Outputs start as NaN, so an
+per-token gradient instead of its own rounding residue. Outputs start as NaN, so an
 element the kernels never write fails the comparison.
 """
 import numpy as np
@@ -74,8 +74,13 @@ def gpu_backward(cfg, ins, dout, calls=1):
     return first
 
 
+# the per-token gradients, whose scale sets the floor for a gradient that
+# vanishes (the parameter gradients sum over all tokens and are larger)
+PER_TOKEN = ("c", "b", "x", "z", "adt", "dt", "trap")
+
+
 def compare(got, ref, label, tol=BWD_TOL):
-    floor = 1e-3 * max(float(np.max(np.abs(ref[k]))) for k in KEYS if ref[k].size)
+    floor = 1e-3 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
     for k in KEYS:
         if ref[k].size == 0:
             continue
@@ -176,3 +181,99 @@ def test_siso_backward_rejects_bad_calls():
     with pytest.raises(m3.M3Error) as e:
         m3.m3_siso_backward(good, dev(dout), *args, ws)
     assert e.value.status == m3.M3_ERR_INVALID_ARGUMENT
+
+
+# --- MIMO adjoints (`mamba3_mimo_backward`, the fifteen of `Mamba3MimoBackward`)
+
+MKEYS = oracle.MIMO_GRAD_NAMES
+
+
+def mimo_grad_shapes(cfg):
+    B, L, H = cfg["batch_size"], cfg["sequence_length"], cfg["num_heads"]
+    P, N, A, R = cfg["head_dim"], cfg["state_size"], cfg["num_rope_angles"], cfg["mimo_rank"]
+    G = cfg["num_groups"] or H
+    return dict(c=(B, L, R * G, N), b=(B, L, R * G, N), x=(B, L, H, P), z=(B, L, H, P),
+                adt=(B, L, H), dt=(B, L, H), trap=(B, L, H), angle=(B, L, A), c_bias=(H, R, N),
+                b_bias=(H, R, N), d=(H,), mimo_x=(H, R, P), mimo_z=(H, R, P), mimo_o=(H, R, P),
+                norm_weight=(H, P))
+
+
+def gpu_mimo_backward(cfg, ins, dout, calls=1):
+    import torch
+    c = m3.ssm_config(cfg, m3.M3_MATH_FP32)
+    d = {k: dev(ins[k]) for k in MKEYS}
+    if cfg["num_rope_angles"] == 0:
+        d["angle"] = None
+    go = dev(dout)
+    ws = torch.empty(m3.m3_mimo_backward_workspace(c), dtype=torch.uint8, device="cuda")
+    first = None
+    for _ in range(calls):
+        g = {k: torch.full(s, float("nan"), device="cuda") for k, s in mimo_grad_shapes(cfg).items()}
+        if cfg["num_rope_angles"] == 0:
+            g["angle"] = None
+        m3.m3_mimo_backward(c, go, *[d[k] for k in MKEYS], *[g[k] for k in MKEYS], ws)
+        torch.cuda.synchronize()
+        got = {k: (np.zeros(mimo_grad_shapes(cfg)[k], np.float32) if g[k] is None
+                   else g[k].cpu().numpy()) for k in MKEYS}
+        if first is None:
+            first = got
+        else:
+            for k in MKEYS:
+                assert np.array_equal(first[k], got[k]), f"call-to-call difference in {k}"
+    return first
+
+
+def mimo_compare(got, ref, label, tol=BWD_TOL):
+    floor = 1e-3 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
+    for k in MKEYS:
+        if ref[k].size == 0:
+            continue
+        assert np.all(np.isfinite(got[k])), f"{label} {k}: unwritten or non-finite elements"
+        if np.max(np.abs(ref[k])) < floor:
+            err = float(np.max(np.abs(got[k].astype(np.float64) - ref[k]))) / floor
+            assert err <= tol, (label, k, "against the floor", err)
+        else:
+            check_close(got[k], ref[k], tol, f"{label} grad {k}")
+
+
+def mimo_case(B, L, H, G, P, N, A, R, norm, has_z=1, has_d=1, seed=80):
+    w = gen.Workload("mbwd", B, L, H, G, P, N, A, mimo_rank=R, has_z=has_z, has_d=has_d,
+                     has_output_norm=norm, seed_index=seed)
+    ins = gen.scan_inputs(w)
+    ins["d"] = np.linspace(0.5, 1.5, H, dtype=np.float32)
+    return w.cfg(), ins, gen.output_gradient(w)
+
+
+MIMO_CASES = {
+    # the MIMO R4 workload's head shape with the norm, on a shorter sequence
+    "r4_norm": dict(B=1, L=40, H=2, G=1, P=64, N=64, A=32, R=4, norm=1),
+    # rank 2 without the norm, heads sharing groups, a ragged last tile
+    "r2_groups": dict(B=2, L=33, H=4, G=2, P=32, N=32, A=8, R=2, norm=0),
+    # rank 3 (the rank-4 instance with three ranks), no gate, odd sizes
+    "r3_odd": dict(B=1, L=21, H=2, G=1, P=24, N=20, A=5, R=3, norm=1, has_z=0),
+    # rank 8
+    "r8": dict(B=1, L=17, H=1, G=1, P=16, N=16, A=4, R=8, norm=1),
+    # rank 1 with the norm and N = 128
+    "r1_norm_n128": dict(B=1, L=30, H=2, G=2, P=16, N=128, A=32, R=1, norm=1),
+    # rank 5, P N = 4000, no skip, A = 0
+    "r5_p40_n100": dict(B=1, L=12, H=2, G=1, P=40, N=100, A=0, R=5, norm=0, has_d=0),
+}
+
+
+@pytest.mark.parametrize("name", list(MIMO_CASES))
+def test_mimo_backward_matches_oracle(name):
+    cfg, ins, dout = mimo_case(**MIMO_CASES[name])
+    got = gpu_mimo_backward(cfg, ins, dout, calls=2)
+    ref = oracle.mimo_backward(cfg, dout, *[ins[k] for k in MKEYS])
+    mimo_compare(got, ref, name)
+
+
+def test_mimo_backward_r4_workload():
+    """The MIMO R4 workload (B4 L4096 H32 G1 P64 N64 A32 R4 with the output
+    norm) whole: every one of the fifteen gradients against the oracle."""
+    w = gen.MIMO_R4
+    cfg, ins = w.cfg(), gen.scan_inputs(w)
+    dout = gen.output_gradient(w)
+    got = gpu_mimo_backward(cfg, ins, dout)
+    ref = oracle.mimo_backward(cfg, dout, *[ins[k] for k in MKEYS])
+    mimo_compare(got, ref, "mimo r4 workload")
