@@ -6,8 +6,10 @@ oracle), on the same seeded inputs and output gradient.
 Bar: the FP32 bar of the forward, 1e-5 normwise (max|gpu - oracle| / max|oracle|
 per gradient), for all eleven gradients. A gradient that vanishes in exact
 arithmetic (with one token, the angle adjoint: q_t . k_t does not depend on
-theta_t) is compared against a floor of 1e-3 times the call's largest
-per-token gradient instead of its own rounding residue. Outputs start as NaN, so an
+theta_t; with one token from a zero state, d adt as well) is compared
+against a floor of 1e-2 times the call's largest per-token gradient instead
+of its own rounding residue: the kernels form it as a difference of terms of
+that size, whose rounding is absolute. Outputs start as NaN, so an
 element the kernels never write fails the comparison.
 """
 import numpy as np
@@ -80,7 +82,7 @@ PER_TOKEN = ("c", "b", "x", "z", "adt", "dt", "trap")
 
 
 def compare(got, ref, label, tol=BWD_TOL):
-    floor = 1e-3 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
+    floor = 1e-2 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
     for k in KEYS:
         if ref[k].size == 0:
             continue
@@ -224,7 +226,7 @@ def gpu_mimo_backward(cfg, ins, dout, calls=1):
 
 
 def mimo_compare(got, ref, label, tol=BWD_TOL):
-    floor = 1e-3 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
+    floor = 1e-2 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
     for k in MKEYS:
         if ref[k].size == 0:
             continue

@@ -137,3 +137,30 @@ def test_step_sweep(w):
     got, _ = run_gpu_steps(w, ins, w.sequence_length, mimo=mimo)
     ref = oracle_scan(w.cfg(), ins, mimo=mimo)
     check_close(got, ref, TOL[FP32], "step " + _id(w))
+
+
+BWD_SISO = [w.with_(sequence_length=min(w.sequence_length, 300)) for w in SISO[:16]]
+BWD_MIMO = [w.with_(sequence_length=min(w.sequence_length, 130)) for w in MIMO[:10]]
+
+
+@pytest.mark.parametrize("w", BWD_SISO, ids=_id)
+def test_siso_backward_sweep(w):
+    """m3_siso_backward on the drawn SISO geometries (up to 300 tokens) against
+    the oracle's adjoints (FP32 bar, per-token floor for vanishing gradients)."""
+    from test_gpu_backward import compare, gpu_backward
+    ins = gen.scan_inputs(w)
+    dout = gen.output_gradient(w)
+    got = gpu_backward(w.cfg(), ins, dout)
+    ref = oracle.siso_backward(w.cfg(), dout, *[ins[k] for k in oracle.GRAD_NAMES])
+    compare(got, ref, "backward " + _id(w))
+
+
+@pytest.mark.parametrize("w", BWD_MIMO, ids=_id)
+def test_mimo_backward_sweep(w):
+    """m3_mimo_backward on the drawn MIMO geometries (up to 130 tokens)."""
+    from test_gpu_backward import gpu_mimo_backward, mimo_compare
+    ins = gen.scan_inputs(w)
+    dout = gen.output_gradient(w)
+    got = gpu_mimo_backward(w.cfg(), ins, dout)
+    ref = oracle.mimo_backward(w.cfg(), dout, *[ins[k] for k in oracle.MIMO_GRAD_NAMES])
+    mimo_compare(got, ref, "mimo backward " + _id(w))
