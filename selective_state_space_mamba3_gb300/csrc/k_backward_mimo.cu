@@ -26,9 +26,11 @@
 //    then dx_t = sum_r dv_{t,r} mimo_x[r], the mimo_x sums, and the running
 //    sums for d adt and the angle as in the SISO adjoints;
 //  * k_mbwd_finish: d dt, d trap and the ordered sums over heads and batch.
-// A tile holds 16 / RM tokens (RM = 1, 2, 4 or 8, the instance's rank bound),
-// at most 16 (token, rank) rows; the thread layout of the sweeps is that of
-// the SISO adjoint kernels.
+// A tile holds tokens_per_tile(RM) tokens (RM = 1, 2, 4 or 8, the
+// instance's rank bound): 16 for RM = 1, else 32 / RM (one block per SM
+// leaves the shared memory for 32 (token, rank) rows, halving the block
+// barriers per token); the thread layout of the sweeps is that of the SISO
+// adjoint kernels.
 #include <algorithm>
 
 #include "k_backward.cuh"
@@ -42,15 +44,17 @@ struct MBwdWs {
 
 namespace {
 
+__host__ __device__ constexpr int tokens_per_tile(int RM) { return RM == 1 ? 16 : 32 / RM; }
+
 struct MBwdLayout {
   int Npad, Ppad, AS;
   int q, k, v, dy, y, part, coef, th, cs, sn, dth, red, floats;
 };
 
-// kTM = 16 / RM tokens per tile, arrays sized for RM >= R ranks.
+// tokens_per_tile(RM) tokens per tile, arrays sized for RM >= R ranks.
 inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB) {
   MBwdLayout l;
-  const int kTM = 16 / RM, R = RM;
+  const int kTM = tokens_per_tile(RM), R = RM;
   l.Npad = 64 * NB;
   l.Ppad = 16 * RPT;
   l.AS = A > 0 ? A : 1;
@@ -140,7 +144,7 @@ namespace {
 template <int RPT, int NB, int RM, bool DQ>
 __global__ void __launch_bounds__(kBT, 1)
     k_mbwd_fwd(ScanGeom g, ScanArgs a, MBwdWs w, MBwdLayout lay) {
-  constexpr int kTM = 16 / RM;
+  constexpr int kTM = tokens_per_tile(RM);
   const int R = g.R;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
@@ -478,7 +482,7 @@ namespace {
 template <int RPT, int NB, int RM>
 __global__ void __launch_bounds__(kBT, 1)
     k_mbwd_rev(ScanGeom g, ScanArgs a, BwdArgs o, MBwdWs w, MBwdLayout lay) {
-  constexpr int kTM = 16 / RM;
+  constexpr int kTM = tokens_per_tile(RM);
   const int R = g.R;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
@@ -596,19 +600,77 @@ __global__ void __launch_bounds__(kBT, 1)
       pp[0] = s;
     }
     // the rank cross products of each token: dyv[r'][r] = dy_{r'} . v_r,
-    // qk[r'][r] = q_{r'} . k_r (one warp per (token, r', r) pair)
-    for (int i = warp; i < tv * R * R; i += kWarps) {
-      const int tt = i / (R * R), rr = i - tt * R * R, r1 = rr / R, r = rr - r1 * R;
-      float dv = 0.f, qk = 0.f;
-      for (int p = lane; p < P; p += 32)
-        dv = fmaf(sdy[(tt * R + r1) * Ppad + p], sv[(tt * R + r) * Ppad + p], dv);
-      for (int n = lane; n < N; n += 32)
-        qk = fmaf(sq[(tt * R + r1) * Npad + n], sk[(tt * R + r) * Npad + n], qk);
-      dv = warp_sum(dv);
-      qk = warp_sum(qk);
-      if (lane == 0) {
-        sred[tt * kRed + rr] = dv;
-        sred[tt * kRed + R * R + rr] = qk;
+    // qk[r'][r] = q_{r'} . k_r
+    if constexpr (RM <= 4) {
+      // a warp per token: each lane sums its columns of all 2 RM^2 products,
+      // then one halving exchange leaves lane l with product l / (32 / V)
+      constexpr int V = 2 * RM * RM;
+      for (int tt = warp; tt < tv; tt += kWarps) {
+        float v[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) v[i] = 0.f;
+        for (int p = lane; p < P; p += 32) {
+          float dyp[RM], vp[RM];
+#pragma unroll
+          for (int r = 0; r < RM; ++r) {
+            dyp[r] = r < R ? sdy[(tt * R + r) * Ppad + p] : 0.f;
+            vp[r] = r < R ? sv[(tt * R + r) * Ppad + p] : 0.f;
+          }
+#pragma unroll
+          for (int r1 = 0; r1 < RM; ++r1)
+#pragma unroll
+            for (int r = 0; r < RM; ++r) v[r1 * RM + r] = fmaf(dyp[r1], vp[r], v[r1 * RM + r]);
+        }
+        for (int n = lane; n < N; n += 32) {
+          float qn[RM], kn[RM];
+#pragma unroll
+          for (int r = 0; r < RM; ++r) {
+            qn[r] = r < R ? sq[(tt * R + r) * Npad + n] : 0.f;
+            kn[r] = r < R ? sk[(tt * R + r) * Npad + n] : 0.f;
+          }
+#pragma unroll
+          for (int r1 = 0; r1 < RM; ++r1)
+#pragma unroll
+            for (int r = 0; r < RM; ++r)
+              v[RM * RM + r1 * RM + r] = fmaf(qn[r1], kn[r], v[RM * RM + r1 * RM + r]);
+        }
+        int idx = 0, o = 16;
+#pragma unroll
+        for (int c = V; c > 1; c >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < c / 2; ++i) {
+            const float send = up ? v[i] : v[i + c / 2];
+            const float keep = up ? v[i + c / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+          if (up) idx += c / 2;
+          o >>= 1;
+        }
+        float tot = v[0];
+#pragma unroll
+        for (int x = 32 / V / 2; x > 0; x >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, x);
+        if ((lane & (32 / V - 1)) == 0) {
+          const int half = idx >= RM * RM, j = idx - half * RM * RM;
+          const int r1 = j / RM, r = j - r1 * RM;
+          if (r1 < R && r < R) sred[tt * kRed + half * R * R + r1 * R + r] = tot;
+        }
+      }
+    } else {
+      // one warp per (token, r', r) pair
+      for (int i = warp; i < tv * R * R; i += kWarps) {
+        const int tt = i / (R * R), rr = i - tt * R * R, r1 = rr / R, r = rr - r1 * R;
+        float dv = 0.f, qk = 0.f;
+        for (int p = lane; p < P; p += 32)
+          dv = fmaf(sdy[(tt * R + r1) * Ppad + p], sv[(tt * R + r) * Ppad + p], dv);
+        for (int n = lane; n < N; n += 32)
+          qk = fmaf(sq[(tt * R + r1) * Npad + n], sk[(tt * R + r) * Npad + n], qk);
+        dv = warp_sum(dv);
+        qk = warp_sum(qk);
+        if (lane == 0) {
+          sred[tt * kRed + rr] = dv;
+          sred[tt * kRed + R * R + rr] = qk;
+        }
       }
     }
     __syncthreads();
