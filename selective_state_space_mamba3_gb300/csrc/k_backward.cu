@@ -83,18 +83,22 @@ inline BwdLayout bwd_layout(int A, int RPT, int NB) {
 // of the tile's tv tokens from the running angles in sth, writing the cosines
 // and sines to scs / ssn: q = Rot(theta)(C + c_bias), k = Rot(theta)(B + b_bias),
 // split-half pairs (u, u + A) rotated by (u cos - w sin, u sin + w cos).
+template <int NB>
 __device__ __forceinline__ void stage_qk(const ScanGeom& g, const ScanArgs& a, int b, int h,
                                          int grp, int t0, int tv, const BwdLayout& lay,
                                          float* sq, float* sk, int koff, const float* sth,
                                          float* scs, float* ssn) {
-  const int N = g.N, A = g.A, U = N - A;
-  for (int i = threadIdx.x; i < tv * U; i += kBT) {
-    const int tt = i / U, u = i - tt * U;
+  constexpr int Npad = 64 * NB;
+  const int N = g.N, A = g.A;
+  // item (tt, u): u < A the pair (u, u + A), 2A <= u < N the plain dim u
+  for (int i = threadIdx.x; i < tv * Npad; i += kBT) {
+    const int tt = i / Npad, u = i - tt * Npad;
+    if ((u >= A && u < 2 * A) || u >= N) continue;
     const int64_t row = (((int64_t)b * g.L + t0 + tt) * g.G + grp) * N;
     const float* cb = a.c_bias + (int64_t)h * N;
     const float* bb = a.b_bias + (int64_t)h * N;
-    float* qd = sq + tt * lay.Npad;
-    float* kd = sk + (tt + koff) * lay.Npad;
+    float* qd = sq + tt * Npad;
+    float* kd = sk + (tt + koff) * Npad;
     if (u < A) {
       float sn, cs;
       sincosf(sth[tt * lay.AS + u], &sn, &cs);
@@ -107,9 +111,8 @@ __device__ __forceinline__ void stage_qk(const ScanGeom& g, const ScanArgs& a, i
       kd[u] = bu * cs - bw * sn;
       kd[u + A] = bu * sn + bw * cs;
     } else {
-      const int n = u + A;
-      qd[n] = a.c[row + n] + cb[n];
-      kd[n] = a.b[row + n] + bb[n];
+      qd[u] = a.c[row + u] + cb[u];
+      kd[u] = a.b[row + u] + bb[u];
     }
   }
 }
@@ -140,7 +143,8 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
   float* sdz = sm + lay.dz;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rq = lane >> 4, cq = lane & 15;
   const int P = g.P, N = g.N, A = g.A, L = g.L, H = g.H;
-  const int Npad = lay.Npad, Ppad = lay.Ppad, AS = lay.AS;
+  constexpr int Npad = 64 * NB, Ppad = 16 * RPT;
+  const int AS = lay.AS;
   const int bh = blockIdx.x, b = bh / H, h = bh % H, hpg = H / g.G, grp = h / hpg;
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
@@ -169,8 +173,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       scoef[tid * 8 + 1] = (1.f - lam) * dtv * al;
       scoef[tid * 8 + 2] = lam * dtv;
     }
-    for (int i = tid; i < tv * P; i += kBT) {
-      const int tt = i / P, p = i - tt * P;
+    for (int i = tid; i < tv * Ppad; i += kBT) {
+      const int tt = i / Ppad, p = i - tt * Ppad;
+      if (p >= P) continue;
       const int64_t e = (((int64_t)b * L + t0 + tt) * H + h) * P + p;
       const float go = o.dout[e];
       sv[(tt + 1) * Ppad + p] = a.x[e];
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     }
     __syncthreads();
     // (2) rotated q_t into sq[tt], k_t into sk[tt + 1] (sk[0]: previous token)
-    stage_qk(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
+    stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
     // (3) the recurrence over the tile's tokens
     for (int tt = 0; tt < tv; ++tt) {
@@ -269,8 +274,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       for (int u = lane; u < A; u += 32) w.dthq[tix * A + u] = dq[u + A] * q[u] - dq[u] * q[u + A];
     }
     // (5c) dz_t = dout_t (y_t + D x_t) silu'(z_t); the D sum
-    for (int i = tid; i < tv * P; i += kBT) {
-      const int tt = i / P, p = i - tt * P;
+    for (int i = tid; i < tv * Ppad; i += kBT) {
+      const int tt = i / Ppad, p = i - tt * Ppad;
+      if (p >= P) continue;
       const float xv = sv[(tt + 1) * Ppad + p];
       o.gz[(((int64_t)b * L + t0 + tt) * H + h) * P + p] =
           g.has_z ? sdz[tt * Ppad + p] * fmaf(dskip, xv, sy[tt * Ppad + p]) : 0.f;
@@ -318,7 +324,8 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
   float* sred = sm + lay.red;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rq = lane >> 4, cq = lane & 15;
   const int P = g.P, N = g.N, A = g.A, L = g.L, H = g.H;
-  const int Npad = lay.Npad, Ppad = lay.Ppad, AS = lay.AS;
+  constexpr int Npad = 64 * NB, Ppad = 16 * RPT;
+  const int AS = lay.AS;
   const int bh = blockIdx.x, b = bh / H, h = bh % H, hpg = H / g.G, grp = h / hpg;
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
@@ -354,8 +361,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       scoef[tid * 8 + 3] = s1;
       scoef[tid * 8 + 4] = dtv;
     }
-    for (int i = tid; i < tv * P; i += kBT) {
-      const int tt = i / P, p = i - tt * P;
+    for (int i = tid; i < tv * Ppad; i += kBT) {
+      const int tt = i / Ppad, p = i - tt * Ppad;
+      if (p >= P) continue;
       const int64_t e = (((int64_t)b * L + t0 + tt) * H + h) * P + p;
       const float go = o.dout[e];
       sv[tt * Ppad + p] = a.x[e];
@@ -366,13 +374,14 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       }
       sdy[tt * Ppad + p] = dyv;
     }
-    for (int i = tid; i < tv * A; i += kBT) {
-      const int tt = i / A, u = i - tt * A;
+    for (int i = tid; i < tv * 64; i += kBT) {
+      const int tt = i >> 6, u = i & 63;
+      if (u >= A) continue;
       sth[tt * AS + u] = w.theta[((int64_t)bh * L + t0 + tt) * A + u];
     }
     __syncthreads();
     // (2) rotated q_t into sq[tt], k_t into sk[tt]
-    stage_qk(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
+    stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
     __syncthreads();
     // (3) the adjoint recurrence, last token first
     for (int tt = tv - 1; tt >= 0; --tt) {
@@ -447,8 +456,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
           fmaf(scoef[tt * 8 + 1], spart[tt * kWarps * Npad + n],
                scoef[tt * 8 + 2] * sred[tt * 8] * sq[tt * Npad + n]);
     }
-    for (int i = tid; i < tv * P; i += kBT) {
-      const int tt = i / P, p = i - tt * P;
+    for (int i = tid; i < tv * Ppad; i += kBT) {
+      const int tt = i / Ppad, p = i - tt * Ppad;
+      if (p >= P) continue;
       const float coef = fmaf(scoef[tt * 8 + 2], sred[tt * 8 + 1], dskip);
       o.gx[(((int64_t)b * L + t0 + tt) * H + h) * P + p] =
           fmaf(scoef[tt * 8 + 1], smk[tt * Ppad + p], coef * sdy[tt * Ppad + p]);
@@ -478,8 +488,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
         }
       }
     }
-    for (int i = tid; i < tv * A; i += kBT) {
-      const int tt = i / A, u = i - tt * A;
+    for (int i = tid; i < tv * 64; i += kBT) {
+      const int tt = i >> 6, u = i & 63;
+      if (u >= A) continue;
       const float* dk = spart + (tt * kWarps + 1) * Npad;
       const float* k = sk + tt * Npad;
       sdth[tt * AS + u] = w.dthq[((int64_t)bh * L + t0 + tt) * A + u] +
@@ -496,8 +507,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     __syncthreads();
     // (10) theta_t = theta_{t-1} + dt_t angle_t: d angle (this head) and the
     // angle part of d dt
-    for (int i = tid; i < tv * A; i += kBT) {
-      const int tt = i / A, u = i - tt * A;
+    for (int i = tid; i < tv * 64; i += kBT) {
+      const int tt = i >> 6, u = i & 63;
+      if (u >= A) continue;
       w.dang_h[(((int64_t)b * L + t0 + tt) * H + h) * A + u] = sdth[tt * AS + u] * scoef[tt * 8 + 4];
     }
     for (int tt = warp; tt < tv; tt += kWarps) {
