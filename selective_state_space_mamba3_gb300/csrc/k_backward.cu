@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     // (2) rotated q_t into sq[tt], k_t into sk[tt + 1] (sk[0]: previous token)
     stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
-    // (3) the recurrence over the tile's tokens
+    // (3) the recurrence over the tile's tokens, the next tile's operands
+    // prefetched into L2 meanwhile
+    if (t0 + kT < L)
+      prefetch_tile(g, a, o.dout, nullptr, bh, b, h, grp, t0 + kT, min(kT, L - t0 - kT));
     for (int tt = 0; tt < tv; ++tt) {
       const float al = scoef[tt * 8], sal = scoef[tt * 8 + 1], gm = scoef[tt * 8 + 2];
       float kp[4 * NB], kc[4 * NB], qv[4 * NB];
@@ -383,7 +386,9 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     // (2) rotated q_t into sq[tt], k_t into sk[tt]
     stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
     __syncthreads();
-    // (3) the adjoint recurrence, last token first
+    // (3) the adjoint recurrence, last token first, the previous tile's
+    // operands prefetched into L2 meanwhile
+    if (t0 > 0) prefetch_tile(g, a, o.dout, w.theta, bh, b, h, grp, t0 - kT, kT);
     for (int tt = tv - 1; tt >= 0; --tt) {
       const float al1 = scoef[tt * 8];
       float kv[4 * NB], qv[4 * NB];

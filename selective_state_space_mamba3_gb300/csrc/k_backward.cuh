@@ -94,5 +94,41 @@ __device__ __forceinline__ float unrotate(const float* gr, const float* cs, cons
   return gr[n];
 }
 
+// L2 prefetch of the 128-byte lines of [p, p + bytes).
+__device__ __forceinline__ void prefetch_range(const float* p, int bytes) {
+  const uintptr_t first = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
+  const uintptr_t last = reinterpret_cast<uintptr_t>(p) + bytes;
+  for (uintptr_t q = first; q < last; q += 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+}
+
+// L2 prefetch of the operands a sweep stages for tokens [t0, t0 + tv) of
+// (b, h): the x, dout and z rows, the group's C and B rows (rank rows
+// grp R .. grp R + R - 1), the scalars, the angle row and, when given, the
+// saved running angles of the sequence. Thread i takes item i of 8 per token.
+__device__ __forceinline__ void prefetch_tile(const ScanGeom& g, const ScanArgs& a,
+                                              const float* dout, const float* theta, int bh,
+                                              int b, int h, int grp, int t0, int tv) {
+  const int P = g.P, N = g.N, H = g.H, L = g.L, A = g.A, R = g.R;
+  for (int i = threadIdx.x; i < tv * 8; i += kBT) {
+    const int tt = i >> 3, k = i & 7;
+    const int64_t tok = (int64_t)b * L + t0 + tt, s = tok * H + h;
+    switch (k) {
+      case 0: prefetch_range(a.x + s * P, P * 4); break;
+      case 1: prefetch_range(dout + s * P, P * 4); break;
+      case 2: if (g.has_z) prefetch_range(a.z + s * P, P * 4); break;
+      case 3: prefetch_range(a.c + (tok * g.G * R + (int64_t)grp * R) * N, R * N * 4); break;
+      case 4: prefetch_range(a.b + (tok * g.G * R + (int64_t)grp * R) * N, R * N * 4); break;
+      case 5:
+        prefetch_range(a.adt + s, 4);
+        prefetch_range(a.dt + s, 4);
+        prefetch_range(a.trap + s, 4);
+        break;
+      case 6: if (A > 0) prefetch_range(a.angle + tok * A, A * 4); break;
+      default: if (theta && A > 0) prefetch_range(theta + ((int64_t)bh * L + t0 + tt) * A, A * 4); break;
+    }
+  }
+}
+
 }  // namespace
 }  // namespace m3
