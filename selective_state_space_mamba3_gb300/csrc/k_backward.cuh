@@ -106,17 +106,23 @@ __device__ __forceinline__ void prefetch_range(const float* p, int bytes) {
 // (b, h): the x, dout and z rows, the group's C and B rows (rank rows
 // grp R .. grp R + R - 1), the scalars, the angle row and, when given, the
 // saved running angles of the sequence. Thread i takes item i of 8 per token.
+// (dout may be null: not prefetched; yd, when given, is the MIMO readout /
+// adjoint array [B H][L][R P], prefetched in place of z.)
 __device__ __forceinline__ void prefetch_tile(const ScanGeom& g, const ScanArgs& a,
                                               const float* dout, const float* theta, int bh,
-                                              int b, int h, int grp, int t0, int tv) {
+                                              int b, int h, int grp, int t0, int tv,
+                                              const float* yd = nullptr) {
   const int P = g.P, N = g.N, H = g.H, L = g.L, A = g.A, R = g.R;
   for (int i = threadIdx.x; i < tv * 8; i += kBT) {
     const int tt = i >> 3, k = i & 7;
     const int64_t tok = (int64_t)b * L + t0 + tt, s = tok * H + h;
     switch (k) {
       case 0: prefetch_range(a.x + s * P, P * 4); break;
-      case 1: prefetch_range(dout + s * P, P * 4); break;
-      case 2: if (g.has_z) prefetch_range(a.z + s * P, P * 4); break;
+      case 1: if (dout) prefetch_range(dout + s * P, P * 4); break;
+      case 2:
+        if (yd) prefetch_range(yd + ((int64_t)bh * L + t0 + tt) * R * P, R * P * 4);
+        else if (g.has_z) prefetch_range(a.z + s * P, P * 4);
+        break;
       case 3: prefetch_range(a.c + (tok * g.G * R + (int64_t)grp * R) * N, R * N * 4); break;
       case 4: prefetch_range(a.b + (tok * g.G * R + (int64_t)grp * R) * N, R * N * 4); break;
       case 5:

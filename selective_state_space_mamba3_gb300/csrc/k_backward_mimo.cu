@@ -204,6 +204,10 @@ __global__ void __launch_bounds__(kBT, 1)
     __syncthreads();
     stage_qk_ranks(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
+    // the next tile's operands into L2 while the recurrence runs
+    if (t0 + kTM < L)
+      prefetch_tile(g, a, nullptr, DQ ? w.theta : nullptr, bh, b, h, grp, t0 + kTM,
+                    min(kTM, L - t0 - kTM), DQ ? w.yd : nullptr);
     for (int tt = 0; tt < tv; ++tt) {
       const float al = scoef[tt * 8], sal = scoef[tt * 8 + 1], gm = scoef[tt * 8 + 2];
 #pragma unroll
@@ -549,6 +553,8 @@ __global__ void __launch_bounds__(kBT, 1)
     __syncthreads();
     stage_qk_ranks(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
     __syncthreads();
+    // the previous tile's operands into L2 while the recurrence runs
+    if (t0 > 0) prefetch_tile(g, a, nullptr, w.theta, bh, b, h, grp, t0 - kTM, kTM, w.yd);
     for (int tt = tv - 1; tt >= 0; --tt) {
       const float al1 = scoef[tt * 8];
 #pragma unroll
