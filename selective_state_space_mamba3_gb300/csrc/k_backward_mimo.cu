@@ -40,6 +40,7 @@ namespace m3 {
 struct MBwdWs {
   float *theta, *dthq, *Q, *dgam, *ds, *yd, *dc_h, *db_h, *dang_h;
   float *pcb, *pbb, *pd, *pmx, *pmz, *pmo, *pnw;
+  int out_tb;  // token blocks per sequence of k_mbwd_out (pd, pmz, pmo, pnw per block)
 };
 
 namespace {
@@ -342,19 +343,22 @@ __global__ void __launch_bounds__(kBT, 1)
 
 namespace {
 
-// Per token of one (b, h) (a warp per token, lane p = lane + 32 j): from
+// Per token of one (b, h) (a warp per token, lane p = lane + 32 j; block
+// bh * out_tb + tb takes the tb-th of out_tb equal token ranges): from
 // y_{t,r} in the workspace, o_t = sum_r mimo_o[r] y_{t,r} silu(z_t mimo_z[r]),
 // the norm's adjoint d o = rho w dout - rho^3 o (1/P) sum_j dout_j w_j o_j (or
 // d o = dout), then dy_{t,r} = d o mimo_o[r] silu(.) over y_{t,r}, dz_t, and
-// this (b, h)'s sums for mimo_o, mimo_z, norm_weight and D. P <= 128.
-template <int RM>
+// the block's sums for mimo_o, mimo_z, norm_weight and D. P <= 128.
+template <int RM, int kJ>  // kJ: P <= 32 kJ
 __global__ void __launch_bounds__(kBT) k_mbwd_out(ScanGeom g, ScanArgs a, BwdArgs o,
                                                   MBwdWs w) {
-  constexpr int kJ = 4;  // p = lane + 32 j
   __shared__ float red[kWarps][RM * 128 + 1];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = g.P, L = g.L, H = g.H, R = g.R;
-  const int bh = blockIdx.x, b = bh / H, h = bh % H;
+  const int blk = blockIdx.x, bh = blk / w.out_tb, tb = blk - bh * w.out_tb;
+  const int b = bh / H, h = bh % H;
+  const int per = (L + w.out_tb - 1) / w.out_tb;
+  const int t_end = min(L, (tb + 1) * per);
   float mo[kJ][RM], mz[kJ][RM], mx[kJ][RM], nw[kJ];
   float smo[kJ][RM], smz[kJ][RM], snw[kJ], sd = 0.f;
 #pragma unroll
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kBT) k_mbwd_out(ScanGeom g, ScanArgs a, BwdArg
       smo[j][r] = smz[j][r] = 0.f;
     }
   }
-  for (int t = warp; t < L; t += kWarps) {
+  for (int t = tb * per + warp; t < t_end; t += kWarps) {
     const int64_t e0 = (((int64_t)b * L + t) * H + h) * P;
     float* yd = w.yd + ((int64_t)bh * L + t) * R * P;
     float y[kJ][RM], gate[kJ][RM], dgate[kJ][RM], zv[kJ], go[kJ], ov[kJ];
@@ -461,18 +465,18 @@ __global__ void __launch_bounds__(kBT) k_mbwd_out(ScanGeom g, ScanArgs a, BwdArg
         const int r = i / P, p = i - r * P;
         float s = 0.f;
         for (int x = 0; x < kWarps; ++x) s += red[x][r * 128 + p];
-        dst[((int64_t)bh * R + r) * P + p] = s;
+        dst[((int64_t)blk * R + r) * P + p] = s;
       }
     } else {
       for (int p = tid; p < P; p += kBT) {
         float s = 0.f;
         for (int x = 0; x < kWarps; ++x) s += red[x][p];
-        w.pnw[(int64_t)bh * P + p] = s;
+        w.pnw[(int64_t)blk * P + p] = s;
       }
       if (tid == 0) {
         float s = 0.f;
         for (int x = 0; x < kWarps; ++x) s += red[x][128];
-        w.pd[bh] = s;
+        w.pd[blk] = s;
       }
     }
     __syncthreads();
@@ -883,26 +887,33 @@ __global__ void __launch_bounds__(kBT) k_mbwd_finish(ScanGeom g, ScanArgs a, MBw
     case 4:
       for (int64_t i = i0; i < H; i += stride) {
         float s = 0.f;
-        for (int b = 0; b < B; ++b) s += w.pd[(int64_t)b * H + i];
+        for (int b = 0; b < B; ++b)
+          for (int tb = 0; tb < w.out_tb; ++tb) s += w.pd[((int64_t)b * H + i) * w.out_tb + tb];
         o.g.gd[i] = g.has_d ? s : 0.f;
       }
       break;
     default:
       for (int64_t i = i0; i < (int64_t)H * R * P; i += stride) {
+        const int64_t hh = i / (R * P), rp = i - hh * R * P;
         float sx = 0.f, sz = 0.f, so = 0.f;
         for (int b = 0; b < B; ++b) {
-          const int64_t j = (int64_t)b * H * R * P + i;
-          sx += w.pmx[j];
-          sz += w.pmz[j];
-          so += w.pmo[j];
+          sx += w.pmx[(int64_t)b * H * R * P + i];
+          for (int tb = 0; tb < w.out_tb; ++tb) {
+            const int64_t j = (((int64_t)b * H + hh) * w.out_tb + tb) * R * P + rp;
+            sz += w.pmz[j];
+            so += w.pmo[j];
+          }
         }
         o.gmx[i] = sx;
         o.gmz[i] = g.has_z ? sz : 0.f;
         o.gmo[i] = so;
       }
       for (int64_t i = i0; i < (int64_t)H * P; i += stride) {
+        const int64_t hh = i / P, p = i - hh * P;
         float s = 0.f;
-        for (int b = 0; b < B; ++b) s += w.pnw[(int64_t)b * H * P + i];
+        for (int b = 0; b < B; ++b)
+          for (int tb = 0; tb < w.out_tb; ++tb)
+            s += w.pnw[(((int64_t)b * H + hh) * w.out_tb + tb) * P + p];
         o.gnw[i] = g.has_norm ? s : 0.f;
       }
       break;
@@ -912,6 +923,7 @@ __global__ void __launch_bounds__(kBT) k_mbwd_finish(ScanGeom g, ScanArgs a, MBw
 struct MBwdPlan {
   size_t theta, dthq, Q, dgam, ds, yd, dc_h, db_h, dang_h, pcb, pbb, pd, pmx, pmz, pmo, pnw, bytes;
   bool own_c, own_ang;
+  int out_tb;
 };
 
 MBwdPlan mbwd_plan(const ScanGeom& g) {
@@ -936,11 +948,15 @@ MBwdPlan mbwd_plan(const ScanGeom& g) {
   p.dang_h = take(p.own_ang ? BL * g.H * g.A : 0);
   p.pcb = take(bh * R * g.N);
   p.pbb = take(bh * R * g.N);
-  p.pd = take(bh);
+  // k_mbwd_out: about four blocks per SM, ranges of at least 64 tokens
+  p.out_tb = (int)std::max<int64_t>(
+      1, std::min<int64_t>((g.L + 63) / 64, (4 * 152 + (int64_t)bh - 1) / (int64_t)bh));
+  const size_t nb = bh * (size_t)p.out_tb;
+  p.pd = take(nb);
   p.pmx = take(bh * R * g.P);
-  p.pmz = take(bh * R * g.P);
-  p.pmo = take(bh * R * g.P);
-  p.pnw = take(bh * g.P);
+  p.pmz = take(nb * R * g.P);
+  p.pmo = take(nb * R * g.P);
+  p.pnw = take(nb * g.P);
   p.bytes = off;
   return p;
 }
@@ -966,7 +982,10 @@ cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
   }
   const unsigned grid = (unsigned)(g.B * g.H);
   k_mbwd_fwd<RPT, NB, RM, false><<<grid, kBT, smem, s>>>(g, a, w, lay);
-  k_mbwd_out<RM><<<grid, kBT, 0, s>>>(g, a, o.g, w);
+  const unsigned out_grid = grid * (unsigned)w.out_tb;
+  if (g.P <= 32) k_mbwd_out<RM, 1><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
+  else if (g.P <= 64) k_mbwd_out<RM, 2><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
+  else k_mbwd_out<RM, 4><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
   k_mbwd_fwd<RPT, NB, RM, true><<<grid, kBT, smem, s>>>(g, a, w, lay);
   k_mbwd_rev<RPT, NB, RM><<<grid, kBT, smem, s>>>(g, a, o.g, w, lay);
   count_launches(4);
@@ -1015,6 +1034,7 @@ cudaError_t launch_mimo_backward(const ScanGeom& g, const ScanArgs& a, const MBw
   w.pmz = f(p.pmz);
   w.pmo = f(p.pmo);
   w.pnw = f(p.pnw);
+  w.out_tb = p.out_tb;
   cudaError_t e;
   // instances for up to 1, 2, 4 or 8 ranks (16 / that many tokens per tile)
   if (g.R == 1) e = launch_mbwd_rank<1>(g, a, o, w, s);
