@@ -242,9 +242,10 @@ int m3_siso_backward(const m3_ssm_config* cfg, const float* grad_out, const floa
  * grad_d without has_d, grad_norm_weight without has_output_norm. The scan
  * starts from a zero state.
  * Arithmetic: FP32 on the CUDA cores whatever cfg->math_mode says: a forward
- * sweep for the readouts y_{t,r}, a per-token pass for the norm, gate and
- * mimo_o adjoints, a second forward sweep for the query gradients, a reverse
- * sweep and a reduction in a fixed order (repeated calls give the same bits).
+ * sweep for the readouts y_{t,r} (recording the state at every tile start), a
+ * per-token pass for the norm, gate and mimo_o adjoints, a pass over all
+ * tiles at once for the query gradients, a reverse sweep and a reduction in a
+ * fixed order (repeated calls give the same bits).
  * Checks: those of m3_mimo_forward, plus B*L*H*R*N, B*L*H*R*P and B*L*H*A
  * below 2^32; every pointer but angle / grad_angle (when A == 0) non-NULL and
  * 16-byte aligned. workspace: at least m3_mimo_backward_workspace() bytes,

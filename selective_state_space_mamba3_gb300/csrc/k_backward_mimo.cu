@@ -8,11 +8,12 @@
 // the output norm out_t = o_t rho_t w. The gradient of y_{t,r} depends on the
 // whole row o_t through the norm, so the forward sweep runs twice:
 //  * k_mbwd_fwd<..., false>: the state, y_{t,r} for every (t, r) into the
-//    workspace (and the running angle);
+//    workspace (and the running angle, and the state at every tile start);
 //  * k_mbwd_out: per token the norm, gate and contraction adjoints: dy_{t,r}
 //    (over y_{t,r} in place), dz, and the per-(b, h) sums for mimo_o, mimo_z,
 //    norm_weight and D;
-//  * k_mbwd_fwd<..., true>: the state again and dq_{t,r} = h_t^T dy_{t,r}: the
+//  * k_mbwd_fwd<..., true>: one tile per block, all tiles at once, the state
+//    again from the tile's recorded start and dq_{t,r} = h_t^T dy_{t,r}: the
 //    C gradient parts, Q_t = sum_r q_{t,r} . dq_{t,r}, the query part of the
 //    angle adjoint;
 //  * k_mbwd_rev: the adjoint state Lam_t = a_{t+1} Lam_{t+1} + sum_r dy_{t,r}
@@ -40,7 +41,9 @@ namespace m3 {
 struct MBwdWs {
   float *theta, *dthq, *Q, *dgam, *ds, *yd, *dc_h, *db_h, *dang_h;
   float *pcb, *pbb, *pd, *pmx, *pmz, *pmo, *pnw;
-  int out_tb;  // token blocks per sequence of k_mbwd_out (pd, pmz, pmo, pnw per block)
+  float* ckpt;  // [B H][tiles][Ppad][Npad] the state before each tile's first token
+  int out_tb;   // token blocks per sequence of k_mbwd_out (pd, pmz, pmo, pnw per block)
+  int tiles;    // tiles per sequence (pcb holds one c_bias sum per (b, h, tile))
 };
 
 namespace {
@@ -52,8 +55,10 @@ struct MBwdLayout {
   int q, k, v, dy, y, part, coef, th, cs, sn, dth, red, floats;
 };
 
-// tokens_per_tile(RM) tokens per tile, arrays sized for RM >= R ranks.
-inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB) {
+// tokens_per_tile(RM) tokens per tile, arrays sized for RM >= R ranks. The
+// query-gradient kernel (dq) uses neither the readout rows nor the reverse
+// sweep's arrays and leaves them out (two of its blocks then fit an SM).
+inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB, bool dq = false) {
   MBwdLayout l;
   const int kTM = tokens_per_tile(RM), R = RM;
   l.Npad = 64 * NB;
@@ -69,14 +74,14 @@ inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB) {
   l.k = take((kTM + 1) * R * l.Npad);
   l.v = take((kTM + 1) * R * l.Ppad);
   l.dy = take(kTM * R * l.Ppad);
-  l.y = take(kTM * R * l.Ppad);
+  l.y = take(dq ? 0 : kTM * R * l.Ppad);
   l.part = take(kTM * kWarps * R * l.Npad);
   l.coef = take(kTM * 8);
   l.th = take(kTM * l.AS);
   l.cs = take(kTM * l.AS);
   l.sn = take(kTM * l.AS);
-  l.dth = take(kTM * l.AS);
-  l.red = take(kTM * (2 * R * R + R + 8));
+  l.dth = take(dq ? 0 : kTM * l.AS);
+  l.red = take(dq ? 0 : kTM * (2 * R * R + R + 8));
   l.floats = off;
   return l;
 }
@@ -139,11 +144,15 @@ __device__ __forceinline__ void stage_values(const ScanGeom& g, const ScanArgs& 
 
 namespace {
 
-// The forward sweep of one (b, h): the state in registers (rows of the thread
-// as in the SISO sweeps), each token's y_{t,r} (DQ = false) or dq_{t,r} = h_t^T
-// dy_{t,r} (DQ = true).
+// DQ = false: the forward sweep of one (b, h), the state in registers (rows
+// of the thread as in the SISO sweeps): each token's y_{t,r}, and the state
+// before each tile's first token into the workspace.
+// DQ = true: one tile of one (b, h) per block, parallel over tiles: the state
+// from that record, the previous token's key and value staged, and each
+// token's dq_{t,r} = h_t^T dy_{t,r} with the C gradient parts, Q_t and the
+// query part of the angle adjoint.
 template <int RPT, int NB, int RM, bool DQ>
-__global__ void __launch_bounds__(kBT, 1)
+__global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
     k_mbwd_fwd(ScanGeom g, ScanArgs a, MBwdWs w, MBwdLayout lay) {
   constexpr int kTM = tokens_per_tile(RM);
   const int R = g.R;
@@ -161,7 +170,11 @@ __global__ void __launch_bounds__(kBT, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rq = lane >> 4, cq = lane & 15;
   const int P = g.P, N = g.N, A = g.A, L = g.L, H = g.H;
   const int Npad = lay.Npad, Ppad = lay.Ppad, AS = lay.AS;
-  const int bh = blockIdx.x, b = bh / H, h = bh % H, grp = h / (H / g.G);
+  const int ntiles = (L + kTM - 1) / kTM;
+  const int bh = DQ ? (int)(blockIdx.x / ntiles) : (int)blockIdx.x;
+  const int tile_first = DQ ? (int)(blockIdx.x % ntiles) : 0;
+  const int tile_end = DQ ? tile_first + 1 : ntiles;
+  const int b = bh / H, h = bh % H, grp = h / (H / g.G);
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
 
@@ -171,6 +184,20 @@ __global__ void __launch_bounds__(kBT, 1)
   for (int i = 0; i < RPT; ++i)
 #pragma unroll
     for (int e = 0; e < 4 * NB; ++e) hs[i][e] = 0.f;
+  if (DQ && tile_first > 0) {
+    const float* ck = w.ckpt + ((int64_t)bh * ntiles + tile_first) * Ppad * Npad;
+#pragma unroll
+    for (int i = 0; i < RPT; ++i)
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        const float4 v =
+            *reinterpret_cast<const float4*>(ck + (prow0 + i) * Npad + 64 * j + 4 * cq);
+        hs[i][4 * j] = v.x;
+        hs[i][4 * j + 1] = v.y;
+        hs[i][4 * j + 2] = v.z;
+        hs[i][4 * j + 3] = v.w;
+      }
+  }
   float th_run = 0.f;
   constexpr int kCb = (RM * 128 + kBT - 1) / kBT;  // c_bias sums per thread (R Npad <= 128 RM)
   float cbacc[kCb];
@@ -178,9 +205,17 @@ __global__ void __launch_bounds__(kBT, 1)
   for (int j = 0; j < kCb; ++j) cbacc[j] = 0.f;
   __syncthreads();
 
-  const int ntiles = (L + kTM - 1) / kTM;
-  for (int tile = 0; tile < ntiles; ++tile) {
+  for (int tile = tile_first; tile < tile_end; ++tile) {
     const int t0 = tile * kTM, tv = min(kTM, L - t0);
+    if (DQ && t0 > 0) {
+      // the previous token's value and key into slot 0 (its q row is
+      // overwritten by the tile's own staging below)
+      for (int u = tid; u < A; u += kBT) sth[u] = w.theta[((int64_t)bh * L + t0 - 1) * A + u];
+      stage_values(g, a, w, bh, b, h, t0 - 1, 1, lay, sv, 0, nullptr);
+      __syncthreads();
+      stage_qk_ranks(g, a, b, h, grp, t0 - 1, 1, lay, sq, sk, 0, sth, scs, ssn);
+      __syncthreads();
+    }
     if (tid < tv) {
       const int64_t s = ((int64_t)b * L + t0 + tid) * H + h;
       const float al = expf(a.adt[s]), dtv = a.dt[s], lam = sigmoid_f(a.trap[s]);
@@ -205,10 +240,21 @@ __global__ void __launch_bounds__(kBT, 1)
     __syncthreads();
     stage_qk_ranks(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
-    // the next tile's operands into L2 while the recurrence runs
-    if (t0 + kTM < L)
-      prefetch_tile(g, a, nullptr, DQ ? w.theta : nullptr, bh, b, h, grp, t0 + kTM,
-                    min(kTM, L - t0 - kTM), DQ ? w.yd : nullptr);
+    if constexpr (!DQ) {
+      // the state before this tile's first token, for the query-gradient kernel
+      if (tile > 0) {
+        float* ck = w.ckpt + ((int64_t)bh * ntiles + tile) * Ppad * Npad;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i)
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            *reinterpret_cast<float4*>(ck + (prow0 + i) * Npad + 64 * j + 4 * cq) =
+                make_float4(hs[i][4 * j], hs[i][4 * j + 1], hs[i][4 * j + 2], hs[i][4 * j + 3]);
+      }
+      // the next tile's operands into L2 while the recurrence runs
+      if (t0 + kTM < L)
+        prefetch_tile(g, a, nullptr, nullptr, bh, b, h, grp, t0 + kTM, min(kTM, L - t0 - kTM));
+    }
     for (int tt = 0; tt < tv; ++tt) {
       const float al = scoef[tt * 8], sal = scoef[tt * 8 + 1], gm = scoef[tt * 8 + 2];
 #pragma unroll
@@ -333,7 +379,7 @@ __global__ void __launch_bounds__(kBT, 1)
       const int idx = tid + kBT * j;
       if (idx < R * Npad) {
         const int r = idx / Npad, n = idx - r * Npad;
-        if (n < N) w.pcb[((int64_t)bh * R + r) * N + n] = cbacc[j];
+        if (n < N) w.pcb[(((int64_t)bh * ntiles + tile_first) * R + r) * N + n] = cbacc[j];
       }
     }
   }
@@ -875,9 +921,11 @@ __global__ void __launch_bounds__(kBT) k_mbwd_finish(ScanGeom g, ScanArgs a, MBw
       break;
     case 3:
       for (int64_t i = i0; i < (int64_t)H * R * N; i += stride) {
+        const int64_t hh = i / (R * N), rn = i - hh * R * N;
         float sc = 0.f, sb = 0.f;
         for (int b = 0; b < B; ++b) {
-          sc += w.pcb[(int64_t)b * H * R * N + i];
+          for (int tl = 0; tl < w.tiles; ++tl)
+            sc += w.pcb[(((int64_t)b * H + hh) * w.tiles + tl) * R * N + rn];
           sb += w.pbb[(int64_t)b * H * R * N + i];
         }
         o.g.gc_bias[i] = sc;
@@ -921,9 +969,10 @@ __global__ void __launch_bounds__(kBT) k_mbwd_finish(ScanGeom g, ScanArgs a, MBw
 }
 
 struct MBwdPlan {
-  size_t theta, dthq, Q, dgam, ds, yd, dc_h, db_h, dang_h, pcb, pbb, pd, pmx, pmz, pmo, pnw, bytes;
+  size_t theta, dthq, Q, dgam, ds, yd, dc_h, db_h, dang_h, pcb, pbb, pd, pmx, pmz, pmo, pnw,
+      ckpt, bytes;
   bool own_c, own_ang;
-  int out_tb;
+  int out_tb, tiles;
 };
 
 MBwdPlan mbwd_plan(const ScanGeom& g) {
@@ -946,7 +995,13 @@ MBwdPlan mbwd_plan(const ScanGeom& g) {
   p.dc_h = take(p.own_c ? BL * g.H * R * g.N : 0);
   p.db_h = take(p.own_c ? BL * g.H * R * g.N : 0);
   p.dang_h = take(p.own_ang ? BL * g.H * g.A : 0);
-  p.pcb = take(bh * R * g.N);
+  // the instance's rank bound and tile length (as launch_mimo_backward picks it)
+  const int rm = g.R == 1 ? 1 : g.R == 2 ? 2 : g.R <= 4 ? 4 : 8;
+  const int ktm = tokens_per_tile(rm);
+  p.tiles = (g.L + ktm - 1) / ktm;
+  const size_t ppad = g.P <= 32 ? 32 : g.P <= 64 ? 64 : 128, npad = g.N <= 64 ? 64 : 128;
+  p.ckpt = take(bh * (size_t)p.tiles * ppad * npad);
+  p.pcb = take(bh * (size_t)p.tiles * R * g.N);
   p.pbb = take(bh * R * g.N);
   // k_mbwd_out: about four blocks per SM, ranges of at least 64 tokens
   p.out_tb = (int)std::max<int64_t>(
@@ -965,7 +1020,9 @@ template <int RPT, int NB, int RM>
 cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
                         const MBwdWs& w, cudaStream_t s) {
   const MBwdLayout lay = mbwd_layout(g.A, RM, RPT, NB);
+  const MBwdLayout lay_dq = mbwd_layout(g.A, RM, RPT, NB, true);
   const size_t smem = (size_t)lay.floats * sizeof(float);
+  const size_t smem_dq = (size_t)lay_dq.floats * sizeof(float);
   static bool attr_set = false;  // per instance: the opt-in above 48 KB, for A up to 64
   if (!attr_set) {
     const int most = mbwd_layout(64, RM, RPT, NB).floats * (int)sizeof(float);
@@ -973,7 +1030,8 @@ cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_mbwd_fwd<RPT, NB, RM, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               mbwd_layout(64, RM, RPT, NB, true).floats * (int)sizeof(float));
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_mbwd_rev<RPT, NB, RM>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, most);
@@ -986,7 +1044,7 @@ cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
   if (g.P <= 32) k_mbwd_out<RM, 1><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
   else if (g.P <= 64) k_mbwd_out<RM, 2><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
   else k_mbwd_out<RM, 4><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
-  k_mbwd_fwd<RPT, NB, RM, true><<<grid, kBT, smem, s>>>(g, a, w, lay);
+  k_mbwd_fwd<RPT, NB, RM, true><<<grid * (unsigned)w.tiles, kBT, smem_dq, s>>>(g, a, w, lay_dq);
   k_mbwd_rev<RPT, NB, RM><<<grid, kBT, smem, s>>>(g, a, o.g, w, lay);
   count_launches(4);
   return cudaGetLastError();
@@ -1035,6 +1093,8 @@ cudaError_t launch_mimo_backward(const ScanGeom& g, const ScanArgs& a, const MBw
   w.pmo = f(p.pmo);
   w.pnw = f(p.pnw);
   w.out_tb = p.out_tb;
+  w.ckpt = f(p.ckpt);
+  w.tiles = p.tiles;
   cudaError_t e;
   // instances for up to 1, 2, 4 or 8 ranks (16 / that many tokens per tile)
   if (g.R == 1) e = launch_mbwd_rank<1>(g, a, o, w, s);
