@@ -58,10 +58,13 @@ __device__ __forceinline__ void cols_sum_store(const float (&v)[4 * NB], int rq,
   }
 }
 
-// Loads RPT consecutive floats (16-byte aligned for RPT % 4 == 0, else 8-byte).
+// Loads RPT consecutive floats (16-byte aligned for RPT % 4 == 0, 8-byte for
+// RPT = 2).
 template <int RPT>
 __device__ __forceinline__ void load_rows(const float* src, float (&d)[RPT]) {
-  if constexpr (RPT % 4 == 0) {
+  if constexpr (RPT == 1) {
+    d[0] = src[0];
+  } else if constexpr (RPT % 4 == 0) {
 #pragma unroll
     for (int i = 0; i < RPT; i += 4) {
       const float4 t = *reinterpret_cast<const float4*>(src + i);
@@ -108,12 +111,13 @@ __device__ __forceinline__ void prefetch_range(const float* p, int bytes) {
 // saved running angles of the sequence. Thread i takes item i of 8 per token.
 // (dout may be null: not prefetched; yd, when given, is the MIMO readout /
 // adjoint array [B H][L][R P], prefetched in place of z.)
+template <int BT = kBT>
 __device__ __forceinline__ void prefetch_tile(const ScanGeom& g, const ScanArgs& a,
                                               const float* dout, const float* theta, int bh,
                                               int b, int h, int grp, int t0, int tv,
                                               const float* yd = nullptr) {
   const int P = g.P, N = g.N, H = g.H, L = g.L, A = g.A, R = g.R;
-  for (int i = threadIdx.x; i < tv * 8; i += kBT) {
+  for (int i = threadIdx.x; i < tv * 8; i += BT) {
     const int tt = i >> 3, k = i & 7;
     const int64_t tok = (int64_t)b * L + t0 + tt, s = tok * H + h;
     switch (k) {

@@ -27,11 +27,11 @@
 //    then dx_t = sum_r dv_{t,r} mimo_x[r], the mimo_x sums, and the running
 //    sums for d adt and the angle as in the SISO adjoints;
 //  * k_mbwd_finish: d dt, d trap and the ordered sums over heads and batch.
-// A tile holds tokens_per_tile(RM) tokens (RM = 1, 2, 4 or 8, the
-// instance's rank bound): 16 for RM = 1, else 32 / RM (one block per SM
-// leaves the shared memory for 32 (token, rank) rows, halving the block
-// barriers per token); the thread layout of the sweeps is that of the SISO
-// adjoint kernels.
+// A tile holds tokens_per_tile(RM, NB) tokens (RM = 1, 2, 4 or 8, the
+// instance's rank bound): for N <= 64, 16 when RM = 1, else 32 / RM; for
+// N > 64 half of that for RM > 1. The two sweeps run 512 threads (16 warps)
+// per (b, h), one block per SM, with the thread layout of the SISO adjoint
+// kernels; the query-gradient pass runs 256 threads per (b, h, tile).
 #include <algorithm>
 
 #include "k_backward.cuh"
@@ -48,21 +48,25 @@ struct MBwdWs {
 
 namespace {
 
-__host__ __device__ constexpr int tokens_per_tile(int RM) { return RM == 1 ? 16 : 32 / RM; }
+// (the sweeps' column partials, tokens x 16 warps x RM x 64 NB floats, stay
+// within 128 KB)
+__host__ __device__ constexpr int tokens_per_tile(int RM, int NB) {
+  return NB == 1 ? (RM == 1 ? 16 : 32 / RM) : 16 / RM;
+}
 
 struct MBwdLayout {
   int Npad, Ppad, AS;
   int q, k, v, dy, y, part, coef, th, cs, sn, dth, red, floats;
 };
 
-// tokens_per_tile(RM) tokens per tile, arrays sized for RM >= R ranks. The
+// tokens_per_tile(RM, NB) tokens per tile, arrays sized for RM >= R ranks. The
 // query-gradient kernel (dq) uses neither the readout rows nor the reverse
 // sweep's arrays and leaves them out (two of its blocks then fit an SM).
-inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB, bool dq = false) {
+inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB, bool dq = false, int warps = 16) {
   MBwdLayout l;
-  const int kTM = tokens_per_tile(RM), R = RM;
+  const int kTM = tokens_per_tile(RM, NB), R = RM;
   l.Npad = 64 * NB;
-  l.Ppad = 16 * RPT;
+  l.Ppad = 2 * warps * RPT;
   l.AS = A > 0 ? A : 1;
   int off = 0;
   auto take = [&](int n) {
@@ -75,7 +79,7 @@ inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB, bool dq = false) {
   l.v = take((kTM + 1) * R * l.Ppad);
   l.dy = take(kTM * R * l.Ppad);
   l.y = take(dq ? 0 : kTM * R * l.Ppad);
-  l.part = take(kTM * kWarps * R * l.Npad);
+  l.part = take(kTM * warps * R * l.Npad);
   l.coef = take(kTM * 8);
   l.th = take(kTM * l.AS);
   l.cs = take(kTM * l.AS);
@@ -88,13 +92,14 @@ inline MBwdLayout mbwd_layout(int A, int RM, int RPT, int NB, bool dq = false) {
 
 // Rotated, biased q_{t,r} (into sq[tt R + r]) and k_{t,r} (into
 // sk[(tt + koff) R + r]) of the tile's tokens; cos / sin into scs / ssn.
+template <int BT>
 __device__ __forceinline__ void stage_qk_ranks(const ScanGeom& g, const ScanArgs& a, int b,
                                                int h, int grp, int t0, int tv,
                                                const MBwdLayout& lay, float* sq, float* sk,
                                                int koff, const float* sth, float* scs,
                                                float* ssn) {
   const int N = g.N, A = g.A, U = N - A, R = g.R;
-  for (int i = threadIdx.x; i < tv * R * U; i += kBT) {
+  for (int i = threadIdx.x; i < tv * R * U; i += BT) {
     const int row = i / U, u = i - row * U;  // row = tt R + r
     const int tt = row / R, r = row - tt * R;
     const int64_t src = (((int64_t)b * g.L + t0 + tt) * g.G * R + (int64_t)grp * R + r) * N;
@@ -126,12 +131,13 @@ __device__ __forceinline__ void stage_qk_ranks(const ScanGeom& g, const ScanArgs
 // Per-token scalars a_t, s_t a_t, g_t (forward sweeps) into scoef, the values
 // v_{t,r} = x_t mimo_x[r] into sv[(tt + voff) R + r], and, with dy, the
 // workspace's dy_{t,r} into sdy[tt R + r].
+template <int BT>
 __device__ __forceinline__ void stage_values(const ScanGeom& g, const ScanArgs& a,
                                              const MBwdWs& w, int bh, int b, int h, int t0,
                                              int tv, const MBwdLayout& lay, float* sv, int voff,
                                              float* sdy) {
   const int P = g.P, L = g.L, H = g.H, R = g.R;
-  for (int i = threadIdx.x; i < tv * R * P; i += kBT) {
+  for (int i = threadIdx.x; i < tv * R * P; i += BT) {
     const int row = i / P, p = i - row * P;
     const int tt = row / R, r = row - tt * R;
     const float xv = a.x[(((int64_t)b * L + t0 + tt) * H + h) * P + p];
@@ -151,10 +157,10 @@ namespace {
 // from that record, the previous token's key and value staged, and each
 // token's dq_{t,r} = h_t^T dy_{t,r} with the C gradient parts, Q_t and the
 // query part of the angle adjoint.
-template <int RPT, int NB, int RM, bool DQ>
-__global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
+template <int RPT, int NB, int RM, bool DQ, int BT>
+__global__ void __launch_bounds__(BT, DQ ? 2 : 1)
     k_mbwd_fwd(ScanGeom g, ScanArgs a, MBwdWs w, MBwdLayout lay) {
-  constexpr int kTM = tokens_per_tile(RM);
+  constexpr int kTM = tokens_per_tile(RM, NB), kW = BT / 32;
   const int R = g.R;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
 
-  for (int i = tid; i < lay.part; i += kBT) sm[i] = 0.f;
+  for (int i = tid; i < lay.part; i += BT) sm[i] = 0.f;
   float hs[RPT][4 * NB];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
       }
   }
   float th_run = 0.f;
-  constexpr int kCb = (RM * 128 + kBT - 1) / kBT;  // c_bias sums per thread (R Npad <= 128 RM)
+  constexpr int kCb = (RM * 128 + BT - 1) / BT;  // c_bias sums per thread (R Npad <= 128 RM)
   float cbacc[kCb];
 #pragma unroll
   for (int j = 0; j < kCb; ++j) cbacc[j] = 0.f;
@@ -210,10 +216,10 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
     if (DQ && t0 > 0) {
       // the previous token's value and key into slot 0 (its q row is
       // overwritten by the tile's own staging below)
-      for (int u = tid; u < A; u += kBT) sth[u] = w.theta[((int64_t)bh * L + t0 - 1) * A + u];
-      stage_values(g, a, w, bh, b, h, t0 - 1, 1, lay, sv, 0, nullptr);
+      for (int u = tid; u < A; u += BT) sth[u] = w.theta[((int64_t)bh * L + t0 - 1) * A + u];
+      stage_values<BT>(g, a, w, bh, b, h, t0 - 1, 1, lay, sv, 0, nullptr);
       __syncthreads();
-      stage_qk_ranks(g, a, b, h, grp, t0 - 1, 1, lay, sq, sk, 0, sth, scs, ssn);
+      stage_qk_ranks<BT>(g, a, b, h, grp, t0 - 1, 1, lay, sq, sk, 0, sth, scs, ssn);
       __syncthreads();
     }
     if (tid < tv) {
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
       scoef[tid * 8 + 1] = (1.f - lam) * dtv * al;
       scoef[tid * 8 + 2] = lam * dtv;
     }
-    stage_values(g, a, w, bh, b, h, t0, tv, lay, sv, 1, DQ ? sdy : nullptr);
+    stage_values<BT>(g, a, w, bh, b, h, t0, tv, lay, sv, 1, DQ ? sdy : nullptr);
     if (!DQ && tid < A) {
       for (int tt = 0; tt < tv; ++tt) {
         const int64_t tok = (int64_t)b * L + t0 + tt;
@@ -233,12 +239,12 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
       }
     }
     if (DQ)
-      for (int i = tid; i < tv * A; i += kBT) {
+      for (int i = tid; i < tv * A; i += BT) {
         const int tt = i / A, u = i - tt * A;
         sth[tt * AS + u] = w.theta[((int64_t)bh * L + t0 + tt) * A + u];
       }
     __syncthreads();
-    stage_qk_ranks(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
+    stage_qk_ranks<BT>(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
     if constexpr (!DQ) {
       // the state before this tile's first token, for the query-gradient kernel
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
       }
       // the next tile's operands into L2 while the recurrence runs
       if (t0 + kTM < L)
-        prefetch_tile(g, a, nullptr, nullptr, bh, b, h, grp, t0 + kTM, min(kTM, L - t0 - kTM));
+        prefetch_tile<BT>(g, a, nullptr, nullptr, bh, b, h, grp, t0 + kTM, min(kTM, L - t0 - kTM));
     }
     for (int tt = 0; tt < tv; ++tt) {
       const float al = scoef[tt * 8], sal = scoef[tt * 8 + 1], gm = scoef[tt * 8 + 2];
@@ -303,14 +309,14 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
             for (int i = 0; i < RPT; ++i) acc = fmaf(hs[i][e], dyr[i], acc);
             dq[e] = acc;
           }
-          cols_sum_store<NB>(dq, rq, cq, spart + ((tt * kWarps + warp) * R + r) * Npad);
+          cols_sum_store<NB>(dq, rq, cq, spart + ((tt * kW + warp) * R + r) * Npad);
         }
       }
     }
     __syncthreads();
     if constexpr (!DQ) {
       // y_{t,r} = h_t q_{t,r} + D v_{t,r} into the workspace
-      for (int i = tid; i < tv * R * P; i += kBT) {
+      for (int i = tid; i < tv * R * P; i += BT) {
         const int row = i / P, p = i - row * P;
         const int tt = row / R, r = row - tt * R;
         w.yd[(((int64_t)bh * L + t0 + tt) * R + r) * P + p] =
@@ -318,26 +324,26 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
       }
     } else {
       // dq_{t,r}: the warps' column sums, into slot 0
-      for (int i = tid; i < tv * R * Npad; i += kBT) {
+      for (int i = tid; i < tv * R * Npad; i += BT) {
         const int row = i / Npad, n = i - row * Npad;
         const int tt = row / R, r = row - tt * R;
-        float* pp = spart + (tt * kWarps * R + r) * Npad + n;
+        float* pp = spart + (tt * kW * R + r) * Npad + n;
         float s = pp[0];
 #pragma unroll
-        for (int x = 1; x < kWarps; ++x) s += pp[x * R * Npad];
+        for (int x = 1; x < kW; ++x) s += pp[x * R * Npad];
         pp[0] = s;
       }
       __syncthreads();
       // the head's C gradient parts Rot(theta)^T dq_{t,r} and the c_bias sums
-      // (thread tid + kBT j keeps the sum of (r, n) = that index over R Npad)
+      // (thread tid + BT j keeps the sum of (r, n) = that index over R Npad)
 #pragma unroll
       for (int j = 0; j < kCb; ++j) {
-        const int idx = tid + kBT * j;
+        const int idx = tid + BT * j;
         if (idx < R * Npad) {
           const int r = idx / Npad, n = idx - r * Npad;
           if (n < N)
             for (int tt = 0; tt < tv; ++tt) {
-              const float v = unrotate(spart + (tt * kWarps * R + r) * Npad, scs + tt * AS,
+              const float v = unrotate(spart + (tt * kW * R + r) * Npad, scs + tt * AS,
                                        ssn + tt * AS, n, A);
               w.dc_h[((((int64_t)b * L + t0 + tt) * H + h) * R + r) * N + n] = v;
               cbacc[j] += v;
@@ -345,10 +351,10 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
         }
       }
       // Q_t = sum_r q_{t,r} . dq_{t,r} and the query part of theta_t's adjoint
-      for (int tt = warp; tt < tv; tt += kWarps) {
+      for (int tt = warp; tt < tv; tt += kW) {
         float s = 0.f;
         for (int r = 0; r < R; ++r) {
-          const float* dq = spart + (tt * kWarps * R + r) * Npad;
+          const float* dq = spart + (tt * kW * R + r) * Npad;
           const float* q = sq + (tt * R + r) * Npad;
           for (int n = lane; n < N; n += 32) s = fmaf(q[n], dq[n], s);
         }
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
         for (int u = lane; u < A; u += 32) {
           float d = 0.f;
           for (int r = 0; r < R; ++r) {
-            const float* dq = spart + (tt * kWarps * R + r) * Npad;
+            const float* dq = spart + (tt * kW * R + r) * Npad;
             const float* q = sq + (tt * R + r) * Npad;
             d += dq[u + A] * q[u] - dq[u] * q[u + A];
           }
@@ -368,15 +374,15 @@ __global__ void __launch_bounds__(kBT, DQ ? 2 : 1)
     }
     // this tile's last token becomes the next tile's previous token
     if (tv == kTM) {
-      for (int i = tid; i < R * Npad; i += kBT) sk[i] = sk[kTM * R * Npad + i];
-      for (int i = tid; i < R * Ppad; i += kBT) sv[i] = sv[kTM * R * Ppad + i];
+      for (int i = tid; i < R * Npad; i += BT) sk[i] = sk[kTM * R * Npad + i];
+      for (int i = tid; i < R * Ppad; i += BT) sv[i] = sv[kTM * R * Ppad + i];
     }
     __syncthreads();
   }
   if constexpr (DQ) {
 #pragma unroll
     for (int j = 0; j < kCb; ++j) {
-      const int idx = tid + kBT * j;
+      const int idx = tid + BT * j;
       if (idx < R * Npad) {
         const int r = idx / Npad, n = idx - r * Npad;
         if (n < N) w.pcb[(((int64_t)bh * ntiles + tile_first) * R + r) * N + n] = cbacc[j];
@@ -533,10 +539,10 @@ __global__ void __launch_bounds__(kBT) k_mbwd_out(ScanGeom g, ScanArgs a, BwdArg
 namespace {
 
 // The reverse sweep of one (b, h) with R ranks (see the file comment).
-template <int RPT, int NB, int RM>
-__global__ void __launch_bounds__(kBT, 1)
+template <int RPT, int NB, int RM, int BT>
+__global__ void __launch_bounds__(BT, 1)
     k_mbwd_rev(ScanGeom g, ScanArgs a, BwdArgs o, MBwdWs w, MBwdLayout lay) {
-  constexpr int kTM = tokens_per_tile(RM);
+  constexpr int kTM = tokens_per_tile(RM, NB), kW = BT / 32;
   const int R = g.R;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
@@ -559,18 +565,18 @@ __global__ void __launch_bounds__(kBT, 1)
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
 
-  for (int i = tid; i < lay.part; i += kBT) sm[i] = 0.f;
+  for (int i = tid; i < lay.part; i += BT) sm[i] = 0.f;
   float lam[RPT][4 * NB];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
 #pragma unroll
     for (int e = 0; e < 4 * NB; ++e) lam[i][e] = 0.f;
   float gth = 0.f, cadt = 0.f;
-  constexpr int kCb = (RM * 128 + kBT - 1) / kBT;
+  constexpr int kCb = (RM * 128 + BT - 1) / BT;
   float bbacc[kCb];
 #pragma unroll
   for (int j = 0; j < kCb; ++j) bbacc[j] = 0.f;
-  // mimo_x sums: thread keeps column p = tid % Ppad for every rank (Ppad divides kBT)
+  // mimo_x sums: thread keeps column p = tid % Ppad for every rank (Ppad divides BT)
   float mxacc[RM];
 #pragma unroll
   for (int r = 0; r < RM; ++r) mxacc[r] = 0.f;
@@ -595,16 +601,16 @@ __global__ void __launch_bounds__(kBT, 1)
       scoef[tid * 8 + 3] = s1;
       scoef[tid * 8 + 4] = dtv;
     }
-    stage_values(g, a, w, bh, b, h, t0, tv, lay, sv, 0, sdy);
-    for (int i = tid; i < tv * A; i += kBT) {
+    stage_values<BT>(g, a, w, bh, b, h, t0, tv, lay, sv, 0, sdy);
+    for (int i = tid; i < tv * A; i += BT) {
       const int tt = i / A, u = i - tt * A;
       sth[tt * AS + u] = w.theta[((int64_t)bh * L + t0 + tt) * A + u];
     }
     __syncthreads();
-    stage_qk_ranks(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
+    stage_qk_ranks<BT>(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
     __syncthreads();
     // the previous tile's operands into L2 while the recurrence runs
-    if (t0 > 0) prefetch_tile(g, a, nullptr, w.theta, bh, b, h, grp, t0 - kTM, kTM, w.yd);
+    if (t0 > 0) prefetch_tile<BT>(g, a, nullptr, w.theta, bh, b, h, grp, t0 - kTM, kTM, w.yd);
     for (int tt = tv - 1; tt >= 0; --tt) {
       const float al1 = scoef[tt * 8];
 #pragma unroll
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(kBT, 1)
         int row;
         const float msum = rows_sum16<RPT>(mk, cq, row);
         if ((cq & (16 / RPT - 1)) == 0) smk[(tt * R + r) * Ppad + prow0 + row] = msum;
-        cols_sum_store<NB>(mv, rq, cq, spart + ((tt * kWarps + warp) * R + r) * Npad);
+        cols_sum_store<NB>(mv, rq, cq, spart + ((tt * kW + warp) * R + r) * Npad);
       }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -646,13 +652,13 @@ __global__ void __launch_bounds__(kBT, 1)
     }
     __syncthreads();
     // M^T v_{t,r}: the warps' column sums, into slot 0
-    for (int i = tid; i < tv * R * Npad; i += kBT) {
+    for (int i = tid; i < tv * R * Npad; i += BT) {
       const int row = i / Npad, n = i - row * Npad;
       const int tt = row / R, r = row - tt * R;
-      float* pp = spart + (tt * kWarps * R + r) * Npad + n;
+      float* pp = spart + (tt * kW * R + r) * Npad + n;
       float s = pp[0];
 #pragma unroll
-      for (int x = 1; x < kWarps; ++x) s += pp[x * R * Npad];
+      for (int x = 1; x < kW; ++x) s += pp[x * R * Npad];
       pp[0] = s;
     }
     // the rank cross products of each token: dyv[r'][r] = dy_{r'} . v_r,
@@ -661,7 +667,7 @@ __global__ void __launch_bounds__(kBT, 1)
       // a warp per token: each lane sums its columns of all 2 RM^2 products,
       // then one halving exchange leaves lane l with product l / (32 / V)
       constexpr int V = 2 * RM * RM;
-      for (int tt = warp; tt < tv; tt += kWarps) {
+      for (int tt = warp; tt < tv; tt += kW) {
         float v[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) v[i] = 0.f;
@@ -714,7 +720,7 @@ __global__ void __launch_bounds__(kBT, 1)
       }
     } else {
       // one warp per (token, r', r) pair
-      for (int i = warp; i < tv * R * R; i += kWarps) {
+      for (int i = warp; i < tv * R * R; i += kW) {
         const int tt = i / (R * R), rr = i - tt * R * R, r1 = rr / R, r = rr - r1 * R;
         float dv = 0.f, qk = 0.f;
         for (int p = lane; p < P; p += 32)
@@ -731,7 +737,7 @@ __global__ void __launch_bounds__(kBT, 1)
     }
     __syncthreads();
     // v_r . M k_r; dg_t, ds_{t+1} and the d adt term
-    for (int tt = warp; tt < tv; tt += kWarps) {
+    for (int tt = warp; tt < tv; tt += kW) {
       float vmk_all = 0.f;
       for (int r = 0; r < R; ++r) {
         float s = 0.f;
@@ -755,18 +761,18 @@ __global__ void __launch_bounds__(kBT, 1)
     }
     __syncthreads();
     // dk_{t,r} into slot 1; dv_{t,r}, dx_t and the mimo_x sums
-    for (int i = tid; i < tv * R * Npad; i += kBT) {
+    for (int i = tid; i < tv * R * Npad; i += BT) {
       const int row = i / Npad, n = i - row * Npad;
       const int tt = row / R, r = row - tt * R;
       const float* red = sred + tt * kRed;
       float acc = 0.f;
       for (int r1 = 0; r1 < R; ++r1) acc = fmaf(red[r1 * R + r], sq[(tt * R + r1) * Npad + n], acc);
-      spart[((tt * kWarps + 1) * R + r) * Npad + n] =
-          fmaf(scoef[tt * 8 + 1], spart[(tt * kWarps * R + r) * Npad + n], scoef[tt * 8 + 2] * acc);
+      spart[((tt * kW + 1) * R + r) * Npad + n] =
+          fmaf(scoef[tt * 8 + 1], spart[(tt * kW * R + r) * Npad + n], scoef[tt * 8 + 2] * acc);
     }
     {
       const int p = tid % Ppad;
-      for (int tt = tid / Ppad; tt < tv; tt += kBT / Ppad) {
+      for (int tt = tid / Ppad; tt < tv; tt += BT / Ppad) {
         if (p >= P) continue;
         const float* red = sred + tt * kRed;
         const int64_t e = (((int64_t)b * L + t0 + tt) * H + h) * P + p;
@@ -801,23 +807,23 @@ __global__ void __launch_bounds__(kBT, 1)
     // theta's adjoint: the query part plus every rank's key part
 #pragma unroll
     for (int j = 0; j < kCb; ++j) {
-      const int idx = tid + kBT * j;
+      const int idx = tid + BT * j;
       if (idx < R * Npad) {
         const int r = idx / Npad, n = idx - r * Npad;
         if (n < N)
           for (int tt = 0; tt < tv; ++tt) {
-            const float v = unrotate(spart + ((tt * kWarps + 1) * R + r) * Npad, scs + tt * AS,
+            const float v = unrotate(spart + ((tt * kW + 1) * R + r) * Npad, scs + tt * AS,
                                      ssn + tt * AS, n, A);
             w.db_h[((((int64_t)b * L + t0 + tt) * H + h) * R + r) * N + n] = v;
             bbacc[j] += v;
           }
       }
     }
-    for (int i = tid; i < tv * A; i += kBT) {
+    for (int i = tid; i < tv * A; i += BT) {
       const int tt = i / A, u = i - tt * A;
       float d = w.dthq[((int64_t)bh * L + t0 + tt) * A + u];
       for (int r = 0; r < R; ++r) {
-        const float* dk = spart + ((tt * kWarps + 1) * R + r) * Npad;
+        const float* dk = spart + ((tt * kW + 1) * R + r) * Npad;
         const float* k = sk + (tt * R + r) * Npad;
         d += dk[u + A] * k[u] - dk[u] * k[u + A];
       }
@@ -831,11 +837,11 @@ __global__ void __launch_bounds__(kBT, 1)
       }
     }
     __syncthreads();
-    for (int i = tid; i < tv * A; i += kBT) {
+    for (int i = tid; i < tv * A; i += BT) {
       const int tt = i / A, u = i - tt * A;
       w.dang_h[(((int64_t)b * L + t0 + tt) * H + h) * A + u] = sdth[tt * AS + u] * scoef[tt * 8 + 4];
     }
-    for (int tt = warp; tt < tv; tt += kWarps) {
+    for (int tt = warp; tt < tv; tt += kW) {
       const int64_t tok = (int64_t)b * L + t0 + tt;
       float s = 0.f;
       for (int u = lane; u < A; u += 32) s = fmaf(sdth[tt * AS + u], a.angle[tok * A + u], s);
@@ -846,7 +852,7 @@ __global__ void __launch_bounds__(kBT, 1)
   }
 #pragma unroll
   for (int j = 0; j < kCb; ++j) {
-    const int idx = tid + kBT * j;
+    const int idx = tid + BT * j;
     if (idx < R * Npad) {
       const int r = idx / Npad, n = idx - r * Npad;
       if (n < N) w.pbb[((int64_t)bh * R + r) * N + n] = bbacc[j];
@@ -854,12 +860,12 @@ __global__ void __launch_bounds__(kBT, 1)
   }
   // mimo_x sums: threads sharing a column, in order
 #pragma unroll
-  for (int r = 0; r < RM; ++r) spart[r * kBT + tid] = mxacc[r];
+  for (int r = 0; r < RM; ++r) spart[r * BT + tid] = mxacc[r];
   __syncthreads();
-  for (int i = tid; i < R * P; i += kBT) {
+  for (int i = tid; i < R * P; i += BT) {
     const int r = i / P, p = i - r * P;
     float s = 0.f;
-    for (int x = p; x < kBT; x += Ppad) s += spart[r * kBT + x];
+    for (int x = p; x < BT; x += Ppad) s += spart[r * BT + x];
     w.pmx[((int64_t)bh * R + r) * P + p] = s;
   }
 }
@@ -997,7 +1003,7 @@ MBwdPlan mbwd_plan(const ScanGeom& g) {
   p.dang_h = take(p.own_ang ? BL * g.H * g.A : 0);
   // the instance's rank bound and tile length (as launch_mimo_backward picks it)
   const int rm = g.R == 1 ? 1 : g.R == 2 ? 2 : g.R <= 4 ? 4 : 8;
-  const int ktm = tokens_per_tile(rm);
+  const int ktm = tokens_per_tile(rm, g.N <= 64 ? 1 : 2);
   p.tiles = (g.L + ktm - 1) / ktm;
   const size_t ppad = g.P <= 32 ? 32 : g.P <= 64 ? 64 : 128, npad = g.N <= 64 ? 64 : 128;
   p.ckpt = take(bh * (size_t)p.tiles * ppad * npad);
@@ -1016,36 +1022,43 @@ MBwdPlan mbwd_plan(const ScanGeom& g) {
   return p;
 }
 
+// RPT: rows per thread of the two sweeps (512 threads, 16 warps: P <= 32 RPT);
+// the query-gradient pass runs 256-thread blocks, two per SM, with 2 RPT rows
+// per thread (the same padded row count, so that the state records match).
+constexpr int kSweepBT = 512;
+
 template <int RPT, int NB, int RM>
 cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
                         const MBwdWs& w, cudaStream_t s) {
-  const MBwdLayout lay = mbwd_layout(g.A, RM, RPT, NB);
-  const MBwdLayout lay_dq = mbwd_layout(g.A, RM, RPT, NB, true);
+  constexpr int kSW = kSweepBT / 32;
+  const MBwdLayout lay = mbwd_layout(g.A, RM, RPT, NB, false, kSW);
+  const MBwdLayout lay_dq = mbwd_layout(g.A, RM, 2 * RPT, NB, true, kWarps);
   const size_t smem = (size_t)lay.floats * sizeof(float);
   const size_t smem_dq = (size_t)lay_dq.floats * sizeof(float);
   static bool attr_set = false;  // per instance: the opt-in above 48 KB, for A up to 64
   if (!attr_set) {
-    const int most = mbwd_layout(64, RM, RPT, NB).floats * (int)sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_mbwd_fwd<RPT, NB, RM, false>,
+    const int most = mbwd_layout(64, RM, RPT, NB, false, kSW).floats * (int)sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_mbwd_fwd<RPT, NB, RM, false, kSweepBT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_mbwd_fwd<RPT, NB, RM, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               mbwd_layout(64, RM, RPT, NB, true).floats * (int)sizeof(float));
+      e = cudaFuncSetAttribute(
+          k_mbwd_fwd<2 * RPT, NB, RM, true, kBT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          mbwd_layout(64, RM, 2 * RPT, NB, true, kWarps).floats * (int)sizeof(float));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_mbwd_rev<RPT, NB, RM>,
+      e = cudaFuncSetAttribute(k_mbwd_rev<RPT, NB, RM, kSweepBT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const unsigned grid = (unsigned)(g.B * g.H);
-  k_mbwd_fwd<RPT, NB, RM, false><<<grid, kBT, smem, s>>>(g, a, w, lay);
+  k_mbwd_fwd<RPT, NB, RM, false, kSweepBT><<<grid, kSweepBT, smem, s>>>(g, a, w, lay);
   const unsigned out_grid = grid * (unsigned)w.out_tb;
   if (g.P <= 32) k_mbwd_out<RM, 1><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
   else if (g.P <= 64) k_mbwd_out<RM, 2><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
   else k_mbwd_out<RM, 4><<<out_grid, kBT, 0, s>>>(g, a, o.g, w);
-  k_mbwd_fwd<RPT, NB, RM, true><<<grid * (unsigned)w.tiles, kBT, smem_dq, s>>>(g, a, w, lay_dq);
-  k_mbwd_rev<RPT, NB, RM><<<grid, kBT, smem, s>>>(g, a, o.g, w, lay);
+  k_mbwd_fwd<2 * RPT, NB, RM, true, kBT><<<grid * (unsigned)w.tiles, kBT, smem_dq, s>>>(g, a, w,
+                                                                                      lay_dq);
+  k_mbwd_rev<RPT, NB, RM, kSweepBT><<<grid, kSweepBT, smem, s>>>(g, a, o.g, w, lay);
   count_launches(4);
   return cudaGetLastError();
 }
@@ -1054,14 +1067,14 @@ template <int RM>
 cudaError_t launch_mbwd_rank(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
                              const MBwdWs& w, cudaStream_t s) {
   // (P N <= 4096 for MIMO, so N > 64 leaves P < 64)
-  const int rpt = g.P <= 32 ? 2 : g.P <= 64 ? 4 : 8;
+  const int rpt = g.P <= 32 ? 1 : g.P <= 64 ? 2 : 4;
   const int nb = g.N <= 64 ? 1 : 2;
   switch (rpt * 10 + nb) {
+    case 11: return launch_mbwd<1, 1, RM>(g, a, o, w, s);
+    case 12: return launch_mbwd<1, 2, RM>(g, a, o, w, s);
     case 21: return launch_mbwd<2, 1, RM>(g, a, o, w, s);
     case 22: return launch_mbwd<2, 2, RM>(g, a, o, w, s);
     case 41: return launch_mbwd<4, 1, RM>(g, a, o, w, s);
-    case 42: return launch_mbwd<4, 2, RM>(g, a, o, w, s);
-    case 81: return launch_mbwd<8, 1, RM>(g, a, o, w, s);
     default: return cudaErrorInvalidValue;
   }
 }
