@@ -13,8 +13,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
                 [--mode fp32|tf32] [--no-parts] [--part NAME]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
 mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
-mimo_step, siso_prefill_tf32, siso_backward_fp32, mimo_backward_fp32) and prints its
-JSON, for profiling it alone.
+mimo_step, siso_prefill_tf32, siso_backward_fp32, siso_long_backward_fp32,
+mimo_backward_fp32) and prints its JSON, for profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -697,6 +697,7 @@ def part_by_name(torch, m3, name, peak):
         "mimo_step": lambda: parts_step(torch, m3, peak, mimo=True),
         "siso_prefill_tf32": lambda: parts_prefill(torch, m3, gen.SISO_1B, peak),
         "siso_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_1B, peak),
+        "siso_long_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_LONG, peak),
         "mimo_backward_fp32": lambda: parts_backward_mimo(torch, m3, gen.MIMO_R4, peak),
     }
     if name not in table:
@@ -840,7 +841,7 @@ def run_m3(args):
         for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "mimo_packed_tf32",
                      "siso_long_scan_fp32",
                      "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32",
-                     "siso_backward_fp32", "mimo_backward_fp32"):
+                     "siso_backward_fp32", "siso_long_backward_fp32", "mimo_backward_fp32"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()
 

@@ -50,10 +50,10 @@ struct BwdLayout {
   int q, k, v, dy, y, part, coef, th, cs, sn, dz, dth, red, floats;
 };
 
-inline BwdLayout bwd_layout(int A, int RPT, int NB) {
+inline BwdLayout bwd_layout(int A, int RPT, int NB, int warps = kWarps) {
   BwdLayout l;
   l.Npad = 64 * NB;
-  l.Ppad = 16 * RPT;
+  l.Ppad = 2 * warps * RPT;
   l.AS = A > 0 ? A : 1;
   int off = 0;
   auto take = [&](int n) {
@@ -66,7 +66,7 @@ inline BwdLayout bwd_layout(int A, int RPT, int NB) {
   l.v = take((kT + 1) * l.Ppad);
   l.dy = take(kT * l.Ppad);
   l.y = take(kT * l.Ppad);
-  l.part = take(kT * kWarps * l.Npad);
+  l.part = take(kT * warps * l.Npad);
   l.coef = take(kT * 8);
   l.th = take(kT * l.AS);
   l.cs = take(kT * l.AS);
@@ -83,7 +83,7 @@ inline BwdLayout bwd_layout(int A, int RPT, int NB) {
 // of the tile's tv tokens from the running angles in sth, writing the cosines
 // and sines to scs / ssn: q = Rot(theta)(C + c_bias), k = Rot(theta)(B + b_bias),
 // split-half pairs (u, u + A) rotated by (u cos - w sin, u sin + w cos).
-template <int NB>
+template <int NB, int BT>
 __device__ __forceinline__ void stage_qk(const ScanGeom& g, const ScanArgs& a, int b, int h,
                                          int grp, int t0, int tv, const BwdLayout& lay,
                                          float* sq, float* sk, int koff, const float* sth,
@@ -91,7 +91,7 @@ __device__ __forceinline__ void stage_qk(const ScanGeom& g, const ScanArgs& a, i
   constexpr int Npad = 64 * NB;
   const int N = g.N, A = g.A;
   // item (tt, u): u < A the pair (u, u + A), 2A <= u < N the plain dim u
-  for (int i = threadIdx.x; i < tv * Npad; i += kBT) {
+  for (int i = threadIdx.x; i < tv * Npad; i += BT) {
     const int tt = i / Npad, u = i - tt * Npad;
     if ((u >= A && u < 2 * A) || u >= N) continue;
     const int64_t row = (((int64_t)b * g.L + t0 + tt) * g.G + grp) * N;
@@ -126,9 +126,10 @@ struct BwdWs {
 
 namespace {
 
-template <int RPT, int NB>
-__global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
+template <int RPT, int NB, int BT>
+__global__ void __launch_bounds__(BT, BT > 256 || RPT >= 8 ? 1 : 2)
     k_bwd_fwd(ScanGeom g, ScanArgs a, BwdArgs o, BwdWs w, BwdLayout lay) {
+  constexpr int kW = BT / 32;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
   float* sk = sm + lay.k;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
   float* sdz = sm + lay.dz;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rq = lane >> 4, cq = lane & 15;
   const int P = g.P, N = g.N, A = g.A, L = g.L, H = g.H;
-  constexpr int Npad = 64 * NB, Ppad = 16 * RPT;
+  constexpr int Npad = 64 * NB, Ppad = 2 * kW * RPT;
   const int AS = lay.AS;
   const int bh = blockIdx.x, b = bh / H, h = bh % H, hpg = H / g.G, grp = h / hpg;
   const int prow0 = warp * 2 * RPT + rq * RPT;
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
 
   // zero tiles: the padding (n >= N, p >= P) and the previous-token slots
   // (zero state) are never written otherwise
-  for (int i = tid; i < lay.part; i += kBT) sm[i] = 0.f;
+  for (int i = tid; i < lay.part; i += BT) sm[i] = 0.f;
   float hs[RPT][4 * NB];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       scoef[tid * 8 + 1] = (1.f - lam) * dtv * al;
       scoef[tid * 8 + 2] = lam * dtv;
     }
-    for (int i = tid; i < tv * Ppad; i += kBT) {
+    for (int i = tid; i < tv * Ppad; i += BT) {
       const int tt = i / Ppad, p = i - tt * Ppad;
       if (p >= P) continue;
       const int64_t e = (((int64_t)b * L + t0 + tt) * H + h) * P + p;
@@ -207,12 +208,12 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     }
     __syncthreads();
     // (2) rotated q_t into sq[tt], k_t into sk[tt + 1] (sk[0]: previous token)
-    stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
+    stage_qk<NB, BT>(g, a, b, h, grp, t0, tv, lay, sq, sk, 1, sth, scs, ssn);
     __syncthreads();
     // (3) the recurrence over the tile's tokens, the next tile's operands
     // prefetched into L2 meanwhile
     if (t0 + kT < L)
-      prefetch_tile(g, a, o.dout, nullptr, bh, b, h, grp, t0 + kT, min(kT, L - t0 - kT));
+      prefetch_tile<BT>(g, a, o.dout, nullptr, bh, b, h, grp, t0 + kT, min(kT, L - t0 - kT));
     for (int tt = 0; tt < tv; ++tt) {
       const float al = scoef[tt * 8], sal = scoef[tt * 8 + 1], gm = scoef[tt * 8 + 2];
       float kp[4 * NB], kc[4 * NB], qv[4 * NB];
@@ -241,33 +242,33 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       int row;
       const float ysum = rows_sum16<RPT>(yv, cq, row);
       if ((cq & (16 / RPT - 1)) == 0) sy[tt * Ppad + prow0 + row] = ysum;
-      cols_sum_store<NB>(dq, rq, cq, spart + (tt * kWarps + warp) * Npad);
+      cols_sum_store<NB>(dq, rq, cq, spart + (tt * kW + warp) * Npad);
     }
     __syncthreads();
     // (4) dq_t: the warps' column sums, into slot 0
-    for (int i = tid; i < tv * Npad; i += kBT) {
+    for (int i = tid; i < tv * Npad; i += BT) {
       const int tt = i / Npad, n = i - tt * Npad;
-      float* pp = spart + tt * kWarps * Npad + n;
+      float* pp = spart + tt * kW * Npad + n;
       float s = pp[0];
 #pragma unroll
-      for (int x = 1; x < kWarps; ++x) s += pp[x * Npad];
+      for (int x = 1; x < kW; ++x) s += pp[x * Npad];
       pp[0] = s;
     }
     __syncthreads();
     // (5a) the head's C gradient Rot(theta)^T dq_t and the c_bias sum
     {
       const int n = tid % Npad;
-      for (int tt = tid / Npad; tt < tv; tt += kBT / Npad) {
+      for (int tt = tid / Npad; tt < tv; tt += BT / Npad) {
         if (n < N) {
-          const float v = unrotate(spart + tt * kWarps * Npad, scs + tt * AS, ssn + tt * AS, n, A);
+          const float v = unrotate(spart + tt * kW * Npad, scs + tt * AS, ssn + tt * AS, n, A);
           w.dc_h[(((int64_t)b * L + t0 + tt) * H + h) * N + n] = v;
           cbacc += v;
         }
       }
     }
     // (5b) Q_t = q_t . dq_t and the query part of theta_t's adjoint
-    for (int tt = warp; tt < tv; tt += kWarps) {
-      const float* dq = spart + tt * kWarps * Npad;
+    for (int tt = warp; tt < tv; tt += kW) {
+      const float* dq = spart + tt * kW * Npad;
       const float* q = sq + tt * Npad;
       float s = 0.f;
       for (int n = lane; n < N; n += 32) s = fmaf(q[n], dq[n], s);
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       for (int u = lane; u < A; u += 32) w.dthq[tix * A + u] = dq[u + A] * q[u] - dq[u] * q[u + A];
     }
     // (5c) dz_t = dout_t (y_t + D x_t) silu'(z_t); the D sum
-    for (int i = tid; i < tv * Ppad; i += kBT) {
+    for (int i = tid; i < tv * Ppad; i += BT) {
       const int tt = i / Ppad, p = i - tt * Ppad;
       if (p >= P) continue;
       const float xv = sv[(tt + 1) * Ppad + p];
@@ -287,31 +288,32 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     }
     // (5d) this tile's last key and value become the next tile's previous token
     if (tv == kT) {
-      for (int n = tid; n < Npad; n += kBT) sk[n] = sk[kT * Npad + n];
-      for (int p = tid; p < Ppad; p += kBT) sv[p] = sv[kT * Ppad + p];
+      for (int n = tid; n < Npad; n += BT) sk[n] = sk[kT * Npad + n];
+      for (int p = tid; p < Ppad; p += BT) sv[p] = sv[kT * Ppad + p];
     }
     __syncthreads();
   }
   // per-(b, h) shares of the c_bias and D sums
   spart[tid] = cbacc;
-  spart[kBT + tid] = dsum;
+  spart[BT + tid] = dsum;
   __syncthreads();
   if (tid < N) {
     float s = 0.f;
-    for (int x = tid; x < kBT; x += Npad) s += spart[x];
+    for (int x = tid; x < BT; x += Npad) s += spart[x];
     w.pcb[(int64_t)bh * N + tid] = s;
   }
   if (warp == 0) {
     float s = 0.f;
-    for (int x = lane; x < kBT; x += 32) s += spart[kBT + x];
+    for (int x = lane; x < BT; x += 32) s += spart[BT + x];
     s = warp_sum(s);
     if (lane == 0) w.pd[bh] = s;
   }
 }
 
-template <int RPT, int NB>
-__global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
+template <int RPT, int NB, int BT>
+__global__ void __launch_bounds__(BT, BT > 256 || RPT >= 8 ? 1 : 2)
     k_bwd_rev(ScanGeom g, ScanArgs a, BwdArgs o, BwdWs w, BwdLayout lay) {
+  constexpr int kW = BT / 32;
   extern __shared__ __align__(16) float sm[];
   float* sq = sm + lay.q;
   float* sk = sm + lay.k;
@@ -327,13 +329,13 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
   float* sred = sm + lay.red;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, rq = lane >> 4, cq = lane & 15;
   const int P = g.P, N = g.N, A = g.A, L = g.L, H = g.H;
-  constexpr int Npad = 64 * NB, Ppad = 16 * RPT;
+  constexpr int Npad = 64 * NB, Ppad = 2 * kW * RPT;
   const int AS = lay.AS;
   const int bh = blockIdx.x, b = bh / H, h = bh % H, hpg = H / g.G, grp = h / hpg;
   const int prow0 = warp * 2 * RPT + rq * RPT;
   const float dskip = g.has_d ? a.d[h] : 0.f;
 
-  for (int i = tid; i < lay.part; i += kBT) sm[i] = 0.f;
+  for (int i = tid; i < lay.part; i += BT) sm[i] = 0.f;
   float lam[RPT][4 * NB];
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       scoef[tid * 8 + 3] = s1;
       scoef[tid * 8 + 4] = dtv;
     }
-    for (int i = tid; i < tv * Ppad; i += kBT) {
+    for (int i = tid; i < tv * Ppad; i += BT) {
       const int tt = i / Ppad, p = i - tt * Ppad;
       if (p >= P) continue;
       const int64_t e = (((int64_t)b * L + t0 + tt) * H + h) * P + p;
@@ -377,18 +379,18 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       }
       sdy[tt * Ppad + p] = dyv;
     }
-    for (int i = tid; i < tv * 64; i += kBT) {
+    for (int i = tid; i < tv * 64; i += BT) {
       const int tt = i >> 6, u = i & 63;
       if (u >= A) continue;
       sth[tt * AS + u] = w.theta[((int64_t)bh * L + t0 + tt) * A + u];
     }
     __syncthreads();
     // (2) rotated q_t into sq[tt], k_t into sk[tt]
-    stage_qk<NB>(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
+    stage_qk<NB, BT>(g, a, b, h, grp, t0, tv, lay, sq, sk, 0, sth, scs, ssn);
     __syncthreads();
     // (3) the adjoint recurrence, last token first, the previous tile's
     // operands prefetched into L2 meanwhile
-    if (t0 > 0) prefetch_tile(g, a, o.dout, w.theta, bh, b, h, grp, t0 - kT, kT);
+    if (t0 > 0) prefetch_tile<BT>(g, a, o.dout, w.theta, bh, b, h, grp, t0 - kT, kT);
     for (int tt = tv - 1; tt >= 0; --tt) {
       const float al1 = scoef[tt * 8];
       float kv[4 * NB], qv[4 * NB];
@@ -415,21 +417,21 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
       int row;
       const float msum = rows_sum16<RPT>(mk, cq, row);
       if ((cq & (16 / RPT - 1)) == 0) smk[tt * Ppad + prow0 + row] = msum;
-      cols_sum_store<NB>(mv, rq, cq, spart + (tt * kWarps + warp) * Npad);
+      cols_sum_store<NB>(mv, rq, cq, spart + (tt * kW + warp) * Npad);
     }
     __syncthreads();
     // (4) M^T v_t: the warps' column sums, into slot 0
-    for (int i = tid; i < tv * Npad; i += kBT) {
+    for (int i = tid; i < tv * Npad; i += BT) {
       const int tt = i / Npad, n = i - tt * Npad;
-      float* pp = spart + tt * kWarps * Npad + n;
+      float* pp = spart + tt * kW * Npad + n;
       float s = pp[0];
 #pragma unroll
-      for (int x = 1; x < kWarps; ++x) s += pp[x * Npad];
+      for (int x = 1; x < kW; ++x) s += pp[x * Npad];
       pp[0] = s;
     }
     __syncthreads();
     // (5) per token: dy . v, q . k, v . M k; dg_t, ds_{t+1} and the d adt term
-    for (int tt = warp; tt < tv; tt += kWarps) {
+    for (int tt = warp; tt < tv; tt += kW) {
       float dyv = 0.f, vmk = 0.f, qk = 0.f;
       for (int p = lane; p < P; p += 32) {
         const float v = sv[tt * Ppad + p];
@@ -455,13 +457,13 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     }
     __syncthreads();
     // (6) dk_t into slot 1; dv_t = dx_t
-    for (int i = tid; i < tv * Npad; i += kBT) {
+    for (int i = tid; i < tv * Npad; i += BT) {
       const int tt = i / Npad, n = i - tt * Npad;
-      spart[(tt * kWarps + 1) * Npad + n] =
-          fmaf(scoef[tt * 8 + 1], spart[tt * kWarps * Npad + n],
+      spart[(tt * kW + 1) * Npad + n] =
+          fmaf(scoef[tt * 8 + 1], spart[tt * kW * Npad + n],
                scoef[tt * 8 + 2] * sred[tt * 8] * sq[tt * Npad + n]);
     }
-    for (int i = tid; i < tv * Ppad; i += kBT) {
+    for (int i = tid; i < tv * Ppad; i += BT) {
       const int tt = i / Ppad, p = i - tt * Ppad;
       if (p >= P) continue;
       const float coef = fmaf(scoef[tt * 8 + 2], sred[tt * 8 + 1], dskip);
@@ -484,19 +486,19 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     // adjoint at each token: the query part plus the key part
     {
       const int n = tid % Npad;
-      for (int tt = tid / Npad; tt < tv; tt += kBT / Npad) {
+      for (int tt = tid / Npad; tt < tv; tt += BT / Npad) {
         if (n < N) {
           const float v =
-              unrotate(spart + (tt * kWarps + 1) * Npad, scs + tt * AS, ssn + tt * AS, n, A);
+              unrotate(spart + (tt * kW + 1) * Npad, scs + tt * AS, ssn + tt * AS, n, A);
           w.db_h[(((int64_t)b * L + t0 + tt) * H + h) * N + n] = v;
           bbacc += v;
         }
       }
     }
-    for (int i = tid; i < tv * 64; i += kBT) {
+    for (int i = tid; i < tv * 64; i += BT) {
       const int tt = i >> 6, u = i & 63;
       if (u >= A) continue;
-      const float* dk = spart + (tt * kWarps + 1) * Npad;
+      const float* dk = spart + (tt * kW + 1) * Npad;
       const float* k = sk + tt * Npad;
       sdth[tt * AS + u] = w.dthq[((int64_t)bh * L + t0 + tt) * A + u] +
                           (dk[u + A] * k[u] - dk[u] * k[u + A]);
@@ -512,12 +514,12 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
     __syncthreads();
     // (10) theta_t = theta_{t-1} + dt_t angle_t: d angle (this head) and the
     // angle part of d dt
-    for (int i = tid; i < tv * 64; i += kBT) {
+    for (int i = tid; i < tv * 64; i += BT) {
       const int tt = i >> 6, u = i & 63;
       if (u >= A) continue;
       w.dang_h[(((int64_t)b * L + t0 + tt) * H + h) * A + u] = sdth[tt * AS + u] * scoef[tt * 8 + 4];
     }
-    for (int tt = warp; tt < tv; tt += kWarps) {
+    for (int tt = warp; tt < tv; tt += kW) {
       const int64_t tok = (int64_t)b * L + t0 + tt;
       float s = 0.f;
       for (int u = lane; u < A; u += 32) s = fmaf(sdth[tt * AS + u], a.angle[tok * A + u], s);
@@ -530,7 +532,7 @@ __global__ void __launch_bounds__(kBT, RPT >= 8 ? 1 : 2)
   __syncthreads();
   if (tid < N) {
     float s = 0.f;
-    for (int x = tid; x < kBT; x += Npad) s += spart[x];
+    for (int x = tid; x < BT; x += Npad) s += spart[x];
     w.pbb[(int64_t)bh * N + tid] = s;
   }
 }
@@ -638,27 +640,38 @@ BwdPlan bwd_plan(const ScanGeom& g) {
   return p;
 }
 
-template <int RPT, int NB>
+template <int RPT, int NB, int BT>
 cudaError_t launch_bwd_sweeps(const ScanGeom& g, const ScanArgs& a, const BwdArgs& o,
                               const BwdWs& w, cudaStream_t s) {
-  const BwdLayout lay = bwd_layout(g.A, RPT, NB);
+  const BwdLayout lay = bwd_layout(g.A, RPT, NB, BT / 32);
   const size_t smem = (size_t)lay.floats * sizeof(float);
   static bool attr_set = false;  // per instance: the opt-in above 48 KB, for A up to 64
   if (!attr_set) {
-    const int most = bwd_layout(64, RPT, NB).floats * (int)sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_fwd<RPT, NB>,
+    const int most = bwd_layout(64, RPT, NB, BT / 32).floats * (int)sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_fwd<RPT, NB, BT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_bwd_rev<RPT, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               most);
+      e = cudaFuncSetAttribute(k_bwd_rev<RPT, NB, BT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const unsigned grid = (unsigned)(g.B * g.H);
-  k_bwd_fwd<RPT, NB><<<grid, kBT, smem, s>>>(g, a, o, w, lay);
-  k_bwd_rev<RPT, NB><<<grid, kBT, smem, s>>>(g, a, o, w, lay);
+  k_bwd_fwd<RPT, NB, BT><<<grid, BT, smem, s>>>(g, a, o, w, lay);
+  k_bwd_rev<RPT, NB, BT><<<grid, BT, smem, s>>>(g, a, o, w, lay);
   count_launches(2);
   return cudaGetLastError();
+}
+
+// SMs of the current device (also the answer when none can be queried).
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
 }
 }  // namespace
 
@@ -683,16 +696,30 @@ cudaError_t launch_siso_backward(const ScanGeom& g, const ScanArgs& a, const Bwd
   w.pcb = f(p.pcb);
   w.pbb = f(p.pbb);
   w.pd = f(p.pd);
-  const int rpt = g.P <= 32 ? 2 : g.P <= 64 ? 4 : 8;
   const int nb = g.N <= 64 ? 1 : 2;
   cudaError_t e;
-  switch (rpt * 10 + nb) {
-    case 21: e = launch_bwd_sweeps<2, 1>(g, a, o, w, s); break;
-    case 22: e = launch_bwd_sweeps<2, 2>(g, a, o, w, s); break;
-    case 41: e = launch_bwd_sweeps<4, 1>(g, a, o, w, s); break;
-    case 42: e = launch_bwd_sweeps<4, 2>(g, a, o, w, s); break;
-    case 81: e = launch_bwd_sweeps<8, 1>(g, a, o, w, s); break;
-    default: e = launch_bwd_sweeps<8, 2>(g, a, o, w, s); break;
+  if ((int64_t)g.B * g.H < device_sms()) {
+    // fewer sequences than SMs: one 512-thread block (16 warps) per sequence
+    const int rpt = g.P <= 32 ? 1 : g.P <= 64 ? 2 : 4;
+    switch (rpt * 10 + nb) {
+      case 11: e = launch_bwd_sweeps<1, 1, 512>(g, a, o, w, s); break;
+      case 12: e = launch_bwd_sweeps<1, 2, 512>(g, a, o, w, s); break;
+      case 21: e = launch_bwd_sweeps<2, 1, 512>(g, a, o, w, s); break;
+      case 22: e = launch_bwd_sweeps<2, 2, 512>(g, a, o, w, s); break;
+      case 41: e = launch_bwd_sweeps<4, 1, 512>(g, a, o, w, s); break;
+      default: e = launch_bwd_sweeps<4, 2, 512>(g, a, o, w, s); break;
+    }
+  } else {
+    // two 256-thread blocks per SM
+    const int rpt = g.P <= 32 ? 2 : g.P <= 64 ? 4 : 8;
+    switch (rpt * 10 + nb) {
+      case 21: e = launch_bwd_sweeps<2, 1, kBT>(g, a, o, w, s); break;
+      case 22: e = launch_bwd_sweeps<2, 2, kBT>(g, a, o, w, s); break;
+      case 41: e = launch_bwd_sweeps<4, 1, kBT>(g, a, o, w, s); break;
+      case 42: e = launch_bwd_sweeps<4, 2, kBT>(g, a, o, w, s); break;
+      case 81: e = launch_bwd_sweeps<8, 1, kBT>(g, a, o, w, s); break;
+      default: e = launch_bwd_sweeps<8, 2, kBT>(g, a, o, w, s); break;
+    }
   }
   if (e != cudaSuccess) return e;
   const int64_t most = std::max<int64_t>({(int64_t)g.B * g.L * g.H, (int64_t)g.B * g.L * g.G * g.N,
