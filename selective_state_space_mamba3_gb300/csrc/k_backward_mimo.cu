@@ -434,6 +434,14 @@ __global__ void __launch_bounds__(kBT) k_mbwd_out(ScanGeom g, ScanArgs a, BwdArg
   for (int t = tb * per + warp; t < t_end; t += kWarps) {
     const int64_t e0 = (((int64_t)b * L + t) * H + h) * P;
     float* yd = w.yd + ((int64_t)bh * L + t) * R * P;
+    // this warp's next token into L2 while this one is formed
+    if (t + kWarps < t_end && lane < 4) {
+      const int64_t e1 = e0 + (int64_t)kWarps * H * P;
+      if (lane == 0) prefetch_range(yd + (int64_t)kWarps * R * P, R * P * 4);
+      else if (lane == 1) prefetch_range(a.x + e1, P * 4);
+      else if (lane == 2) prefetch_range(o.dout + e1, P * 4);
+      else if (g.has_z) prefetch_range(a.z + e1, P * 4);
+    }
     float y[kJ][RM], gate[kJ][RM], dgate[kJ][RM], zv[kJ], go[kJ], ov[kJ];
     float ms = 0.f, cdot = 0.f;
 #pragma unroll
