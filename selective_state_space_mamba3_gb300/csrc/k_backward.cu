@@ -645,8 +645,7 @@ cudaError_t launch_bwd_sweeps(const ScanGeom& g, const ScanArgs& a, const BwdArg
                               const BwdWs& w, cudaStream_t s) {
   const BwdLayout lay = bwd_layout(g.A, RPT, NB, BT / 32);
   const size_t smem = (size_t)lay.floats * sizeof(float);
-  static bool attr_set = false;  // per instance: the opt-in above 48 KB, for A up to 64
-  if (!attr_set) {
+  {  // the opt-in above 48 KB, for A up to 64 (set on every call: it is per device)
     const int most = bwd_layout(64, RPT, NB, BT / 32).floats * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_bwd_fwd<RPT, NB, BT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
@@ -654,7 +653,6 @@ cudaError_t launch_bwd_sweeps(const ScanGeom& g, const ScanArgs& a, const BwdArg
       e = cudaFuncSetAttribute(k_bwd_rev<RPT, NB, BT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const unsigned grid = (unsigned)(g.B * g.H);
   k_bwd_fwd<RPT, NB, BT><<<grid, BT, smem, s>>>(g, a, o, w, lay);

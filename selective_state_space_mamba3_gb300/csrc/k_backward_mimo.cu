@@ -1043,8 +1043,7 @@ cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
   const MBwdLayout lay_dq = mbwd_layout(g.A, RM, 2 * RPT, NB, true, kWarps);
   const size_t smem = (size_t)lay.floats * sizeof(float);
   const size_t smem_dq = (size_t)lay_dq.floats * sizeof(float);
-  static bool attr_set = false;  // per instance: the opt-in above 48 KB, for A up to 64
-  if (!attr_set) {
+  {  // the opt-in above 48 KB, for A up to 64 (set on every call: it is per device)
     const int most = mbwd_layout(64, RM, RPT, NB, false, kSW).floats * (int)sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_mbwd_fwd<RPT, NB, RM, false, kSweepBT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, most);
@@ -1056,7 +1055,6 @@ cudaError_t launch_mbwd(const ScanGeom& g, const ScanArgs& a, const MBwdArgs& o,
       e = cudaFuncSetAttribute(k_mbwd_rev<RPT, NB, RM, kSweepBT>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const unsigned grid = (unsigned)(g.B * g.H);
   k_mbwd_fwd<RPT, NB, RM, false, kSweepBT><<<grid, kSweepBT, smem, s>>>(g, a, w, lay);
