@@ -232,3 +232,50 @@ def test_mimo_packed_entry_checks_rank(lib):
         m3.M3_ERR_INVALID_ARGUMENT
     assert call(siso_cfg(mimo_rank=9), ctypes.byref(pc)) == m3.M3_ERR_INVALID_ARGUMENT
     assert call(cfg, ctypes.byref(pc), ptr=None) == m3.M3_ERR_INVALID_ARGUMENT
+
+
+def test_backward_entries_check_before_launch(lib):
+    """m3_siso_backward / m3_mimo_backward: the geometry rules of the forward
+    calls, a workspace of the queried size (never 0 bytes), and non-NULL,
+    16-byte-aligned pointers, all checked on the host (the fake pointers are
+    never dereferenced)."""
+    n = ctypes.c_size_t(0)
+    good = siso_cfg()
+    assert lib.m3_siso_backward_workspace(ctypes.byref(good), ctypes.byref(n)) == m3.M3_OK
+    need = n.value
+    assert need > 0
+    for bad in (siso_cfg(mimo_rank=2), siso_cfg(has_output_norm=1), siso_cfg(head_dim=129),
+                siso_cfg(num_heads=3, num_groups=2)):
+        assert lib.m3_siso_backward_workspace(ctypes.byref(bad), ctypes.byref(n)) == \
+            m3.M3_ERR_INVALID_ARGUMENT
+    args = [FAKE] * 23  # grad_out, the 11 operands, the 11 gradients
+    assert lib.m3_siso_backward(ctypes.byref(good), *args, None, 0, None) == m3.M3_ERR_WORKSPACE
+    assert lib.m3_siso_backward(ctypes.byref(good), *args, FAKE, need - 1, None) == \
+        m3.M3_ERR_WORKSPACE
+    assert lib.m3_siso_backward(ctypes.byref(good), *args, FAKE_ODD, need, None) == \
+        m3.M3_ERR_UNALIGNED
+    for i in range(23):
+        if i in (8, 19):  # angle and grad_angle may be NULL only when A == 0
+            continue
+        a = list(args)
+        a[i] = None
+        assert lib.m3_siso_backward(ctypes.byref(good), *a, FAKE, need, None) == \
+            m3.M3_ERR_INVALID_ARGUMENT, i
+        a[i] = FAKE_ODD
+        assert lib.m3_siso_backward(ctypes.byref(good), *a, FAKE, need, None) == \
+            m3.M3_ERR_UNALIGNED, i
+    a = list(args)
+    a[8] = None  # angle with A > 0
+    assert lib.m3_siso_backward(ctypes.byref(good), *a, FAKE, need, None) == \
+        m3.M3_ERR_INVALID_ARGUMENT
+    mimo = siso_cfg(mimo_rank=4, has_output_norm=1, head_dim=16, state_size=32)
+    assert lib.m3_mimo_backward_workspace(ctypes.byref(mimo), ctypes.byref(n)) == m3.M3_OK
+    assert n.value > 0
+    for bad in (siso_cfg(mimo_rank=9), siso_cfg(mimo_rank=4, head_dim=128, state_size=64)):
+        assert lib.m3_mimo_backward_workspace(ctypes.byref(bad), ctypes.byref(n)) == \
+            m3.M3_ERR_INVALID_ARGUMENT
+    margs = [FAKE] * 31  # grad_out, the 15 operands, the 15 gradients
+    assert lib.m3_mimo_backward(ctypes.byref(mimo), *margs, None, 0, None) == m3.M3_ERR_WORKSPACE
+    margs[15] = None  # norm_weight
+    assert lib.m3_mimo_backward(ctypes.byref(mimo), *margs, FAKE, 1 << 40, None) == \
+        m3.M3_ERR_INVALID_ARGUMENT
