@@ -4,12 +4,12 @@ eleven adjoints of `SsmBackward`) against the oracle's reverse-mode adjoints
 oracle), on the same seeded inputs and output gradient.
 
 Bar: the FP32 bar of the forward, 1e-5 normwise (max|gpu - oracle| / max|oracle|
-per gradient), for all eleven gradients. A gradient that vanishes in exact
-arithmetic (with one token, the angle adjoint: q_t . k_t does not depend on
-theta_t; with one token from a zero state, d adt as well) is compared
-against a floor of 1e-2 times the call's largest per-token gradient instead
-of its own rounding residue: the kernels form it as a difference of terms of
-that size, whose rounding is absolute. Outputs start as NaN, so an
+per gradient), for all eleven gradients. The two gradients that vanish in
+exact arithmetic with a single token from a zero state (the angle adjoint:
+q_t . k_t does not depend on theta_t; d adt: the state then holds no decayed
+term) are compared against a floor of 1e-2 times the call's largest
+per-token gradient instead of their own rounding residue: the kernels form
+them as differences of terms of that size, whose rounding is absolute. Outputs start as NaN, so an
 element the kernels never write fails the comparison.
 """
 import numpy as np
@@ -81,13 +81,18 @@ def gpu_backward(cfg, ins, dout, calls=1):
 PER_TOKEN = ("c", "b", "x", "z", "adt", "dt", "trap")
 
 
+# gradients that vanish in exact arithmetic when every sequence has one token
+VANISH_AT_L1 = ("adt", "angle")
+
+
 def compare(got, ref, label, tol=BWD_TOL):
     floor = 1e-2 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
+    one_token = ref["x"].shape[1] == 1
     for k in KEYS:
         if ref[k].size == 0:
             continue
         assert np.all(np.isfinite(got[k])), f"{label} {k}: unwritten or non-finite elements"
-        if np.max(np.abs(ref[k])) < floor:
+        if one_token and k in VANISH_AT_L1:
             err = float(np.max(np.abs(got[k].astype(np.float64) - ref[k]))) / floor
             assert err <= tol, (label, k, "against the floor", err)
         else:
@@ -227,11 +232,12 @@ def gpu_mimo_backward(cfg, ins, dout, calls=1):
 
 def mimo_compare(got, ref, label, tol=BWD_TOL):
     floor = 1e-2 * max(float(np.max(np.abs(ref[k]))) for k in PER_TOKEN)
+    one_token = ref["x"].shape[1] == 1
     for k in MKEYS:
         if ref[k].size == 0:
             continue
         assert np.all(np.isfinite(got[k])), f"{label} {k}: unwritten or non-finite elements"
-        if np.max(np.abs(ref[k])) < floor:
+        if one_token and k in VANISH_AT_L1:
             err = float(np.max(np.abs(got[k].astype(np.float64) - ref[k]))) / floor
             assert err <= tol, (label, k, "against the floor", err)
         else:
@@ -279,3 +285,13 @@ def test_mimo_backward_r4_workload():
     got = gpu_mimo_backward(cfg, ins, dout)
     ref = oracle.mimo_backward(cfg, dout, *[ins[k] for k in MKEYS])
     mimo_compare(got, ref, "mimo r4 workload")
+
+
+def test_siso_backward_long_context_heads():
+    """The long-context head shape (G4 P64 N128 A64) over 4,096 tokens of 8
+    heads: one 512-thread sweep block per sequence (fewer sequences than SMs),
+    256 tiles carried in order, every gradient against the oracle."""
+    cfg, ins, dout = case(B=1, L=4096, H=8, G=4, P=64, N=128, A=64, seed=73)
+    got = gpu_backward(cfg, ins, dout)
+    ref = oracle.siso_backward(cfg, dout, *[ins[k] for k in KEYS], threads=8)
+    compare(got, ref, "long-context heads")
