@@ -11,7 +11,9 @@ the source pages are silent are listed at the top of `m3_oracle.cpp`.
 
 Pinned functions (see tests/test_oracle_pins.py): preprocess, SISO scan, SISO
 step (as the scan with explicit state), MIMO scan, MIMO step; SISO and MIMO
-adjoints (tests/test_oracle_backward_pins.py: central differences of the scans).
+adjoints (tests/test_oracle_backward_pins.py: central differences of the scans);
+the preprocess adjoint (tests/test_oracle_preprocess_backward_pins.py: central
+differences of the preprocess, the RMS norm's scale invariance, the clamps).
 """
 from __future__ import annotations
 
@@ -50,6 +52,9 @@ def _load():
             lib = ctypes.CDLL(build())
             lib.m3o_preprocess.restype = ctypes.c_int
             lib.m3o_preprocess.argtypes = [_i64] * 7 + [_f64] * 4 + [_ptr] * 10 + [ctypes.c_int]
+            lib.m3o_preprocess_backward.restype = ctypes.c_int
+            lib.m3o_preprocess_backward.argtypes = ([_i64] * 7 + [_f64] * 4 + [_ptr] * 12 +
+                                                    [ctypes.c_int])
             lib.m3o_scan.restype = ctypes.c_int
             lib.m3o_scan.argtypes = [_i64] * 8 + [ctypes.c_int] * 3 + [_ptr] * 20 + [ctypes.c_int]
             lib.m3o_siso_backward.restype = ctypes.c_int
@@ -94,6 +99,32 @@ def preprocess(projected, dt_bias, *, inner_size, state_size, num_heads, num_rop
     if st != 0:
         raise ValueError("oracle preprocess: invalid geometry")
     return outs
+
+
+PRE_GRAD_NAMES = ("x", "z", "bh", "ch", "dt", "adt", "trap", "angle")
+
+
+def preprocess_backward(projected, dt_bias, grads, *, inner_size, state_size, num_heads,
+                        num_rope_angles, num_groups, mimo_rank, epsilon, dt_min, dt_max, a_floor,
+                        threads=None):
+    """Adjoint of the fused projection preprocess. grads: dict of the eight
+    output gradients (PRE_GRAD_NAMES, the shapes `preprocess` returns, read as
+    float32). Returns dict of float64 arrays projected [rows, W], dt_bias [H]."""
+    projected = _f32(projected)
+    dt_bias = _f32(dt_bias)
+    rows, W = projected.shape
+    I, N, H, A, G, R = inner_size, state_size, num_heads, num_rope_angles, num_groups, mimo_rank
+    g = {k: _f32(grads[k]) for k in PRE_GRAD_NAMES}
+    out = dict(projected=np.zeros((rows, W)), dt_bias=np.zeros((H,)))
+    st = _load().m3o_preprocess_backward(rows, I, N, H, A, G, R, float(np.float32(epsilon)),
+                                         float(np.float32(dt_min)), float(np.float32(dt_max)),
+                                         float(np.float32(a_floor)), _p(projected), _p(dt_bias),
+                                         *[_p(g[k]) for k in PRE_GRAD_NAMES],
+                                         _p(out["projected"]), _p(out["dt_bias"]),
+                                         threads or default_threads())
+    if st != 0:
+        raise ValueError("oracle preprocess_backward: invalid geometry")
+    return out
 
 
 def scan(cfg, c, b, x, z, adt, dt, trap, angle, c_bias, b_bias, d, mimo_x=None, mimo_z=None,

@@ -145,6 +145,88 @@ int m3o_preprocess(i64 rows, i64 inner, i64 N, i64 H, i64 A, i64 G, i64 R, doubl
 }
 
 // ---------------------------------------------------------------------------
+// Adjoint of the fused projection preprocess. Follows
+// `Mamba3PreprocessBackward` / `mamba3_preprocess_backward` of mamba3.rs: from
+// the projection, dt_bias and the gradients of the eight preprocess outputs
+// (x, z, bh, ch, dt, adt, trap, angle, the order of
+// `Mamba3PreprocessResult::matrices`), the gradient of the packed projection
+// [rows, W] and of dt_bias [H]. The pages give only the kernel's bindings
+// (projection, dt_bias and the eight output gradients in; the projection
+// gradient and per-(row, head) dt_bias partials out, the partials summed over
+// rows by a second kernel), so each step below is the chain rule applied to
+// m3o_preprocess above:
+//   z, x, trap, angle columns: the output gradient itself (identity slices);
+//   B / C row u (N values) -> y = u s, s = 1 / sqrt(mean(u^2) + eps):
+//     du_n = s g_n - s^3 u_n (sum_m g_m u_m) / N;
+//   dt = clamp(softplus(dt_raw + dt_bias), dt_min, dt_max),
+//   adt = -a_mag dt with a_mag = max(softplus(a_raw), a_floor):
+//     ddt_total = g_dt - a_mag g_adt;
+//     d dt_raw = ddt_total * sigmoid(dt_raw + dt_bias)   while the clamp passes;
+//     d a_raw  = -dt g_adt * sigmoid(a_raw)               while the floor passes;
+//   d dt_bias[h] = sum over rows of d dt_raw[row, h].
+// READING (bounds): the clamp passes the gradient for dt_min <= softplus <=
+// dt_max, the floor for softplus(a_raw) >= a_floor (bounds inclusive, as the
+// forward's "inclusive" dt bounds; at an exact tie the forward value is the
+// same on both sides, so either derivative is a valid one-sided choice).
+// Returns 0, or 1 for an invalid geometry.
+int m3o_preprocess_backward(i64 rows, i64 inner, i64 N, i64 H, i64 A, i64 G, i64 R, double eps,
+                            double dt_min, double dt_max, double a_floor, const float* projected,
+                            const float* dt_bias, const float* gx, const float* gz,
+                            const float* gbh, const float* gch, const float* gdt,
+                            const float* gadt, const float* gtrap, const float* gangle,
+                            double* gproj, double* gdt_bias, int threads) {
+  if (rows <= 0 || inner <= 0 || N <= 0 || H <= 0 || G <= 0 || R <= 0 || 2 * A > N) return 1;
+  const i64 bc = G * R * N;
+  const i64 W = 2 * inner + 2 * bc + 3 * H + A;
+  const i64 o_b = 2 * inner, o_c = o_b + bc, o_s = o_c + bc;
+  parallel_for(rows, threads, [&](i64 r) {
+    const float* p = projected + r * W;
+    double* gp = gproj + r * W;
+    for (i64 i = 0; i < inner; ++i) {
+      gp[i] = gz[r * inner + i];
+      gp[inner + i] = gx[r * inner + i];
+    }
+    for (int which = 0; which < 2; ++which) {
+      const float* src = p + (which == 0 ? o_b : o_c);
+      const float* g = (which == 0 ? gbh : gch) + r * bc;
+      double* dst = gp + (which == 0 ? o_b : o_c);
+      for (i64 j = 0; j < G * R; ++j) {
+        double ms = 0.0, gu = 0.0;
+        for (i64 n = 0; n < N; ++n) {
+          const double u = src[j * N + n];
+          ms += u * u;
+          gu += (double)g[j * N + n] * u;
+        }
+        ms /= (double)N;
+        const double s = 1.0 / std::sqrt(ms + eps);
+        for (i64 n = 0; n < N; ++n)
+          dst[j * N + n] = s * (double)g[j * N + n] - s * s * s * (double)src[j * N + n] * gu / (double)N;
+      }
+    }
+    for (i64 h = 0; h < H; ++h) {
+      const double raw = (double)p[o_s + h] + (double)dt_bias[h];
+      const double sp = softplus(raw);
+      const double dt = std::min(std::max(sp, dt_min), dt_max);
+      const double sa = softplus((double)p[o_s + H + h]);
+      const double a_mag = std::max(sa, a_floor);
+      const double g_dt = (double)gdt[r * H + h], g_adt = (double)gadt[r * H + h];
+      const bool dt_pass = sp >= dt_min && sp <= dt_max;
+      const bool a_pass = sa >= a_floor;
+      gp[o_s + h] = dt_pass ? (g_dt - a_mag * g_adt) * sigmoid(raw) : 0.0;
+      gp[o_s + H + h] = a_pass ? -dt * g_adt * sigmoid((double)p[o_s + H + h]) : 0.0;
+      gp[o_s + 2 * H + h] = gtrap[r * H + h];
+    }
+    for (i64 a = 0; a < A; ++a) gp[o_s + 3 * H + a] = gangle[r * A + a];
+  });
+  for (i64 h = 0; h < H; ++h) {
+    double s = 0.0;
+    for (i64 r = 0; r < rows; ++r) s += gproj[r * W + o_s + h];
+    gdt_bias[h] = s;
+  }
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
 // SISO / MIMO selective-state recurrence, token by token.
 //
 // Follows `mamba3_siso` / `mamba3_mimo` (operand layouts C/B [B,L,R*G,N],
