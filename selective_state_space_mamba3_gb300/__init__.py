@@ -4,8 +4,9 @@ The product is the C-ABI library `libm3.so` (declared in include/m3.h):
 m3_preprocess, m3_siso_forward, m3_mimo_forward, m3_siso_step, m3_mimo_step,
 m3_siso_backward, m3_mimo_backward.
 This package holds its CUDA sources (`csrc/`), the in-tree build (`build.py`),
-a ctypes binding with the same entry-point names (`_binding.py`) and the
-seeded synthetic input generators (`inputs.py`).
+a ctypes binding with the same entry-point names (`_binding.py`), torch.autograd
+bindings that pair each scan with its adjoints (`autograd.py`) and the seeded
+synthetic input generators (`inputs.py`).
 """
 from ._binding import (  # noqa: F401
     M3_OK, M3_ERR_INVALID_ARGUMENT, M3_ERR_UNALIGNED, M3_ERR_WORKSPACE, M3_ERR_CUDA,

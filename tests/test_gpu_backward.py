@@ -295,3 +295,32 @@ def test_siso_backward_long_context_heads():
     got = gpu_backward(cfg, ins, dout)
     ref = oracle.siso_backward(cfg, dout, *[ins[k] for k in KEYS], threads=8)
     compare(got, ref, "long-context heads")
+
+
+@pytest.mark.parametrize("mimo", [False, True], ids=["siso", "mimo"])
+def test_autograd_binding(mimo):
+    """selective_state_space_mamba3_gb300.autograd: loss = sum(out * W) through
+    torch.autograd; the .grad of every operand equals the oracle's adjoints for
+    grad_out = W, and the forward equals the oracle's scan."""
+    import torch
+    from selective_state_space_mamba3_gb300 import autograd as m3ag
+    if mimo:
+        cfg, ins, dout = mimo_case(B=1, L=40, H=2, G=1, P=32, N=32, A=8, R=2, norm=1)
+        keys = MKEYS
+    else:
+        cfg, ins, dout = case(B=2, L=50, H=4, G=2, P=16, N=32, A=8)
+        keys = KEYS
+    t = {k: dev(ins[k]).requires_grad_(True) for k in keys}
+    fn = m3ag.mimo_scan if mimo else m3ag.siso_scan
+    out = fn(cfg, *[t[k] for k in keys])
+    (out * dev(dout)).sum().backward()
+    torch.cuda.synchronize()
+    if mimo:
+        ref = oracle.mimo_backward(cfg, dout, *[ins[k] for k in keys])
+        ref_out = oracle.scan(cfg, *[ins[k] for k in KEYS], **{k: ins[k] for k in MKEYS[11:]})
+    else:
+        ref = oracle.siso_backward(cfg, dout, *[ins[k] for k in keys])
+        ref_out = oracle.scan(cfg, *[ins[k] for k in KEYS])
+    check_close(out.detach().cpu().numpy(), ref_out, BWD_TOL, "autograd forward")
+    for k in keys:
+        check_close(t[k].grad.cpu().numpy(), ref[k], BWD_TOL, f"autograd grad {k}")
