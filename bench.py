@@ -14,7 +14,7 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
 mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
 mimo_step, siso_prefill_tf32, siso_backward_fp32, siso_long_backward_fp32,
-mimo_backward_fp32) and prints its JSON, for profiling it alone.
+mimo_backward_fp32, preprocess_backward) and prints its JSON, for profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -64,6 +64,18 @@ def bytes_per_row_preprocess(w):
     width = gen.packed_width(w.num_heads * w.head_dim, w.state_size, w.num_heads,
                              w.num_rope_angles, G, w.mimo_rank)
     return 4 * 2 * width
+
+
+def bytes_per_row_preprocess_backward(w):
+    """Algorithmic bytes of one row of the preprocess adjoint: the eight output
+    gradients read (W floats in all), the B / C rows and the dt / a columns of
+    the packed row read (2 G R N + 2 H floats; the other columns' gradients do
+    not depend on the projection), and the projection gradient row written
+    (W floats). The dt_bias sums (H floats per row, re-read) are not counted."""
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    width = gen.packed_width(w.num_heads * w.head_dim, w.state_size, w.num_heads,
+                             w.num_rope_angles, G, w.mimo_rank)
+    return 4 * (2 * width + 2 * G * w.mimo_rank * w.state_size + 2 * w.num_heads)
 
 
 def bytes_per_step_call(w):
@@ -684,6 +696,39 @@ def parts_backward_mimo(torch, m3, w, peak):
             "flops": w.tokens * flops_per_token_backward_mimo(w)}
 
 
+def parts_preprocess_backward(torch, m3, w, peak):
+    """Supplementary: m3_preprocess_backward (the adjoint of the projection
+    preprocess: the packed projection and dt_bias gradients) at workload w's
+    layer shape, device-resident inputs; HBM-bound streaming."""
+    p = gen.layer_projection(w)
+    G = w.num_heads if w.num_groups == 0 else w.num_groups
+    kw = dict(inner_size=w.num_heads * w.head_dim, state_size=w.state_size,
+              num_heads=w.num_heads, num_rope_angles=w.num_rope_angles, num_groups=G,
+              mimo_rank=w.mimo_rank, **gen.PRE_DEFAULT)
+    rows = p["projected"].shape[0]
+    I, bc, H, A = kw["inner_size"], G * w.mimo_rank * w.state_size, w.num_heads, w.num_rope_angles
+    shapes = dict(x=(rows, I), z=(rows, I), bh=(rows, bc), ch=(rows, bc), dt=(rows, H),
+                  adt=(rows, H), trap=(rows, H), angle=(rows, A))
+    gr = {k: torch.from_numpy(v).cuda() for k, v in gen.preprocess_output_gradient(w, shapes).items()}
+    proj = torch.from_numpy(p["projected"]).cuda()
+    dtb = torch.from_numpy(p["dt_bias"]).cuda()
+    del p
+    cfg = m3.preprocess_config(**kw)
+    gp = torch.empty_like(proj)
+    gb = torch.empty_like(dtb)
+    ws = torch.empty(max(m3.m3_preprocess_backward_workspace(cfg, rows), 16), dtype=torch.uint8,
+                     device="cuda")
+    fn = lambda: m3.m3_preprocess_backward(cfg, rows, proj, dtb, *[gr[k] for k in gen.PRE_OUTPUTS],
+                                           gp, gb, ws)
+    for _ in range(3):
+        fn()
+    ms = time_events(torch, fn, 5)
+    nbytes = rows * bytes_per_row_preprocess_backward(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name + " (layer rows)", "rows": rows, "ms": round(ms, 4),
+            "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4), "algorithmic_bytes": nbytes}
+
+
 def part_by_name(torch, m3, name, peak):
     """One supplementary part, by its key in the JSON line's `parts`."""
     table = {
@@ -699,6 +744,7 @@ def part_by_name(torch, m3, name, peak):
         "siso_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_1B, peak),
         "siso_long_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_LONG, peak),
         "mimo_backward_fp32": lambda: parts_backward_mimo(torch, m3, gen.MIMO_R4, peak),
+        "preprocess_backward": lambda: parts_preprocess_backward(torch, m3, gen.SISO_1B, peak),
     }
     if name not in table:
         raise SystemExit(f"bench.py: unknown part {name!r}; one of {sorted(table)}")
@@ -841,7 +887,8 @@ def run_m3(args):
         for name in ("siso_scan_fp32", "mimo_scan_fp32", "mimo_scan_tf32", "mimo_packed_tf32",
                      "siso_long_scan_fp32",
                      "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32",
-                     "siso_backward_fp32", "siso_long_backward_fp32", "mimo_backward_fp32"):
+                     "siso_backward_fp32", "siso_long_backward_fp32", "mimo_backward_fp32",
+                     "preprocess_backward"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()
 

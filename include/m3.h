@@ -4,6 +4,7 @@
  * Operations follow oarust 0.8.6 `src/rs/ml/matrix/mamba3.rs` (docs.rs source
  * view) and the `oa::ml::matrix` API reference:
  *   m3_preprocess     - `mamba3_preprocess`   (fused split + B/C RMS + dt/adt)
+ *   m3_preprocess_backward - `mamba3_preprocess_backward` (its adjoint)
  *   m3_siso_forward   - `mamba3_siso`         (SISO selective-state recurrence)
  *   m3_mimo_forward   - `mamba3_mimo`         (shared-state MIMO recurrence)
  *   m3_siso_step      - `mamba3_siso_step`    (one token, explicit state)
@@ -110,6 +111,37 @@ typedef struct {
 int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
                   const float* dt_bias, float* x, float* z, float* bh, float* ch, float* dt,
                   float* adt, float* trap, float* angle, m3_stream_t stream);
+
+/*
+ * m3_preprocess_backward - the adjoint of m3_preprocess
+ * (`mamba3_preprocess_backward`, `Mamba3PreprocessBackward`): the gradients of
+ * the packed projection and of dt_bias from those of the eight outputs.
+ *
+ * projected [rows, W] and dt_bias [H] as given to m3_preprocess; grad_x,
+ * grad_z [rows, I]; grad_bh, grad_ch [rows, G*R*N]; grad_dt, grad_adt,
+ * grad_trap [rows, H]; grad_angle [rows, A] (may be NULL when A == 0).
+ * Outputs: grad_projected [rows, W], every column written:
+ *   z, x, trap, angle columns = their output gradients;
+ *   each B / C N-row u with output gradient g: s g - s^3 u (sum g u) / N,
+ *     s = 1 / sqrt(mean u^2 + epsilon);
+ *   dt_raw column = (grad_dt - a_mag grad_adt) sigmoid(dt_raw + dt_bias) while
+ *     dt_min <= softplus(dt_raw + dt_bias) <= dt_max, else 0;
+ *   a_raw column = -dt grad_adt sigmoid(a_raw) while softplus(a_raw) >= a_floor,
+ *     else 0 (a_mag, dt as m3_preprocess computes them);
+ * grad_dt_bias [H] = the dt_raw column summed over rows, in a fixed order that
+ * depends on rows alone (the result is bit-identical from call to call).
+ * Checks: as m3_preprocess, plus a workspace of at least
+ * m3_preprocess_backward_workspace() bytes (16-byte aligned, device scratch
+ * used only during the call's kernels; M3_ERR_WORKSPACE when missing or small).
+ */
+int m3_preprocess_backward_workspace(const m3_preprocess_config* cfg, int64_t rows,
+                                     size_t* bytes);
+int m3_preprocess_backward(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
+                           const float* dt_bias, const float* grad_x, const float* grad_z,
+                           const float* grad_bh, const float* grad_ch, const float* grad_dt,
+                           const float* grad_adt, const float* grad_trap,
+                           const float* grad_angle, float* grad_projected, float* grad_dt_bias,
+                           void* workspace, size_t workspace_bytes, m3_stream_t stream);
 
 /*
  * m3_siso_forward - the Mamba-3 SISO selective-state recurrence over a whole

@@ -2,7 +2,7 @@
 
 The product is the C-ABI library `libm3.so` (declared in include/m3.h):
 m3_preprocess, m3_siso_forward, m3_mimo_forward, m3_siso_step, m3_mimo_step,
-m3_siso_backward, m3_mimo_backward.
+m3_siso_backward, m3_mimo_backward, m3_preprocess_backward.
 This package holds its CUDA sources (`csrc/`), the in-tree build (`build.py`),
 a ctypes binding with the same entry-point names (`_binding.py`), torch.autograd
 bindings that pair each scan with its adjoints (`autograd.py`) and the seeded
@@ -19,5 +19,5 @@ from ._binding import (  # noqa: F401
     m3_siso_step, m3_mimo_step, m3_workspace_status, LIB_PATH, m3_siso_prefill_workspace,
     m3_mimo_prefill_workspace, m3_siso_prefill, m3_mimo_prefill, m3_selftest_wait_timeout,
     m3_siso_backward_workspace, m3_siso_backward, m3_mimo_backward_workspace,
-    m3_mimo_backward)
+    m3_mimo_backward, m3_preprocess_backward_workspace, m3_preprocess_backward)
 from . import inputs  # noqa: F401

@@ -25,7 +25,8 @@ M3_ERR_DEVICE_STATE = 6
 M3_MATH_FP32 = 0
 M3_MATH_TF32 = 1
 
-EXPORTED = ("m3_preprocess", "m3_siso_forward_workspace", "m3_siso_forward",
+EXPORTED = ("m3_preprocess", "m3_preprocess_backward_workspace", "m3_preprocess_backward",
+            "m3_siso_forward_workspace", "m3_siso_forward",
             "m3_siso_forward_static", "m3_siso_forward_static_status",
             "m3_siso_forward_packed_workspace", "m3_siso_forward_packed",
             "m3_mimo_forward_packed_workspace", "m3_mimo_forward_packed", "m3_siso_prefill_workspace", "m3_siso_prefill",
@@ -92,6 +93,11 @@ def load_library():
         lib = ctypes.CDLL(LIB_PATH)
         cfgp = ctypes.POINTER(SsmConfig)
         lib.m3_preprocess.argtypes = [ctypes.POINTER(PreprocessConfig), ctypes.c_int64] + [_vp] * 11
+        lib.m3_preprocess_backward_workspace.argtypes = [ctypes.POINTER(PreprocessConfig),
+                                                         ctypes.c_int64,
+                                                         ctypes.POINTER(ctypes.c_size_t)]
+        lib.m3_preprocess_backward.argtypes = ([ctypes.POINTER(PreprocessConfig), ctypes.c_int64] +
+                                               [_vp] * 13 + [ctypes.c_size_t, _vp])
         lib.m3_siso_forward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_mimo_forward_workspace.argtypes = [cfgp, ctypes.POINTER(ctypes.c_size_t)]
         lib.m3_siso_forward.argtypes = [cfgp] + [_vp] * 13 + [ctypes.c_size_t, _vp]
@@ -162,6 +168,24 @@ def m3_preprocess(cfg: PreprocessConfig, rows, projected, dt_bias, x, z, bh, ch,
     lib = load_library()
     _check(lib.m3_preprocess(ctypes.byref(cfg), int(rows), *[_ptr(t) for t in (
         projected, dt_bias, x, z, bh, ch, dt, adt, trap, angle)], _stream(stream)), "m3_preprocess")
+
+
+def m3_preprocess_backward_workspace(cfg: PreprocessConfig, rows) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().m3_preprocess_backward_workspace(ctypes.byref(cfg), int(rows),
+                                                           ctypes.byref(n)),
+           "m3_preprocess_backward_workspace")
+    return n.value
+
+
+def m3_preprocess_backward(cfg: PreprocessConfig, rows, projected, dt_bias, grad_x, grad_z,
+                           grad_bh, grad_ch, grad_dt, grad_adt, grad_trap, grad_angle,
+                           grad_projected, grad_dt_bias, workspace=None, stream=None):
+    wp, wn = _ws(workspace)
+    _check(load_library().m3_preprocess_backward(ctypes.byref(cfg), int(rows), *[_ptr(t) for t in (
+        projected, dt_bias, grad_x, grad_z, grad_bh, grad_ch, grad_dt, grad_adt, grad_trap,
+        grad_angle, grad_projected, grad_dt_bias)], wp, wn, _stream(stream)),
+        "m3_preprocess_backward")
 
 
 def m3_siso_forward_workspace(cfg: SsmConfig) -> int:

@@ -377,6 +377,39 @@ int m3_preprocess(const m3_preprocess_config* cfg, int64_t rows, const float* pr
   return cuda_status(launch_preprocess(g, projected, dt_bias, o, (cudaStream_t)stream));
 }
 
+int m3_preprocess_backward_workspace(const m3_preprocess_config* cfg, int64_t rows,
+                                     size_t* bytes) {
+  if (!bytes) return M3_ERR_INVALID_ARGUMENT;
+  PreGeom g;
+  const int st = resolve_pre(cfg, rows, &g);
+  if (st != M3_OK) return st;
+  *bytes = preprocess_backward_workspace_bytes(g);
+  return M3_OK;
+}
+
+int m3_preprocess_backward(const m3_preprocess_config* cfg, int64_t rows, const float* projected,
+                           const float* dt_bias, const float* grad_x, const float* grad_z,
+                           const float* grad_bh, const float* grad_ch, const float* grad_dt,
+                           const float* grad_adt, const float* grad_trap,
+                           const float* grad_angle, float* grad_projected, float* grad_dt_bias,
+                           void* workspace, size_t workspace_bytes, m3_stream_t stream) {
+  NvtxRange nvtx_range("m3_preprocess_backward");
+  PreGeom g;
+  int st = resolve_pre(cfg, rows, &g);
+  if (st != M3_OK) return st;
+  st = check_ptrs({projected, dt_bias, grad_x, grad_z, grad_bh, grad_ch, grad_dt, grad_adt,
+                   grad_trap, grad_projected, grad_dt_bias});
+  if (st != M3_OK) return st;
+  if ((st = check_angle_ptr(grad_angle, g.A)) != M3_OK) return st;
+  const size_t need = preprocess_backward_workspace_bytes(g);
+  if (!workspace || workspace_bytes < need) return M3_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return M3_ERR_UNALIGNED;
+  PreGrads gr{grad_x, grad_z, grad_bh, grad_ch, grad_dt, grad_adt, grad_trap, grad_angle};
+  return cuda_status(launch_preprocess_backward(g, projected, dt_bias, gr, grad_projected,
+                                                grad_dt_bias, (float*)workspace,
+                                                (cudaStream_t)stream));
+}
+
 }  // extern "C"
 
 namespace m3 {

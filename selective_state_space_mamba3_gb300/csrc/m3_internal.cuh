@@ -51,6 +51,12 @@ struct PreOut {
   float *x, *z, *bh, *ch, *dt, *adt, *trap, *angle;
 };
 
+// Gradients of the eight preprocess outputs (`mamba3_preprocess_backward`), in
+// the layouts of PreOut.
+struct PreGrads {
+  const float *x, *z, *bh, *ch, *dt, *adt, *trap, *angle;
+};
+
 // Recurrent-state inputs / outputs of the chunked scan. A CTA handles segment
 // `seg` of sequence `bh`: tokens [seg * seg_len, min(L, (seg + 1) * seg_len)).
 // States are "pre-loaded" (h plus the next token's trapezoid term), fp32,
@@ -92,6 +98,12 @@ cudaError_t launch_row_pre(const PreGeom& g, const float* projected, const float
                            float* inv, float* dt, float* adt, cudaStream_t s);
 cudaError_t launch_preprocess(const PreGeom& g, const float* projected, const float* dt_bias,
                               const PreOut& o, cudaStream_t s);
+// The preprocess adjoint: gproj [rows, W] and gdt_bias [H]; `partial` holds
+// preprocess_backward_workspace_bytes(g) of per-(chunk of rows, head) sums.
+size_t preprocess_backward_workspace_bytes(const PreGeom& g);
+cudaError_t launch_preprocess_backward(const PreGeom& g, const float* projected,
+                                       const float* dt_bias, const PreGrads& gr, float* gproj,
+                                       float* gdt_bias, float* partial, cudaStream_t s);
 cudaError_t launch_step(const ScanGeom& g, const ScanArgs& a, const StepState& st,
                         cudaStream_t s);
 // st: optional step state (null ssm: zero state, nothing written back).

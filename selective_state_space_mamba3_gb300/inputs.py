@@ -199,6 +199,16 @@ def scan_params(w: Workload, salt: int = 0):
     return out
 
 
+PRE_OUTPUTS = ("x", "z", "bh", "ch", "dt", "adt", "trap", "angle")
+
+
+def preprocess_output_gradient(w: Workload, shapes: dict, salt: int = 0):
+    """Gradients of the eight preprocess outputs fed to the preprocess adjoint:
+    each ~ N(0,1), in the shape `shapes` gives for it (name -> shape)."""
+    rng = rng_for(w, 600 + salt)
+    return {k: _normal(rng, shapes[k]) for k in PRE_OUTPUTS}
+
+
 def output_gradient(w: Workload, salt: int = 0, *, length=None):
     """The gradient of the scan output fed to the SISO backward: dout ~ N(0,1)
     in the output layout [B, L, H, P]."""

@@ -279,3 +279,45 @@ def test_backward_entries_check_before_launch(lib):
     margs[15] = None  # norm_weight
     assert lib.m3_mimo_backward(ctypes.byref(mimo), *margs, FAKE, 1 << 40, None) == \
         m3.M3_ERR_INVALID_ARGUMENT
+
+
+def test_preprocess_backward_checks_before_launch(lib):
+    """m3_preprocess_backward: the m3_preprocess geometry rules, a workspace of
+    the queried size, non-NULL 16-byte-aligned pointers (grad_angle may be NULL
+    only when A == 0), all checked on the host."""
+    n = ctypes.c_size_t(0)
+    good = pre_cfg()
+    assert lib.m3_preprocess_backward_workspace(ctypes.byref(good), 64, ctypes.byref(n)) == m3.M3_OK
+    need = n.value
+    assert need > 0
+    assert lib.m3_preprocess_backward_workspace(ctypes.byref(good), 64, None) == \
+        m3.M3_ERR_INVALID_ARGUMENT
+    for bad in BAD_PRE:
+        assert lib.m3_preprocess_backward_workspace(ctypes.byref(pre_cfg(**bad)), 64,
+                                                    ctypes.byref(n)) == m3.M3_ERR_INVALID_ARGUMENT
+        assert lib.m3_preprocess_backward(ctypes.byref(pre_cfg(**bad)), 64, *([FAKE] * 12), FAKE,
+                                          need, None) == m3.M3_ERR_INVALID_ARGUMENT
+    assert lib.m3_preprocess_backward(ctypes.byref(good), 0, *([FAKE] * 12), FAKE, need, None) == \
+        m3.M3_ERR_INVALID_ARGUMENT
+    args = [FAKE] * 12  # projected, dt_bias, the 8 output gradients, the 2 results
+    assert lib.m3_preprocess_backward(ctypes.byref(good), 64, *args, None, 0, None) == \
+        m3.M3_ERR_WORKSPACE
+    assert lib.m3_preprocess_backward(ctypes.byref(good), 64, *args, FAKE, need - 1, None) == \
+        m3.M3_ERR_WORKSPACE
+    assert lib.m3_preprocess_backward(ctypes.byref(good), 64, *args, FAKE_ODD, need, None) == \
+        m3.M3_ERR_UNALIGNED
+    for i in range(12):
+        a = list(args)
+        a[i] = None
+        assert lib.m3_preprocess_backward(ctypes.byref(good), 64, *a, FAKE, need, None) == \
+            m3.M3_ERR_INVALID_ARGUMENT, i
+        a[i] = FAKE_ODD
+        assert lib.m3_preprocess_backward(ctypes.byref(good), 64, *a, FAKE, need, None) == \
+            m3.M3_ERR_UNALIGNED, i
+    # grad_angle NULL is accepted without rotary angles (no GPU here: the launch fails)
+    a = list(args)
+    a[9] = None
+    no_rot = pre_cfg(num_rope_angles=0)
+    assert lib.m3_preprocess_backward_workspace(ctypes.byref(no_rot), 64, ctypes.byref(n)) == m3.M3_OK
+    assert lib.m3_preprocess_backward(ctypes.byref(no_rot), 64, *a, FAKE, n.value, None) == \
+        m3.M3_ERR_CUDA
