@@ -4,12 +4,15 @@
 //
 // HBM-bound streaming: every byte of `projected` is read once and every output
 // byte written once. One 256-thread block handles one row at a time
-// (grid-stride over rows): the z|x slices move as 128-bit streaming loads and
-// stores (four loads in flight per thread before their stores), each B/C row
-// is owned by one warp whose lanes hold one float4 each
-// (N <= 128) and reduce the mean square with shuffles, and the 3H + A scalar
-// columns are mapped by the first threads. Rows whose width or slice offsets
-// are not multiples of 4 floats take the scalar path of the same kernel.
+// (grid-stride over rows), no block barriers. Every thread first issues its
+// share of the z|x slices (128-bit streaming loads, four in flight), then does
+// its own column task while they land, then stores them. The column tasks are
+// spread so that no warp chains more than one: each B/C row is owned by one
+// warp, from the last warp down, whose lanes hold one float4 each (N <= 128)
+// and reduce the mean square with shuffles; the 3H scalar columns go to the
+// threads from 0, the A angle columns to the warp after those. Rows whose
+// width or slice offsets are not multiples of 4 floats take the scalar path of
+// the same kernel.
 #include "m3_internal.cuh"
 
 namespace m3 {
@@ -18,25 +21,82 @@ namespace {
 constexpr int kThreads = 256;
 
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float* __restrict__ proj,
+__global__ void __launch_bounds__(kThreads, 4) k_preprocess(PreGeom g, const float* __restrict__ proj,
                                                          const float* __restrict__ dt_bias,
                                                          PreOut o) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nwarps = kThreads / 32;
+  constexpr int nwarps = kThreads / 32;
   const int I = g.I, N = g.N, H = g.H, A = g.A, W = g.W;
   const int RG = g.G * g.R;
   const int BC = RG * N;
+  const int aoff = ((H + 31) / 32 * 32) % kThreads;
+  const int ta = tid >= aoff ? tid - aoff : tid - aoff + kThreads;
   for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
     const float* p = proj + r * (int64_t)W;
-    // z | x slices (columns [0, 2I)): four float4 loads per thread in flight
-    // before their stores (memory-level parallelism of the stream).
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+    const int I4 = I >> 2, Z4 = 2 * I4;
+    float4* z4 = reinterpret_cast<float4*>(o.z + r * (int64_t)I);
+    float4* x4 = reinterpret_cast<float4*>(o.x + r * (int64_t)I);
+    float4 v[4];
     if (VEC) {
-      const float4* p4 = reinterpret_cast<const float4*>(p);
-      const int I4 = I >> 2, Z4 = 2 * I4;
-      float4* z4 = reinterpret_cast<float4*>(o.z + r * (int64_t)I);
-      float4* x4 = reinterpret_cast<float4*>(o.x + r * (int64_t)I);
-      for (int base = tid; base < Z4; base += 4 * kThreads) {
-        float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = tid + u * kThreads;
+        if (i < Z4) v[u] = __ldcs(p4 + i);
+      }
+    }
+    // B rows then C rows (columns [2I, 2I + 2BC)), one warp per N-row.
+    for (int j = nwarps - 1 - warp; j < 2 * RG; j += nwarps) {
+      const float* src = p + 2 * I + (int64_t)j * N;
+      float* dst = (j < RG ? o.bh + r * (int64_t)BC + (int64_t)j * N
+                           : o.ch + r * (int64_t)BC + (int64_t)(j - RG) * N);
+      if (VEC && N <= 128) {
+        const int N4 = N >> 2;
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < N4) u = __ldcs(reinterpret_cast<const float4*>(src) + lane);
+        // (the fused packed-projection scan reduces in this same order: lane
+        // = float4 group, then the 16-8-4-2-1 butterfly)
+        const float ss = warp_sum(sumsq4(u));
+        const float inv = rms_inv(ss, N, g.eps);
+        if (lane < N4)
+          __stcs(reinterpret_cast<float4*>(dst) + lane,
+                 make_float4(__fmul_rn(u.x, inv), __fmul_rn(u.y, inv), __fmul_rn(u.z, inv),
+                             __fmul_rn(u.w, inv)));
+      } else {
+        float ss = 0.f;
+        for (int n = lane; n < N; n += 32) {
+          float x = src[n];
+          ss += x * x;
+        }
+        ss = warp_sum(ss);
+        const float inv = rms_inv(ss, N, g.eps);
+        for (int n = lane; n < N; n += 32) __stcs(dst + n, src[n] * inv);
+      }
+    }
+    // dt_raw | a_raw | trap (H each) | angle (A).
+    const float* s = p + 2 * I + 2 * BC;
+    for (int h = tid; h < H; h += kThreads) {
+      const float d = pre_dt(__ldcs(s + h), __ldg(dt_bias + h), g.dt_min, g.dt_max);
+      __stcs(o.dt + r * (int64_t)H + h, d);
+      __stcs(o.adt + r * (int64_t)H + h, pre_adt(__ldcs(s + H + h), g.a_floor, d));
+      __stcs(o.trap + r * (int64_t)H + h, __ldcs(s + 2 * H + h));
+    }
+    for (int a = ta; a < A; a += kThreads)
+      __stcs(o.angle + r * (int64_t)A + a, __ldcs(s + 3 * H + a));
+    // z | x slices (columns [0, 2I)): the loads issued above, then the rest
+    // four at a time
+    if (VEC) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = tid + u * kThreads;
+        if (i < Z4) {
+          if (i < I4)
+            __stcs(z4 + i, v[u]);
+          else
+            __stcs(x4 + (i - I4), v[u]);
+        }
+      }
+      for (int base = tid + 4 * kThreads; base < Z4; base += 4 * kThreads) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = base + u * kThreads;
@@ -55,50 +115,13 @@ __global__ void __launch_bounds__(kThreads) k_preprocess(PreGeom g, const float*
       }
     } else {
       for (int i = tid; i < 2 * I; i += kThreads) {
-        float v = __ldcs(p + i);
+        float x = __ldcs(p + i);
         if (i < I)
-          __stcs(o.z + r * (int64_t)I + i, v);
+          __stcs(o.z + r * (int64_t)I + i, x);
         else
-          __stcs(o.x + r * (int64_t)I + (i - I), v);
+          __stcs(o.x + r * (int64_t)I + (i - I), x);
       }
     }
-    // B rows then C rows (columns [2I, 2I + 2BC)), one warp per N-row.
-    for (int j = warp; j < 2 * RG; j += nwarps) {
-      const float* src = p + 2 * I + (int64_t)j * N;
-      float* dst = (j < RG ? o.bh + r * (int64_t)BC + (int64_t)j * N
-                           : o.ch + r * (int64_t)BC + (int64_t)(j - RG) * N);
-      if (VEC && N <= 128) {
-        const int N4 = N >> 2;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < N4) v = __ldcs(reinterpret_cast<const float4*>(src) + lane);
-        // (the fused packed-projection scan reduces in this same order: lane
-        // = float4 group, then the 16-8-4-2-1 butterfly)
-        const float ss = warp_sum(sumsq4(v));
-        const float inv = rms_inv(ss, N, g.eps);
-        if (lane < N4)
-          __stcs(reinterpret_cast<float4*>(dst) + lane,
-                 make_float4(__fmul_rn(v.x, inv), __fmul_rn(v.y, inv), __fmul_rn(v.z, inv),
-                             __fmul_rn(v.w, inv)));
-      } else {
-        float ss = 0.f;
-        for (int n = lane; n < N; n += 32) {
-          float v = src[n];
-          ss += v * v;
-        }
-        ss = warp_sum(ss);
-        const float inv = rms_inv(ss, N, g.eps);
-        for (int n = lane; n < N; n += 32) __stcs(dst + n, src[n] * inv);
-      }
-    }
-    // dt_raw | a_raw | trap (H each) | angle (A).
-    const float* s = p + 2 * I + 2 * BC;
-    for (int h = tid; h < H; h += kThreads) {
-      const float d = pre_dt(__ldcs(s + h), __ldg(dt_bias + h), g.dt_min, g.dt_max);
-      __stcs(o.dt + r * (int64_t)H + h, d);
-      __stcs(o.adt + r * (int64_t)H + h, pre_adt(__ldcs(s + H + h), g.a_floor, d));
-      __stcs(o.trap + r * (int64_t)H + h, __ldcs(s + 2 * H + h));
-    }
-    for (int a = tid; a < A; a += kThreads) __stcs(o.angle + r * (int64_t)A + a, __ldcs(s + 3 * H + a));
   }
 }
 

@@ -324,3 +324,41 @@ def test_autograd_binding(mimo):
     check_close(out.detach().cpu().numpy(), ref_out, BWD_TOL, "autograd forward")
     for k in keys:
         check_close(t[k].grad.cpu().numpy(), ref[k], BWD_TOL, f"autograd grad {k}")
+
+
+def test_autograd_preprocess_into_scan():
+    """The tiny workload trained end to end through the autograd binding:
+    preprocess -> SISO scan -> sum(out * W). The projection and dt_bias
+    gradients equal the oracle's chain (the scan adjoints of the oracle's
+    preprocess outputs, fed to the oracle's preprocess adjoint)."""
+    import torch
+    from selective_state_space_mamba3_gb300 import autograd as m3ag
+    w = gen.TINY_SISO
+    p = gen.tiny_projection(w)
+    pkw = dict(inner_size=32, state_size=16, num_heads=2, num_rope_angles=8, num_groups=1,
+               mimo_rank=1, **gen.TINY_PRE)
+    cfg = w.cfg()
+    dout = gen.output_gradient(w)
+    proj = dev(p["projected"]).requires_grad_(True)
+    dtb = dev(p["dt_bias"]).requires_grad_(True)
+    x, z, bh, ch, dt, adt, trap, angle = m3ag.preprocess(pkw, proj, dtb)
+    shp = lambda t, *s: t.reshape(*s)
+    out = m3ag.siso_scan(cfg, shp(ch, 1, 64, 1, 16), shp(bh, 1, 64, 1, 16), shp(x, 1, 64, 2, 16),
+                         shp(z, 1, 64, 2, 16), shp(adt, 1, 64, 2), shp(dt, 1, 64, 2),
+                         shp(trap, 1, 64, 2), shp(angle, 1, 64, 8), dev(p["c_bias"]),
+                         dev(p["b_bias"]), dev(p["d"]))
+    (out * dev(dout)).sum().backward()
+    torch.cuda.synchronize()
+    pre = oracle.preprocess(p["projected"], p["dt_bias"], **pkw)
+    f = lambda k, *s: pre[k].astype(np.float32).reshape(s)
+    sc = dict(c=f("ch", 1, 64, 1, 16), b=f("bh", 1, 64, 1, 16), x=f("x", 1, 64, 2, 16),
+              z=f("z", 1, 64, 2, 16), adt=f("adt", 1, 64, 2), dt=f("dt", 1, 64, 2),
+              trap=f("trap", 1, 64, 2), angle=f("angle", 1, 64, 8), c_bias=p["c_bias"],
+              b_bias=p["b_bias"], d=p["d"])
+    g = oracle.siso_backward(cfg, dout, *[sc[k] for k in KEYS])
+    pg = {"x": g["x"].reshape(64, 32), "z": g["z"].reshape(64, 32), "bh": g["b"].reshape(64, 16),
+          "ch": g["c"].reshape(64, 16), "dt": g["dt"].reshape(64, 2), "adt": g["adt"].reshape(64, 2),
+          "trap": g["trap"].reshape(64, 2), "angle": g["angle"].reshape(64, 8)}
+    ref = oracle.preprocess_backward(p["projected"], p["dt_bias"], pg, **pkw)
+    check_close(proj.grad.cpu().numpy(), ref["projected"], BWD_TOL, "autograd d projected")
+    check_close(dtb.grad.cpu().numpy(), ref["dt_bias"], BWD_TOL, "autograd d dt_bias")
