@@ -383,20 +383,23 @@ int64_t bias_chunk_rows(int64_t rows) {
   return c < kBiasChunk ? kBiasChunk : c;
 }
 
-cudaError_t launch_dependent(void (*kernel)(int, int64_t, const float*, float*), unsigned grid,
-                             unsigned block, cudaStream_t s, int H, int64_t n, const float* in,
-                             float* out) {
+// Launch configuration of a programmatic dependent of the previous kernel on
+// the stream (the kernel waits for it with griddepcontrol.wait before reading
+// its results). Used in place: cfg points at the object's own attribute.
+struct PdlLaunch {
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, H, n, in, out);
-}
+  cudaLaunchConfig_t cfg;
+  PdlLaunch(unsigned grid, unsigned block, cudaStream_t s) : cfg{} {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  PdlLaunch(const PdlLaunch&) = delete;
+};
 
 }  // namespace
 
@@ -445,21 +448,13 @@ cudaError_t launch_preprocess_backward(const PreGeom& g, const float* projected,
   const int64_t nchunk = (g.rows + chunk - 1) / chunk;
   const int hblocks = (g.H + 31) / 32;
   if (nchunk * hblocks > 0x7fffffff) return cudaErrorInvalidValue;
-  {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(nchunk * hblocks));
-    cfg.blockDim = dim3(kThreads);
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, k_pre_bias_part, g, (const float*)gproj, chunk, hblocks, partial);
-    if (e != cudaSuccess) return e;
-  }
-  e = launch_dependent(k_pre_bias_sum, (unsigned)hblocks, kSumThreads, s, (int)g.H, nchunk,
-                       partial, gdt_bias);
+  PdlLaunch part(static_cast<unsigned>(nchunk * hblocks), kThreads, s);
+  e = cudaLaunchKernelEx(&part.cfg, k_pre_bias_part, g, static_cast<const float*>(gproj), chunk,
+                         hblocks, partial);
+  if (e != cudaSuccess) return e;
+  PdlLaunch sum(static_cast<unsigned>(hblocks), kSumThreads, s);
+  e = cudaLaunchKernelEx(&sum.cfg, k_pre_bias_sum, static_cast<int>(g.H), nchunk,
+                         static_cast<const float*>(partial), gdt_bias);
   count_launches(3);
   return e;
 }
