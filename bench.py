@@ -14,7 +14,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl m3|reference]
 --part NAME runs only one supplementary part (siso_scan_fp32, mimo_scan_fp32,
 mimo_scan_tf32, mimo_packed_tf32, siso_long_scan_fp32, siso_long_scan_tf32, siso_step,
 mimo_step, siso_prefill_tf32, siso_backward_fp32, siso_long_backward_fp32,
-mimo_backward_fp32, preprocess_backward) and prints its JSON, for profiling it alone.
+mimo_backward_fp32, preprocess_backward, train_step_fp32) and prints its JSON, for
+profiling it alone.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas, weak scaling, no collective on the data path).
 """
@@ -729,6 +730,47 @@ def parts_preprocess_backward(torch, m3, w, peak):
             "hbm_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4), "algorithmic_bytes": nbytes}
 
 
+def parts_train_step(torch, m3, w, peak):
+    """Supplementary: one training step of the layer's scan through the
+    torch.autograd binding (selective_state_space_mamba3_gb300.autograd): the
+    packed projection -> m3_preprocess -> m3_siso_forward (FP32-exact) -> loss
+    sum(out * W) -> m3_siso_backward -> m3_preprocess_backward, i.e. the
+    projection and dt_bias gradients (and those of c_bias, b_bias, D).
+    Device-resident inputs; the torch elementwise ops of the loss run beside."""
+    from selective_state_space_mamba3_gb300 import autograd as m3ag
+    p = gen.layer_projection(w)
+    sp = gen.scan_params(w)
+    B, L, H, P, N, A = (w.batch_size, w.sequence_length, w.num_heads, w.head_dim, w.state_size,
+                        w.num_rope_angles)
+    G = H if w.num_groups == 0 else w.num_groups
+    pkw = dict(inner_size=H * P, state_size=N, num_heads=H, num_rope_angles=A, num_groups=G,
+               mimo_rank=1, **gen.PRE_DEFAULT)
+    proj = torch.from_numpy(p["projected"]).cuda().requires_grad_(True)
+    dtb = torch.from_numpy(p["dt_bias"]).cuda().requires_grad_(True)
+    par = {k: torch.from_numpy(sp[k]).cuda().requires_grad_(True) for k in ("c_bias", "b_bias", "d")}
+    wgt = torch.from_numpy(gen.output_gradient(w)).cuda()
+    cfg = w.cfg()
+
+    def step():
+        x, z, bh, ch, dt, adt, trap, ang = m3ag.preprocess(pkw, proj, dtb)
+        out = m3ag.siso_scan(cfg, ch.view(B, L, G, N), bh.view(B, L, G, N), x.view(B, L, H, P),
+                             z.view(B, L, H, P), adt.view(B, L, H), dt.view(B, L, H),
+                             trap.view(B, L, H), ang.view(B, L, A), par["c_bias"], par["b_bias"],
+                             par["d"])
+        (out * wgt).sum().backward()
+        proj.grad = None
+        dtb.grad = None
+        for v in par.values():
+            v.grad = None
+    for _ in range(3):
+        step()
+    ms = time_events(torch, step, 5)
+    return {"workload": w.name, "mode": "fp32", "ms": round(ms, 4),
+            "tokens_per_s": round(w.tokens / (ms * 1e-3)),
+            "entry": "autograd: m3_preprocess, m3_siso_forward, m3_siso_backward, "
+                     "m3_preprocess_backward"}
+
+
 def part_by_name(torch, m3, name, peak):
     """One supplementary part, by its key in the JSON line's `parts`."""
     table = {
@@ -745,6 +787,7 @@ def part_by_name(torch, m3, name, peak):
         "siso_long_backward_fp32": lambda: parts_backward(torch, m3, gen.SISO_LONG, peak),
         "mimo_backward_fp32": lambda: parts_backward_mimo(torch, m3, gen.MIMO_R4, peak),
         "preprocess_backward": lambda: parts_preprocess_backward(torch, m3, gen.SISO_1B, peak),
+        "train_step_fp32": lambda: parts_train_step(torch, m3, gen.SISO_1B, peak),
     }
     if name not in table:
         raise SystemExit(f"bench.py: unknown part {name!r}; one of {sorted(table)}")
@@ -888,7 +931,7 @@ def run_m3(args):
                      "siso_long_scan_fp32",
                      "siso_long_scan_tf32", "siso_step", "mimo_step", "siso_prefill_tf32",
                      "siso_backward_fp32", "siso_long_backward_fp32", "mimo_backward_fp32",
-                     "preprocess_backward"):
+                     "preprocess_backward", "train_step_fp32"):
             parts[name] = part_by_name(torch, m3, name, peak)
             torch.cuda.empty_cache()
 
