@@ -65,7 +65,8 @@ def test_preprocess_tiny_unaligned_width():
                      oracle.preprocess(p["projected"], p["dt_bias"], **kw))
 
 
-@pytest.mark.parametrize("w", [gen.SISO_1B, gen.MIMO_R4], ids=["siso_layer", "mimo_layer"])
+@pytest.mark.parametrize("w", [gen.SISO_1B, gen.MIMO_R4, gen.SISO_LONG],
+                         ids=["siso_layer", "mimo_layer", "long_context_layer"])
 def test_preprocess_layer_shape(w):
     p = gen.layer_projection(w)
     kw = dict(inner_size=w.num_heads * w.head_dim, state_size=w.state_size,

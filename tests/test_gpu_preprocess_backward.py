@@ -179,7 +179,8 @@ def test_many_heads():
     check(proj, dtb, grads, kw)
 
 
-@pytest.mark.parametrize("w", [gen.SISO_1B, gen.MIMO_R4], ids=["siso_layer", "mimo_layer"])
+@pytest.mark.parametrize("w", [gen.SISO_1B, gen.MIMO_R4, gen.SISO_LONG],
+                         ids=["siso_layer", "mimo_layer", "long_context_layer"])
 def test_layer_shape(w):
     """The layer's packed projection (the distributions of the preprocess parity
     tests) at full size, every element compared, and a second call bit-identical."""
