@@ -195,3 +195,32 @@ def test_layer_shape(w):
     got, got_b = check(p["projected"], p["dt_bias"], grads, kw)
     again, again_b = gpu_preprocess_backward(p["projected"], p["dt_bias"], grads, kw)
     assert np.array_equal(got, again) and np.array_equal(got_b, again_b)
+
+
+@pytest.mark.parametrize("rows, heads, angles", [(1, 3, 2), (7, 1, 4), (129, 2, 0)],
+                         ids=["one_row", "one_head", "no_angles_null_pointer"])
+def test_degenerate_sizes(rows, heads, angles):
+    """One row (one block, one dt_bias partial), one head, and A = 0 with the
+    angle gradient passed as a NULL pointer (129 rows: two partial chunks)."""
+    import torch
+    kw = dict(inner_size=8, state_size=8, num_heads=heads, num_rope_angles=angles, num_groups=1,
+              mimo_rank=2, epsilon=1e-5, dt_min=1e-2, dt_max=0.5, a_floor=0.5)
+    proj, dtb, grads = _random_case(rows, kw, seed=23)
+    _mask_ties(proj, dtb, grads, kw)
+    if angles:
+        check(proj, dtb, grads, kw)
+        return
+    cfg = m3.preprocess_config(**kw)
+    gp = torch.full(proj.shape, float("nan"), device="cuda")
+    gb = torch.full((heads,), float("nan"), device="cuda")
+    ws = torch.empty(max(m3.m3_preprocess_backward_workspace(cfg, rows), 16), dtype=torch.uint8,
+                     device="cuda")
+    g = [None if k == "angle" else dev(grads[k]) for k in NAMES]
+    m3.m3_preprocess_backward(cfg, rows, dev(proj), dev(dtb), *g, gp, gb, ws)
+    torch.cuda.synchronize()
+    ref = oracle.preprocess_backward(proj, dtb, grads, **kw)
+    assert np.all(np.isfinite(gp.cpu().numpy()))
+    err = np.max(np.abs(gp.cpu().numpy() - ref["projected"])) / np.max(np.abs(ref["projected"]))
+    assert err <= 4e-6, err
+    bound = 1e-5 * np.sum(np.abs(ref["projected"][:, -3 * heads:-2 * heads]), axis=0) + 1e-30
+    assert np.all(np.abs(gb.cpu().numpy() - ref["dt_bias"]) <= bound)
